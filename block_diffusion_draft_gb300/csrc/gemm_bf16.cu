@@ -1,0 +1,466 @@
+// gemm_bf16.cu -- tcgen05 projection GEMM for the bf16 path.
+//
+// C = A * B^T where A holds token rows (bf16, K contiguous) and B the weight
+// rows of an nn.Linear (bf16, [N, K]).  One CTA computes one 128 x 128 output
+// tile over one slice of K:
+//   warp 0      TMA producer: 128x64 A and B boxes, 128-byte swizzle,
+//               STAGES-deep mbarrier ring
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128,
+//               N=128, K=16 per instruction), fp32 accumulator in TMEM
+//   warps 2..5  epilogue: one accumulator row (token) per thread, read with
+//               tcgen05.ld
+// When K is split across CTAs, every CTA writes its fp32 partial tile, and
+// the last CTA to finish a tile (atomic counter) adds the others' partials
+// and runs the epilogue; it also resets the counter for the next launch.
+//
+// Epilogues:
+//   EPI_BF16  plain bf16 store (o_proj)
+//   EPI_F32   plain fp32 store (fc, before hidden_norm)
+//   EPI_QKV   the fused QKV projection of the draft layer: per-head RMSNorm
+//             (q_norm / k_norm), NeoX RoPE at the row's position, Q scaled by
+//             head_dim^-0.5*log2(e) into the Q buffer, K and V appended to the
+//             draft cache.  ("vllm.model_executor.models.qwen3_dflash",
+//             DFlashQwen3Attention.forward: qkv_proj -> split -> per-head
+//             RMSNorm -> rotary; "DFlash源码导读（二）", steps 1-4.)
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace df {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6;
+constexpr int kThreads = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
+constexpr int HD = 128;  // head_dim of the bf16 path
+
+struct Plan {
+  int a0_rows, a1_rows, n_m0, n_m1;
+  int n_tiles, n_q_tiles, n_kb, splits, units_q;
+  int ldc;
+  float* partial;
+  int* counters;
+  void* c;
+  int* err;
+};
+
+DF_DEV void decode_unit(const Plan& p, int u, int& m_tile, int& n_tile,
+                        int& split) {
+  if (u < p.units_q) {
+    const int per = p.splits * p.n_m0;
+    n_tile = u / per;
+    const int r = u - n_tile * per;
+    split = r / p.n_m0;
+    m_tile = r - split * p.n_m0;
+  } else {
+    u -= p.units_q;
+    const int mt = p.n_m0 + p.n_m1;
+    const int per = p.splits * mt;
+    const int nn = u / per;
+    const int r = u - nn * per;
+    n_tile = p.n_q_tiles + nn;
+    split = r / mt;
+    m_tile = r - split * mt;
+  }
+}
+
+DF_DEV void store_bf16_row(void* dst, const float* v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    d4[i] = w;
+  }
+}
+
+// per-head RMSNorm over the 128 values, then NeoX rotation (pairs j, j+64)
+// with the row's (cos, sin) table, then an optional scale
+DF_DEV void norm_rope(float* v, const float* w, float eps, const float2* rope_row,
+                      float scale) {
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < HD; ++j) ss = fmaf(v[j], v[j], ss);
+  const float inv = rsqrtf(ss * (1.f / HD) + eps);
+#pragma unroll
+  for (int j = 0; j < HD; ++j) v[j] *= inv * __ldg(w + j);
+  const float4* r4 = reinterpret_cast<const float4*>(rope_row);
+#pragma unroll
+  for (int jj = 0; jj < HD / 4; ++jj) {
+    const float4 cs = __ldg(r4 + jj);  // cos_j, sin_j, cos_j+1, sin_j+1
+    const int j = 2 * jj;
+    const float a0 = v[j], b0 = v[j + HD / 2];
+    const float a1 = v[j + 1], b1 = v[j + 1 + HD / 2];
+    v[j] = (a0 * cs.x - b0 * cs.y) * scale;
+    v[j + HD / 2] = (b0 * cs.x + a0 * cs.y) * scale;
+    v[j + 1] = (a1 * cs.z - b1 * cs.w) * scale;
+    v[j + 1 + HD / 2] = (b1 * cs.z + a1 * cs.w) * scale;
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0,
+                     const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ Plan p,
+                     const __grid_constant__ QkvOut qo,
+                     const __grid_constant__ SeqTable st) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accb = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int m_tile, n_tile, split;
+  decode_unit(p, blockIdx.x, m_tile, n_tile, split);
+  const int kb0 = (int)((long long)split * p.n_kb / p.splits);
+  const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
+  const int nkb = kb1 - kb0;
+  const bool from_a0 = m_tile < p.n_m0;
+  const int a_row0 = (from_a0 ? m_tile : m_tile - p.n_m0) * BM;
+  const int n0 = n_tile * BN;
+  const int tile_id = n_tile * (p.n_m0 + p.n_m1) + m_tile;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(from_a0 ? &tmA0 : &tmA1);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* ma = from_a0 ? &tmA0 : &tmA1;
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+        const int kx = (kb0 + i) * BK;
+        tma_load_2d(sA + s * A_BYTES, ma, &full[s], kx, a_row0, pol_a);
+        tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kx, n0, pol_w);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(&full[s], ph, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sA + s * A_BYTES);
+        const uint32_t b_base = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+          tc_mma_bf16(tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(accb);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const bool ok = mbar_wait(accb, 0, abort_flag, p.err);
+    tc_fence_after();
+    float v[BN];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      float t[32];
+      tmem_ld32(trow + c * 32, t);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[c * 32 + i] = ok ? t[i] : 0.f;
+    }
+    bool last = true;
+    if (p.splits > 1) {
+      float4* mine = reinterpret_cast<float4*>(
+          p.partial + ((size_t)tile_id * p.splits + split) * (BM * BN));
+#pragma unroll
+      for (int c4 = 0; c4 < BN / 4; ++c4)
+        __stcg(mine + c4 * BM + r,
+               make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (r == 0) {
+        const int old = atomicAdd(p.counters + tile_id, 1);
+        *last_flag = (old == p.splits - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      last = *last_flag != 0;
+      if (last) {
+        __threadfence();
+        for (int s2 = 0; s2 < p.splits; ++s2) {
+          if (s2 == split) continue;
+          const float4* other = reinterpret_cast<const float4*>(
+              p.partial + ((size_t)tile_id * p.splits + s2) * (BM * BN));
+#pragma unroll
+          for (int c4 = 0; c4 < BN / 4; ++c4) {
+            const float4 t = __ldcg(other + c4 * BM + r);
+            v[4 * c4] += t.x;
+            v[4 * c4 + 1] += t.y;
+            v[4 * c4 + 2] += t.z;
+            v[4 * c4 + 3] += t.w;
+          }
+        }
+        if (r == 0) p.counters[tile_id] = 0;
+      }
+    }
+    if (last) {
+      if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
+        const int row = a_row0 + r;
+        if (row < p.a0_rows) {
+          if constexpr (EPI == EPI_BF16) {
+            store_bf16_row(reinterpret_cast<__nv_bfloat16*>(p.c) +
+                               (size_t)row * p.ldc + n0,
+                           v);
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(
+                reinterpret_cast<float*>(p.c) + (size_t)row * p.ldc + n0);
+#pragma unroll
+            for (int c4 = 0; c4 < BN / 4; ++c4)
+              d4[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                                   v[4 * c4 + 3]);
+          }
+        }
+      } else {
+        // ---------------- fused QKV epilogue: one head (128 columns) per tile
+        const int grow = a_row0 + r;
+        const bool valid = from_a0 ? grow < p.a0_rows : grow < p.a1_rows;
+        if (valid) {
+          int b, pos_idx, crow, t = 0;
+          if (from_a0) {  // noise (block) row
+            b = grow / st.q_len;
+            t = grow - b * st.q_len;
+            const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
+            pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
+            crow = st.cache_len[b] + nb + t;
+          } else {  // new context row: find its sequence
+            int lo = 0, hi = st.n;
+            while (hi - lo > 1) {
+              const int mid = (lo + hi) >> 1;
+              if (st.ctx_off[mid] <= grow) lo = mid; else hi = mid;
+            }
+            b = lo;
+            const int rr = grow - st.ctx_off[b];
+            pos_idx = st.ctx_off[b] + b * st.q_len + rr;
+            crow = st.cache_len[b] + rr;
+          }
+          const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
+          if (n0 < q_cols + kv_cols) {
+            int pos = qo.positions[pos_idx];
+            if (pos < 0 || pos >= qo.max_pos) {
+              record_error(p.err, 2 /* DFLASH_DEV_POSITION */);
+              pos = 0;
+            }
+            const float2* rope_row = qo.rope + (size_t)pos * (HD / 2);
+            if (n0 < q_cols) {
+              const int hq = n0 / HD;
+              const int h = hq / qo.groups, gi = hq - h * qo.groups;
+              const int nblk = st.q_len / qo.q_block;
+              const int blk = t / qo.q_block, tt = t - blk * qo.q_block;
+              const size_t qrow =
+                  ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) *
+                      qo.q_block + tt;
+              norm_rope(v, qo.q_norm, qo.eps, rope_row, qo.q_scale);
+              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD, v);
+            } else {
+              const int h = (n0 - q_cols) / HD;
+              norm_rope(v, qo.k_norm, qo.eps, rope_row, 1.f);
+              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
+                                 (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
+                             v);
+            }
+          } else {
+            const int h = (n0 - q_cols - kv_cols) / HD;
+            store_bf16_row(reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
+                               (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
+                           v);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                  void*, const cuuint64_t*, const cuuint64_t*,
+                                  const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+int choose_splits(int tiles, int n_kb, int num_sms) {
+  if (tiles >= num_sms) return 1;
+  int s = (num_sms + tiles - 1) / tiles;
+  s = std::min(s, std::max(1, n_kb / 4));
+  return std::max(1, std::min(s, 16));
+}
+
+struct Geometry {
+  int n_m0, n_m1, n_tiles, n_q_tiles, n_kb, tiles, splits;
+};
+
+Geometry geometry(int rows0, int rows1, int n, int k, int q_cols, int num_sms) {
+  Geometry g;
+  g.n_m0 = (rows0 + BM - 1) / BM;
+  g.n_m1 = (rows1 + BM - 1) / BM;
+  g.n_tiles = n / BN;
+  g.n_q_tiles = q_cols / BN;
+  g.n_kb = k / BK;
+  g.tiles = g.n_q_tiles * g.n_m0 + (g.n_tiles - g.n_q_tiles) * (g.n_m0 + g.n_m1);
+  g.splits = choose_splits(g.tiles, g.n_kb, num_sms);
+  return g;
+}
+
+}  // namespace
+
+int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
+                        int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return -1;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || (cols % 8) != 0 || rows <= 0)
+    return -2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                  dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
+size_t gemm_scratch_bytes(int rows0, int rows1, int n, int k, int q_cols,
+                          int num_sms, int* n_counters) {
+  Geometry g = geometry(rows0, rows1, n, k, q_cols, num_sms);
+  const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
+  if (n_counters) *n_counters = dense_tiles;
+  if (g.splits <= 1) return 0;
+  return (size_t)dense_tiles * g.splits * BM * BN * sizeof(float);
+}
+
+int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
+                     const QkvOut* qkv, const SeqTable* seqs,
+                     const GemmScratch& scr, int num_sms, int* err,
+                     cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(gemm_bf16_kernel<EPI_BF16>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaFuncSetAttribute(gemm_bf16_kernel<EPI_F32>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaFuncSetAttribute(gemm_bf16_kernel<EPI_QKV>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    attr_done = true;
+  }
+  if (s.n % BN != 0 || s.k % BK != 0 || s.q_cols % BN != 0) return cudaErrorInvalidValue;
+  Geometry g = geometry(s.a0_rows, s.a1_rows, s.n, s.k, s.q_cols, num_sms);
+  if (g.tiles == 0) return cudaSuccess;
+  Plan p;
+  p.a0_rows = s.a0_rows;
+  p.a1_rows = s.a1_rows;
+  p.n_m0 = g.n_m0;
+  p.n_m1 = g.n_m1;
+  p.n_tiles = g.n_tiles;
+  p.n_q_tiles = g.n_q_tiles;
+  p.n_kb = g.n_kb;
+  p.splits = g.splits;
+  p.units_q = g.n_q_tiles * g.splits * g.n_m0;
+  p.ldc = ldc;
+  p.c = c;
+  p.err = err;
+  p.partial = scr.partial;
+  p.counters = scr.counters;
+  if (g.splits > 1) {
+    const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * BN * 4;
+    if (scr.partial == nullptr || scr.partial_bytes < need ||
+        scr.n_counters < g.n_tiles * (g.n_m0 + g.n_m1))
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap ma0, ma1;
+  if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, BM) != 0)
+    return cudaErrorInvalidValue;
+  if (s.a1_rows > 0) {
+    if (make_tmap_bf16_rows(&ma1, s.a1, s.a1_rows, s.k, BM) != 0)
+      return cudaErrorInvalidValue;
+  } else {
+    ma1 = ma0;
+  }
+  static QkvOut zero_q{};
+  static SeqTable zero_st{};
+  const QkvOut& qo = qkv ? *qkv : zero_q;
+  const SeqTable& st = seqs ? *seqs : zero_st;
+  const int units = g.tiles * g.splits;
+  dim3 grid(units), block(kThreads);
+  switch (epi) {
+    case EPI_BF16:
+      gemm_bf16_kernel<EPI_BF16><<<grid, block, SMEM_BYTES, stream>>>(
+          ma0, ma1, *s.b_map, p, qo, st);
+      break;
+    case EPI_F32:
+      gemm_bf16_kernel<EPI_F32><<<grid, block, SMEM_BYTES, stream>>>(
+          ma0, ma1, *s.b_map, p, qo, st);
+      break;
+    default:
+      gemm_bf16_kernel<EPI_QKV><<<grid, block, SMEM_BYTES, stream>>>(
+          ma0, ma1, *s.b_map, p, qo, st);
+      break;
+  }
+  return (int)cudaGetLastError();
+}
+
+}  // namespace df

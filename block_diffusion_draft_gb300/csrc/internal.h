@@ -1,0 +1,122 @@
+// internal.h -- structures shared by the host API and the kernels, and the
+// host-side launchers each kernel file exports.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace df {
+
+constexpr int kMaxBatch = 512;
+
+// Per-sequence bookkeeping of one forward call, passed to kernels by value.
+struct SeqTable {
+  int n;                       // sequences
+  int q_len;                   // block rows per sequence
+  int ctx_off[kMaxBatch + 1];  // prefix sums of new context rows
+  int cache_len[kMaxBatch];    // rows cached before this call
+};
+
+// Where the QKV projection epilogue puts its results.
+struct QkvOut {
+  int n_heads, n_kv, groups;
+  int q_block;       // rows of one block inside the Q buffer layout
+  int cap;           // key rows per (sequence, kv head) in the K/V storage
+  int max_pos;
+  float eps;
+  float q_scale;     // head_dim^-0.5 * log2(e), folded into Q
+  const int* positions;
+  const float2* rope;      // [max_pos][head_dim/2] (cos, sin)
+  const float* q_norm;     // [head_dim] fp32
+  const float* k_norm;     // [head_dim] fp32
+  void* qbuf;              // [B][n_kv][n_blocks][groups][q_block][d]
+  void* cache_k;           // [B][n_kv][cap][d]
+  void* cache_v;
+};
+
+// ----------------------------------------------------------- bf16 GEMM
+// C = A * B^T with A [rows, K] (token rows; two sources A0 then A1) and B
+// [N, K] (weights), both bf16 K-contiguous; fp32 accumulation on tcgen05.
+enum GemmEpi { EPI_BF16 = 0, EPI_F32 = 1, EPI_QKV = 2 };
+
+struct GemmShape {
+  const void* a0; int a0_rows;   // noise rows (or the only source)
+  const void* a1; int a1_rows;   // context rows (may be 0)
+  const CUtensorMap* b_map;      // weights, built once at create
+  int n, k;
+  int q_cols;                    // leading columns computed from A0 only
+};
+
+struct GemmScratch {
+  float* partial; size_t partial_bytes;
+  int* counters; int n_counters;
+};
+
+int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
+                     const QkvOut* qkv, const SeqTable* seqs,
+                     const GemmScratch& scr, int num_sms, int* err,
+                     cudaStream_t st);
+size_t gemm_scratch_bytes(int rows0, int rows1, int n, int k, int q_cols,
+                          int num_sms, int* n_counters);
+int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
+                        int cols, int box_rows);
+
+// ----------------------------------------------------------- attention
+// Per-sequence key ranges of an inference attention call.
+struct AttnSeqs {
+  int len[kMaxBatch];          // keys of the sequence after this call's append
+  int lo[kMaxBatch];           // first key any query of the block can see
+  int n_chunks[kMaxBatch];     // splits of [lo, len) per kv head
+  int unit_off[kMaxBatch + 1]; // first work unit of the sequence
+};
+
+struct AttnArgs {
+  int mode;          // 0 = inference (cache), 1 = packed training
+  int batch, n_kv, groups, head_dim;
+  int q_len;         // query rows per sequence (all blocks)
+  int q_block;       // rows per block (q_len for inference)
+  int n_blocks;      // blocks per sequence (1 for inference)
+  int tile_blocks;   // blocks per 128-row Q tile
+  int cap;           // key rows per (sequence, head) in the K/V storage
+  int window;        // sliding window (0 = full)
+  int seq;           // packed: context rows per sequence
+  const int* anchors;  // packed: [B][n_blocks]
+  int n_units;
+  int chunk;         // inference: keys per split
+  float* part_o;     // [units][128 rows][d] fp32 partial outputs
+  float* part_ml;    // [units][2][128] running max (log2 units) and sum
+  int* counters;     // [B * n_kv]
+  void* out;         // [B*q_len][n_heads*d]
+  int* err;
+};
+
+int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
+                     long long q_rows_total, const void* cache_k,
+                     const void* cache_v, long long kv_rows_total,
+                     cudaStream_t st);
+
+// ----------------------------------------------------------- small kernels
+int launch_rope_table(float2* tab, int max_pos, int half, float theta,
+                      cudaStream_t st);
+int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
+                       float eps, void* out, int out_bf16, cudaStream_t st);
+int launch_to_f32(const void* src, int src_bf16, float* dst, size_t n,
+                  cudaStream_t st);
+int launch_packed_positions(const int* anchors, int batch, int seq,
+                            int n_blocks, int block_size, int* pos, int* err,
+                            cudaStream_t st);
+
+// ----------------------------------------------------------- fp32 path
+int launch_gemm_f32(const float* a, int rows, const float* b, int n, int k,
+                    float* c, int ldc, cudaStream_t st);
+int launch_qkv_post_f32(const float* qkv_noise, int rows_noise,
+                        const float* qkv_ctx, int rows_ctx, const QkvOut& o,
+                        const SeqTable* seqs, int head_dim, int* err,
+                        cudaStream_t st);
+int launch_attn_f32(const AttnArgs& a, const AttnSeqs* seqs, const float* qbuf,
+                    const float* k, const float* v, cudaStream_t st);
+
+}  // namespace df

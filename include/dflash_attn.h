@@ -1,0 +1,221 @@
+/*
+ * dflash_attn.h -- C ABI of the GB300 DFlash draft attention library
+ * (libdflash_attn.so).
+ *
+ * One draft attention layer of a DFlash block-diffusion drafter
+ * (Qwen3DFlashAttention): queries from a block of noise tokens (one anchor
+ * plus mask tokens), keys and values from the projected target-model context
+ * followed by the block, per-head q/k RMSNorm, RoPE over the
+ * [context | block] window, grouped KV heads, non-causal softmax (optionally
+ * a symmetric sliding-window band), o_proj, and a draft KV cache that is
+ * cropped back to the accepted prefix after verification.
+ *
+ * Page citations name the page by title and the section or symbol on it:
+ *   [P3] "DFlash源码导读（二）：Qwen3DFlashAttention注意力实现全解析"
+ *   [P4] "nemo_automodel.components.speculative.dflash.draft_qwen3"
+ *   [P5] "vllm.model_executor.models.qwen3_dflash"
+ *
+ * Conventions for every call:
+ *  - Every entry point returns an int status: DFLASH_OK (0) or a negative
+ *    DFLASH_ERR_* code; dflash_last_error() then returns a message for the
+ *    calling thread.  No C++ exception crosses this boundary.
+ *  - Arguments are checked on the host before anything is enqueued.  A call
+ *    that fails a check enqueues no work and leaves every object unchanged.
+ *  - "device" pointers are CUDA device memory of the device that was current
+ *    when the layer was created; "host" pointers are ordinary CPU memory that
+ *    is read only during the call.  The caller owns every pointer it passes.
+ *    Device tensors handed to a bf16 layer must start on a 16-byte boundary.
+ *  - Tensors are dense, row-major, in the layer's dtype (DFLASH_BF16 or
+ *    DFLASH_FP32) unless stated otherwise; integer tensors are int32.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously; outputs are valid once the stream has
+ *    reached that point.
+ *  - Handles are not thread-safe: one thread (or external locking) per layer
+ *    handle and per cache at a time.  One layer's calls share its scratch, so
+ *    calls of one layer must not run concurrently on different streams.
+ *  - Faults found on the device (a position outside [0, max_position), an
+ *    anchor outside [0, seq], a bounded wait that ran out) do not stop the
+ *    kernels: the offending value is clamped, a code is recorded in the
+ *    layer's device error word, and dflash_device_error() reports it.
+ */
+#ifndef DFLASH_ATTN_H
+#define DFLASH_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dflash_attn dflash_attn;   /* one layer: weights + scratch */
+typedef struct dflash_cache dflash_cache; /* one draft KV cache */
+typedef void* dflash_stream;              /* a cudaStream_t */
+
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_ARG = -1,         /* null pointer, bad enum, non-positive size  */
+  DFLASH_ERR_SHAPE = -2,       /* sizes inconsistent with the layer/cache    */
+  DFLASH_ERR_CAPACITY = -3,    /* cache rows would exceed its capacity       */
+  DFLASH_ERR_RANGE = -4,       /* crop length above the current length, ...  */
+  DFLASH_ERR_CUDA = -5,        /* a CUDA runtime call failed                 */
+  DFLASH_ERR_DEVICE = -6,      /* a kernel recorded a device-side fault      */
+  DFLASH_ERR_UNSUPPORTED = -7, /* valid request this build does not handle   */
+  DFLASH_ERR_MEMORY = -8       /* device allocation failed                   */
+};
+
+enum { DFLASH_BF16 = 0, DFLASH_FP32 = 1 };
+
+/* Device-side fault codes reported by dflash_device_error(). */
+enum {
+  DFLASH_DEV_OK = 0,
+  DFLASH_DEV_WAIT_TIMEOUT = 1, /* a pipeline wait gave up (kernel returned)  */
+  DFLASH_DEV_POSITION = 2,     /* position outside [0, max_position)         */
+  DFLASH_DEV_ANCHOR = 3        /* anchor outside [0, seq]                    */
+};
+
+/* Layer scalars.  [P3] step 1: head_dim is the explicit value, else
+ * hidden / n_heads; num_key_value_groups = n_heads / n_kv_heads.
+ * [P4] Qwen3DFlashAttention: scaling = head_dim^-0.5; sliding_window only on
+ * sliding-attention layers ([P3] step 5).  [P5] DFlashQwen3Model: fc takes
+ * n_target_layers * hidden concatenated features. */
+typedef struct {
+  int32_t hidden;          /* H                                              */
+  int32_t n_heads;         /* query heads                                    */
+  int32_t n_kv_heads;      /* key/value heads; divides n_heads               */
+  int32_t head_dim;        /* d; 0 -> hidden / n_heads                       */
+  int32_t n_target_layers; /* fc input width = n_target_layers * hidden; 0 = no fc */
+  float rms_eps;           /* eps of q_norm, k_norm and hidden_norm          */
+  float rope_theta;        /* RoPE base                                      */
+  int32_t sliding_window;  /* 0 = full attention; W > 0 keeps keys with
+                              |query key index - key index| < W ([P4]
+                              _sliding_window_mask)                          */
+  int32_t max_position;    /* positions must lie in [0, max_position);
+                              0 -> 131072                                    */
+  int32_t dtype;           /* DFLASH_BF16 or DFLASH_FP32                     */
+} dflash_attn_config;
+
+/* Message for the last failed call on this thread ("" if none). */
+const char* dflash_last_error(void);
+
+/* ABI version of this header (major * 100 + minor). */
+int dflash_abi_version(void);
+
+/* Create one layer on the current CUDA device.
+ * [P4] Qwen3DFlashAttention members q_proj, k_proj, v_proj, o_proj, q_norm,
+ * k_norm; [P5] DFlashQwen3Attention (no biases); [P5] DFlashQwen3Model fc and
+ * hidden_norm.
+ *   wq [n_heads*d, H], wk [n_kv*d, H], wv [n_kv*d, H], wo [H, n_heads*d],
+ *   q_norm_w [d], k_norm_w [d], fc_w [H, n_target_layers*H] (may be NULL when
+ *   n_target_layers == 0), hidden_norm_w [H] (NULL iff fc_w is NULL).
+ * All are device pointers in cfg->dtype, nn.Linear [out, in] layout.  They
+ * are copied into library-owned memory before the call returns; the caller
+ * may free them afterwards.
+ * Errors: _ARG (null out/weights, bad dtype), _SHAPE (non-positive sizes,
+ * n_heads % n_kv_heads != 0, odd head_dim; bf16 layers need head_dim 128 and
+ * hidden % 128 == 0), _CUDA, _MEMORY.  On error *out is set to NULL. */
+int dflash_attn_create(const dflash_attn_config* cfg, const void* wq,
+                       const void* wk, const void* wv, const void* wo,
+                       const void* q_norm_w, const void* k_norm_w,
+                       const void* fc_w, const void* hidden_norm_w,
+                       dflash_attn** out);
+
+/* Free the layer and its scratch.  Waits for the device to finish the
+ * layer's outstanding work.  NULL is accepted (no-op). */
+int dflash_attn_destroy(dflash_attn* attn);
+
+/* Optional: size the layer's scratch for calls up to these sizes now, so
+ * that later calls of at most that size allocate nothing.
+ * max_rows = largest (batch*q_len + total new context rows) of a forward, or
+ * rows of a ctx_project; max_keys = largest total key rows of one sequence;
+ * max_batch = largest batch. */
+int dflash_attn_reserve(dflash_attn* attn, int max_batch, int max_rows,
+                        int max_keys);
+
+/* Draft KV cache for `batch` sequences of up to `capacity_rows` rows each.
+ * [P3] step 4 (DynamicCache update/crop).  Layout of the device storage:
+ * K and V each [batch][n_kv_heads][capacity_rows][head_dim] in the layer
+ * dtype; K rows are stored after k_norm and RoPE, V rows raw.  Lengths start
+ * at 0 and are mirrored on the host.  The cache may be used with any layer
+ * whose n_kv_heads, head_dim and dtype match the one given here. */
+int dflash_cache_create(const dflash_attn* attn, int batch, int capacity_rows,
+                        dflash_cache** out);
+int dflash_cache_destroy(dflash_cache* cache);
+
+/* Copy the current row counts into host_len[batch] (host memory). */
+int dflash_cache_lengths(const dflash_cache* cache, int32_t* host_len);
+
+/* Device pointers to the K and V storage (layout above), and the geometry.
+ * For inspection and tests; writing through them is the caller's risk. */
+int dflash_cache_data(const dflash_cache* cache, void** k, void** v,
+                      int32_t* batch, int32_t* n_kv_heads,
+                      int32_t* capacity_rows, int32_t* head_dim);
+
+/* Crop each sequence b to its first host_keep[b] rows (host memory).
+ * [P3] step 4: after verification the cache is cut back to the accepted
+ * prefix.  No data moves: rows at or beyond the new length are dead and are
+ * overwritten by the next append.  keep == len is a no-op.
+ * Errors: _RANGE if any keep < 0 or keep > current length (nothing changes). */
+int dflash_cache_crop(dflash_cache* cache, const int32_t* host_keep);
+
+/* Context projection ([P3] 看懂注意力数据流; [P5] combine_hidden_states and
+ * precompute_and_store_context_kv's hidden_norm):
+ *   target_hidden = hidden_norm(fc(target_layers))
+ * target_layers [rows, n_target_layers*H] and target_hidden [rows, H] are
+ * device tensors.  rows may be 0 (nothing is enqueued).
+ * Errors: _UNSUPPORTED if the layer has no fc, _ARG, _SHAPE. */
+int dflash_ctx_project(dflash_attn* attn, const void* target_layers, int rows,
+                       void* target_hidden, dflash_stream stream);
+
+/* One inference step of the layer for `batch` sequences.
+ * [P3] steps 1-4 and 关键设计; [P4] Qwen3DFlashAttention.forward,
+ * apply_rotary_pos_emb, _sliding_window_mask; [P5] DFlashQwen3Attention.forward.
+ *   noise_hidden  device [batch, q_len, H]: the block embeddings
+ *   target_hidden device [sum_b n_ctx[b], H]: new context rows, sequence-major
+ *                 (may be NULL when every n_ctx is 0)
+ *   host_n_ctx    host   [batch]: new context rows per sequence (>= 0)
+ *   positions     device [sum_b (n_ctx[b] + q_len)]: per sequence its context
+ *                 rows' positions, then the block's q_len positions
+ *   out           device [batch, q_len, H]
+ * For sequence b with L_b cached rows, the call appends n_ctx[b] context rows
+ * and then the q_len block rows (K after k_norm + RoPE, V raw) at cache rows
+ * L_b .. L_b + n_ctx[b] + q_len - 1, sets its length to that sum, and attends
+ * every block query to all rows of the sequence (non-causal; on a layer with
+ * sliding_window W only to keys whose index is within W of the query's index
+ * L_b + n_ctx[b] + t).  The block rows stay in the cache until a crop.
+ * Requires batch == cache batch <= 512; bf16 layers also need
+ * (n_heads/n_kv_heads) * q_len <= 128.
+ * Errors: _ARG, _SHAPE, _CAPACITY (L_b + n_ctx[b] + q_len > capacity; nothing
+ * is appended for any sequence), _CUDA. */
+int dflash_attn_forward(dflash_attn* attn, dflash_cache* cache, int batch,
+                        int q_len, const void* noise_hidden,
+                        const void* target_hidden, const int32_t* host_n_ctx,
+                        const int32_t* positions, void* out,
+                        dflash_stream stream);
+
+/* Training-layout forward with no cache ([P4] module docstring: each block's
+ * queries see the context strictly before its anchor plus their own block,
+ * bidirectionally; training is one forward with no cache).
+ *   noise_hidden  device [batch, n_blocks*block_size, H]
+ *   target_hidden device [batch, seq, H]  (projected context)
+ *   anchors       device [batch, n_blocks]  int32, each in [0, seq]
+ *   out           device [batch, n_blocks*block_size, H]
+ * Context row j sits at position j, row t of block k at anchors[k] + t.
+ * Blocks may share positions; anchors need not be sorted (sorted anchors
+ * balance the work best).  Layers with sliding_window > 0 are _UNSUPPORTED.
+ * bf16 layers need (n_heads/n_kv_heads) * block_size <= 128. */
+int dflash_attn_forward_packed(dflash_attn* attn, int batch, int seq,
+                               int n_blocks, int block_size,
+                               const void* noise_hidden,
+                               const void* target_hidden,
+                               const int32_t* anchors, void* out,
+                               dflash_stream stream);
+
+/* Wait for the device, then report and clear the layer's device error word
+ * (DFLASH_DEV_*).  Returns DFLASH_ERR_DEVICE when the word was non-zero. */
+int dflash_device_error(dflash_attn* attn, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_ATTN_H */

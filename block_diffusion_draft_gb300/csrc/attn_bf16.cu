@@ -1,0 +1,480 @@
+// attn_bf16.cu -- non-causal GQA attention of the draft layer on tcgen05.
+//
+// One CTA owns one work unit: a (sequence, kv head) pair and a range of keys.
+// Its Q tile stacks every query head of the KV group times the block rows
+// (groups * q_len rows, at most 128; the MMA is always M = 128 and surplus
+// rows are ignored), so each K/V row is read once for all heads of the group
+// ("DFlash源码导读（二）" step 1: GQA with num_key_value_groups).
+//
+//   warp 0      TMA producer: Q tile once, then K and V tiles of 128 keys
+//               (two 64-column boxes each, 128-byte swizzle) into a 3-stage ring
+//   warp 1      TMEM allocator + MMA issuer:
+//                 S(j) = Q K(j)^T          -> TMEM columns [128*(j&1), +128)
+//                 O   += P(j) V(j)         -> TMEM columns [256, 384)
+//               S(j+1) is issued before waiting for P(j) so the tensor core
+//               overlaps the softmax of tile j.
+//   warps 2..5  softmax, one query row per thread: mask, running max in log2
+//               units (Q is pre-scaled by head_dim^-0.5*log2 e), exp2, bf16 P
+//               written into the K slot of the same stage (K(j) is dead once
+//               S(j) completed), lazy O rescale (only when the max grows by
+//               more than 2^8), final normalisation or split partials.
+//
+// Masks ("nemo_automodel...draft_qwen3", _sliding_window_mask and the module
+// docstring): every row carries up to two allowed key intervals.
+//   inference, full layer   [unit start, unit end)
+//   inference, band layer   the same, cut to |query index - key| < W
+//   packed training         [0, anchor) and the row's own block
+// A key range split across CTAs is merged by the last CTA of the
+// (sequence, kv head) to finish, with the usual log-sum-exp rescaling.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace df {
+namespace {
+
+constexpr int HD = 128;
+constexpr int BKEY = 128;    // keys per tile
+constexpr int NST = 3;       // K/V stages
+constexpr int kThreads = 192;
+constexpr uint32_t TILE_BYTES = 128 * HD * 2;   // 32 KB: 128 rows x 128 bf16
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column box
+constexpr size_t SMEM_BYTES = 1024 + TILE_BYTES * (1 + 2 * NST) + 512;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t O_COL = 256;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
+
+struct Unit {
+  int b, h;
+  int q_row0;       // first row of the Q tile in the Q buffer
+  int rows;         // real query rows in the tile
+  long long kv_row0;  // first K/V storage row of (b, h)
+  int s0_lo, s0_hi, s1_lo, s1_hi;  // key segments
+  int blk0;         // packed: first block of the tile
+  int direct;       // 1: this unit covers all keys of its rows
+  int n_split;      // inference: units of this (b, h)
+  int split_base;   // inference: first unit of this (b, h)
+};
+
+DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
+  Unit w;
+  const int rows_per_block = a.groups * a.q_block;
+  if (a.mode == 0) {
+    int lo = 0, hi = a.batch;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sq.unit_off[mid] <= u) lo = mid; else hi = mid;
+    }
+    w.b = lo;
+    const int nch = sq.n_chunks[w.b];
+    const int r = u - sq.unit_off[w.b];
+    w.h = r / nch;
+    const int c = r - w.h * nch;
+    w.s0_lo = sq.lo[w.b] + c * a.chunk;
+    w.s0_hi = min(sq.len[w.b], w.s0_lo + a.chunk);
+    w.s1_lo = w.s1_hi = 0;
+    w.q_row0 = (w.b * a.n_kv + w.h) * rows_per_block;
+    w.rows = rows_per_block;
+    w.blk0 = 0;
+    w.direct = nch == 1;
+    w.n_split = nch;
+    w.split_base = sq.unit_off[w.b] + w.h * nch;
+  } else {
+    const int n_tiles = (a.n_blocks + a.tile_blocks - 1) / a.tile_blocks;
+    const int per = a.batch * a.n_kv;
+    const int p_rev = u / per;
+    const int rem = u - p_rev * per;
+    w.b = rem / a.n_kv;
+    w.h = rem - w.b * a.n_kv;
+    const int p = n_tiles - 1 - p_rev;  // longest (latest anchors) first
+    w.blk0 = p * a.tile_blocks;
+    const int nbt = min(a.tile_blocks, a.n_blocks - w.blk0);
+    w.rows = nbt * rows_per_block;
+    w.q_row0 = ((w.b * a.n_kv + w.h) * a.n_blocks + w.blk0) * rows_per_block;
+    int amax = 0;
+    for (int k = 0; k < nbt; ++k) {
+      int an = a.anchors[w.b * a.n_blocks + w.blk0 + k];
+      an = min(max(an, 0), a.seq);
+      amax = max(amax, an);
+    }
+    w.s0_lo = 0;
+    w.s0_hi = amax;
+    w.s1_lo = a.seq + w.blk0 * a.q_block;
+    w.s1_hi = w.s1_lo + nbt * a.q_block;
+    w.direct = 1;
+    w.n_split = 1;
+    w.split_base = u;
+  }
+  w.kv_row0 = ((long long)w.b * a.n_kv + w.h) * a.cap;
+  return w;
+}
+
+DF_DEV int n_tiles_of(const Unit& w) {
+  const int n0 = w.s0_hi > w.s0_lo ? (w.s0_hi - w.s0_lo + BKEY - 1) / BKEY : 0;
+  const int n1 = w.s1_hi > w.s1_lo ? (w.s1_hi - w.s1_lo + BKEY - 1) / BKEY : 0;
+  return n0 + n1;
+}
+
+DF_DEV int tile_start(const Unit& w, int j) {
+  const int n0 = w.s0_hi > w.s0_lo ? (w.s0_hi - w.s0_lo + BKEY - 1) / BKEY : 0;
+  return j < n0 ? w.s0_lo + j * BKEY : w.s1_lo + (j - n0) * BKEY;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ AttnArgs a,
+                     const __grid_constant__ AttnSeqs sq) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + TILE_BYTES;                  // [NST] K / P slots
+  uint8_t* sV = sK + NST * TILE_BYTES;              // [NST] V slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * TILE_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* kv_empty = v_full + NST;
+  uint64_t* s_full = kv_empty + NST;  // [2]
+  uint64_t* p_full = s_full + 2;      // [2]
+  uint64_t* o_done = p_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Unit w = decode(a, sq, blockIdx.x);
+  const int T = n_tiles_of(w);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+    }
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_kv = a.mode == 0 ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_q = policy_evict_first();
+      mbar_arrive_expect_tx(q_full, TILE_BYTES);
+      tma_load_2d(sQ, &tmQ, q_full, 0, w.q_row0, pol_q);
+      tma_load_2d(sQ + HALF_BYTES, &tmQ, q_full, 64, w.q_row0, pol_q);
+      for (int j = 0; j < T; ++j) {
+        const int s = j % NST;
+        const uint32_t ph = (j / NST) & 1;
+        if (!mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, a.err)) break;
+        const int y = (int)(w.kv_row0 + tile_start(w, j));
+        mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
+        tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
+        tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
+        mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
+        tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
+        tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, BKEY, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
+      const uint32_t q_base = smem_u32(sQ);
+      bool alive = mbar_wait(q_full, 0, abort_flag, a.err);
+      auto issue_s = [&](int j) {
+        const int s = j % NST;
+        if (!mbar_wait(&k_full[s], (j / NST) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(sK + s * TILE_BYTES);
+        const uint32_t d_col = tmem + (uint32_t)((j & 1) * BKEY);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+          tc_mma_bf16(d_col, sdesc_sw128(q_base + off, 16, 1024),
+                      sdesc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (alive) alive = issue_s(0);
+      for (int j = 0; j < T && alive; ++j) {
+        if (j + 1 < T && !issue_s(j + 1)) break;
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, a.err)) break;
+        const int s = j % NST;
+        if (!mbar_wait(&v_full[s], (j / NST) & 1, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t p_base = smem_u32(sK + s * TILE_BYTES);
+        const uint32_t v_base = smem_u32(sV + s * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BKEY / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(p_base + (kk >> 2) * HALF_BYTES + (kk & 3) * 32,
+                                          16, 1024);
+          const uint64_t bd = sdesc_sw128(v_base + kk * 16 * 128, HALF_BYTES, 1024);
+          tc_mma_bf16(tmem + O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(o_done);
+        tc_commit(&kv_empty[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const bool real = r < w.rows;
+    // this row's allowed key intervals
+    int i1_lo = 0, i1_hi = 0, i2_lo = 0, i2_hi = 0;
+    int out_token = 0, out_col = 0;
+    {
+      const int rows_per_block = a.groups * a.q_block;
+      const int kb = r / rows_per_block;
+      const int within = r - kb * rows_per_block;
+      const int gi = within / a.q_block;
+      const int t = within - gi * a.q_block;
+      out_col = (w.h * a.groups + gi) * HD;
+      if (a.mode == 0) {
+        out_token = w.b * a.q_len + t;
+        i1_lo = w.s0_lo;
+        i1_hi = w.s0_hi;
+        if (a.window > 0) {
+          const int qi = sq.len[w.b] - a.q_len + t;
+          i1_lo = max(i1_lo, qi - a.window + 1);
+          i1_hi = min(i1_hi, qi + a.window);
+        }
+      } else {
+        const int blk = w.blk0 + kb;
+        out_token = w.b * a.q_len + blk * a.q_block + t;
+        if (real) {
+          int an = a.anchors[w.b * a.n_blocks + blk];
+          if (an < 0 || an > a.seq) {
+            record_error(a.err, 3 /* DFLASH_DEV_ANCHOR */);
+            an = min(max(an, 0), a.seq);
+          }
+          i1_lo = 0;
+          i1_hi = an;
+          i2_lo = a.seq + blk * a.q_block;
+          i2_hi = i2_lo + a.q_block;
+        }
+      }
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < T; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, a.err)))
+        break;
+      tc_fence_after();
+      float s[BKEY];
+#pragma unroll
+      for (int c = 0; c < BKEY / 32; ++c) {
+        float tt[32];
+        tmem_ld32(trow + sb * BKEY + c * 32, tt);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = tt[i];
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (real) {
+        const int t0 = tile_start(w, j);
+        if (!(t0 >= i1_lo && t0 + BKEY <= i1_hi)) {
+#pragma unroll
+          for (int c = 0; c < BKEY; ++c) {
+            const int key = t0 + c;
+            const bool ok = (key >= i1_lo && key < i1_hi) || (key >= i2_lo && key < i2_hi);
+            if (!ok) s[c] = -INFINITY;
+          }
+        }
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BKEY; ++c) tmax = fmaxf(tmax, s[c]);
+        float m_new = m_run;
+        if (m_run == -INFINITY || tmax > m_run + kRescaleThreshold) m_new = fmaxf(m_run, tmax);
+        if (m_new != m_run) {
+          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+          rescale = j > 0;
+        }
+        const float mm = (m_new == -INFINITY) ? 0.f : m_new;
+        float sum = 0.f;
+        uint8_t* prow = sK + (j % NST) * TILE_BYTES + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < BKEY / 8; ++ch) {
+          float pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pv[e] = fast_exp2(s[ch * 8 + e] - mm);
+            sum += pv[e];
+          }
+          uint4 pk;
+          pk.x = pack_bf16x2(pv[0], pv[1]);
+          pk.y = pack_bf16x2(pv[2], pv[3]);
+          pk.z = pack_bf16x2(pv[4], pv[5]);
+          pk.w = pack_bf16x2(pv[6], pv[7]);
+          const int atom = ch >> 3;
+          const int pos = (ch & 7) ^ (r & 7);
+          *reinterpret_cast<uint4*>(prow + atom * HALF_BYTES + pos * 16) = pk;
+        }
+        l_run = l_run * alpha + sum;
+        m_run = m_new;
+      }
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, a.err)))
+          break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float f = rescale ? alpha : 1.f;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          float o[32];
+          tmem_ld32(trow + O_COL + c * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st32(trow + O_COL + c * 32, o);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[sb]);
+    }
+    // ------------------------------------------------------------ finish
+    bool have_o = __all_sync(0xffffffffu, T > 0 && !*abort_flag);
+    if (have_o) {
+      have_o = __all_sync(0xffffffffu, mbar_wait(o_done, (T - 1) & 1, abort_flag, a.err));
+      tc_fence_after();
+    }
+    float o[HD];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      float tt[32];
+      tmem_ld32(trow + O_COL + c * 32, tt);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[c * 32 + i] = have_o ? tt[i] : 0.f;
+    }
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    const int ld_out = a.n_kv * a.groups * HD;
+    bool write_final = w.direct;
+    if (!w.direct) {
+      const int u = blockIdx.x;
+      if (real) {
+        float4* po = reinterpret_cast<float4*>(a.part_o + (size_t)u * 128 * HD);
+#pragma unroll
+        for (int c4 = 0; c4 < HD / 4; ++c4)
+          __stcg(po + c4 * 128 + r,
+                 make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
+        __stcg(a.part_ml + (size_t)u * 256 + r, m_run);
+        __stcg(a.part_ml + (size_t)u * 256 + 128 + r, l_run);
+      }
+      __threadfence();
+      named_bar_sync(1, 128);
+      const int pair = w.b * a.n_kv + w.h;
+      if (r == 0) {
+        const int old = atomicAdd(a.counters + pair, 1);
+        *last_flag = (old == w.n_split - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (*last_flag) {
+        __threadfence();
+        if (real) {
+          float mx = -INFINITY;
+          for (int c = 0; c < w.n_split; ++c)
+            mx = fmaxf(mx, __ldcg(a.part_ml + (size_t)(w.split_base + c) * 256 + r));
+          const float mref = (mx == -INFINITY) ? 0.f : mx;
+          float L = 0.f;
+#pragma unroll
+          for (int i = 0; i < HD; ++i) o[i] = 0.f;
+          for (int c = 0; c < w.n_split; ++c) {
+            const size_t uc = (size_t)(w.split_base + c);
+            const float mc = __ldcg(a.part_ml + uc * 256 + r);
+            const float lc = __ldcg(a.part_ml + uc * 256 + 128 + r);
+            const float f = (mc == -INFINITY) ? 0.f : fast_exp2(mc - mref);
+            L += f * lc;
+            if (f != 0.f) {
+              const float4* pc = reinterpret_cast<const float4*>(a.part_o + uc * 128 * HD);
+#pragma unroll
+              for (int c4 = 0; c4 < HD / 4; ++c4) {
+                const float4 t4 = __ldcg(pc + c4 * 128 + r);
+                o[4 * c4] += f * t4.x;
+                o[4 * c4 + 1] += f * t4.y;
+                o[4 * c4 + 2] += f * t4.z;
+                o[4 * c4 + 3] += f * t4.w;
+              }
+            }
+          }
+          l_run = L;
+        }
+        if (r == 0) a.counters[pair] = 0;
+        write_final = true;
+      }
+    }
+    if (write_final && real) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)out_token * ld_out + out_col);
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        uint4 pk;
+        pk.x = pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv);
+        pk.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+        pk.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+        pk.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+        dst[i] = pk;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
+                     long long q_rows_total, const void* cache_k,
+                     const void* cache_v, long long kv_rows_total,
+                     cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_BYTES);
+    attr_done = true;
+  }
+  if (a.n_units <= 0) return cudaSuccess;
+  if (kv_rows_total >= (1LL << 31) || q_rows_total >= (1LL << 31))
+    return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv;
+  if (make_tmap_bf16_rows(&mq, qbuf, q_rows_total, HD, 128) != 0 ||
+      make_tmap_bf16_rows(&mk, cache_k, kv_rows_total, HD, 128) != 0 ||
+      make_tmap_bf16_rows(&mv, cache_v, kv_rows_total, HD, 128) != 0)
+    return cudaErrorInvalidValue;
+  static AttnSeqs zero_seqs{};
+  attn_bf16_kernel<<<a.n_units, kThreads, SMEM_BYTES, stream>>>(
+      mq, mk, mv, a, seqs ? *seqs : zero_seqs);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace df

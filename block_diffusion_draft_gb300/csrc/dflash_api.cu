@@ -1,0 +1,641 @@
+// dflash_api.cu -- the C ABI (include/dflash_attn.h): handles, argument
+// checks, scratch management and the launch sequence of each call.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/dflash_attn.h"
+#include "internal.h"
+
+using namespace df;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? DFLASH_ERR_MEMORY : DFLASH_ERR_CUDA,
+              "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DF_CUDA(call, what)                      \
+  do {                                           \
+    cudaError_t _e = (cudaError_t)(call);        \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+size_t dtype_size(int dt) { return dt == DFLASH_BF16 ? 2 : 4; }
+
+// device buffer that only grows
+struct Buf {
+  void* p = nullptr;
+  size_t bytes = 0;
+  cudaError_t ensure(size_t need, bool zero = false) {
+    if (need <= bytes) return cudaSuccess;
+    if (p) {
+      cudaDeviceSynchronize();
+      cudaFree(p);
+      p = nullptr;
+      bytes = 0;
+    }
+    need = (need + 255) & ~size_t(255);
+    cudaError_t e = cudaMalloc(&p, need);
+    if (e != cudaSuccess) return e;
+    bytes = need;
+    if (zero) e = cudaMemset(p, 0, need);
+    return e;
+  }
+  void release() {
+    if (p) cudaFree(p);
+    p = nullptr;
+    bytes = 0;
+  }
+};
+
+}  // namespace
+
+struct dflash_attn {
+  dflash_attn_config cfg;
+  int device = 0, num_sms = 0;
+  int H = 0, d = 0, nq = 0, nkv = 0, g = 0, nL = 0, max_pos = 0, dt = 0;
+  void* w_qkv = nullptr;  // [(nq + 2 nkv) d, H]
+  void* w_o = nullptr;    // [H, nq d]
+  void* w_fc = nullptr;   // [H, nL H]
+  float* q_norm = nullptr;
+  float* k_norm = nullptr;
+  float* hidden_norm = nullptr;
+  float2* rope = nullptr;
+  int* err = nullptr;
+  CUtensorMap tm_qkv, tm_o, tm_fc;
+  // scratch
+  Buf qbuf, attn_out, gemm_partial, gemm_counters, part_o, part_ml, attn_counters,
+      zbuf, proj_noise, proj_ctx, packed_k, packed_v, packed_pos;
+};
+
+struct dflash_cache {
+  int batch = 0, cap = 0, nkv = 0, d = 0, dt = 0, device = 0;
+  void* k = nullptr;
+  void* v = nullptr;
+  std::vector<int> len;
+};
+
+namespace {
+
+int check_attn(const dflash_attn* a) {
+  if (a == nullptr) return fail(DFLASH_ERR_ARG, "null layer handle");
+  return DFLASH_OK;
+}
+
+// scratch needed by the bf16 GEMM for a given shape
+int ensure_gemm_scratch(dflash_attn* a, int rows0, int rows1, int n, int k, int q_cols) {
+  int n_counters = 0;
+  const size_t bytes = gemm_scratch_bytes(rows0, rows1, n, k, q_cols, a->num_sms, &n_counters);
+  DF_CUDA(a->gemm_partial.ensure(std::max<size_t>(bytes, 256)), "scratch allocation");
+  DF_CUDA(a->gemm_counters.ensure((size_t)std::max(n_counters, 64) * sizeof(int), true),
+          "scratch allocation");
+  return DFLASH_OK;
+}
+
+GemmScratch gemm_scratch(dflash_attn* a) {
+  GemmScratch s;
+  s.partial = static_cast<float*>(a->gemm_partial.p);
+  s.partial_bytes = a->gemm_partial.bytes;
+  s.counters = static_cast<int*>(a->gemm_counters.p);
+  s.n_counters = (int)(a->gemm_counters.bytes / sizeof(int));
+  return s;
+}
+
+QkvOut make_qkv_out(const dflash_attn* a, const int* positions, void* qbuf,
+                    void* k, void* v, int cap, int q_block) {
+  QkvOut o;
+  o.n_heads = a->nq;
+  o.n_kv = a->nkv;
+  o.groups = a->g;
+  o.q_block = q_block;
+  o.cap = cap;
+  o.max_pos = a->max_pos;
+  o.eps = a->cfg.rms_eps;
+  const double scale = 1.0 / std::sqrt((double)a->d);
+  // the bf16 path works in log2 units (exp2 softmax); the fp32 path in e
+  o.q_scale = (float)(a->dt == DFLASH_BF16 ? scale * 1.4426950408889634 : scale);
+  o.positions = positions;
+  o.rope = a->rope;
+  o.q_norm = a->q_norm;
+  o.k_norm = a->k_norm;
+  o.qbuf = qbuf;
+  o.cache_k = k;
+  o.cache_v = v;
+  return o;
+}
+
+// Projections + norm + RoPE + append for `rows_noise` block rows and
+// `rows_ctx` context rows whose bookkeeping is in `st`.
+int run_qkv(dflash_attn* a, const void* noise, int rows_noise, const void* ctx,
+            int rows_ctx, const QkvOut& o, const SeqTable& st, cudaStream_t s) {
+  const int nqkv = (a->nq + 2 * a->nkv) * a->d;
+  if (a->dt == DFLASH_BF16) {
+    int r = ensure_gemm_scratch(a, rows_noise, rows_ctx, nqkv, a->H, a->nq * a->d);
+    if (r) return r;
+    GemmShape gs{noise, rows_noise, ctx, rows_ctx, &a->tm_qkv, nqkv, a->H, a->nq * a->d};
+    DF_CUDA(launch_gemm_bf16(gs, EPI_QKV, nullptr, 0, &o, &st, gemm_scratch(a),
+                             a->num_sms, a->err, s),
+            "QKV projection launch");
+  } else {
+    const int nkv2 = 2 * a->nkv * a->d;
+    DF_CUDA(a->proj_noise.ensure((size_t)std::max(rows_noise, 1) * nqkv * 4), "scratch");
+    DF_CUDA(a->proj_ctx.ensure((size_t)std::max(rows_ctx, 1) * nkv2 * 4), "scratch");
+    float* pn = static_cast<float*>(a->proj_noise.p);
+    float* pc = static_cast<float*>(a->proj_ctx.p);
+    const float* w = static_cast<const float*>(a->w_qkv);
+    DF_CUDA(launch_gemm_f32(static_cast<const float*>(noise), rows_noise, w, nqkv, a->H,
+                            pn, nqkv, s), "fp32 projection");
+    if (rows_ctx > 0)
+      DF_CUDA(launch_gemm_f32(static_cast<const float*>(ctx), rows_ctx,
+                              w + (size_t)a->nq * a->d * a->H, nkv2, a->H, pc, nkv2, s),
+              "fp32 projection");
+    DF_CUDA(launch_qkv_post_f32(pn, rows_noise, pc, rows_ctx, o, &st, a->d, a->err, s),
+            "fp32 norm/rope");
+  }
+  return DFLASH_OK;
+}
+
+int run_o_proj(dflash_attn* a, int rows, void* out, cudaStream_t s) {
+  if (a->dt == DFLASH_BF16) {
+    int r = ensure_gemm_scratch(a, rows, 0, a->H, a->nq * a->d, 0);
+    if (r) return r;
+    GemmShape gs{a->attn_out.p, rows, nullptr, 0, &a->tm_o, a->H, a->nq * a->d, 0};
+    DF_CUDA(launch_gemm_bf16(gs, EPI_BF16, out, a->H, nullptr, nullptr, gemm_scratch(a),
+                             a->num_sms, a->err, s),
+            "o_proj launch");
+  } else {
+    DF_CUDA(launch_gemm_f32(static_cast<const float*>(a->attn_out.p), rows,
+                            static_cast<const float*>(a->w_o), a->H, a->nq * a->d,
+                            static_cast<float*>(out), a->H, s),
+            "fp32 o_proj");
+  }
+  return DFLASH_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_last_error(void) { return g_err.c_str(); }
+
+int dflash_abi_version(void) { return 100; }
+
+int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const void* wk,
+                       const void* wv, const void* wo, const void* q_norm_w,
+                       const void* k_norm_w, const void* fc_w, const void* hidden_norm_w,
+                       dflash_attn** out) {
+  if (out == nullptr) return fail(DFLASH_ERR_ARG, "out is null");
+  *out = nullptr;
+  if (cfg_in == nullptr) return fail(DFLASH_ERR_ARG, "config is null");
+  dflash_attn_config cfg = *cfg_in;
+  if (cfg.dtype != DFLASH_BF16 && cfg.dtype != DFLASH_FP32)
+    return fail(DFLASH_ERR_ARG, "dtype must be DFLASH_BF16 or DFLASH_FP32");
+  if (!wq || !wk || !wv || !wo || !q_norm_w || !k_norm_w)
+    return fail(DFLASH_ERR_ARG, "a required weight pointer is null");
+  if ((fc_w == nullptr) != (hidden_norm_w == nullptr))
+    return fail(DFLASH_ERR_ARG, "fc_w and hidden_norm_w must both be given or both null");
+  if (cfg.hidden <= 0 || cfg.n_heads <= 0 || cfg.n_kv_heads <= 0 || cfg.head_dim < 0 ||
+      cfg.n_target_layers < 0 || cfg.sliding_window < 0 || cfg.max_position < 0 ||
+      !(cfg.rms_eps >= 0.f) || !(cfg.rope_theta > 0.f))
+    return fail(DFLASH_ERR_SHAPE, "non-positive or invalid layer scalar");
+  if (cfg.head_dim == 0) cfg.head_dim = cfg.hidden / cfg.n_heads;
+  if (cfg.max_position == 0) cfg.max_position = 131072;
+  if (cfg.n_heads % cfg.n_kv_heads != 0)
+    return fail(DFLASH_ERR_SHAPE, "n_heads (%d) must be a multiple of n_kv_heads (%d)",
+                cfg.n_heads, cfg.n_kv_heads);
+  if (cfg.head_dim % 2 != 0 || cfg.head_dim <= 0)
+    return fail(DFLASH_ERR_SHAPE, "head_dim must be even and positive");
+  if ((fc_w != nullptr) != (cfg.n_target_layers > 0))
+    return fail(DFLASH_ERR_SHAPE, "fc_w must be given exactly when n_target_layers > 0");
+  if (cfg.dtype == DFLASH_BF16) {
+    if (cfg.head_dim != 128)
+      return fail(DFLASH_ERR_SHAPE, "bf16 layers need head_dim 128 (got %d)", cfg.head_dim);
+    if (cfg.hidden % 128 != 0)
+      return fail(DFLASH_ERR_SHAPE, "bf16 layers need hidden %% 128 == 0");
+  } else if (cfg.head_dim > 256) {
+    return fail(DFLASH_ERR_SHAPE, "fp32 layers need head_dim <= 256");
+  }
+  dflash_attn* a = new dflash_attn();
+  a->cfg = cfg;
+  cudaGetDevice(&a->device);
+  cudaDeviceGetAttribute(&a->num_sms, cudaDevAttrMultiProcessorCount, a->device);
+  a->H = cfg.hidden;
+  a->d = cfg.head_dim;
+  a->nq = cfg.n_heads;
+  a->nkv = cfg.n_kv_heads;
+  a->g = cfg.n_heads / cfg.n_kv_heads;
+  a->nL = cfg.n_target_layers;
+  a->max_pos = cfg.max_position;
+  a->dt = cfg.dtype;
+  const size_t es = dtype_size(a->dt);
+  const size_t H = a->H, d = a->d, nq = a->nq, nkv = a->nkv;
+  auto cleanup = [&](int code) {
+    dflash_attn_destroy(a);
+    return code;
+  };
+  cudaError_t e;
+  e = cudaMalloc(&a->w_qkv, (nq + 2 * nkv) * d * H * es);
+  if (e == cudaSuccess) e = cudaMalloc(&a->w_o, H * nq * d * es);
+  if (e == cudaSuccess && fc_w) e = cudaMalloc(&a->w_fc, H * a->nL * H * es);
+  if (e == cudaSuccess) e = cudaMalloc(&a->q_norm, d * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&a->k_norm, d * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&a->hidden_norm, H * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&a->rope, (size_t)a->max_pos * (d / 2) * sizeof(float2));
+  if (e == cudaSuccess) e = cudaMalloc(&a->err, sizeof(int));
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "weight allocation"));
+  char* wqkv = static_cast<char*>(a->w_qkv);
+  e = cudaMemcpy(wqkv, wq, nq * d * H * es, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(wqkv + nq * d * H * es, wk, nkv * d * H * es, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(wqkv + (nq + nkv) * d * H * es, wv, nkv * d * H * es,
+                   cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(a->w_o, wo, H * nq * d * es, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess && fc_w)
+    e = cudaMemcpy(a->w_fc, fc_w, H * a->nL * H * es, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess) e = cudaMemset(a->err, 0, sizeof(int));
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "weight copy"));
+  const int bf = a->dt == DFLASH_BF16;
+  if ((e = (cudaError_t)launch_to_f32(q_norm_w, bf, a->q_norm, d, 0)) != cudaSuccess ||
+      (e = (cudaError_t)launch_to_f32(k_norm_w, bf, a->k_norm, d, 0)) != cudaSuccess)
+    return cleanup(cuda_fail(e, "norm weight conversion"));
+  if (hidden_norm_w) {
+    if ((e = (cudaError_t)launch_to_f32(hidden_norm_w, bf, a->hidden_norm, H, 0)) !=
+        cudaSuccess)
+      return cleanup(cuda_fail(e, "norm weight conversion"));
+  }
+  if ((e = (cudaError_t)launch_rope_table(a->rope, a->max_pos, (int)(d / 2), cfg.rope_theta,
+                                          0)) != cudaSuccess)
+    return cleanup(cuda_fail(e, "rope table"));
+  if (bf) {
+    if (make_tmap_bf16_rows(&a->tm_qkv, a->w_qkv, (nq + 2 * nkv) * d, (int)H, 128) != 0 ||
+        make_tmap_bf16_rows(&a->tm_o, a->w_o, H, (int)(nq * d), 128) != 0 ||
+        (fc_w && make_tmap_bf16_rows(&a->tm_fc, a->w_fc, H, (int)(a->nL * H), 128) != 0))
+      return cleanup(fail(DFLASH_ERR_CUDA, "tensor map encoding failed"));
+  }
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess)
+    return cleanup(cuda_fail(e, "layer set-up"));
+  *out = a;
+  return DFLASH_OK;
+}
+
+int dflash_attn_destroy(dflash_attn* a) {
+  if (a == nullptr) return DFLASH_OK;
+  cudaDeviceSynchronize();
+  cudaFree(a->w_qkv);
+  cudaFree(a->w_o);
+  cudaFree(a->w_fc);
+  cudaFree(a->q_norm);
+  cudaFree(a->k_norm);
+  cudaFree(a->hidden_norm);
+  cudaFree(a->rope);
+  cudaFree(a->err);
+  for (Buf* b : {&a->qbuf, &a->attn_out, &a->gemm_partial, &a->gemm_counters, &a->part_o,
+                 &a->part_ml, &a->attn_counters, &a->zbuf, &a->proj_noise, &a->proj_ctx,
+                 &a->packed_k, &a->packed_v, &a->packed_pos})
+    b->release();
+  delete a;
+  return DFLASH_OK;
+}
+
+int dflash_attn_reserve(dflash_attn* a, int max_batch, int max_rows, int max_keys) {
+  if (int r = check_attn(a)) return r;
+  if (max_batch <= 0 || max_rows <= 0 || max_keys <= 0 || max_batch > kMaxBatch)
+    return fail(DFLASH_ERR_ARG, "reserve sizes must be positive (batch <= %d)", kMaxBatch);
+  const size_t es = dtype_size(a->dt);
+  const size_t qd = (size_t)a->nq * a->d;
+  DF_CUDA(a->qbuf.ensure((size_t)max_rows * qd * es), "scratch allocation");
+  DF_CUDA(a->attn_out.ensure((size_t)max_rows * qd * es), "scratch allocation");
+  if (a->dt == DFLASH_BF16) {
+    const int nqkv = (a->nq + 2 * a->nkv) * a->d;
+    if (int r = ensure_gemm_scratch(a, max_rows, max_rows, nqkv, a->H, a->nq * a->d)) return r;
+    if (int r = ensure_gemm_scratch(a, max_rows, 0, a->H, a->nq * a->d, 0)) return r;
+    if (a->nL > 0) {
+      if (int r = ensure_gemm_scratch(a, max_rows, 0, a->H, a->nL * a->H, 0)) return r;
+    }
+    const size_t units = (size_t)max_batch * a->nkv * (max_keys / 256 + 2) + 2 * a->num_sms;
+    DF_CUDA(a->part_o.ensure(units * 128 * 128 * 4), "scratch allocation");
+    DF_CUDA(a->part_ml.ensure(units * 256 * 4), "scratch allocation");
+    DF_CUDA(a->attn_counters.ensure((size_t)max_batch * a->nkv * 4, true),
+            "scratch allocation");
+  }
+  if (a->nL > 0) DF_CUDA(a->zbuf.ensure((size_t)max_rows * a->H * 4), "scratch allocation");
+  return DFLASH_OK;
+}
+
+int dflash_cache_create(const dflash_attn* a, int batch, int capacity_rows,
+                        dflash_cache** out) {
+  if (out == nullptr) return fail(DFLASH_ERR_ARG, "out is null");
+  *out = nullptr;
+  if (int r = check_attn(a)) return r;
+  if (batch <= 0 || capacity_rows <= 0)
+    return fail(DFLASH_ERR_ARG, "batch and capacity_rows must be positive");
+  if (batch > kMaxBatch) return fail(DFLASH_ERR_SHAPE, "batch above %d", kMaxBatch);
+  dflash_cache* c = new dflash_cache();
+  c->batch = batch;
+  c->cap = capacity_rows;
+  c->nkv = a->nkv;
+  c->d = a->d;
+  c->dt = a->dt;
+  c->device = a->device;
+  c->len.assign(batch, 0);
+  const size_t bytes = (size_t)batch * a->nkv * capacity_rows * a->d * dtype_size(a->dt);
+  cudaError_t e = cudaMalloc(&c->k, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&c->v, bytes);
+  if (e == cudaSuccess) e = cudaMemset(c->k, 0, bytes);
+  if (e == cudaSuccess) e = cudaMemset(c->v, 0, bytes);
+  if (e != cudaSuccess) {
+    dflash_cache_destroy(c);
+    return cuda_fail(e, "cache allocation");
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+int dflash_cache_destroy(dflash_cache* c) {
+  if (c == nullptr) return DFLASH_OK;
+  cudaDeviceSynchronize();
+  cudaFree(c->k);
+  cudaFree(c->v);
+  delete c;
+  return DFLASH_OK;
+}
+
+int dflash_cache_lengths(const dflash_cache* c, int32_t* host_len) {
+  if (c == nullptr || host_len == nullptr) return fail(DFLASH_ERR_ARG, "null argument");
+  for (int b = 0; b < c->batch; ++b) host_len[b] = c->len[b];
+  return DFLASH_OK;
+}
+
+int dflash_cache_data(const dflash_cache* c, void** k, void** v, int32_t* batch,
+                      int32_t* n_kv_heads, int32_t* capacity_rows, int32_t* head_dim) {
+  if (c == nullptr) return fail(DFLASH_ERR_ARG, "null cache");
+  if (k) *k = c->k;
+  if (v) *v = c->v;
+  if (batch) *batch = c->batch;
+  if (n_kv_heads) *n_kv_heads = c->nkv;
+  if (capacity_rows) *capacity_rows = c->cap;
+  if (head_dim) *head_dim = c->d;
+  return DFLASH_OK;
+}
+
+int dflash_cache_read(const dflash_cache* c, void* k_dst, void* v_dst,
+                      dflash_stream stream) {
+  if (c == nullptr || k_dst == nullptr || v_dst == nullptr)
+    return fail(DFLASH_ERR_ARG, "null argument");
+  const size_t bytes = (size_t)c->batch * c->nkv * c->cap * c->d * dtype_size(c->dt);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DF_CUDA(cudaMemcpyAsync(k_dst, c->k, bytes, cudaMemcpyDeviceToDevice, s), "cache copy");
+  DF_CUDA(cudaMemcpyAsync(v_dst, c->v, bytes, cudaMemcpyDeviceToDevice, s), "cache copy");
+  return DFLASH_OK;
+}
+
+int dflash_cache_crop(dflash_cache* c, const int32_t* host_keep) {
+  if (c == nullptr || host_keep == nullptr) return fail(DFLASH_ERR_ARG, "null argument");
+  for (int b = 0; b < c->batch; ++b)
+    if (host_keep[b] < 0 || host_keep[b] > c->len[b])
+      return fail(DFLASH_ERR_RANGE, "crop(%d) of sequence %d outside [0, %d]", host_keep[b],
+                  b, c->len[b]);
+  for (int b = 0; b < c->batch; ++b) c->len[b] = host_keep[b];
+  return DFLASH_OK;
+}
+
+int dflash_ctx_project(dflash_attn* a, const void* x, int rows, void* y,
+                       dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (a->nL == 0) return fail(DFLASH_ERR_UNSUPPORTED, "layer was created without fc");
+  if (rows < 0) return fail(DFLASH_ERR_ARG, "rows must be >= 0");
+  if (rows == 0) return DFLASH_OK;
+  if (x == nullptr || y == nullptr) return fail(DFLASH_ERR_ARG, "null tensor");
+  if (a->dt == DFLASH_BF16 && (!aligned16(x) || !aligned16(y)))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int K = a->nL * a->H;
+  DF_CUDA(a->zbuf.ensure((size_t)rows * a->H * 4), "scratch allocation");
+  float* z = static_cast<float*>(a->zbuf.p);
+  if (a->dt == DFLASH_BF16) {
+    if (int r = ensure_gemm_scratch(a, rows, 0, a->H, K, 0)) return r;
+    GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, a->H, K, 0};
+    DF_CUDA(launch_gemm_bf16(gs, EPI_F32, z, a->H, nullptr, nullptr, gemm_scratch(a),
+                             a->num_sms, a->err, s),
+            "fc launch");
+  } else {
+    DF_CUDA(launch_gemm_f32(static_cast<const float*>(x), rows,
+                            static_cast<const float*>(a->w_fc), a->H, K, z, a->H, s),
+            "fp32 fc");
+  }
+  DF_CUDA(launch_row_rmsnorm(z, rows, a->H, a->hidden_norm, a->cfg.rms_eps, y,
+                             a->dt == DFLASH_BF16, s),
+          "hidden_norm launch");
+  return DFLASH_OK;
+}
+
+int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
+                        const void* noise, const void* target_hidden,
+                        const int32_t* host_n_ctx, const int32_t* positions, void* out,
+                        dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (c == nullptr) return fail(DFLASH_ERR_ARG, "null cache");
+  if (noise == nullptr || host_n_ctx == nullptr || positions == nullptr || out == nullptr)
+    return fail(DFLASH_ERR_ARG, "null tensor");
+  if (batch <= 0 || q_len <= 0) return fail(DFLASH_ERR_ARG, "batch and q_len must be positive");
+  if (batch != c->batch)
+    return fail(DFLASH_ERR_SHAPE, "batch %d differs from the cache batch %d", batch, c->batch);
+  if (c->nkv != a->nkv || c->d != a->d || c->dt != a->dt)
+    return fail(DFLASH_ERR_SHAPE, "cache geometry does not match the layer");
+  if (a->dt == DFLASH_BF16 && a->g * q_len > 128)
+    return fail(DFLASH_ERR_UNSUPPORTED, "groups * q_len = %d above 128", a->g * q_len);
+  long long total_ctx = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (host_n_ctx[b] < 0) return fail(DFLASH_ERR_ARG, "n_ctx[%d] < 0", b);
+    total_ctx += host_n_ctx[b];
+    if ((long long)c->len[b] + host_n_ctx[b] + q_len > c->cap)
+      return fail(DFLASH_ERR_CAPACITY, "sequence %d: %d cached + %d + %d rows exceed capacity %d",
+                  b, c->len[b], host_n_ctx[b], q_len, c->cap);
+  }
+  if (total_ctx > 0 && target_hidden == nullptr)
+    return fail(DFLASH_ERR_ARG, "target_hidden is null but n_ctx is not all zero");
+  const long long rows_noise = (long long)batch * q_len;
+  if (rows_noise + total_ctx > (1LL << 30)) return fail(DFLASH_ERR_SHAPE, "too many rows");
+  if (a->dt == DFLASH_BF16 &&
+      (!aligned16(noise) || !aligned16(out) || (total_ctx > 0 && !aligned16(target_hidden))))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t es = dtype_size(a->dt);
+  const size_t qd = (size_t)a->nq * a->d;
+
+  SeqTable st;
+  st.n = batch;
+  st.q_len = q_len;
+  st.ctx_off[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    st.ctx_off[b + 1] = st.ctx_off[b] + host_n_ctx[b];
+    st.cache_len[b] = c->len[b];
+  }
+  DF_CUDA(a->qbuf.ensure(rows_noise * qd * es), "scratch allocation");
+  DF_CUDA(a->attn_out.ensure(rows_noise * qd * es), "scratch allocation");
+  QkvOut o = make_qkv_out(a, positions, a->qbuf.p, c->k, c->v, c->cap, q_len);
+  if (int r = run_qkv(a, noise, (int)rows_noise, target_hidden, (int)total_ctx, o, st, s))
+    return r;
+
+  // attention work list: per sequence the visible key range, split in chunks
+  AttnSeqs sq;
+  long long total_keys = 0;
+  for (int b = 0; b < batch; ++b) {
+    sq.len[b] = c->len[b] + host_n_ctx[b] + q_len;
+    sq.lo[b] = a->cfg.sliding_window > 0
+                   ? std::max(0, sq.len[b] - q_len - a->cfg.sliding_window + 1)
+                   : 0;
+    total_keys += (long long)a->nkv * (sq.len[b] - sq.lo[b]);
+  }
+  int chunk = (int)((total_keys + 2LL * a->num_sms - 1) / (2LL * a->num_sms));
+  chunk = std::max(256, (chunk + 127) / 128 * 128);
+  sq.unit_off[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    sq.n_chunks[b] = std::max(1, (sq.len[b] - sq.lo[b] + chunk - 1) / chunk);
+    sq.unit_off[b + 1] = sq.unit_off[b] + a->nkv * sq.n_chunks[b];
+  }
+  AttnArgs aa{};
+  aa.mode = 0;
+  aa.batch = batch;
+  aa.n_kv = a->nkv;
+  aa.groups = a->g;
+  aa.head_dim = a->d;
+  aa.q_len = q_len;
+  aa.q_block = q_len;
+  aa.n_blocks = 1;
+  aa.tile_blocks = 1;
+  aa.cap = c->cap;
+  aa.window = a->cfg.sliding_window;
+  aa.n_units = sq.unit_off[batch];
+  aa.chunk = chunk;
+  aa.out = a->attn_out.p;
+  aa.err = a->err;
+  if (a->dt == DFLASH_BF16) {
+    DF_CUDA(a->part_o.ensure((size_t)aa.n_units * 128 * 128 * 4), "scratch allocation");
+    DF_CUDA(a->part_ml.ensure((size_t)aa.n_units * 256 * 4), "scratch allocation");
+    DF_CUDA(a->attn_counters.ensure((size_t)batch * a->nkv * 4, true), "scratch allocation");
+    aa.part_o = static_cast<float*>(a->part_o.p);
+    aa.part_ml = static_cast<float*>(a->part_ml.p);
+    aa.counters = static_cast<int*>(a->attn_counters.p);
+    DF_CUDA(launch_attn_bf16(aa, &sq, a->qbuf.p, rows_noise * a->nq, c->k, c->v,
+                             (long long)batch * a->nkv * c->cap, s),
+            "attention launch");
+  } else {
+    DF_CUDA(launch_attn_f32(aa, &sq, static_cast<const float*>(a->qbuf.p),
+                            static_cast<const float*>(c->k), static_cast<const float*>(c->v),
+                            s),
+            "fp32 attention launch");
+  }
+  if (int r = run_o_proj(a, (int)rows_noise, out, s)) return r;
+  for (int b = 0; b < batch; ++b) c->len[b] = sq.len[b];
+  return DFLASH_OK;
+}
+
+int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
+                               int block_size, const void* noise, const void* target_hidden,
+                               const int32_t* anchors, void* out, dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (noise == nullptr || target_hidden == nullptr || anchors == nullptr || out == nullptr)
+    return fail(DFLASH_ERR_ARG, "null tensor");
+  if (batch <= 0 || seq <= 0 || n_blocks <= 0 || block_size <= 0)
+    return fail(DFLASH_ERR_ARG, "sizes must be positive");
+  if (batch > kMaxBatch) return fail(DFLASH_ERR_SHAPE, "batch above %d", kMaxBatch);
+  if (a->cfg.sliding_window > 0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "packed layout on a sliding-window layer");
+  if (a->dt == DFLASH_BF16 && a->g * block_size > 128)
+    return fail(DFLASH_ERR_UNSUPPORTED, "groups * block_size = %d above 128",
+                a->g * block_size);
+  const long long q_len = (long long)n_blocks * block_size;
+  const long long per = seq + q_len;
+  if ((long long)batch * per > (1LL << 30)) return fail(DFLASH_ERR_SHAPE, "too many rows");
+  if (a->dt == DFLASH_BF16 && (!aligned16(noise) || !aligned16(out) || !aligned16(target_hidden)))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t es = dtype_size(a->dt);
+  const size_t qd = (size_t)a->nq * a->d;
+  const long long rows_noise = batch * q_len;
+  DF_CUDA(a->packed_pos.ensure((size_t)batch * per * 4), "scratch allocation");
+  DF_CUDA(a->packed_k.ensure((size_t)batch * a->nkv * per * a->d * es), "scratch allocation");
+  DF_CUDA(a->packed_v.ensure((size_t)batch * a->nkv * per * a->d * es), "scratch allocation");
+  DF_CUDA(a->qbuf.ensure(rows_noise * qd * es), "scratch allocation");
+  DF_CUDA(a->attn_out.ensure(rows_noise * qd * es), "scratch allocation");
+  int* pos = static_cast<int*>(a->packed_pos.p);
+  DF_CUDA(launch_packed_positions(anchors, batch, seq, n_blocks, block_size, pos, a->err, s),
+          "positions launch");
+  SeqTable st;
+  st.n = batch;
+  st.q_len = (int)q_len;
+  for (int b = 0; b <= batch; ++b) st.ctx_off[b] = b * seq;
+  for (int b = 0; b < batch; ++b) st.cache_len[b] = 0;
+  QkvOut o = make_qkv_out(a, pos, a->qbuf.p, a->packed_k.p, a->packed_v.p, (int)per, block_size);
+  if (int r = run_qkv(a, noise, (int)rows_noise, target_hidden, batch * seq, o, st, s)) return r;
+  AttnArgs aa{};
+  aa.mode = 1;
+  aa.batch = batch;
+  aa.n_kv = a->nkv;
+  aa.groups = a->g;
+  aa.head_dim = a->d;
+  aa.q_len = (int)q_len;
+  aa.q_block = block_size;
+  aa.n_blocks = n_blocks;
+  aa.tile_blocks = std::max(1, 128 / (a->g * block_size));
+  aa.cap = (int)per;
+  aa.window = 0;
+  aa.seq = seq;
+  aa.anchors = anchors;
+  aa.out = a->attn_out.p;
+  aa.err = a->err;
+  if (a->dt == DFLASH_BF16) {
+    const int n_tiles = (n_blocks + aa.tile_blocks - 1) / aa.tile_blocks;
+    aa.n_units = batch * a->nkv * n_tiles;
+    DF_CUDA(launch_attn_bf16(aa, nullptr, a->qbuf.p, rows_noise * a->nq, a->packed_k.p,
+                             a->packed_v.p, (long long)batch * a->nkv * per, s),
+            "attention launch");
+  } else {
+    DF_CUDA(launch_attn_f32(aa, nullptr, static_cast<const float*>(a->qbuf.p),
+                            static_cast<const float*>(a->packed_k.p),
+                            static_cast<const float*>(a->packed_v.p), s),
+            "fp32 attention launch");
+  }
+  return run_o_proj(a, (int)rows_noise, out, s);
+}
+
+int dflash_device_error(dflash_attn* a, int32_t* code) {
+  if (int r = check_attn(a)) return r;
+  DF_CUDA(cudaDeviceSynchronize(), "device synchronize");
+  int h = 0;
+  DF_CUDA(cudaMemcpy(&h, a->err, sizeof(int), cudaMemcpyDeviceToHost), "error word read");
+  if (code) *code = h;
+  if (h != 0) {
+    // a kernel that gave up may have left split counters raised: clear them
+    cudaMemset(a->err, 0, sizeof(int));
+    if (a->gemm_counters.p) cudaMemset(a->gemm_counters.p, 0, a->gemm_counters.bytes);
+    if (a->attn_counters.p) cudaMemset(a->attn_counters.p, 0, a->attn_counters.bytes);
+    cudaDeviceSynchronize();
+    return fail(DFLASH_ERR_DEVICE, "device-side fault code %d", h);
+  }
+  return DFLASH_OK;
+}
+
+}  // extern "C"

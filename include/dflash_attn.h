@@ -150,6 +150,12 @@ int dflash_cache_data(const dflash_cache* cache, void** k, void** v,
                       int32_t* batch, int32_t* n_kv_heads,
                       int32_t* capacity_rows, int32_t* head_dim);
 
+/* Copy the whole K and V storage (layout above) into caller device buffers
+ * k_dst and v_dst, each batch*n_kv_heads*capacity_rows*head_dim elements,
+ * on `stream`.  For inspection and tests. */
+int dflash_cache_read(const dflash_cache* cache, void* k_dst, void* v_dst,
+                      dflash_stream stream);
+
 /* Crop each sequence b to its first host_keep[b] rows (host memory).
  * [P3] step 4: after verification the cache is cut back to the accepted
  * prefix.  No data moves: rows at or beyond the new length are dead and are

@@ -1,0 +1,76 @@
+"""The C ABI library builds, loads and exports what the header declares.
+
+No compute call here: every call below fails its host-side argument check
+before touching CUDA, so this runs on machines without a GPU.
+"""
+import ctypes
+
+import pytest
+
+from block_diffusion_draft_gb300 import build
+from block_diffusion_draft_gb300 import dflash_attn as D
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return D.lib()
+
+
+def test_every_declared_function_is_exported(L):
+    names = D.declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(D._SIGNATURES), "binding and header disagree"
+
+
+def test_abi_version(L):
+    assert L.dflash_abi_version() == 100
+
+
+def test_create_rejects_null_config(L):
+    out = ctypes.c_void_p(123)
+    rc = L.dflash_attn_create(None, None, None, None, None, None, None, None, None,
+                              ctypes.byref(out))
+    assert rc == -1 and out.value is None
+    assert b"config" in L.dflash_last_error()
+
+
+def test_create_rejects_bad_shapes_before_touching_the_device(L):
+    fake = ctypes.c_void_p(0x1000)
+    out = ctypes.c_void_p()
+
+    def create(**kw):
+        base = dict(hidden=256, n_heads=4, n_kv_heads=2, head_dim=0, n_target_layers=0,
+                    rms_eps=1e-6, rope_theta=1e6, sliding_window=0, max_position=0,
+                    dtype=0)
+        base.update(kw)
+        cfg = D.Config(*[base[f] for f, _ in D.Config._fields_])
+        return L.dflash_attn_create(ctypes.byref(cfg), fake, fake, fake, fake, fake,
+                                    fake, None, None, ctypes.byref(out))
+
+    assert create(n_heads=3, n_kv_heads=2) == -2          # groups not integral
+    assert create(dtype=7) == -1                          # bad dtype
+    assert create(hidden=0) == -2                         # non-positive
+    assert create(head_dim=64) == -2                      # bf16 needs head_dim 128
+    assert create(n_target_layers=2) == -2                # fc missing
+    assert create(dtype=1, head_dim=512, hidden=2048) == -2  # fp32 head_dim limit
+
+
+def test_calls_reject_null_handles(L):
+    assert L.dflash_cache_crop(None, None) == -1
+    assert L.dflash_cache_lengths(None, None) == -1
+    assert L.dflash_ctx_project(None, None, 0, None, None) == -1
+    assert L.dflash_attn_forward(None, None, 1, 16, None, None, None, None, None, None) == -1
+    assert L.dflash_attn_forward_packed(None, 1, 1, 1, 1, None, None, None, None, None) == -1
+    assert L.dflash_attn_reserve(None, 1, 1, 1) == -1
+    assert L.dflash_attn_destroy(None) == 0
+    assert L.dflash_cache_destroy(None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(D, "_LIB", None)
+    monkeypatch.setattr(D, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        D.lib()

@@ -1,0 +1,172 @@
+"""GPU vs oracle parity on small shapes that still span several tiles,
+ragged tails, split key ranges and split-K projections.  Every call goes
+through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_draft_gb300 import workloads as W
+from oracle import dflash_oracle as O
+
+import helpers as T
+
+pytestmark = pytest.mark.gpu
+
+
+def small_bf16(**kw):
+    base = dict(hidden=1024, n_heads=8, n_kv_heads=2, head_dim=128, batch=3,
+                n_target_layers=2, max_position=8192)
+    base.update(kw)
+    return W.spec("qwen3_8b_single", **base)
+
+
+def test_tiny_fp32_workload_matches_oracle():
+    # tiny fp32 layer: 112 rows prefilled through forward + crop, then a step
+    # with 16 new context rows and a 16-row block (128 context rows in all)
+    sp = W.SPECS["tiny_fp32"]
+    sc = T.Scenario(sp, seed=0, capacity=256)
+    got, ref = sc.step([sp.prefill])
+    T.assert_close(got, ref, "fp32", "prefill step")
+    sc.crop([sp.prefill])
+    got, ref = sc.step([sp.n_new])
+    T.assert_close(got, ref, "fp32", "step")
+    assert sc.cache.lengths() == [sp.prefill + sp.n_new + sp.block_size]
+    for k, ko, v, vo in sc.compare_cache():
+        T.assert_close(k, ko, "fp32", "cache K")
+        T.assert_close(v, vo, "fp32", "cache V")
+
+
+@pytest.mark.parametrize("gains", [False, True])
+def test_bf16_ragged_batch_two_steps(gains):
+    sp = small_bf16()
+    sc = T.Scenario(sp, seed=1, capacity=1024, random_gains=gains)
+    # ragged prefill: 0, 1 and 300 context rows (several key tiles + tail)
+    got, ref = sc.step([0, 1, 300])
+    T.assert_close(got, ref, "bf16", "prefill")
+    sc.crop([0, 1, 300])
+    got, ref = sc.step([5, 0, 129])
+    T.assert_close(got, ref, "bf16", "step 2")
+    assert sc.cache.lengths() == [21, 17, 445]
+    for k, ko, v, vo in sc.compare_cache():
+        T.assert_close(k, ko, "bf16", "cache K")
+        T.assert_close(v, vo, "bf16", "cache V")
+
+
+def test_bf16_long_sequence_splits_keys_across_ctas():
+    # one sequence with 2000 keys: the key range is split over several CTAs
+    # and merged by the last one
+    sp = small_bf16(batch=1)
+    sc = T.Scenario(sp, seed=2, capacity=4096)
+    got, ref = sc.step([1983])
+    T.assert_close(got, ref, "bf16", "long")
+
+
+def test_bf16_full_q_tile_groups8():
+    # 8 query heads per kv head x 16 rows = a full 128-row Q tile
+    sp = small_bf16(n_heads=8, n_kv_heads=1, batch=2)
+    sc = T.Scenario(sp, seed=3, capacity=512)
+    got, ref = sc.step([40, 200])
+    T.assert_close(got, ref, "bf16", "g8")
+
+
+def test_bf16_sliding_window_band():
+    sp = small_bf16(sliding_window=100, batch=2)
+    sc = T.Scenario(sp, seed=4, capacity=1024)
+    got, ref = sc.step([50, 400])
+    T.assert_close(got, ref, "bf16", "band prefill")
+    sc.crop([50, 400])
+    got, ref = sc.step([16, 3])
+    T.assert_close(got, ref, "bf16", "band step")
+
+
+def test_bf16_ctx_project_matches_oracle():
+    sp = small_bf16()
+    w = W.weights(sp, 5)
+    cfg, lw = T.oracle_layer(sp, w)
+    attn = T.gpu_layer(sp, w)
+    for rows in (1, 16, 200):
+        x = W.target_layer_rows(sp, 5, 0, rows, rows)
+        y = attn.ctx_project(x.cuda())
+        torch.cuda.synchronize()
+        ref = O.ctx_project(cfg, lw, T.f64(x))
+        T.assert_close(T.f64(y), ref, "bf16", f"ctx_project rows={rows}")
+
+
+def test_fp32_ctx_project_matches_oracle():
+    sp = W.SPECS["tiny_fp32"]
+    w = W.weights(sp, 6)
+    cfg, lw = T.oracle_layer(sp, w)
+    attn = T.gpu_layer(sp, w)
+    x = W.target_layer_rows(sp, 6, 0, 0, 37)
+    y = attn.ctx_project(x.cuda())
+    torch.cuda.synchronize()
+    T.assert_close(T.f64(y), O.ctx_project(cfg, lw, T.f64(x)), "fp32", "fp32 ctx_project")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_packed_training_layout_matches_oracle(dtype):
+    if dtype == "bf16":
+        sp = small_bf16(batch=2, seq=300, n_blocks=9)
+    else:
+        sp = W.spec("tiny_fp32", batch=2, seq=100, n_blocks=5)
+    seed = 7
+    w = W.weights(sp, seed)
+    cfg, lw = T.oracle_layer(sp, w)
+    attn = T.gpu_layer(sp, w)
+    bs = sp.block_size
+    th = torch.stack([W.hidden_rows(sp, seed, "hidden", 0, b, sp.seq) for b in range(sp.batch)])
+    nz = torch.stack([W.hidden_rows(sp, seed, "noise", 0, b, sp.n_blocks * bs)
+                      for b in range(sp.batch)])
+    anchors = W.anchors(sp, seed)
+    anchors[1, -1] = sp.seq   # a block that sees the whole context
+    anchors[0, 0] = 0         # and one that sees none of it
+    out = attn.forward_packed(nz.cuda(), th.cuda(), anchors.cuda(), bs)
+    torch.cuda.synchronize()
+    ref = O.forward_packed(cfg, lw, T.f64(nz), T.f64(th), anchors.numpy(), bs)
+    T.assert_close(T.f64(out), ref, dtype, "packed")
+    assert attn.device_error() == 0
+
+
+def test_capacity_overflow_appends_nothing():
+    sp = small_bf16(batch=2)
+    sc = T.Scenario(sp, seed=8, capacity=64)
+    with pytest.raises(Exception, match="CAPACITY"):
+        sc.attn.forward(sc.cache, torch.zeros(2, 16, sp.hidden, dtype=torch.bfloat16,
+                                              device="cuda"),
+                        torch.zeros(60, sp.hidden, dtype=torch.bfloat16, device="cuda"),
+                        [10, 50], torch.zeros(60 + 32, dtype=torch.int32, device="cuda"))
+    assert sc.cache.lengths() == [0, 0]
+
+
+def test_crop_is_exact_and_reappend_reproduces_cache():
+    sp = small_bf16(batch=2)
+    sc = T.Scenario(sp, seed=9, capacity=512)
+    sc.step([100, 37])
+    k1, v1 = sc.cache.read()
+    L = sc.cache.lengths()
+    assert L == [116, 53]
+    with pytest.raises(Exception, match="RANGE"):
+        sc.cache.crop([117, 0])
+    assert sc.cache.lengths() == L
+    sc.cache.crop([100, 37])
+    assert sc.cache.lengths() == [100, 37]
+    # re-append the same block rows at the same positions: the cache is
+    # bit-identical to before the crop
+    nz = torch.stack([W.hidden_rows(sp, 9, "noise", 0, b, 16) for b in range(2)]).cuda()
+    pos = torch.cat([W.window_positions(n, 0, 16) for n in (100, 37)]).cuda()
+    sc.attn.forward(sc.cache, nz, None, [0, 0], pos)
+    k2, v2 = sc.cache.read()
+    torch.cuda.synchronize()
+    for b, n in enumerate(L):
+        assert torch.equal(k1[b, :, :n], k2[b, :, :n])
+        assert torch.equal(v1[b, :, :n], v2[b, :, :n])
+
+
+def test_bad_position_is_reported_not_faulted():
+    sp = small_bf16(batch=1)
+    sc = T.Scenario(sp, seed=10, capacity=64)
+    pos = torch.full((16,), sp.max_position + 5, dtype=torch.int32, device="cuda")
+    nz = torch.zeros(1, 16, sp.hidden, dtype=torch.bfloat16, device="cuda")
+    sc.attn.forward(sc.cache, nz, None, [0], pos)
+    assert sc.attn.device_error() == 2
+    assert sc.attn.device_error() == 0

@@ -1,0 +1,614 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash draft attention layer on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  ctx_project (fc + hidden_norm of the step's new context rows)
+  -> forward (QKV projection + q/k norm + RoPE + cache append, split-KV
+     attention, o_proj)
+  -> crop (back to the accepted prefix).
+The default workload is the Qwen3-8B-shaped single-sequence draft layer:
+4096 cached rows, 16 new context rows, a 16-row block, fc 20480 -> 4096.
+The metric is draft-attention blocks/s per layer (one block = one sequence's
+block through one layer).  Inputs are synthetic, seeded, N(0,1) hidden
+states and N(0,0.02) weights.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) each rank runs an
+independent replica of the workload on its own GPU (the layer needs no
+exchange between sequences): value = blocks of all ranks / slowest rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft-attn blocks/s per layer; achieved HBM GB/s (or tensor util) vs GB300 peak"
+UNIT = "blocks/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_single")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="bound on the timed oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="skip the nvidia-smi sampler (for profiler runs)")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# peaks and clocks
+# --------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for t, s in self.samples if t0 - 0.05 <= t <= t1 + 0.05]
+        if not rows and self.samples:  # region shorter than a sample period
+            rows = [min(self.samples, key=lambda x: abs(x[0] - (t0 + t1) / 2))[1]]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# workloads
+# --------------------------------------------------------------------------
+class ServingWorkload:
+    """Inference steps of one layer: ctx_project -> forward -> crop."""
+
+    def __init__(self, sp, seed, device, n_steps):
+        import torch
+        from block_diffusion_draft_gb300 import DFlashAttention, DraftCache
+        from block_diffusion_draft_gb300 import workloads as W
+
+        self.sp, self.dev = sp, device
+        self.W = W
+        w = W.weights(sp, seed)
+        self.attn = DFlashAttention(w, hidden=sp.hidden, n_heads=sp.n_heads,
+                                    n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
+                                    n_target_layers=sp.n_target_layers,
+                                    rms_eps=sp.rms_eps, rope_theta=sp.rope_theta,
+                                    sliding_window=sp.sliding_window,
+                                    max_position=sp.max_position, device=device)
+        del w
+        self.fixed = sp.prefill > 0  # every step identical (crop back each time)
+        sched = W.serving_schedule(sp, seed, steps=1 if self.fixed else n_steps)
+        self.sched = sched
+        B, q = sp.batch, sp.block_size
+        pre = sched.prefill
+        grow = 0 if self.fixed else sum(max(s.n_ctx) for s in sched.steps)
+        self.cap = max(pre) + grow + 2 * (q + sp.block_size) + 16
+        self.cache = DraftCache(self.attn, B, self.cap)
+        # prefill: context rows at positions 0.., one block, then crop
+        th = torch.cat([W.hidden_rows(sp, seed, "hidden", 1000, b, pre[b]) for b in range(B)])
+        nz = torch.stack([W.hidden_rows(sp, seed, "noise", 1000, b, q) for b in range(B)])
+        pos = torch.cat([W.window_positions(0, pre[b], q) for b in range(B)])
+        self.attn.forward(self.cache, nz.to(device), th.to(device), pre, pos.to(device))
+        self.cache.crop(pre)
+        del th
+        torch.cuda.synchronize(device)
+        # per-step inputs (host copies kept pinned for the end-to-end leg)
+        self.steps = []
+        L = list(pre)
+        for s, st in enumerate(sched.steps):
+            n_ctx = st.n_ctx
+            x = torch.cat([W.target_layer_rows(sp, seed, s, b, n_ctx[b]) for b in range(B)])
+            nz = torch.stack([W.hidden_rows(sp, seed, "noise", s, b, q) for b in range(B)])
+            pos = torch.cat([W.window_positions(L[b], n_ctx[b], q) for b in range(B)])
+            keep = [L[b] + n_ctx[b] for b in range(B)] if not self.fixed else list(pre)
+            self.steps.append(dict(n_ctx=n_ctx, keep=keep, len_before=list(L),
+                                   x_h=x.pin_memory(), nz_h=nz.pin_memory(),
+                                   pos_h=pos.pin_memory(),
+                                   x=x.to(device), nz=nz.to(device), pos=pos.to(device)))
+            if not self.fixed:
+                L = keep
+        rows = max(int(sum(st["n_ctx"])) for st in self.steps)
+        self.th_buf = torch.empty(rows, sp.hidden, dtype=torch.bfloat16, device=device)
+        self.out_buf = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16, device=device)
+        self.out_h = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()
+        self.blocks_per_step = B
+        self.launches_per_step = 5
+
+    def _inputs(self, i):
+        return self.steps[i % len(self.steps)]
+
+    def reset(self):
+        """Back to the post-prefill cache state (fixed workloads stay there)."""
+        if not self.fixed:
+            self.cache.crop(self.sched.prefill)
+
+    def step(self, i):
+        st = self._inputs(i)
+        n = int(sum(st["n_ctx"]))
+        th = self.th_buf[:n]
+        self.attn.ctx_project(st["x"], out=th)
+        self.attn.forward(self.cache, st["nz"], th, st["n_ctx"], st["pos"], out=self.out_buf)
+        self.cache.crop(st["keep"])
+
+    def step_e2e(self, i):
+        """The same step from pinned host buffers, result read back to host."""
+        st = self._inputs(i)
+        st["x"].copy_(st["x_h"], non_blocking=True)
+        st["nz"].copy_(st["nz_h"], non_blocking=True)
+        st["pos"].copy_(st["pos_h"], non_blocking=True)
+        self.step(i)
+        self.out_h.copy_(self.out_buf, non_blocking=True)
+
+    def io_bytes(self, i):
+        st = self._inputs(i)
+        h2d = sum(t.numel() * t.element_size() for t in (st["x_h"], st["nz_h"], st["pos_h"]))
+        return h2d, self.out_h.numel() * self.out_h.element_size()
+
+    def kernel_bytes(self, i):
+        """Algorithmic HBM bytes of each kernel of step i (each operand read
+        once, each result written once)."""
+        sp, st = self.sp, self._inputs(i)
+        H, d, nq, nkv, q, B = sp.hidden, sp.head_dim, sp.n_heads, sp.n_kv_heads, \
+            sp.block_size, sp.batch
+        n = int(sum(st["n_ctx"]))
+        K = sp.n_target_layers * H
+        keys = 0
+        for b in range(B):
+            ln = st["len_before"][b] + st["n_ctx"][b] + q
+            lo = max(0, ln - q - sp.sliding_window + 1) if sp.sliding_window else 0
+            keys += ln - lo
+        return {
+            "fc": H * K * 2 + n * K * 2 + n * H * 4,
+            "norm": n * H * 4 + n * H * 2,
+            "qkv": (nq + 2 * nkv) * d * H * 2 + (B * q + n) * H * 2
+                   + B * q * nq * d * 2 + (B * q + n) * 2 * nkv * d * 2,
+            "attn": keys * nkv * d * 2 * 2 + 2 * B * q * nq * d * 2,
+            "o_proj": H * nq * d * 2 + B * q * nq * d * 2 + B * q * H * 2,
+        }
+
+    def kernel_flops(self, i):
+        return {}
+
+    def config(self):
+        sp = self.sp
+        c = {"workload": sp.name, "batch": sp.batch, "hidden": sp.hidden,
+             "heads": f"{sp.n_heads}/{sp.n_kv_heads}", "head_dim": sp.head_dim,
+             "block_size": sp.block_size, "fc_in": sp.n_target_layers * sp.hidden,
+             "new_ctx_rows": self.steps[0]["n_ctx"][0] if self.fixed else "U{1..16}",
+             "cached_ctx": sp.prefill if self.fixed else f"U[{sp.prefill_lo},{sp.prefill_hi}]",
+             "sliding_window": sp.sliding_window,
+             "step": "ctx_project + forward + crop",
+             "l2": "flushed (512 MiB write) before every timed step"}
+        return c
+
+
+class PackedWorkload:
+    """Packed training layout forward (no cache): one call per step."""
+
+    def __init__(self, sp, seed, device, n_steps):
+        import torch
+        from block_diffusion_draft_gb300 import DFlashAttention
+        from block_diffusion_draft_gb300 import workloads as W
+
+        self.sp, self.dev = sp, device
+        w = W.weights(sp, seed, with_fc=False)
+        self.attn = DFlashAttention(w, hidden=sp.hidden, n_heads=sp.n_heads,
+                                    n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
+                                    n_target_layers=0, rms_eps=sp.rms_eps,
+                                    rope_theta=sp.rope_theta,
+                                    max_position=sp.max_position, device=device)
+        B, S, nb, bs = sp.batch, sp.seq, sp.n_blocks, sp.block_size
+        th = torch.stack([W.hidden_rows(sp, seed, "hidden", 0, b, S) for b in range(B)])
+        nz = torch.stack([W.hidden_rows(sp, seed, "noise", 0, b, nb * bs) for b in range(B)])
+        an = W.anchors(sp, seed)
+        self.th_h, self.nz_h, self.an_h = th.pin_memory(), nz.pin_memory(), an.pin_memory()
+        self.th, self.nz, self.an = th.to(device), nz.to(device), an.to(device)
+        self.out = torch.empty_like(self.nz)
+        self.out_h = torch.empty_like(self.nz_h).pin_memory()
+        self.blocks_per_step = B * nb
+        self.launches_per_step = 5
+        self.anchors_np = an.numpy()
+        self.fixed = True
+
+    def reset(self):
+        pass
+
+    def step(self, i):
+        self.attn.forward_packed(self.nz, self.th, self.an, self.sp.block_size, out=self.out)
+
+    def step_e2e(self, i):
+        for d, h in ((self.th, self.th_h), (self.nz, self.nz_h), (self.an, self.an_h)):
+            d.copy_(h, non_blocking=True)
+        self.step(i)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+    def io_bytes(self, i):
+        h2d = sum(t.numel() * t.element_size() for t in (self.th_h, self.nz_h, self.an_h))
+        return h2d, self.out_h.numel() * self.out_h.element_size()
+
+    def kernel_flops(self, i):
+        sp = self.sp
+        H, d, nq, nkv = sp.hidden, sp.head_dim, sp.n_heads, sp.n_kv_heads
+        B, S, nb, bs = sp.batch, sp.seq, sp.n_blocks, sp.block_size
+        rq, rc = B * nb * bs, B * S
+        attn = 0
+        for b in range(B):
+            for a in self.anchors_np[b]:
+                attn += 4 * nq * bs * d * (min(int(a), S) + bs)
+        return {"qkv": 2 * rq * H * (nq + 2 * nkv) * d + 2 * rc * H * 2 * nkv * d,
+                "attn": attn, "o_proj": 2 * rq * nq * d * H}
+
+    def kernel_bytes(self, i):
+        return {}
+
+    def config(self):
+        sp = self.sp
+        return {"workload": sp.name, "batch": sp.batch, "seq": sp.seq,
+                "n_blocks": sp.n_blocks, "block_size": sp.block_size,
+                "hidden": sp.hidden, "heads": f"{sp.n_heads}/{sp.n_kv_heads}",
+                "head_dim": sp.head_dim, "step": "forward_packed",
+                "l2": "flushed (512 MiB write) before every timed step"}
+
+
+def make_workload(name, seed, device, n_steps):
+    from block_diffusion_draft_gb300 import workloads as W
+    sp = W.SPECS[name]
+    if sp.seq > 0:
+        return PackedWorkload(sp, seed, device, n_steps)
+    return ServingWorkload(sp, seed, device, n_steps)
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline
+# --------------------------------------------------------------------------
+class OracleRunner:
+    """The fp64 oracle on a bounded sample of the same workload.
+
+    Serving workloads: one sequence of the batch (sequences are independent),
+    prefilled once, then one oracle step = ctx_project + forward + crop of that
+    sequence.  Packed workload: one oracle step = forward_packed of sequence 0
+    over 8 sampled blocks (the oracle recomputes the sequence's context K/V in
+    every call, as it stands)."""
+
+    def __init__(self, name, seed):
+        import torch
+        from block_diffusion_draft_gb300 import workloads as W
+        from oracle import dflash_oracle as O
+
+        self.O, self.W = O, W
+        self.sp = sp = W.SPECS[name]
+        f64 = lambda t: t.to(torch.float64).numpy()
+        w = W.weights(sp, seed, with_fc=sp.seq == 0)
+        self.cfg = O.LayerConfig(hidden=sp.hidden, n_heads=sp.n_heads,
+                                 n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
+                                 rms_eps=sp.rms_eps, rope_theta=sp.rope_theta,
+                                 sliding_window=sp.sliding_window,
+                                 n_target_layers=sp.n_target_layers if sp.seq == 0 else 0)
+        self.lw = O.LayerWeights(
+            *(f64(w[k]) for k in ("wq", "wk", "wv", "wo", "q_norm", "k_norm")),
+            fc=f64(w["fc"]) if "fc" in w else None,
+            hidden_norm=f64(w["hidden_norm"]) if "fc" in w else None)
+        del w
+        q = sp.block_size
+        if sp.seq > 0:
+            self.an = W.anchors(sp, seed).numpy()[:1]
+            self.th = f64(W.hidden_rows(sp, seed, "hidden", 0, 0, sp.seq))[None]
+            self.nz = f64(W.hidden_rows(sp, seed, "noise", 0, 0, sp.n_blocks * q))[None]
+            self.blocks = list(range(sp.n_blocks - 1, -1, -sp.n_blocks // 8))[:8]
+            self.blocks_per_step = len(self.blocks)
+            self.sample = (f"forward_packed of sequence 0 over {len(self.blocks)} blocks "
+                           "per step (context K/V recomputed per call)")
+        else:
+            sched = W.serving_schedule(sp, seed, steps=1)
+            self.pre = pre = sched.prefill[0]
+            self.cache = O.DraftCache(sp.n_kv_heads, sp.head_dim, 1)
+            th = f64(W.hidden_rows(sp, seed, "hidden", 1000, 0, pre))
+            nz = f64(W.hidden_rows(sp, seed, "noise", 1000, 0, q))
+            O.forward(self.cfg, self.lw, self.cache, nz[None], [th],
+                      [W.window_positions(0, pre, q).numpy()])
+            self.cache.crop([pre])
+            n = sched.steps[0].n_ctx[0]
+            self.x = f64(W.target_layer_rows(sp, seed, 0, 0, n))
+            self.nzs = f64(W.hidden_rows(sp, seed, "noise", 0, 0, q))[None]
+            self.pos = W.window_positions(pre, n, q).numpy()
+            self.blocks_per_step = 1
+            self.sample = ("ctx_project + forward + crop of one sequence per step "
+                           f"({pre} cached rows, {n} new, block {q})")
+
+    def step(self):
+        O, sp = self.O, self.sp
+        if sp.seq > 0:
+            O.forward_packed(self.cfg, self.lw, self.nz, self.th, self.an,
+                             sp.block_size, seqs=[0], blocks=self.blocks)
+        else:
+            t = O.ctx_project(self.cfg, self.lw, self.x)
+            O.forward(self.cfg, self.lw, self.cache, self.nzs, [t], [self.pos])
+            self.cache.crop([self.pre])
+
+    def time(self, steps, budget_s):
+        t0 = time.perf_counter()
+        n = 0
+        while n < steps:
+            self.step()
+            n += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return n, dt
+
+
+def oracle_baseline(name, seed, budget_s):
+    r = OracleRunner(name, seed)
+    r.step()  # warm-up
+    n, dt = r.time(10 ** 6, budget_s)
+    return {"value": n * r.blocks_per_step / dt, "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} oracle steps in {dt:.1f} s: {r.sample}; fp64 numpy, BLAS "
+                      "threads = all host cores"}
+
+
+# --------------------------------------------------------------------------
+# main
+# --------------------------------------------------------------------------
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        Wm = max(1, args.warmup)
+        r = OracleRunner(args.workload, args.seed)
+        for _ in range(Wm):
+            r.step()
+        n, dt = r.time(args.steps, budget_s=240.0)
+        value = n * r.blocks_per_step / dt
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+                "n_gpus": args.gpus, "steps": n, "warmup": Wm,
+                "ms_per_step": 1000.0 * dt / n, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
+                "config": {"workload": args.workload, "arm": "fp64 CPU oracle"},
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                                 "kind": "oracle", "sample": r.sample},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import __graft_entry__ as G
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        G.build()
+    if dist is not None:
+        dist.barrier()
+    G.build()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    K, Wm = args.steps, max(3, args.warmup)
+    wl = make_workload(args.workload, args.seed + (rank if world > 1 else 0), device, K + Wm)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    # warm-up (also sizes every scratch buffer)
+    for i in range(Wm):
+        wl.step(i)
+    torch.cuda.synchronize(device)
+    if wl.fixed:
+        # identical steps: capture one into a CUDA graph to take the host out
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            wl.step(0)
+            torch.cuda.synchronize(device)
+            with torch.cuda.graph(graph, stream=s):
+                wl.step(0)
+        torch.cuda.current_stream(device).wait_stream(s)
+        run = lambda i: graph.replay()
+    else:
+        run = wl.step
+    wl.reset()
+    torch.cuda.synchronize(device)
+
+    # ---------------------------------------------------------- timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(device.index) if rank == 0 and not args.no_clocks else None
+    # keep the GPU busy while the sampler starts
+    t_load = time.time()
+    while time.time() - t_load < (1.0 if clocks else 0.0):
+        for i in range(20):
+            run(i)
+        torch.cuda.synchronize(device)
+    wl.reset()
+    barrier()
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        run(i)
+        ev[i][1].record()
+    torch.cuda.synchronize(device)
+    barrier()
+    t1 = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = float(np.mean(step_ms))
+    if clocks:
+        time.sleep(0.1)
+        clocks.stop()
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.blocks_per_step / (ms / 1000.0)
+
+    # ---------------------------------------------------- per-kernel timing
+    wl.reset()
+    wl.attn.trace(True)
+    for i in range(K):
+        flush.zero_()
+        wl.step(i)
+    torch.cuda.synchronize(device)
+    tr = wl.attn.trace_read()
+    wl.attn.trace(False)
+    kb = [wl.kernel_bytes(i) for i in range(K)]
+    kf = [wl.kernel_flops(i) for i in range(K)]
+    per_kernel = {}
+    for name, (tot_ms, n) in tr.items():
+        per_kernel[name] = {"avg_us": 1000.0 * tot_ms / n, "launches": n}
+        if kb[0].get(name):
+            per_kernel[name]["gbs"] = sum(k[name] for k in kb) / (tot_ms / 1000.0) / 1e9
+        if kf[0].get(name):
+            per_kernel[name]["tflops"] = sum(k[name] for k in kf) / (tot_ms / 1000.0) / 1e12
+    dom = max(tr, key=lambda k: tr[k][0])
+    pk = peaks()
+    tot_ms, n = tr[dom]
+    if kf[0].get(dom):
+        ach = sum(k[dom] for k in kf) / (tot_ms / 1000.0) / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak,
+                "peak_source": f"{pk['source']} bf16 sustained"}
+    else:
+        ach = sum(k[dom] for k in kb) / (tot_ms / 1000.0) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak,
+                "unit": "GB/s", "frac": ach / peak, "peak_source": f"{pk['source']} hbm"}
+    roof["traffic"] = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        tj = json.load(open(tfile)).get(f"{args.workload}:{dom}")
+        if tj:
+            roof["traffic"] = tj.get("bytes_per_launch")
+
+    # ---------------------------------------------------- end to end (host)
+    wl.reset()
+    h2d, d2h = wl.io_bytes(0)
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    torch.cuda.synchronize(device)
+    for i in range(K):
+        flush.zero_()
+        e_ev[i][0].record()
+        wl.step_e2e(i)
+        e_ev[i][1].record()
+    torch.cuda.synchronize(device)
+    e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
+    if dist is not None:
+        t = torch.tensor([e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e = {"value": world * wl.blocks_per_step / (e_ms / 1000.0), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+    err = wl.attn.device_error()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
+            "config": dict(wl.config(), parallelism=f"replicas x{world}",
+                           timing="CUDA graph of one step" if wl.fixed else "eager"),
+            "roofline": roof, "kernels": per_kernel,
+            "clocks": clocks.summary(t0, t1) if clocks else None,
+            "e2e": e2e, "gpu_launches": K * wl.launches_per_step,
+            "device_error": err}
+    step_bytes = sum(kb[0].values()) if kb[0] else None
+    if step_bytes:
+        line["step_achieved_gbs"] = step_bytes / (ms / 1000.0) / 1e9
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(args.workload, args.seed, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

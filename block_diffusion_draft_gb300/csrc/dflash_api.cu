@@ -81,6 +81,11 @@ struct dflash_attn {
   float2* rope = nullptr;
   int* err = nullptr;
   CUtensorMap tm_qkv, tm_o, tm_fc;
+  // launch trace
+  bool trace = false;
+  struct Rec { int kind; cudaEvent_t e0, e1; };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> event_pool;
   // scratch
   Buf qbuf, attn_out, gemm_partial, gemm_counters, part_o, part_ml, attn_counters,
       zbuf, proj_noise, proj_ctx, packed_k, packed_v, packed_pos;
@@ -94,6 +99,38 @@ struct dflash_cache {
 };
 
 namespace {
+
+cudaEvent_t take_event(dflash_attn* a) {
+  if (!a->event_pool.empty()) {
+    cudaEvent_t e = a->event_pool.back();
+    a->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// brackets one launch with events on its stream while tracing is on
+struct TraceScope {
+  dflash_attn* a;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t e0 = nullptr;
+  TraceScope(dflash_attn* a_, int kind_, cudaStream_t s_) : a(a_), kind(kind_), s(s_) {
+    if (a->trace) {
+      e0 = take_event(a);
+      cudaEventRecord(e0, s);
+    }
+  }
+  ~TraceScope() {
+    if (a->trace && e0) {
+      cudaEvent_t e1 = take_event(a);
+      cudaEventRecord(e1, s);
+      a->recs.push_back({kind, e0, e1});
+    }
+  }
+};
 
 int check_attn(const dflash_attn* a) {
   if (a == nullptr) return fail(DFLASH_ERR_ARG, "null layer handle");
@@ -151,6 +188,7 @@ int run_qkv(dflash_attn* a, const void* noise, int rows_noise, const void* ctx,
     int r = ensure_gemm_scratch(a, rows_noise, rows_ctx, nqkv, a->H, a->nq * a->d);
     if (r) return r;
     GemmShape gs{noise, rows_noise, ctx, rows_ctx, &a->tm_qkv, nqkv, a->H, a->nq * a->d};
+    TraceScope tr(a, DFLASH_K_QKV, s);
     DF_CUDA(launch_gemm_bf16(gs, EPI_QKV, nullptr, 0, &o, &st, gemm_scratch(a),
                              a->num_sms, a->err, s),
             "QKV projection launch");
@@ -161,6 +199,7 @@ int run_qkv(dflash_attn* a, const void* noise, int rows_noise, const void* ctx,
     float* pn = static_cast<float*>(a->proj_noise.p);
     float* pc = static_cast<float*>(a->proj_ctx.p);
     const float* w = static_cast<const float*>(a->w_qkv);
+    TraceScope tr(a, DFLASH_K_QKV, s);
     DF_CUDA(launch_gemm_f32(static_cast<const float*>(noise), rows_noise, w, nqkv, a->H,
                             pn, nqkv, s), "fp32 projection");
     if (rows_ctx > 0)
@@ -177,11 +216,13 @@ int run_o_proj(dflash_attn* a, int rows, void* out, cudaStream_t s) {
   if (a->dt == DFLASH_BF16) {
     int r = ensure_gemm_scratch(a, rows, 0, a->H, a->nq * a->d, 0);
     if (r) return r;
+    TraceScope tr(a, DFLASH_K_OPROJ, s);
     GemmShape gs{a->attn_out.p, rows, nullptr, 0, &a->tm_o, a->H, a->nq * a->d, 0};
     DF_CUDA(launch_gemm_bf16(gs, EPI_BF16, out, a->H, nullptr, nullptr, gemm_scratch(a),
                              a->num_sms, a->err, s),
             "o_proj launch");
   } else {
+    TraceScope tr(a, DFLASH_K_OPROJ, s);
     DF_CUDA(launch_gemm_f32(static_cast<const float*>(a->attn_out.p), rows,
                             static_cast<const float*>(a->w_o), a->H, a->nq * a->d,
                             static_cast<float*>(out), a->H, s),
@@ -310,6 +351,11 @@ int dflash_attn_destroy(dflash_attn* a) {
   cudaFree(a->hidden_norm);
   cudaFree(a->rope);
   cudaFree(a->err);
+  for (auto& r : a->recs) {
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  for (cudaEvent_t e : a->event_pool) cudaEventDestroy(e);
   for (Buf* b : {&a->qbuf, &a->attn_out, &a->gemm_partial, &a->gemm_counters, &a->part_o,
                  &a->part_ml, &a->attn_counters, &a->zbuf, &a->proj_noise, &a->proj_ctx,
                  &a->packed_k, &a->packed_v, &a->packed_pos})
@@ -436,14 +482,17 @@ int dflash_ctx_project(dflash_attn* a, const void* x, int rows, void* y,
   if (a->dt == DFLASH_BF16) {
     if (int r = ensure_gemm_scratch(a, rows, 0, a->H, K, 0)) return r;
     GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, a->H, K, 0};
+    TraceScope tr(a, DFLASH_K_FC, s);
     DF_CUDA(launch_gemm_bf16(gs, EPI_F32, z, a->H, nullptr, nullptr, gemm_scratch(a),
                              a->num_sms, a->err, s),
             "fc launch");
   } else {
+    TraceScope tr(a, DFLASH_K_FC, s);
     DF_CUDA(launch_gemm_f32(static_cast<const float*>(x), rows,
                             static_cast<const float*>(a->w_fc), a->H, K, z, a->H, s),
             "fp32 fc");
   }
+  TraceScope tr(a, DFLASH_K_NORM, s);
   DF_CUDA(launch_row_rmsnorm(z, rows, a->H, a->hidden_norm, a->cfg.rms_eps, y,
                              a->dt == DFLASH_BF16, s),
           "hidden_norm launch");
@@ -538,10 +587,12 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
     aa.part_o = static_cast<float*>(a->part_o.p);
     aa.part_ml = static_cast<float*>(a->part_ml.p);
     aa.counters = static_cast<int*>(a->attn_counters.p);
+    TraceScope tr(a, DFLASH_K_ATTN, s);
     DF_CUDA(launch_attn_bf16(aa, &sq, a->qbuf.p, rows_noise * a->nq, c->k, c->v,
                              (long long)batch * a->nkv * c->cap, s),
             "attention launch");
   } else {
+    TraceScope tr(a, DFLASH_K_ATTN, s);
     DF_CUDA(launch_attn_f32(aa, &sq, static_cast<const float*>(a->qbuf.p),
                             static_cast<const float*>(c->k), static_cast<const float*>(c->v),
                             s),
@@ -581,8 +632,11 @@ int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
   DF_CUDA(a->qbuf.ensure(rows_noise * qd * es), "scratch allocation");
   DF_CUDA(a->attn_out.ensure(rows_noise * qd * es), "scratch allocation");
   int* pos = static_cast<int*>(a->packed_pos.p);
-  DF_CUDA(launch_packed_positions(anchors, batch, seq, n_blocks, block_size, pos, a->err, s),
-          "positions launch");
+  {
+    TraceScope tr(a, DFLASH_K_MISC, s);
+    DF_CUDA(launch_packed_positions(anchors, batch, seq, n_blocks, block_size, pos, a->err, s),
+            "positions launch");
+  }
   SeqTable st;
   st.n = batch;
   st.q_len = (int)q_len;
@@ -609,16 +663,48 @@ int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
   if (a->dt == DFLASH_BF16) {
     const int n_tiles = (n_blocks + aa.tile_blocks - 1) / aa.tile_blocks;
     aa.n_units = batch * a->nkv * n_tiles;
+    TraceScope tr(a, DFLASH_K_ATTN, s);
     DF_CUDA(launch_attn_bf16(aa, nullptr, a->qbuf.p, rows_noise * a->nq, a->packed_k.p,
                              a->packed_v.p, (long long)batch * a->nkv * per, s),
             "attention launch");
   } else {
+    TraceScope tr(a, DFLASH_K_ATTN, s);
     DF_CUDA(launch_attn_f32(aa, nullptr, static_cast<const float*>(a->qbuf.p),
                             static_cast<const float*>(a->packed_k.p),
                             static_cast<const float*>(a->packed_v.p), s),
             "fp32 attention launch");
   }
   return run_o_proj(a, (int)rows_noise, out, s);
+}
+
+int dflash_trace_enable(dflash_attn* a, int enable) {
+  if (int r = check_attn(a)) return r;
+  DF_CUDA(cudaDeviceSynchronize(), "device synchronize");
+  for (auto& r : a->recs) {
+    a->event_pool.push_back(r.e0);
+    a->event_pool.push_back(r.e1);
+  }
+  a->recs.clear();
+  a->trace = enable != 0;
+  return DFLASH_OK;
+}
+
+int dflash_trace_read(dflash_attn* a, int kind, double* total_ms, int32_t* launches) {
+  if (int r = check_attn(a)) return r;
+  if (kind < 0 || kind >= DFLASH_K_COUNT) return fail(DFLASH_ERR_ARG, "bad kernel kind");
+  double tot = 0.0;
+  int n = 0;
+  for (auto& r : a->recs) {
+    if (r.kind != kind) continue;
+    DF_CUDA(cudaEventSynchronize(r.e1), "event synchronize");
+    float ms = 0.f;
+    DF_CUDA(cudaEventElapsedTime(&ms, r.e0, r.e1), "event elapsed time");
+    tot += ms;
+    ++n;
+  }
+  if (total_ms) *total_ms = tot;
+  if (launches) *launches = n;
+  return DFLASH_OK;
 }
 
 int dflash_device_error(dflash_attn* a, int32_t* code) {

@@ -59,7 +59,12 @@ _SIGNATURES = {
     "dflash_attn_forward_packed": ([c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
+    "dflash_trace_enable": ([c_void_p, c_int], c_int),
+    "dflash_trace_read": ([c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int32)],
+                          c_int),
 }
+
+KERNEL_KINDS = {"fc": 0, "norm": 1, "qkv": 2, "attn": 3, "o_proj": 4, "misc": 5}
 
 
 def declared_functions() -> list:
@@ -183,6 +188,23 @@ class DFlashAttention:
                 self.handle, B, seq, nb, block_size, _p(noise), _p(target_hidden),
                 _p(anchors), _p(out), _stream(self.device)))
         return out
+
+    def trace(self, enable: bool) -> None:
+        """Start (fresh) or stop recording CUDA events around each launch."""
+        with torch.cuda.device(self.device):
+            check(lib().dflash_trace_enable(self.handle, 1 if enable else 0))
+
+    def trace_read(self) -> dict:
+        """{kernel kind: (total ms, launches)} of the current trace."""
+        res = {}
+        for name, kind in KERNEL_KINDS.items():
+            ms, n = ctypes.c_double(0), c_int32(0)
+            with torch.cuda.device(self.device):
+                check(lib().dflash_trace_read(self.handle, kind, ctypes.byref(ms),
+                                              ctypes.byref(n)))
+            if n.value:
+                res[name] = (ms.value, n.value)
+        return res
 
     def device_error(self) -> int:
         code = c_int32(0)

@@ -216,6 +216,27 @@ int dflash_attn_forward_packed(dflash_attn* attn, int batch, int seq,
                                const int32_t* anchors, void* out,
                                dflash_stream stream);
 
+/* Kernel kinds of the per-launch event trace. */
+enum {
+  DFLASH_K_FC = 0,     /* fc projection GEMM of dflash_ctx_project        */
+  DFLASH_K_NORM = 1,   /* hidden_norm row RMSNorm of dflash_ctx_project   */
+  DFLASH_K_QKV = 2,    /* QKV projection + norm + RoPE + cache append     */
+  DFLASH_K_ATTN = 3,   /* attention (with the split merge)                */
+  DFLASH_K_OPROJ = 4,  /* o_proj GEMM                                     */
+  DFLASH_K_MISC = 5,   /* packed-layout positions                         */
+  DFLASH_K_COUNT = 6
+};
+
+/* Launch tracing for measurement: while enabled, every kernel launch of the
+ * layer is bracketed by two CUDA events recorded on its own stream.
+ * dflash_trace_enable(attn, 1) starts a fresh trace, (attn, 0) stops it.
+ * dflash_trace_read waits for the recorded events and returns, for one
+ * kernel kind, the summed device time in milliseconds and the launch count.
+ * Not for use while a stream is being captured into a CUDA graph. */
+int dflash_trace_enable(dflash_attn* attn, int enable);
+int dflash_trace_read(dflash_attn* attn, int kind, double* total_ms,
+                      int32_t* launches);
+
 /* Wait for the device, then report and clear the layer's device error word
  * (DFLASH_DEV_*).  Returns DFLASH_ERR_DEVICE when the word was non-zero. */
 int dflash_device_error(dflash_attn* attn, int32_t* code);

@@ -3,6 +3,8 @@
 both through the same steps, and compare."""
 from __future__ import annotations
 
+import json
+import os
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
@@ -55,8 +57,18 @@ def errors(gpu: np.ndarray, ref: np.ndarray):
     return max_abs, rel
 
 
+def _log(what, dtype, max_abs, rel):
+    path = os.environ.get("DFLASH_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", ""),
+                                "what": what, "dtype": dtype, "max_abs": max_abs,
+                                "rel_l2": rel}) + "\n")
+
+
 def assert_close(gpu, ref, dtype: str, what: str = ""):
     max_abs, rel = errors(gpu, ref)
+    _log(what, dtype, max_abs, rel)
     if dtype == "bf16":
         assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2, \
             f"{what}: max_abs={max_abs:.3e} rel_l2={rel:.3e}"

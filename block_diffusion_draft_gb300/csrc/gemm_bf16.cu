@@ -10,8 +10,9 @@
 //   warps 2..5  epilogue: one accumulator row (token) per thread, read with
 //               tcgen05.ld
 // When K is split across CTAs, every CTA writes its fp32 partial tile, and
-// the last CTA to finish a tile (atomic counter) adds the others' partials
-// and runs the epilogue; it also resets the counter for the next launch.
+// the last CTA to finish a tile (atomic counter) sums all partials in split
+// order (so results are deterministic) and runs the epilogue; it also resets
+// the counter for the next launch.
 //
 // Epilogues:
 //   EPI_BF16  plain bf16 store (o_proj)
@@ -222,14 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, 128);
       last = *last_flag != 0;
       if (last) {
+        // fixed summation order (split 0, 1, ...), whichever CTA came last:
+        // the result does not depend on the finishing order
         __threadfence();
+#pragma unroll
+        for (int i = 0; i < BN; ++i) v[i] = 0.f;
         for (int s2 = 0; s2 < p.splits; ++s2) {
-          if (s2 == split) continue;
-          const float4* other = reinterpret_cast<const float4*>(
+          const float4* part = reinterpret_cast<const float4*>(
               p.partial + ((size_t)tile_id * p.splits + s2) * (BM * BN));
 #pragma unroll
           for (int c4 = 0; c4 < BN / 4; ++c4) {
-            const float4 t = __ldcg(other + c4 * BM + r);
+            const float4 t = __ldcg(part + c4 * BM + r);
             v[4 * c4] += t.x;
             v[4 * c4 + 1] += t.y;
             v[4 * c4 + 2] += t.z;

@@ -138,28 +138,42 @@ def test_capacity_overflow_appends_nothing():
     assert sc.cache.lengths() == [0, 0]
 
 
-def test_crop_is_exact_and_reappend_reproduces_cache():
+def test_crop_is_exact_and_rerun_reproduces_cache_bitwise():
     sp = small_bf16(batch=2)
     sc = T.Scenario(sp, seed=9, capacity=512)
-    sc.step([100, 37])
+    th = torch.cat([W.hidden_rows(sp, 9, "hidden", 0, b, n) for b, n in enumerate((100, 37))])
+    nz = torch.stack([W.hidden_rows(sp, 9, "noise", 0, b, 16) for b in range(2)]).cuda()
+    pos = torch.cat([W.window_positions(0, n, 16) for n in (100, 37)]).cuda()
+    out1 = sc.attn.forward(sc.cache, nz, th.cuda(), [100, 37], pos)
     k1, v1 = sc.cache.read()
     L = sc.cache.lengths()
     assert L == [116, 53]
     with pytest.raises(Exception, match="RANGE"):
         sc.cache.crop([117, 0])
     assert sc.cache.lengths() == L
-    sc.cache.crop([100, 37])
-    assert sc.cache.lengths() == [100, 37]
-    # re-append the same block rows at the same positions: the cache is
-    # bit-identical to before the crop
-    nz = torch.stack([W.hidden_rows(sp, 9, "noise", 0, b, 16) for b in range(2)]).cuda()
-    pos = torch.cat([W.window_positions(n, 0, 16) for n in (100, 37)]).cuda()
-    sc.attn.forward(sc.cache, nz, None, [0, 0], pos)
+    # crop moves no data: rows below the new length are untouched
+    sc.cache.crop([0, 0])
+    assert sc.cache.lengths() == [0, 0]
+    # the identical step again reproduces cache and output bit for bit
+    out2 = sc.attn.forward(sc.cache, nz, th.cuda(), [100, 37], pos)
     k2, v2 = sc.cache.read()
     torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
     for b, n in enumerate(L):
         assert torch.equal(k1[b, :, :n], k2[b, :, :n])
         assert torch.equal(v1[b, :, :n], v2[b, :, :n])
+    # crop to the context rows and re-append the block alone (a different
+    # launch shape): rows match within the bf16 tolerance
+    sc.cache.crop([100, 37])
+    pos2 = torch.cat([W.window_positions(n, 0, 16) for n in (100, 37)]).cuda()
+    sc.attn.forward(sc.cache, nz, None, [0, 0], pos2)
+    k3, v3 = sc.cache.read()
+    torch.cuda.synchronize()
+    assert sc.cache.lengths() == L
+    for b, n in enumerate(L):
+        assert torch.equal(k1[b, :, :n - 16], k3[b, :, :n - 16])
+        T.assert_close(T.f64(k3[b, :, :n]), T.f64(k1[b, :, :n]), "bf16", "re-append K")
+        T.assert_close(T.f64(v3[b, :, :n]), T.f64(v1[b, :, :n]), "bf16", "re-append V")
 
 
 def test_bad_position_is_reported_not_faulted():

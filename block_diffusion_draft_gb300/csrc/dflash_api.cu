@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "../../include/dflash_attn.h"
+#include "handles.h"
 #include "internal.h"
 
 using namespace df;
@@ -40,63 +41,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 size_t dtype_size(int dt) { return dt == DFLASH_BF16 ? 2 : 4; }
 
-// device buffer that only grows
-struct Buf {
-  void* p = nullptr;
-  size_t bytes = 0;
-  cudaError_t ensure(size_t need, bool zero = false) {
-    if (need <= bytes) return cudaSuccess;
-    if (p) {
-      cudaDeviceSynchronize();
-      cudaFree(p);
-      p = nullptr;
-      bytes = 0;
-    }
-    need = (need + 255) & ~size_t(255);
-    cudaError_t e = cudaMalloc(&p, need);
-    if (e != cudaSuccess) return e;
-    bytes = need;
-    if (zero) e = cudaMemset(p, 0, need);
-    return e;
-  }
-  void release() {
-    if (p) cudaFree(p);
-    p = nullptr;
-    bytes = 0;
-  }
-};
-
 }  // namespace
-
-struct dflash_attn {
-  dflash_attn_config cfg;
-  int device = 0, num_sms = 0;
-  int H = 0, d = 0, nq = 0, nkv = 0, g = 0, nL = 0, max_pos = 0, dt = 0;
-  void* w_qkv = nullptr;  // [(nq + 2 nkv) d, H]
-  void* w_o = nullptr;    // [H, nq d]
-  void* w_fc = nullptr;   // [H, nL H]
-  float* q_norm = nullptr;
-  float* k_norm = nullptr;
-  float* hidden_norm = nullptr;
-  float2* rope = nullptr;
-  int* err = nullptr;
-  CUtensorMap tm_qkv, tm_o, tm_fc;
-  // launch trace
-  bool trace = false;
-  struct Rec { int kind; cudaEvent_t e0, e1; };
-  std::vector<Rec> recs;
-  std::vector<cudaEvent_t> event_pool;
-  // scratch
-  Buf qbuf, attn_out, gemm_partial, gemm_counters, part_o, part_ml, attn_counters,
-      zbuf, proj_noise, proj_ctx, packed_k, packed_v, packed_pos;
-};
-
-struct dflash_cache {
-  int batch = 0, cap = 0, nkv = 0, d = 0, dt = 0, device = 0;
-  void* k = nullptr;
-  void* v = nullptr;
-  std::vector<int> len;
-};
 
 namespace {
 
@@ -234,6 +179,9 @@ int run_o_proj(dflash_attn* a, int rows, void* out, cudaStream_t s) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+// error reporting for the allocation-free entry point (noalloc.cu)
+int dflash_noalloc_fail(int code, const char* msg) { return fail(code, "%s", msg); }
 
 extern "C" {
 

@@ -54,6 +54,7 @@ _SIGNATURES = {
     "dflash_cache_read": ([c_void_p, c_void_p, c_void_p, c_void_p], c_int),
     "dflash_cache_crop": ([c_void_p, POINTER(c_int32)], c_int),
     "dflash_ctx_project": ([c_void_p, c_void_p, c_int, c_void_p, c_void_p], c_int),
+    "dflash_ctx_project_noalloc": ([c_void_p, c_void_p, c_int, c_void_p, c_void_p], c_int),
     "dflash_attn_forward": ([c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
                              POINTER(c_int32), c_void_p, c_void_p, c_void_p], c_int),
     "dflash_attn_forward_packed": ([c_void_p, c_int, c_int, c_int, c_int, c_void_p,

@@ -172,6 +172,33 @@ int dflash_cache_crop(dflash_cache* cache, const int32_t* host_keep);
 int dflash_ctx_project(dflash_attn* attn, const void* target_layers, int rows,
                        void* target_hidden, dflash_stream stream);
 
+/* The same context projection as dflash_ctx_project, for callers that must
+ * not have device memory allocated on their behalf.  The pages have no
+ * counterpart: this is a property of this library, not of the method.
+ * Who needs it: code that issues the call while a stream is being captured
+ * into a CUDA graph (cudaMalloc/cudaFree are not permitted then), serving
+ * processes that fix all device memory at start-up and treat any later
+ * allocation as a failure, and hosts whose memory pool must be the only
+ * allocator on the GPU.  dflash_ctx_project may grow layer-owned scratch
+ * with cudaMalloc; this entry point never allocates and never frees.
+ * Its scratch (the fp32 fc output, the split-K partial tiles and their
+ * counters) lives in one fixed 16 MiB array inside the library's device
+ * image, present on every GPU that loads the library until the process
+ * exits.  A request whose scratch would exceed 16 MiB (about rows * H * 4
+ * bytes plus the split-K tiles; e.g. up to 128 rows at H = 4096) is rejected
+ * with DFLASH_ERR_CAPACITY and enqueues nothing.
+ * The first call on a device looks up the array's device address (which may
+ * load the library's device code on that device): make that first call
+ * before any stream capture.  Every call on a device shares the one array
+ * and the array keeps the previous call's contents; the call clears the
+ * parts that must start at zero on `stream` itself.  Calls whose work can
+ * overlap on the GPU (different streams, or other threads) race on the
+ * array: serialise them.  Arguments, layouts and other errors are those of
+ * dflash_ctx_project; the layer's device must be the current device. */
+int dflash_ctx_project_noalloc(dflash_attn* attn, const void* target_layers,
+                               int rows, void* target_hidden,
+                               dflash_stream stream);
+
 /* One inference step of the layer for `batch` sequences.
  * [P3] steps 1-4 and 关键设计; [P4] Qwen3DFlashAttention.forward,
  * apply_rotary_pos_emb, _sliding_window_mask; [P5] DFlashQwen3Attention.forward.

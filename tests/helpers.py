@@ -113,10 +113,11 @@ class Scenario:
         positions = torch.cat(pos).to(dev)
         out = self.attn.forward(self.cache, noise, target, n_ctx, positions)
         torch.cuda.synchronize()
+        # only the followed sequences are widened to fp64 for the oracle
         ref = O.forward(self.cfg, self.lw, self.ocache,
                         np.stack([f64(x) for x in nz]),
-                        [f64(x) for x in th], [p.numpy() for p in pos],
-                        seqs=self.check)
+                        [f64(th[b]) if b in self.check else None for b in range(sp.batch)],
+                        [p.numpy() for p in pos], seqs=self.check)
         got = out.to("cpu", torch.float64).numpy()
         return got[self.check], ref[self.check]
 

@@ -1,0 +1,91 @@
+"""GPU vs oracle parity at the full sizes of the benchmark workloads, in the
+launch configurations the benchmark uses.  The oracle follows a seeded
+sample of sequences (each sequence depends only on its own rows) or blocks;
+cache lengths are checked bit-exact for every sequence."""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_draft_gb300 import workloads as W
+from oracle import dflash_oracle as O
+
+import helpers as T
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _serving(name, check, steps, cap_extra=64):
+    sp = W.SPECS[name]
+    sched = W.serving_schedule(sp, 0, steps=steps)
+    pre = sched.prefill
+    cap = max(pre) + sum(max(s.n_ctx) for s in sched.steps) + 2 * sp.block_size + cap_extra
+    sc = T.Scenario(sp, seed=0, capacity=cap, check=check)
+    # prefill: all cached rows through one forward, then crop to them
+    got, ref = sc.step(pre)
+    T.assert_close(got, ref, "bf16", f"{name} prefill")
+    sc.crop(pre)
+    L = list(pre)
+    for s, st in enumerate(sched.steps):
+        got, ref = sc.step(st.n_ctx)
+        T.assert_close(got, ref, "bf16", f"{name} step {s}")
+        assert sc.cache.lengths() == [L[b] + st.n_ctx[b] + sp.block_size
+                                      for b in range(sp.batch)]
+        L = [L[b] + st.n_ctx[b] for b in range(sp.batch)]
+        sc.crop(L)
+        assert sc.cache.lengths() == L
+    # cached rows of the last step (context rows; the block was cropped)
+    for k, ko, v, vo in sc.compare_cache(rows=64):
+        T.assert_close(k, ko, "bf16", f"{name} cache K")
+        T.assert_close(v, vo, "bf16", f"{name} cache V")
+    assert sc.attn.device_error() == 0
+
+
+def test_qwen3_8b_single_sequence():
+    _serving("qwen3_8b_single", check=[0], steps=2)
+
+
+def test_serving_batch_32_ragged():
+    sp = W.SPECS["serving_b32"]
+    pre = W.serving_schedule(sp, 0, steps=1).prefill
+    check = [int(np.argmax(pre)), int(np.argmin(pre)), 5]
+    _serving("serving_b32", check=check, steps=3)
+
+
+@pytest.mark.parametrize("name", ["long_ctx_full", "long_ctx_swa"])
+def test_long_context(name):
+    _serving(name, check=[2], steps=1)
+
+
+def test_packed_training_full_size():
+    sp = W.SPECS["packed_train"]
+    seed = 0
+    w = W.weights(sp, seed, with_fc=False)
+    cfg, lw = T.oracle_layer(sp, w)
+    attn = T.gpu_layer(sp, w)
+    bs, nb, S = sp.block_size, sp.n_blocks, sp.seq
+    th = torch.stack([W.hidden_rows(sp, seed, "hidden", 0, b, S) for b in range(sp.batch)])
+    nz = torch.stack([W.hidden_rows(sp, seed, "noise", 0, b, nb * bs) for b in range(sp.batch)])
+    anchors = W.anchors(sp, seed)
+    out = attn.forward_packed(nz.cuda(), th.cuda(), anchors.cuda(), bs)
+    torch.cuda.synchronize()
+    got = T.f64(out)
+    blocks = [0, 1, 77, 128, 200, nb - 2, nb - 1]
+    ref = O.forward_packed(cfg, lw, T.f64(nz), T.f64(th), anchors.numpy(), bs,
+                           seqs=[1], blocks=blocks)
+    rows = np.concatenate([np.arange(k * bs, (k + 1) * bs) for k in blocks])
+    T.assert_close(got[1, rows], ref[1, rows], "bf16", "packed full size")
+    assert np.all(np.isfinite(got))
+    assert attn.device_error() == 0
+
+
+def test_ctx_project_full_size():
+    sp = W.SPECS["qwen3_8b_single"]
+    w = W.weights(sp, 3)
+    cfg, lw = T.oracle_layer(sp, w)
+    attn = T.gpu_layer(sp, w)
+    for rows in (16, 300):
+        x = W.target_layer_rows(sp, 3, 0, 0, rows)
+        y = attn.ctx_project(x.cuda())
+        torch.cuda.synchronize()
+        T.assert_close(T.f64(y), O.ctx_project(cfg, lw, T.f64(x)), "bf16",
+                       f"ctx_project rows={rows}")

@@ -24,8 +24,9 @@
 //   inference, full layer   [unit start, unit end)
 //   inference, band layer   the same, cut to |query index - key| < W
 //   packed training         [0, anchor) and the row's own block
-// A key range split across CTAs is merged by the last CTA of the
-// (sequence, kv head) to finish, with the usual log-sum-exp rescaling.
+// A key range split across CTAs leaves per-split partials (unnormalised O,
+// running max, running sum); attn_combine_kernel merges them with the usual
+// log-sum-exp rescaling, one CTA per 8 query rows of a (sequence, kv head).
 #include <algorithm>
 
 #include "internal.h"
@@ -143,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Unit w = decode(a, sq, blockIdx.x);
@@ -175,9 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    grid_dep_wait();
     if (lane == 0) {
       const uint64_t pol_kv = a.mode == 0 ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    grid_dep_wait();
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, BKEY, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
@@ -241,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
+    grid_dep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
@@ -374,59 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     const int ld_out = a.n_kv * a.groups * HD;
-    bool write_final = w.direct;
-    if (!w.direct) {
-      const int u = blockIdx.x;
-      if (real) {
-        float4* po = reinterpret_cast<float4*>(a.part_o + (size_t)u * 128 * HD);
+    const bool write_final = w.direct;
+    if (!w.direct && real) {
+      const size_t u = blockIdx.x;
+      float4* po = reinterpret_cast<float4*>(a.part_o + u * 128 * HD);
 #pragma unroll
-        for (int c4 = 0; c4 < HD / 4; ++c4)
-          __stcg(po + c4 * 128 + r,
-                 make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
-        __stcg(a.part_ml + (size_t)u * 256 + r, m_run);
-        __stcg(a.part_ml + (size_t)u * 256 + 128 + r, l_run);
-      }
-      __threadfence();
-      named_bar_sync(1, 128);
-      const int pair = w.b * a.n_kv + w.h;
-      if (r == 0) {
-        const int old = atomicAdd(a.counters + pair, 1);
-        *last_flag = (old == w.n_split - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, 128);
-      if (*last_flag) {
-        __threadfence();
-        if (real) {
-          float mx = -INFINITY;
-          for (int c = 0; c < w.n_split; ++c)
-            mx = fmaxf(mx, __ldcg(a.part_ml + (size_t)(w.split_base + c) * 256 + r));
-          const float mref = (mx == -INFINITY) ? 0.f : mx;
-          float L = 0.f;
-#pragma unroll
-          for (int i = 0; i < HD; ++i) o[i] = 0.f;
-          for (int c = 0; c < w.n_split; ++c) {
-            const size_t uc = (size_t)(w.split_base + c);
-            const float mc = __ldcg(a.part_ml + uc * 256 + r);
-            const float lc = __ldcg(a.part_ml + uc * 256 + 128 + r);
-            const float f = (mc == -INFINITY) ? 0.f : fast_exp2(mc - mref);
-            L += f * lc;
-            if (f != 0.f) {
-              const float4* pc = reinterpret_cast<const float4*>(a.part_o + uc * 128 * HD);
-#pragma unroll
-              for (int c4 = 0; c4 < HD / 4; ++c4) {
-                const float4 t4 = __ldcg(pc + c4 * 128 + r);
-                o[4 * c4] += f * t4.x;
-                o[4 * c4 + 1] += f * t4.y;
-                o[4 * c4 + 2] += f * t4.z;
-                o[4 * c4 + 3] += f * t4.w;
-              }
-            }
-          }
-          l_run = L;
-        }
-        if (r == 0) a.counters[pair] = 0;
-        write_final = true;
-      }
+      for (int c4 = 0; c4 < HD / 4; ++c4)
+        __stcg(po + c4 * 128 + r,
+               make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
+      __stcg(a.part_ml + u * 256 + r, m_run);
+      __stcg(a.part_ml + u * 256 + 128 + r, l_run);
     }
     if (write_final && real) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -451,6 +412,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merge the split partials of one (sequence, kv head): 8 query rows per CTA,
+// one thread per (row, 4 output columns).  Pairs whose keys fit one unit were
+// finished by the attention kernel and are skipped.
+__global__ void __launch_bounds__(256)
+    attn_combine_kernel(const __grid_constant__ AttnArgs a,
+                        const __grid_constant__ AttnSeqs sq) {
+  grid_dep_launch();
+  const int rows_pair = a.groups * a.q_len;
+  const int groups_per_pair = (rows_pair + 7) / 8;
+  const int pair = blockIdx.x / groups_per_pair;
+  const int b = pair / a.n_kv, h = pair - b * a.n_kv;
+  const int nch = sq.n_chunks[b];
+  if (nch <= 1) return;
+  const int r = (blockIdx.x - pair * groups_per_pair) * 8 + (threadIdx.x >> 5);
+  const int c4 = threadIdx.x & 31;
+  if (r >= rows_pair) return;
+  const size_t base = (size_t)sq.unit_off[b] + (size_t)h * nch;
+  grid_dep_wait();
+  float mx = -INFINITY;
+  for (int c = 0; c < nch; ++c) mx = fmaxf(mx, __ldcg(a.part_ml + (base + c) * 256 + r));
+  const float mref = mx == -INFINITY ? 0.f : mx;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < nch; ++c) {
+    const size_t u = base + c;
+    const float mc = __ldcg(a.part_ml + u * 256 + r);
+    const float lc = __ldcg(a.part_ml + u * 256 + 128 + r);
+    const float4 t = __ldcg(reinterpret_cast<const float4*>(a.part_o + u * 128 * HD) +
+                            c4 * 128 + r);
+    const float f = mc == -INFINITY ? 0.f : fast_exp2(mc - mref);
+    L += f * lc;
+    acc.x += f * t.x;
+    acc.y += f * t.y;
+    acc.z += f * t.z;
+    acc.w += f * t.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int gi = r / a.q_len, t = r - gi * a.q_len;
+  const size_t token = (size_t)b * a.q_len + t;
+  const int ld_out = a.n_kv * a.groups * HD;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + token * ld_out +
+                            (size_t)(h * a.groups + gi) * HD + c4 * 4) = pk;
+}
+
 }  // namespace
 
 int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
@@ -472,9 +481,16 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
       make_tmap_bf16_rows(&mv, cache_v, kv_rows_total, HD, 128) != 0)
     return cudaErrorInvalidValue;
   static AttnSeqs zero_seqs{};
-  attn_bf16_kernel<<<a.n_units, kThreads, SMEM_BYTES, stream>>>(
-      mq, mk, mv, a, seqs ? *seqs : zero_seqs);
-  return (int)cudaGetLastError();
+  const AttnSeqs& sq = seqs ? *seqs : zero_seqs;
+  cudaError_t e = launch_pdl(attn_bf16_kernel, dim3(a.n_units), dim3(kThreads), SMEM_BYTES,
+                             stream, mq, mk, mv, a, sq);
+  if (e != cudaSuccess || a.mode != 0) return (int)e;
+  bool any_split = false;
+  for (int b = 0; b < a.batch; ++b) any_split |= sq.n_chunks[b] > 1;
+  if (!any_split) return cudaSuccess;
+  const int groups_per_pair = (a.groups * a.q_len + 7) / 8;
+  return (int)launch_pdl(attn_combine_kernel, dim3(a.batch * a.n_kv * groups_per_pair),
+                         dim3(256), 0, stream, a, sq);
 }
 
 }  // namespace df

@@ -330,8 +330,6 @@ int dflash_attn_reserve(dflash_attn* a, int max_batch, int max_rows, int max_key
     const size_t units = (size_t)max_batch * a->nkv * (max_keys / 256 + 2) + 2 * a->num_sms;
     DF_CUDA(a->part_o.ensure(units * 128 * 128 * 4), "scratch allocation");
     DF_CUDA(a->part_ml.ensure(units * 256 * 4), "scratch allocation");
-    DF_CUDA(a->attn_counters.ensure((size_t)max_batch * a->nkv * 4, true),
-            "scratch allocation");
   }
   if (a->nL > 0) DF_CUDA(a->zbuf.ensure((size_t)max_rows * a->H * 4), "scratch allocation");
   return DFLASH_OK;
@@ -505,8 +503,9 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
                    : 0;
     total_keys += (long long)a->nkv * (sq.len[b] - sq.lo[b]);
   }
-  int chunk = (int)((total_keys + 2LL * a->num_sms - 1) / (2LL * a->num_sms));
-  chunk = std::max(256, (chunk + 127) / 128 * 128);
+  // about one key chunk per SM, in whole 128-key tiles, at most 4096 keys
+  int chunk = (int)((total_keys + a->num_sms - 1) / a->num_sms);
+  chunk = std::min(4096, std::max(128, (chunk + 127) / 128 * 128));
   sq.unit_off[0] = 0;
   for (int b = 0; b < batch; ++b) {
     sq.n_chunks[b] = std::max(1, (sq.len[b] - sq.lo[b] + chunk - 1) / chunk);
@@ -531,10 +530,8 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
   if (a->dt == DFLASH_BF16) {
     DF_CUDA(a->part_o.ensure((size_t)aa.n_units * 128 * 128 * 4), "scratch allocation");
     DF_CUDA(a->part_ml.ensure((size_t)aa.n_units * 256 * 4), "scratch allocation");
-    DF_CUDA(a->attn_counters.ensure((size_t)batch * a->nkv * 4, true), "scratch allocation");
     aa.part_o = static_cast<float*>(a->part_o.p);
     aa.part_ml = static_cast<float*>(a->part_ml.p);
-    aa.counters = static_cast<int*>(a->attn_counters.p);
     TraceScope tr(a, DFLASH_K_ATTN, s);
     DF_CUDA(launch_attn_bf16(aa, &sq, a->qbuf.p, rows_noise * a->nq, c->k, c->v,
                              (long long)batch * a->nkv * c->cap, s),

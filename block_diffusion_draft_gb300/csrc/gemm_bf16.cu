@@ -3,16 +3,24 @@
 // C = A * B^T where A holds token rows (bf16, K contiguous) and B the weight
 // rows of an nn.Linear (bf16, [N, K]).  One CTA computes one 128 x 128 output
 // tile over one slice of K:
-//   warp 0      TMA producer: 128x64 A and B boxes, 128-byte swizzle,
-//               STAGES-deep mbarrier ring
+//   warp 0      TMA producer: A and B boxes of 64 K-columns, 128-byte swizzle,
+//               an mbarrier ring of as many stages as shared memory holds
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128,
 //               N=128, K=16 per instruction), fp32 accumulator in TMEM
 //   warps 2..5  epilogue: one accumulator row (token) per thread, read with
 //               tcgen05.ld
+// Decode-sized calls have few token rows: the A box then covers only the rows
+// that exist (16, 32, 64) so each stage is mostly weight bytes and more stages
+// fit; the MMA still runs M = 128 and rows past the box are don't-care rows
+// that no epilogue stores.
 // When K is split across CTAs, every CTA writes its fp32 partial tile, and
 // the last CTA to finish a tile (atomic counter) sums all partials in split
 // order (so results are deterministic) and runs the epilogue; it also resets
-// the counter for the next launch.
+// the counter for the next launch.  The split count is chosen so the units
+// fill whole waves of SMs.
+// Kernels launch with programmatic stream serialization: the producer starts
+// streaming weights (which no kernel writes) before waiting for the previous
+// kernel, so the weight fetch overlaps that kernel's tail.
 //
 // Epilogues:
 //   EPI_BF16  plain bf16 store (o_proj)
@@ -31,16 +39,21 @@
 namespace df {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6;
+constexpr int BM = 128, BN = 128, BK = 64, MAX_STAGES = 16;
 constexpr int kThreads = 192;
-constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t A_FULL = BM * BK * 2;  // 16 KB: what one MMA reads of A
 constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
-constexpr int HD = 128;  // head_dim of the bf16 path
+constexpr size_t SMEM_LIMIT = 232448;     // per-CTA opt-in maximum
+constexpr size_t SMEM_FIXED = 1024 + 512; // alignment slack + barriers
+constexpr int HD = 128;                   // head_dim of the bf16 path
+constexpr int M_GROUP = 16;               // m-tiles sharing one pass over N
 
 struct Plan {
   int a0_rows, a1_rows, n_m0, n_m1;
-  int n_tiles, n_q_tiles, n_kb, splits, units_q;
+  int n_tiles, n_q_tiles, n_kb, splits;
+  int stages;
+  uint32_t a_bytes;   // bytes TMA writes per A stage (box rows * 128)
+  int units_q;
   int ldc;
   float* partial;
   int* counters;
@@ -48,23 +61,30 @@ struct Plan {
   int* err;
 };
 
-DF_DEV void decode_unit(const Plan& p, int u, int& m_tile, int& n_tile,
-                        int& split) {
+// Units of one region (M_r m-tiles x N_r n-tiles x splits), ordered by
+// groups of M_GROUP m-tiles, then n-tile, then split, then m-tile: CTAs
+// running together share weight tiles and a bounded set of activation rows.
+DF_DEV void decode_region(int u, int M_r, int N_r, int splits, int& m, int& n,
+                          int& split) {
+  const int full = M_GROUP * N_r * splits;
+  int mb = u / full;
+  const int n_mb = (M_r + M_GROUP - 1) / M_GROUP;
+  if (mb > n_mb - 1) mb = n_mb - 1;
+  const int rem = u - mb * full;
+  const int rows = min(M_GROUP, M_r - mb * M_GROUP);
+  n = rem / (splits * rows);
+  const int r2 = rem - n * splits * rows;
+  split = r2 / rows;
+  m = mb * M_GROUP + (r2 - split * rows);
+}
+
+DF_DEV void decode_unit(const Plan& p, int u, int& m_tile, int& n_tile, int& split) {
   if (u < p.units_q) {
-    const int per = p.splits * p.n_m0;
-    n_tile = u / per;
-    const int r = u - n_tile * per;
-    split = r / p.n_m0;
-    m_tile = r - split * p.n_m0;
+    decode_region(u, p.n_m0, p.n_q_tiles, p.splits, m_tile, n_tile, split);
   } else {
-    u -= p.units_q;
-    const int mt = p.n_m0 + p.n_m1;
-    const int per = p.splits * mt;
-    const int nn = u / per;
-    const int r = u - nn * per;
-    n_tile = p.n_q_tiles + nn;
-    split = r / mt;
-    m_tile = r - split * mt;
+    decode_region(u - p.units_q, p.n_m0 + p.n_m1, p.n_tiles - p.n_q_tiles, p.splits,
+                  m_tile, n_tile, split);
+    n_tile += p.n_q_tiles;
   }
 }
 
@@ -116,11 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* accb = empty + STAGES;
+  const int S = p.stages;
+  // [B stages][A stages][room for the last A stage's full 16 KB MMA read]
+  uint8_t* sB = smem;
+  uint8_t* sA = smem + (size_t)S * B_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sA + (size_t)(S - 1) * p.a_bytes + A_FULL);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* accb = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
@@ -137,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tile_id = n_tile * (p.n_m0 + p.n_m1) + m_tile;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -155,32 +177,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
       const CUtensorMap* ma = from_a0 ? &tmA0 : &tmA1;
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
+      // weights first: they do not depend on the previous kernel
+      const int pre = min(S, nkb);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], p.a_bytes + B_BYTES);
+        tma_load_2d(sB + (size_t)i * B_BYTES, &tmB, &full[i], (kb0 + i) * BK, n0, pol_w);
+      }
+      grid_dep_wait();
       for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+        const int s = i % S;
         const int kx = (kb0 + i) * BK;
-        tma_load_2d(sA + s * A_BYTES, ma, &full[s], kx, a_row0, pol_a);
-        tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kx, n0, pol_w);
+        if (i >= pre) {
+          const uint32_t ph = (i / S) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(&full[s], p.a_bytes + B_BYTES);
+          tma_load_2d(sB + (size_t)s * B_BYTES, &tmB, &full[s], kx, n0, pol_w);
+        }
+        tma_load_2d(sA + (size_t)s * p.a_bytes, ma, &full[s], kx, a_row0, pol_a);
       }
     }
   } else if (warp == 1) {
+    grid_dep_wait();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN, false);
       for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
         if (!mbar_wait(&full[s], ph, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + s * A_BYTES);
-        const uint32_t b_base = smem_u32(sB + s * B_BYTES);
+        const uint32_t a_base = smem_u32(sA + (size_t)s * p.a_bytes);
+        const uint32_t b_base = smem_u32(sB + (size_t)s * B_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
@@ -193,10 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    grid_dep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    const bool ok = mbar_wait(accb, 0, abort_flag, p.err);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
     tc_fence_after();
     float v[BN];
 #pragma unroll
@@ -346,15 +380,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Split count minimising (waves) x (per-unit time), per-unit time in
+// k-block units plus a fixed cost per CTA and a cost for the partial tile.
 int choose_splits(int tiles, int n_kb, int num_sms) {
   if (tiles >= num_sms) return 1;
-  int s = (num_sms + tiles - 1) / tiles;
-  s = std::min(s, std::max(1, n_kb / 4));
-  return std::max(1, std::min(s, 16));
+  const double c_cta = 6.0, c_part = 3.0;
+  int best = 1;
+  double best_t = 1e30;
+  const int max_s = std::max(1, std::min(16, n_kb / 2));
+  for (int s = 1; s <= max_s; ++s) {
+    const int waves = (tiles * s + num_sms - 1) / num_sms;
+    const double t = waves * ((double)n_kb / s + c_cta + (s > 1 ? c_part : 0.0));
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
 }
 
 struct Geometry {
   int n_m0, n_m1, n_tiles, n_q_tiles, n_kb, tiles, splits;
+  int box_rows, stages;
 };
 
 Geometry geometry(int rows0, int rows1, int n, int k, int q_cols, int num_sms) {
@@ -366,7 +413,18 @@ Geometry geometry(int rows0, int rows1, int n, int k, int q_cols, int num_sms) {
   g.n_kb = k / BK;
   g.tiles = g.n_q_tiles * g.n_m0 + (g.n_tiles - g.n_q_tiles) * (g.n_m0 + g.n_m1);
   g.splits = choose_splits(g.tiles, g.n_kb, num_sms);
+  // rows one A box must cover: the most rows any m-tile holds, in 16s
+  const int most = std::min(BM, std::max(rows0, rows1));
+  g.box_rows = std::min(BM, std::max(16, (most + 15) / 16 * 16));
+  const size_t a_bytes = (size_t)g.box_rows * BK * 2;
+  const size_t room = SMEM_LIMIT - SMEM_FIXED - (A_FULL - a_bytes);
+  g.stages = (int)std::min<size_t>(MAX_STAGES, room / (B_BYTES + a_bytes));
   return g;
+}
+
+size_t smem_bytes(const Geometry& g) {
+  return SMEM_FIXED + (size_t)g.stages * (B_BYTES + (size_t)g.box_rows * BK * 2) +
+         (A_FULL - (size_t)g.box_rows * BK * 2);
 }
 
 }  // namespace
@@ -404,11 +462,11 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   static bool attr_done = false;
   if (!attr_done) {
     cudaFuncSetAttribute(gemm_bf16_kernel<EPI_BF16>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
     cudaFuncSetAttribute(gemm_bf16_kernel<EPI_F32>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
     cudaFuncSetAttribute(gemm_bf16_kernel<EPI_QKV>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
     attr_done = true;
   }
   if (s.n % BN != 0 || s.k % BK != 0 || s.q_cols % BN != 0) return cudaErrorInvalidValue;
@@ -423,6 +481,8 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   p.n_q_tiles = g.n_q_tiles;
   p.n_kb = g.n_kb;
   p.splits = g.splits;
+  p.stages = g.stages;
+  p.a_bytes = (uint32_t)g.box_rows * BK * 2;
   p.units_q = g.n_q_tiles * g.splits * g.n_m0;
   p.ldc = ldc;
   p.c = c;
@@ -436,10 +496,10 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
       return cudaErrorInvalidValue;
   }
   CUtensorMap ma0, ma1;
-  if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, BM) != 0)
+  if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, g.box_rows) != 0)
     return cudaErrorInvalidValue;
   if (s.a1_rows > 0) {
-    if (make_tmap_bf16_rows(&ma1, s.a1, s.a1_rows, s.k, BM) != 0)
+    if (make_tmap_bf16_rows(&ma1, s.a1, s.a1_rows, s.k, g.box_rows) != 0)
       return cudaErrorInvalidValue;
   } else {
     ma1 = ma0;
@@ -449,22 +509,23 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   const QkvOut& qo = qkv ? *qkv : zero_q;
   const SeqTable& st = seqs ? *seqs : zero_st;
   const int units = g.tiles * g.splits;
-  dim3 grid(units), block(kThreads);
+  const size_t smem = smem_bytes(g);
+  cudaError_t e;
   switch (epi) {
     case EPI_BF16:
-      gemm_bf16_kernel<EPI_BF16><<<grid, block, SMEM_BYTES, stream>>>(
-          ma0, ma1, *s.b_map, p, qo, st);
+      e = launch_pdl(gemm_bf16_kernel<EPI_BF16>, dim3(units), dim3(kThreads), smem, stream,
+                     ma0, ma1, *s.b_map, p, qo, st);
       break;
     case EPI_F32:
-      gemm_bf16_kernel<EPI_F32><<<grid, block, SMEM_BYTES, stream>>>(
-          ma0, ma1, *s.b_map, p, qo, st);
+      e = launch_pdl(gemm_bf16_kernel<EPI_F32>, dim3(units), dim3(kThreads), smem, stream,
+                     ma0, ma1, *s.b_map, p, qo, st);
       break;
     default:
-      gemm_bf16_kernel<EPI_QKV><<<grid, block, SMEM_BYTES, stream>>>(
-          ma0, ma1, *s.b_map, p, qo, st);
+      e = launch_pdl(gemm_bf16_kernel<EPI_QKV>, dim3(units), dim3(kThreads), smem, stream,
+                     ma0, ma1, *s.b_map, p, qo, st);
       break;
   }
-  return (int)cudaGetLastError();
+  return (int)e;
 }
 
 }  // namespace df

@@ -37,6 +37,25 @@ struct QkvOut {
   void* cache_v;
 };
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes; it must call grid_dep_wait()
+// before touching memory that kernel writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ----------------------------------------------------------- bf16 GEMM
 // C = A * B^T with A [rows, K] (token rows; two sources A0 then A1) and B
 // [N, K] (weights), both bf16 K-contiguous; fp32 accumulation on tcgen05.

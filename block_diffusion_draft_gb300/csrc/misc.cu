@@ -24,30 +24,50 @@ __global__ void rope_table_kernel(float2* tab, int max_pos, int half,
   }
 }
 
-// out[r] = w * z[r] / sqrt(mean(z[r]^2) + eps), one CTA per row
-__global__ void row_rmsnorm_kernel(const float* z, int cols, const float* w,
-                                   float eps, void* out, int out_bf16) {
-  const float* zr = z + (size_t)blockIdx.x * cols;
+// out[r] = w * z[r] / sqrt(mean(z[r]^2) + eps): one CTA per row, the row
+// held in registers (up to kNormVec float4 per thread), one reduction.
+constexpr int kNormThreads = 512;
+constexpr int kNormVec = 8;  // cols <= 512 * 4 * 8 = 16384
+
+__global__ void __launch_bounds__(kNormThreads)
+    row_rmsnorm_kernel(const float* z, int cols, const float* w, float eps, void* out,
+                       int out_bf16) {
+  grid_dep_launch();
+  grid_dep_wait();
+  const float4* zr = reinterpret_cast<const float4*>(z + (size_t)blockIdx.x * cols);
+  const int n4 = cols / 4;
+  float4 x[kNormVec];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < cols; c += blockDim.x) ss = fmaf(zr[c], zr[c], ss);
-  __shared__ float red[32];
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    x[i] = c < n4 ? __ldcg(zr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
+  }
+  __shared__ float red[kNormThreads / 32];
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (threadIdx.x == 0) red[0] = t;
-  }
-  __syncthreads();
-  const float inv = rsqrtf(red[0] / cols + eps);
-  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
-    const float y = zr[c] * inv * w[c];
-    if (out_bf16)
-      reinterpret_cast<__nv_bfloat16*>(out)[(size_t)blockIdx.x * cols + c] =
-          __float2bfloat16_rn(y);
-    else
-      reinterpret_cast<float*>(out)[(size_t)blockIdx.x * cols + c] = y;
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += red[i];
+  const float inv = rsqrtf(tot / cols + eps);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    if (c >= n4) break;
+    const float4 g = __ldg(w4 + c);
+    const float4 y = make_float4(x[i].x * inv * g.x, x[i].y * inv * g.y,
+                                 x[i].z * inv * g.z, x[i].w * inv * g.w);
+    if (out_bf16) {
+      uint2 pk;
+      pk.x = pack_bf16x2(y.x, y.y);
+      pk.y = pack_bf16x2(y.z, y.w);
+      reinterpret_cast<uint2*>(out)[(size_t)blockIdx.x * n4 + c] = pk;
+    } else {
+      reinterpret_cast<float4*>(out)[(size_t)blockIdx.x * n4 + c] = y;
+    }
   }
 }
 
@@ -108,8 +128,9 @@ int launch_rope_table(float2* tab, int max_pos, int half, float theta,
 int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
                        float eps, void* out, int out_bf16, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  row_rmsnorm_kernel<<<rows, 256, 0, st>>>(z, cols, w, eps, out, out_bf16);
-  return cudaGetLastError();
+  if (cols % 4 != 0 || cols > kNormThreads * 4 * kNormVec) return cudaErrorInvalidValue;
+  return launch_pdl(row_rmsnorm_kernel, dim3(rows), dim3(kNormThreads), 0, st, z, cols, w,
+                    eps, out, out_bf16);
 }
 
 int launch_to_f32(const void* src, int src_bf16, float* dst, size_t n,

@@ -243,6 +243,16 @@ DF_DEV void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------ programmatic launch
+// Wait until the grid this one depends on (the previous kernel in the
+// stream) has completed and its memory is visible.  A no-op when the kernel
+// was launched without the programmatic-serialization attribute.
+DF_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream begin launching (its own prologue runs
+// while this grid finishes; it still waits in grid_dep_wait for our results).
+DF_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- misc
 DF_DEV float fast_exp2(float x) {
   float y;

@@ -83,9 +83,11 @@ int check_attn(const dflash_attn* a) {
 }
 
 // scratch needed by the bf16 GEMM for a given shape
-int ensure_gemm_scratch(dflash_attn* a, int rows0, int rows1, int n, int k, int q_cols) {
+int ensure_gemm_scratch(dflash_attn* a, int epi, int rows0, int rows1, int n, int k,
+                        int q_cols) {
   int n_counters = 0;
-  const size_t bytes = gemm_scratch_bytes(rows0, rows1, n, k, q_cols, a->num_sms, &n_counters);
+  const size_t bytes =
+      gemm_scratch_bytes(epi, rows0, rows1, n, k, q_cols, a->num_sms, &n_counters);
   DF_CUDA(a->gemm_partial.ensure(std::max<size_t>(bytes, 256)), "scratch allocation");
   DF_CUDA(a->gemm_counters.ensure((size_t)std::max(n_counters, 64) * sizeof(int), true),
           "scratch allocation");
@@ -130,9 +132,10 @@ int run_qkv(dflash_attn* a, const void* noise, int rows_noise, const void* ctx,
             int rows_ctx, const QkvOut& o, const SeqTable& st, cudaStream_t s) {
   const int nqkv = (a->nq + 2 * a->nkv) * a->d;
   if (a->dt == DFLASH_BF16) {
-    int r = ensure_gemm_scratch(a, rows_noise, rows_ctx, nqkv, a->H, a->nq * a->d);
+    int r = ensure_gemm_scratch(a, EPI_QKV, rows_noise, rows_ctx, nqkv, a->H, a->nq * a->d);
     if (r) return r;
-    GemmShape gs{noise, rows_noise, ctx, rows_ctx, &a->tm_qkv, nqkv, a->H, a->nq * a->d};
+    GemmShape gs{noise, rows_noise, ctx, rows_ctx, &a->tm_qkv, &a->tm_qkv, nqkv, a->H,
+                 a->nq * a->d};
     TraceScope tr(a, DFLASH_K_QKV, s);
     DF_CUDA(launch_gemm_bf16(gs, EPI_QKV, nullptr, 0, &o, &st, gemm_scratch(a),
                              a->num_sms, a->err, s),
@@ -159,10 +162,10 @@ int run_qkv(dflash_attn* a, const void* noise, int rows_noise, const void* ctx,
 
 int run_o_proj(dflash_attn* a, int rows, void* out, cudaStream_t s) {
   if (a->dt == DFLASH_BF16) {
-    int r = ensure_gemm_scratch(a, rows, 0, a->H, a->nq * a->d, 0);
+    int r = ensure_gemm_scratch(a, EPI_BF16, rows, 0, a->H, a->nq * a->d, 0);
     if (r) return r;
     TraceScope tr(a, DFLASH_K_OPROJ, s);
-    GemmShape gs{a->attn_out.p, rows, nullptr, 0, &a->tm_o, a->H, a->nq * a->d, 0};
+    GemmShape gs{a->attn_out.p, rows, nullptr, 0, &a->tm_o, &a->tm_o32, a->H, a->nq * a->d, 0};
     DF_CUDA(launch_gemm_bf16(gs, EPI_BF16, out, a->H, nullptr, nullptr, gemm_scratch(a),
                              a->num_sms, a->err, s),
             "o_proj launch");
@@ -279,7 +282,9 @@ int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const v
   if (bf) {
     if (make_tmap_bf16_rows(&a->tm_qkv, a->w_qkv, (nq + 2 * nkv) * d, (int)H, 128) != 0 ||
         make_tmap_bf16_rows(&a->tm_o, a->w_o, H, (int)(nq * d), 128) != 0 ||
-        (fc_w && make_tmap_bf16_rows(&a->tm_fc, a->w_fc, H, (int)(a->nL * H), 128) != 0))
+        make_tmap_bf16_rows(&a->tm_o32, a->w_o, H, (int)(nq * d), 32) != 0 ||
+        (fc_w && make_tmap_bf16_rows(&a->tm_fc, a->w_fc, H, (int)(a->nL * H), 128) != 0) ||
+        (fc_w && make_tmap_bf16_rows(&a->tm_fc32, a->w_fc, H, (int)(a->nL * H), 32) != 0))
       return cleanup(fail(DFLASH_ERR_CUDA, "tensor map encoding failed"));
   }
   if ((e = cudaDeviceSynchronize()) != cudaSuccess)
@@ -322,10 +327,11 @@ int dflash_attn_reserve(dflash_attn* a, int max_batch, int max_rows, int max_key
   DF_CUDA(a->attn_out.ensure((size_t)max_rows * qd * es), "scratch allocation");
   if (a->dt == DFLASH_BF16) {
     const int nqkv = (a->nq + 2 * a->nkv) * a->d;
-    if (int r = ensure_gemm_scratch(a, max_rows, max_rows, nqkv, a->H, a->nq * a->d)) return r;
-    if (int r = ensure_gemm_scratch(a, max_rows, 0, a->H, a->nq * a->d, 0)) return r;
+    if (int r = ensure_gemm_scratch(a, EPI_QKV, max_rows, max_rows, nqkv, a->H, a->nq * a->d))
+      return r;
+    if (int r = ensure_gemm_scratch(a, EPI_BF16, max_rows, 0, a->H, a->nq * a->d, 0)) return r;
     if (a->nL > 0) {
-      if (int r = ensure_gemm_scratch(a, max_rows, 0, a->H, a->nL * a->H, 0)) return r;
+      if (int r = ensure_gemm_scratch(a, EPI_F32, max_rows, 0, a->H, a->nL * a->H, 0)) return r;
     }
     const size_t units = (size_t)max_batch * a->nkv * (max_keys / 256 + 2) + 2 * a->num_sms;
     DF_CUDA(a->part_o.ensure(units * 128 * 128 * 4), "scratch allocation");
@@ -426,8 +432,8 @@ int dflash_ctx_project(dflash_attn* a, const void* x, int rows, void* y,
   DF_CUDA(a->zbuf.ensure((size_t)rows * a->H * 4), "scratch allocation");
   float* z = static_cast<float*>(a->zbuf.p);
   if (a->dt == DFLASH_BF16) {
-    if (int r = ensure_gemm_scratch(a, rows, 0, a->H, K, 0)) return r;
-    GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, a->H, K, 0};
+    if (int r = ensure_gemm_scratch(a, EPI_F32, rows, 0, a->H, K, 0)) return r;
+    GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, &a->tm_fc32, a->H, K, 0};
     TraceScope tr(a, DFLASH_K_FC, s);
     DF_CUDA(launch_gemm_bf16(gs, EPI_F32, z, a->H, nullptr, nullptr, gemm_scratch(a),
                              a->num_sms, a->err, s),

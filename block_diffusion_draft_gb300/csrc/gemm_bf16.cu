@@ -1,23 +1,26 @@
 // gemm_bf16.cu -- tcgen05 projection GEMM for the bf16 path.
 //
 // C = A * B^T where A holds token rows (bf16, K contiguous) and B the weight
-// rows of an nn.Linear (bf16, [N, K]).  One CTA computes one 128 x 128 output
+// rows of an nn.Linear (bf16, [N, K]).  One CTA computes one 128 x BN output
 // tile over one slice of K:
 //   warp 0      TMA producer: A and B boxes of 64 K-columns, 128-byte swizzle,
 //               an mbarrier ring of as many stages as shared memory holds
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128,
-//               N=128, K=16 per instruction), fp32 accumulator in TMEM
+//               N=BN, K=16 per instruction), fp32 accumulator in TMEM
 //   warps 2..5  epilogue: one accumulator row (token) per thread, read with
 //               tcgen05.ld
-// Decode-sized calls have few token rows: the A box then covers only the rows
-// that exist (16, 32, 64) so each stage is mostly weight bytes and more stages
-// fit; the MMA still runs M = 128 and rows past the box are don't-care rows
-// that no epilogue stores.
-// When K is split across CTAs, every CTA writes its fp32 partial tile, and
-// the last CTA to finish a tile (atomic counter) sums all partials in split
-// order (so results are deterministic) and runs the epilogue; it also resets
-// the counter for the next launch.  The split count is chosen so the units
-// fill whole waves of SMs.
+// Token rows are few in decode-sized calls, so the A box covers only the rows
+// that exist (16, 32, 64 ...) and each pipeline stage is mostly weight bytes;
+// the MMA still runs M = 128 and rows past the box are don't-care rows that no
+// epilogue stores.  When block rows and context rows together fit one tile
+// they share it (two boxes into one A stage), so the K/V weights are streamed
+// once.  Plain epilogues with few rows use BN = 32: enough tiles to fill the
+// GPU without splitting K.  The QKV epilogue needs whole heads (BN = 128) and
+// splits K when the tiles are too few; then every CTA writes the valid rows of
+// its fp32 partial, and the last CTA of a tile (atomic counter) sums all
+// partials in split order (deterministic), spreading the loads over all its
+// epilogue threads and staging the sums through shared memory.  It resets the
+// counter for the next launch.
 // Kernels launch with programmatic stream serialization: the producer starts
 // streaming weights (which no kernel writes) before waiting for the previous
 // kernel, so the weight fetch overlaps that kernel's tail.
@@ -39,20 +42,21 @@
 namespace df {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, MAX_STAGES = 16;
+constexpr int BM = 128, BK = 64, MAX_STAGES = 32;
 constexpr int kThreads = 192;
-constexpr uint32_t A_FULL = BM * BK * 2;  // 16 KB: what one MMA reads of A
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr size_t SMEM_LIMIT = 232448;     // per-CTA opt-in maximum
-constexpr size_t SMEM_FIXED = 1024 + 512; // alignment slack + barriers
-constexpr int HD = 128;                   // head_dim of the bf16 path
-constexpr int M_GROUP = 16;               // m-tiles sharing one pass over N
+constexpr uint32_t A_FULL = BM * BK * 2;   // 16 KB: what one MMA reads of A
+constexpr size_t SMEM_LIMIT = 232448;      // per-CTA opt-in maximum
+constexpr size_t SMEM_FIXED = 1024 + 1024; // alignment slack + barriers
+constexpr int HD = 128;                    // head_dim of the bf16 path
+constexpr int M_GROUP = 16;                // m-tiles sharing one pass over N
 
 struct Plan {
   int a0_rows, a1_rows, n_m0, n_m1;
+  int merged;          // 1: one tile holds A0 rows then A1 rows
+  int box0, box1;      // rows of the A0 / A1 boxes
   int n_tiles, n_q_tiles, n_kb, splits;
   int stages;
-  uint32_t a_bytes;   // bytes TMA writes per A stage (box rows * 128)
+  uint32_t a_bytes;    // bytes per A stage (all boxes of one stage)
   int units_q;
   int ldc;
   float* partial;
@@ -88,10 +92,29 @@ DF_DEV void decode_unit(const Plan& p, int u, int& m_tile, int& n_tile, int& spl
   }
 }
 
-DF_DEV void store_bf16_row(void* dst, const float* v) {
+// Which source row accumulator row r of tile m_tile holds: src 0 = A0
+// (block rows), 1 = A1 (context rows), -1 = no row.
+DF_DEV void row_source(const Plan& p, int m_tile, int r, int& src, int& row) {
+  if (p.merged) {
+    if (r < p.box0) {
+      src = r < p.a0_rows ? 0 : -1;
+      row = r;
+    } else {
+      row = r - p.box0;
+      src = row < p.a1_rows ? 1 : -1;
+    }
+  } else if (m_tile < p.n_m0) {
+    row = m_tile * BM + r;
+    src = row < p.a0_rows ? 0 : -1;
+  } else {
+    row = (m_tile - p.n_m0) * BM + r;
+    src = row < p.a1_rows ? 1 : -1;
+  }
+}
+
+DF_DEV void store_bf16(void* dst, const float* v, int n) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) {
+  for (int i = 0; i < n / 8; ++i) {
     uint4 w;
     w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
     w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
@@ -125,7 +148,7 @@ DF_DEV void norm_rope(float* v, const float* w, float eps, const float2* rope_ro
   }
 }
 
-template <int EPI>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0,
                      const __grid_constant__ CUtensorMap tmA1,
@@ -133,6 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ Plan p,
                      const __grid_constant__ QkvOut qo,
                      const __grid_constant__ SeqTable st) {
+  static_assert(EPI != EPI_QKV || BN == HD, "QKV tiles are one head wide");
+  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr int C4 = BN / 4;  // float4 chunks per row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -166,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(accb, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(from_a0 ? &tmA0 : &tmA1);
+    prefetch_tmap(&tmA0);
+    if (p.merged || !from_a0) prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
@@ -200,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], p.a_bytes + B_BYTES);
           tma_load_2d(sB + (size_t)s * B_BYTES, &tmB, &full[s], kx, n0, pol_w);
         }
-        tma_load_2d(sA + (size_t)s * p.a_bytes, ma, &full[s], kx, a_row0, pol_a);
+        uint8_t* a_dst = sA + (size_t)s * p.a_bytes;
+        tma_load_2d(a_dst, ma, &full[s], kx, a_row0, pol_a);
+        if (p.merged)
+          tma_load_2d(a_dst + (size_t)p.box0 * BK * 2, &tmA1, &full[s], kx, 0, pol_a);
       }
     }
   } else if (warp == 1) {
@@ -229,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..127 within the epilogue warps
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    int src, srow;
+    row_source(p, m_tile, r, src, srow);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
     tc_fence_after();
     float v[BN];
@@ -242,90 +275,121 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool last = true;
     if (p.splits > 1) {
-      float4* mine = reinterpret_cast<float4*>(
-          p.partial + ((size_t)tile_id * p.splits + split) * (BM * BN));
+      // valid rows of this split's partial, row-major [row][BN]
+      float* tile_part = p.partial + (size_t)tile_id * p.splits * (BM * BN);
+      if (src >= 0) {
+        float4* mine = reinterpret_cast<float4*>(tile_part + (size_t)split * (BM * BN) +
+                                                 (size_t)r * BN);
 #pragma unroll
-      for (int c4 = 0; c4 < BN / 4; ++c4)
-        __stcg(mine + c4 * BM + r,
-               make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
+        for (int c4 = 0; c4 < C4; ++c4)
+          __stcg(mine + c4, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                                        v[4 * c4 + 3]));
+      }
       __threadfence();
       named_bar_sync(1, 128);
-      if (r == 0) {
+      if (et == 0) {
         const int old = atomicAdd(p.counters + tile_id, 1);
         *last_flag = (old == p.splits - 1) ? 1 : 0;
       }
       named_bar_sync(1, 128);
       last = *last_flag != 0;
       if (last) {
-        // fixed summation order (split 0, 1, ...), whichever CTA came last:
-        // the result does not depend on the finishing order
+        // sum the splits in fixed order, 8 row-chunks per thread at a time,
+        // into a swizzled fp32 tile in the (now idle) stage buffers
         __threadfence();
+        float4* stile = reinterpret_cast<float4*>(smem);
+        constexpr int ITEMS = BM * C4;
+        for (int it0 = et; it0 < ITEMS; it0 += 128 * 8) {
+          float4 acc[8];
+          int rows[8];
+          bool use[8];
 #pragma unroll
-        for (int i = 0; i < BN; ++i) v[i] = 0.f;
-        for (int s2 = 0; s2 < p.splits; ++s2) {
-          const float4* part = reinterpret_cast<const float4*>(
-              p.partial + ((size_t)tile_id * p.splits + s2) * (BM * BN));
+          for (int j = 0; j < 8; ++j) {
+            const int it = it0 + j * 128;
+            rows[j] = it / C4;
+            int sj, rj;
+            row_source(p, m_tile, rows[j], sj, rj);
+            use[j] = it < ITEMS && sj >= 0;
+            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int s2 = 0; s2 < p.splits; ++s2) {
+            const float4* part =
+                reinterpret_cast<const float4*>(tile_part + (size_t)s2 * (BM * BN));
+            float4 t[8];
 #pragma unroll
-          for (int c4 = 0; c4 < BN / 4; ++c4) {
-            const float4 t = __ldcg(part + c4 * BM + r);
-            v[4 * c4] += t.x;
-            v[4 * c4 + 1] += t.y;
-            v[4 * c4 + 2] += t.z;
-            v[4 * c4 + 3] += t.w;
+            for (int j = 0; j < 8; ++j)
+              t[j] = use[j] ? __ldcg(part + it0 + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc[j].x += t[j].x;
+              acc[j].y += t[j].y;
+              acc[j].z += t[j].z;
+              acc[j].w += t[j].w;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int it = it0 + j * 128;
+            if (use[j]) {
+              const int c4 = it - rows[j] * C4;
+              stile[rows[j] * C4 + (c4 ^ (rows[j] & (C4 - 1)))] = acc[j];
+            }
           }
         }
-        if (r == 0) p.counters[tile_id] = 0;
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int c4 = 0; c4 < C4; ++c4) {
+          const float4 t = stile[r * C4 + (c4 ^ (r & (C4 - 1)))];
+          v[4 * c4] = t.x;
+          v[4 * c4 + 1] = t.y;
+          v[4 * c4 + 2] = t.z;
+          v[4 * c4 + 3] = t.w;
+        }
+        if (et == 0) p.counters[tile_id] = 0;
       }
     }
-    if (last) {
+    if (last && src >= 0) {
       if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
-        const int row = a_row0 + r;
-        if (row < p.a0_rows) {
-          if constexpr (EPI == EPI_BF16) {
-            store_bf16_row(reinterpret_cast<__nv_bfloat16*>(p.c) +
-                               (size_t)row * p.ldc + n0,
-                           v);
-          } else {
-            float4* d4 = reinterpret_cast<float4*>(
-                reinterpret_cast<float*>(p.c) + (size_t)row * p.ldc + n0);
+        if constexpr (EPI == EPI_BF16) {
+          store_bf16(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc + n0, v, BN);
+        } else {
+          float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) +
+                                                 (size_t)srow * p.ldc + n0);
 #pragma unroll
-            for (int c4 = 0; c4 < BN / 4; ++c4)
-              d4[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                                   v[4 * c4 + 3]);
-          }
+          for (int c4 = 0; c4 < C4; ++c4)
+            d4[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
         }
       } else {
         // ---------------- fused QKV epilogue: one head (128 columns) per tile
-        const int grow = a_row0 + r;
-        const bool valid = from_a0 ? grow < p.a0_rows : grow < p.a1_rows;
-        if (valid) {
-          int b, pos_idx, crow, t = 0;
-          if (from_a0) {  // noise (block) row
-            b = grow / st.q_len;
-            t = grow - b * st.q_len;
-            const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
-            pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
-            crow = st.cache_len[b] + nb + t;
-          } else {  // new context row: find its sequence
-            int lo = 0, hi = st.n;
-            while (hi - lo > 1) {
-              const int mid = (lo + hi) >> 1;
-              if (st.ctx_off[mid] <= grow) lo = mid; else hi = mid;
-            }
-            b = lo;
-            const int rr = grow - st.ctx_off[b];
-            pos_idx = st.ctx_off[b] + b * st.q_len + rr;
-            crow = st.cache_len[b] + rr;
+        int b, pos_idx, crow, t = 0;
+        if (src == 0) {  // noise (block) row
+          b = srow / st.q_len;
+          t = srow - b * st.q_len;
+          const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
+          pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
+          crow = st.cache_len[b] + nb + t;
+        } else {  // new context row: find its sequence
+          int lo = 0, hi = st.n;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (st.ctx_off[mid] <= srow) lo = mid; else hi = mid;
           }
-          const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
-          if (n0 < q_cols + kv_cols) {
+          b = lo;
+          const int rr = srow - st.ctx_off[b];
+          pos_idx = st.ctx_off[b] + b * st.q_len + rr;
+          crow = st.cache_len[b] + rr;
+        }
+        const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
+        if (n0 < q_cols + kv_cols) {
+          const bool is_q = n0 < q_cols;
+          if (!is_q || src == 0) {  // queries exist for block rows only
             int pos = qo.positions[pos_idx];
             if (pos < 0 || pos >= qo.max_pos) {
               record_error(p.err, 2 /* DFLASH_DEV_POSITION */);
               pos = 0;
             }
             const float2* rope_row = qo.rope + (size_t)pos * (HD / 2);
-            if (n0 < q_cols) {
+            if (is_q) {
               const int hq = n0 / HD;
               const int h = hq / qo.groups, gi = hq - h * qo.groups;
               const int nblk = st.q_len / qo.q_block;
@@ -334,20 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) *
                       qo.q_block + tt;
               norm_rope(v, qo.q_norm, qo.eps, rope_row, qo.q_scale);
-              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD, v);
+              store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD, v, HD);
             } else {
               const int h = (n0 - q_cols) / HD;
               norm_rope(v, qo.k_norm, qo.eps, rope_row, 1.f);
-              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
-                                 (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
-                             v);
+              store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
+                             (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
+                         v, HD);
             }
-          } else {
-            const int h = (n0 - q_cols - kv_cols) / HD;
-            store_bf16_row(reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
-                               (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
-                           v);
           }
+        } else {
+          const int h = (n0 - q_cols - kv_cols) / HD;
+          store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
+                         (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
+                     v, HD);
         }
       }
     }
@@ -399,32 +463,53 @@ int choose_splits(int tiles, int n_kb, int num_sms) {
   return best;
 }
 
+int round8(int x) { return (x + 7) / 8 * 8; }
+
 struct Geometry {
+  int bn, merged, box0, box1;
   int n_m0, n_m1, n_tiles, n_q_tiles, n_kb, tiles, splits;
-  int box_rows, stages;
+  size_t a_bytes;
+  int stages;
 };
 
-Geometry geometry(int rows0, int rows1, int n, int k, int q_cols, int num_sms) {
+Geometry geometry(int epi, int rows0, int rows1, int n, int k, int q_cols, int num_sms) {
   Geometry g;
-  g.n_m0 = (rows0 + BM - 1) / BM;
-  g.n_m1 = (rows1 + BM - 1) / BM;
-  g.n_tiles = n / BN;
-  g.n_q_tiles = q_cols / BN;
+  // plain epilogues over a handful of rows: narrow tiles, no split of K
+  g.bn = (epi != EPI_QKV && rows1 == 0 && rows0 <= 64 && n % 32 == 0) ? 32 : 128;
+  g.merged = rows1 > 0 && round8(rows0) + round8(rows1) <= BM;
+  if (g.merged) {
+    g.box0 = std::max(8, round8(rows0));
+    g.box1 = std::max(8, round8(rows1));
+    g.n_m0 = 1;
+    g.n_m1 = 0;
+    g.a_bytes = (size_t)(g.box0 + g.box1) * BK * 2;
+  } else {
+    const int most = std::min(BM, std::max(rows0, rows1));
+    g.box0 = g.box1 = std::min(BM, std::max(8, round8(most)));
+    g.n_m0 = (rows0 + BM - 1) / BM;
+    g.n_m1 = (rows1 + BM - 1) / BM;
+    g.a_bytes = (size_t)g.box0 * BK * 2;
+  }
+  g.n_tiles = n / g.bn;
+  g.n_q_tiles = q_cols / g.bn;
   g.n_kb = k / BK;
   g.tiles = g.n_q_tiles * g.n_m0 + (g.n_tiles - g.n_q_tiles) * (g.n_m0 + g.n_m1);
   g.splits = choose_splits(g.tiles, g.n_kb, num_sms);
-  // rows one A box must cover: the most rows any m-tile holds, in 16s
-  const int most = std::min(BM, std::max(rows0, rows1));
-  g.box_rows = std::min(BM, std::max(16, (most + 15) / 16 * 16));
-  const size_t a_bytes = (size_t)g.box_rows * BK * 2;
-  const size_t room = SMEM_LIMIT - SMEM_FIXED - (A_FULL - a_bytes);
-  g.stages = (int)std::min<size_t>(MAX_STAGES, room / (B_BYTES + a_bytes));
+  const size_t b_bytes = (size_t)g.bn * BK * 2;
+  const size_t room = SMEM_LIMIT - SMEM_FIXED - (A_FULL - g.a_bytes);
+  g.stages = (int)std::min<size_t>(MAX_STAGES, room / (b_bytes + g.a_bytes));
   return g;
 }
 
 size_t smem_bytes(const Geometry& g) {
-  return SMEM_FIXED + (size_t)g.stages * (B_BYTES + (size_t)g.box_rows * BK * 2) +
-         (A_FULL - (size_t)g.box_rows * BK * 2);
+  return SMEM_FIXED + (size_t)g.stages * ((size_t)g.bn * BK * 2 + g.a_bytes) +
+         (A_FULL - g.a_bytes);
+}
+
+template <int EPI, int BN>
+void set_smem_attr() {
+  cudaFuncSetAttribute(gemm_bf16_kernel<EPI, BN>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
 }
 
 }  // namespace
@@ -446,13 +531,13 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
-size_t gemm_scratch_bytes(int rows0, int rows1, int n, int k, int q_cols,
+size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_cols,
                           int num_sms, int* n_counters) {
-  Geometry g = geometry(rows0, rows1, n, k, q_cols, num_sms);
+  Geometry g = geometry(epi, rows0, rows1, n, k, q_cols, num_sms);
   const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
   if (n_counters) *n_counters = dense_tiles;
   if (g.splits <= 1) return 0;
-  return (size_t)dense_tiles * g.splits * BM * BN * sizeof(float);
+  return (size_t)dense_tiles * g.splits * BM * g.bn * sizeof(float);
 }
 
 int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
@@ -461,28 +546,31 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
                      cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(gemm_bf16_kernel<EPI_BF16>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
-    cudaFuncSetAttribute(gemm_bf16_kernel<EPI_F32>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
-    cudaFuncSetAttribute(gemm_bf16_kernel<EPI_QKV>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
+    set_smem_attr<EPI_BF16, 32>();
+    set_smem_attr<EPI_BF16, 128>();
+    set_smem_attr<EPI_F32, 32>();
+    set_smem_attr<EPI_F32, 128>();
+    set_smem_attr<EPI_QKV, 128>();
     attr_done = true;
   }
-  if (s.n % BN != 0 || s.k % BK != 0 || s.q_cols % BN != 0) return cudaErrorInvalidValue;
-  Geometry g = geometry(s.a0_rows, s.a1_rows, s.n, s.k, s.q_cols, num_sms);
+  if (s.k % BK != 0) return cudaErrorInvalidValue;
+  Geometry g = geometry(epi, s.a0_rows, s.a1_rows, s.n, s.k, s.q_cols, num_sms);
+  if (s.n % g.bn != 0 || s.q_cols % g.bn != 0) return cudaErrorInvalidValue;
   if (g.tiles == 0) return cudaSuccess;
   Plan p;
   p.a0_rows = s.a0_rows;
   p.a1_rows = s.a1_rows;
   p.n_m0 = g.n_m0;
   p.n_m1 = g.n_m1;
+  p.merged = g.merged;
+  p.box0 = g.box0;
+  p.box1 = g.box1;
   p.n_tiles = g.n_tiles;
   p.n_q_tiles = g.n_q_tiles;
   p.n_kb = g.n_kb;
   p.splits = g.splits;
   p.stages = g.stages;
-  p.a_bytes = (uint32_t)g.box_rows * BK * 2;
+  p.a_bytes = (uint32_t)g.a_bytes;
   p.units_q = g.n_q_tiles * g.splits * g.n_m0;
   p.ldc = ldc;
   p.c = c;
@@ -490,16 +578,16 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   p.partial = scr.partial;
   p.counters = scr.counters;
   if (g.splits > 1) {
-    const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * BN * 4;
+    const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * g.bn * 4;
     if (scr.partial == nullptr || scr.partial_bytes < need ||
         scr.n_counters < g.n_tiles * (g.n_m0 + g.n_m1))
       return cudaErrorInvalidValue;
   }
   CUtensorMap ma0, ma1;
-  if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, g.box_rows) != 0)
+  if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, g.box0) != 0)
     return cudaErrorInvalidValue;
   if (s.a1_rows > 0) {
-    if (make_tmap_bf16_rows(&ma1, s.a1, s.a1_rows, s.k, g.box_rows) != 0)
+    if (make_tmap_bf16_rows(&ma1, s.a1, s.a1_rows, s.k, g.box1) != 0)
       return cudaErrorInvalidValue;
   } else {
     ma1 = ma0;
@@ -508,22 +596,23 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   static SeqTable zero_st{};
   const QkvOut& qo = qkv ? *qkv : zero_q;
   const SeqTable& st = seqs ? *seqs : zero_st;
-  const int units = g.tiles * g.splits;
+  const dim3 grid(g.tiles * g.splits), block(kThreads);
   const size_t smem = smem_bytes(g);
   cudaError_t e;
-  switch (epi) {
-    case EPI_BF16:
-      e = launch_pdl(gemm_bf16_kernel<EPI_BF16>, dim3(units), dim3(kThreads), smem, stream,
-                     ma0, ma1, *s.b_map, p, qo, st);
-      break;
-    case EPI_F32:
-      e = launch_pdl(gemm_bf16_kernel<EPI_F32>, dim3(units), dim3(kThreads), smem, stream,
-                     ma0, ma1, *s.b_map, p, qo, st);
-      break;
-    default:
-      e = launch_pdl(gemm_bf16_kernel<EPI_QKV>, dim3(units), dim3(kThreads), smem, stream,
-                     ma0, ma1, *s.b_map, p, qo, st);
-      break;
+  if (epi == EPI_QKV) {
+    if (g.bn != 128) return cudaErrorInvalidValue;
+    e = launch_pdl(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, ma0, ma1,
+                   *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st);
+  } else if (epi == EPI_BF16) {
+    e = g.bn == 32 ? launch_pdl(gemm_bf16_kernel<EPI_BF16, 32>, grid, block, smem, stream,
+                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st)
+                   : launch_pdl(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream,
+                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st);
+  } else {
+    e = g.bn == 32 ? launch_pdl(gemm_bf16_kernel<EPI_F32, 32>, grid, block, smem, stream,
+                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st)
+                   : launch_pdl(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream,
+                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st);
   }
   return (int)e;
 }

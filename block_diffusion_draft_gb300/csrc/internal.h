@@ -64,7 +64,8 @@ enum GemmEpi { EPI_BF16 = 0, EPI_F32 = 1, EPI_QKV = 2 };
 struct GemmShape {
   const void* a0; int a0_rows;   // noise rows (or the only source)
   const void* a1; int a1_rows;   // context rows (may be 0)
-  const CUtensorMap* b_map;      // weights, built once at create
+  const CUtensorMap* b_map;      // weights, 128-row boxes, built at create
+  const CUtensorMap* b_map32;    // the same weights with 32-row boxes
   int n, k;
   int q_cols;                    // leading columns computed from A0 only
 };
@@ -78,7 +79,7 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
                      const QkvOut* qkv, const SeqTable* seqs,
                      const GemmScratch& scr, int num_sms, int* err,
                      cudaStream_t st);
-size_t gemm_scratch_bytes(int rows0, int rows1, int n, int k, int q_cols,
+size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_cols,
                           int num_sms, int* n_counters);
 int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
                         int cols, int box_rows);

@@ -75,7 +75,8 @@ extern "C" int dflash_ctx_project_noalloc(dflash_attn* a, const void* x, int row
   size_t part_bytes = 0;
   int n_counters = 0;
   if (bf)
-    part_bytes = round256(df::gemm_scratch_bytes(rows, 0, a->H, K, 0, a->num_sms, &n_counters));
+    part_bytes = round256(df::gemm_scratch_bytes(df::EPI_F32, rows, 0, a->H, K, 0, a->num_sms,
+                                                 &n_counters));
   const size_t cnt_bytes = round256((size_t)std::max(n_counters, 1) * sizeof(int));
   const size_t need = z_bytes + part_bytes + cnt_bytes;
   if (need > kScratchBytes) {
@@ -104,7 +105,7 @@ extern "C" int dflash_ctx_project_noalloc(dflash_attn* a, const void* x, int row
     // previous call left, so clear them on this stream first
     e = cudaMemsetAsync(scr.counters, 0, cnt_bytes, s);
     if (e == cudaSuccess) {
-      df::GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, a->H, K, 0};
+      df::GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, &a->tm_fc32, a->H, K, 0};
       e = (cudaError_t)df::launch_gemm_bf16(gs, df::EPI_F32, z, a->H, nullptr, nullptr, scr,
                                             a->num_sms, a->err, s);
     }

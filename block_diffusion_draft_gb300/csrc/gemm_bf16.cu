@@ -14,9 +14,9 @@
 // the MMA still runs M = 128 and rows past the box are don't-care rows that no
 // epilogue stores.  When block rows and context rows together fit one tile
 // they share it (two boxes into one A stage), so the K/V weights are streamed
-// once.  Plain epilogues with few rows use BN = 32: enough tiles to fill the
-// GPU without splitting K.  The QKV epilogue needs whole heads (BN = 128) and
-// splits K when the tiles are too few; then every CTA writes the valid rows of
+// once.  Tiles are 128 columns wide (the QKV epilogue needs whole heads, and
+// 16 KB weight boxes keep TMA requests few), and K is split when the tiles
+// are too few to fill the GPU; then every CTA writes the valid rows of
 // its fp32 partial, and the last CTA of a tile (atomic counter) sums all
 // partials in split order (deterministic), spreading the loads over all its
 // epilogue threads and staging the sums through shared memory.  It resets the
@@ -474,8 +474,10 @@ struct Geometry {
 
 Geometry geometry(int epi, int rows0, int rows1, int n, int k, int q_cols, int num_sms) {
   Geometry g;
-  // plain epilogues over a handful of rows: narrow tiles, no split of K
-  g.bn = (epi != EPI_QKV && rows1 == 0 && rows0 <= 64 && n % 32 == 0) ? 32 : 128;
+  // 128-wide tiles: 16 KB weight boxes (narrower boxes multiply the TMA
+  // requests per byte, which caps per-SM bandwidth below the HBM share)
+  g.bn = 128;
+  (void)epi;
   g.merged = rows1 > 0 && round8(rows0) + round8(rows1) <= BM;
   if (g.merged) {
     g.box0 = std::max(8, round8(rows0));
@@ -546,9 +548,7 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
                      cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    set_smem_attr<EPI_BF16, 32>();
     set_smem_attr<EPI_BF16, 128>();
-    set_smem_attr<EPI_F32, 32>();
     set_smem_attr<EPI_F32, 128>();
     set_smem_attr<EPI_QKV, 128>();
     attr_done = true;
@@ -602,17 +602,13 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   if (epi == EPI_QKV) {
     if (g.bn != 128) return cudaErrorInvalidValue;
     e = launch_pdl(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, ma0, ma1,
-                   *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st);
+                   *s.b_map, p, qo, st);
   } else if (epi == EPI_BF16) {
-    e = g.bn == 32 ? launch_pdl(gemm_bf16_kernel<EPI_BF16, 32>, grid, block, smem, stream,
-                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st)
-                   : launch_pdl(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream,
-                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st);
+    e = launch_pdl(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream, ma0, ma1,
+                   *s.b_map, p, qo, st);
   } else {
-    e = g.bn == 32 ? launch_pdl(gemm_bf16_kernel<EPI_F32, 32>, grid, block, smem, stream,
-                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st)
-                   : launch_pdl(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream,
-                                ma0, ma1, *(g.bn == 32 ? s.b_map32 : s.b_map), p, qo, st);
+    e = launch_pdl(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream, ma0, ma1,
+                   *s.b_map, p, qo, st);
   }
   return (int)e;
 }

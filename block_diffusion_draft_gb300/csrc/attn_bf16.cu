@@ -2,9 +2,8 @@
 //
 // One CTA owns one work unit: a (sequence, kv head) pair and a range of keys.
 // Its Q tile stacks every query head of the KV group times the block rows
-// (groups * q_len rows, at most 128; the MMA is always M = 128 and surplus
-// rows are ignored), so each K/V row is read once for all heads of the group
-// ("DFlash源码导读（二）" step 1: GQA with num_key_value_groups).
+// (groups * q_len rows), so each K/V row is read once for all heads of the
+// group ("DFlash源码导读（二）" step 1: GQA with num_key_value_groups).
 //
 //   warp 0      TMA producer: Q tile once, then K and V tiles of 128 keys
 //               (two 64-column boxes each, 128-byte swizzle) into a 3-stage ring
@@ -13,11 +12,20 @@
 //                 O   += P(j) V(j)         -> TMEM columns [256, 384)
 //               S(j+1) is issued before waiting for P(j) so the tensor core
 //               overlaps the softmax of tile j.
-//   warps 2..5  softmax, one query row per thread: mask, running max in log2
-//               units (Q is pre-scaled by head_dim^-0.5*log2 e), exp2, bf16 P
-//               written into the K slot of the same stage (K(j) is dead once
-//               S(j) completed), lazy O rescale (only when the max grows by
-//               more than 2^8), final normalisation or split partials.
+//   warps 2..5  softmax, one TMEM lane (accumulator row) per thread: mask,
+//               running max in log2 units (Q is pre-scaled by
+//               head_dim^-0.5*log2 e), exp2, bf16 P written into the K slot of
+//               the same stage (K(j) is dead once S(j) completed), lazy O
+//               rescale (only when the max grows by more than 2^8), final
+//               normalisation or split partials.
+// The MMA is always M = 128.  An inference block has groups * q_len <= 64
+// query rows (64 for 4 heads per KV head x 16); then the Q tile holds every
+// row twice ("dual" mode): lane r and lane r + 64 see the same query, lane r
+// takes keys 0..63 and lane r + 64 keys 64..127 of every tile as two
+// independent online-softmax streams (the other half of each P row is zero),
+// and the two are merged at the end.  All four softmax warps work and each
+// thread handles 64 columns per tile.  The packed training layout fills the
+// 128 rows with real queries (two blocks x 4 heads x 16 rows).
 //
 // Masks ("nemo_automodel...draft_qwen3", _sliding_window_mask and the module
 // docstring): every row carries up to two allowed key intervals.
@@ -54,8 +62,6 @@ struct Unit {
   int s0_lo, s0_hi, s1_lo, s1_hi;  // key segments
   int blk0;         // packed: first block of the tile
   int direct;       // 1: this unit covers all keys of its rows
-  int n_split;      // inference: units of this (b, h)
-  int split_base;   // inference: first unit of this (b, h)
 };
 
 DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
@@ -79,8 +85,6 @@ DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
     w.rows = rows_per_block;
     w.blk0 = 0;
     w.direct = nch == 1;
-    w.n_split = nch;
-    w.split_base = sq.unit_off[w.b] + w.h * nch;
   } else {
     const int n_tiles = (a.n_blocks + a.tile_blocks - 1) / a.tile_blocks;
     const int per = a.batch * a.n_kv;
@@ -104,8 +108,6 @@ DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
     w.s1_lo = a.seq + w.blk0 * a.q_block;
     w.s1_hi = w.s1_lo + nbt * a.q_block;
     w.direct = 1;
-    w.n_split = 1;
-    w.split_base = u;
   }
   w.kv_row0 = ((long long)w.b * a.n_kv + w.h) * a.cap;
   return w;
@@ -122,12 +124,14 @@ DF_DEV int tile_start(const Unit& w, int j) {
   return j < n0 ? w.s0_lo + j * BKEY : w.s1_lo + (j - n0) * BKEY;
 }
 
+template <bool DUAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ AttnArgs a,
                      const __grid_constant__ AttnSeqs sq) {
+  constexpr int NC = DUAL ? 64 : 128;  // S columns one thread handles per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,8 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = a.mode == 0 ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
       mbar_arrive_expect_tx(q_full, TILE_BYTES);
-      tma_load_2d(sQ, &tmQ, q_full, 0, w.q_row0, pol_q);
-      tma_load_2d(sQ + HALF_BYTES, &tmQ, q_full, 64, w.q_row0, pol_q);
+      if (DUAL) {  // the 64 query rows twice: smem rows 0..63 and 64..127
+        for (int copy = 0; copy < 2; ++copy)
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(sQ + hf * HALF_BYTES + copy * 64 * 128, &tmQ, q_full, 64 * hf,
+                        w.q_row0, pol_q);
+      } else {
+        tma_load_2d(sQ, &tmQ, q_full, 0, w.q_row0, pol_q);
+        tma_load_2d(sQ + HALF_BYTES, &tmQ, q_full, 64, w.q_row0, pol_q);
+      }
       for (int j = 0; j < T; ++j) {
         const int s = j % NST;
         const uint32_t ph = (j / NST) & 1;
@@ -246,16 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     grid_dep_wait();
     const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const int r = q * 32 + lane;                // TMEM lane (accumulator row)
+    const int qr = DUAL ? (r & 63) : r;         // query row of the tile
+    const int col0 = DUAL ? (r >> 6) * 64 : 0;  // first S column of this thread
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    const bool real = r < w.rows;
+    const bool real = qr < w.rows;
     // this row's allowed key intervals
     int i1_lo = 0, i1_hi = 0, i2_lo = 0, i2_hi = 0;
     int out_token = 0, out_col = 0;
     {
       const int rows_per_block = a.groups * a.q_block;
-      const int kb = r / rows_per_block;
-      const int within = r - kb * rows_per_block;
+      const int kb = qr / rows_per_block;
+      const int within = qr - kb * rows_per_block;
       const int gi = within / a.q_block;
       const int t = within - gi * a.q_block;
       out_col = (w.h * a.groups + gi) * HD;
@@ -290,29 +303,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, a.err)))
         break;
       tc_fence_after();
-      float s[BKEY];
+      float s[NC];
+      {
+        uint32_t raw[NC / 32][32];
 #pragma unroll
-      for (int c = 0; c < BKEY / 32; ++c) {
-        float tt[32];
-        tmem_ld32(trow + sb * BKEY + c * 32, tt);
+        for (int c = 0; c < NC / 32; ++c)
+          tmem_ld32_nowait(trow + sb * BKEY + col0 + c * 32, raw[c]);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = tt[i];
+        for (int c = 0; c < NC / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[c][i]);
       }
       float alpha = 1.f;
       bool rescale = false;
       if (real) {
-        const int t0 = tile_start(w, j);
-        if (!(t0 >= i1_lo && t0 + BKEY <= i1_hi)) {
+        const int k0 = tile_start(w, j) + col0;
+        if (!(k0 >= i1_lo && k0 + NC <= i1_hi)) {
 #pragma unroll
-          for (int c = 0; c < BKEY; ++c) {
-            const int key = t0 + c;
+          for (int c = 0; c < NC; ++c) {
+            const int key = k0 + c;
             const bool ok = (key >= i1_lo && key < i1_hi) || (key >= i2_lo && key < i2_hi);
             if (!ok) s[c] = -INFINITY;
           }
         }
         float tmax = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < BKEY; ++c) tmax = fmaxf(tmax, s[c]);
+        for (int c = 0; c < NC; ++c) tmax = fmaxf(tmax, s[c]);
         float m_new = m_run;
         if (m_run == -INFINITY || tmax > m_run + kRescaleThreshold) m_new = fmaxf(m_run, tmax);
         if (m_new != m_run) {
@@ -322,12 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mm = (m_new == -INFINITY) ? 0.f : m_new;
         float sum = 0.f;
         uint8_t* prow = sK + (j % NST) * TILE_BYTES + r * 128;
+        // this thread's NC columns are 16-byte chunks col0/8 .. col0/8+NC/8-1
+        // of its P row (one 64-key atom per half); in dual mode the other
+        // half of the row is zero
 #pragma unroll
-        for (int ch = 0; ch < BKEY / 8; ++ch) {
+        for (int cc = 0; cc < NC / 8; ++cc) {
           float pv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            pv[e] = fast_exp2(s[ch * 8 + e] - mm);
+            pv[e] = fast_exp2(s[cc * 8 + e] - mm);
             sum += pv[e];
           }
           uint4 pk;
@@ -335,9 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk.y = pack_bf16x2(pv[2], pv[3]);
           pk.z = pack_bf16x2(pv[4], pv[5]);
           pk.w = pack_bf16x2(pv[6], pv[7]);
-          const int atom = ch >> 3;
-          const int pos = (ch & 7) ^ (r & 7);
-          *reinterpret_cast<uint4*>(prow + atom * HALF_BYTES + pos * 16) = pk;
+          const int ch = col0 / 8 + cc;
+          *reinterpret_cast<uint4*>(prow + (ch >> 3) * HALF_BYTES + (((ch & 7) ^ (r & 7)) * 16)) =
+              pk;
+        }
+        if constexpr (DUAL) {
+          const int other = col0 == 0 ? 1 : 0;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4*>(prow + other * HALF_BYTES + ((cc ^ (r & 7)) * 16)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
         l_run = l_run * alpha + sum;
         m_run = m_new;
@@ -369,37 +396,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     float o[HD];
+    {
+      uint32_t raw[HD / 32][32];
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      float tt[32];
-      tmem_ld32(trow + O_COL + c * 32, tt);
+      for (int c = 0; c < HD / 32; ++c) tmem_ld32_nowait(trow + O_COL + c * 32, raw[c]);
+      tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[c * 32 + i] = have_o ? tt[i] : 0.f;
+      for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c * 32 + i] = have_o ? __uint_as_float(raw[c][i]) : 0.f;
     }
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    const int ld_out = a.n_kv * a.groups * HD;
-    const bool write_final = w.direct;
-    if (!w.direct && real) {
-      const size_t u = blockIdx.x;
-      float4* po = reinterpret_cast<float4*>(a.part_o + u * 128 * HD);
+    if constexpr (DUAL) {
+      // lanes 64..127 hand their half (keys 64..127 of every tile) to lanes
+      // 0..63 through shared memory (K slot 0 and the Q tile are idle now)
+      float4* xo = reinterpret_cast<float4*>(sK);
+      float* xm = reinterpret_cast<float*>(sQ);
+      if (r >= 64) {
 #pragma unroll
-      for (int c4 = 0; c4 < HD / 4; ++c4)
-        __stcg(po + c4 * 128 + r,
-               make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
-      __stcg(a.part_ml + u * 256 + r, m_run);
-      __stcg(a.part_ml + u * 256 + 128 + r, l_run);
+        for (int c4 = 0; c4 < HD / 4; ++c4)
+          xo[qr * 32 + (c4 ^ (qr & 31))] =
+              make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+        xm[qr] = m_run;
+        xm[64 + qr] = l_run;
+      }
+      named_bar_sync(1, 128);
+      if (r < 64) {
+        const float mb = xm[qr], lb = xm[64 + qr];
+        const float M = fmaxf(m_run, mb);
+        const float fa = m_run == -INFINITY ? 0.f : fast_exp2(m_run - M);
+        const float fb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
+#pragma unroll
+        for (int c4 = 0; c4 < HD / 4; ++c4) {
+          const float4 t = xo[qr * 32 + (c4 ^ (qr & 31))];
+          o[4 * c4] = fa * o[4 * c4] + fb * t.x;
+          o[4 * c4 + 1] = fa * o[4 * c4 + 1] + fb * t.y;
+          o[4 * c4 + 2] = fa * o[4 * c4 + 2] + fb * t.z;
+          o[4 * c4 + 3] = fa * o[4 * c4 + 3] + fb * t.w;
+        }
+        l_run = fa * l_run + fb * lb;
+        m_run = M;
+      }
     }
-    if (write_final && real) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)out_token * ld_out + out_col);
+    const bool writer = real && (!DUAL || r < 64);
+    if (writer) {
+      if (w.direct) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const int ld_out = a.n_kv * a.groups * HD;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                              (size_t)out_token * ld_out + out_col);
 #pragma unroll
-      for (int i = 0; i < HD / 8; ++i) {
-        uint4 pk;
-        pk.x = pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv);
-        pk.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-        pk.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-        pk.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-        dst[i] = pk;
+        for (int i = 0; i < HD / 8; ++i) {
+          uint4 pk;
+          pk.x = pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv);
+          pk.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+          pk.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+          pk.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+          dst[i] = pk;
+        }
+      } else {
+        const size_t u = blockIdx.x;
+        float4* po = reinterpret_cast<float4*>(a.part_o + u * 128 * HD);
+#pragma unroll
+        for (int c4 = 0; c4 < HD / 4; ++c4)
+          __stcg(po + c4 * 128 + qr,
+                 make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
+        __stcg(a.part_ml + u * 256 + qr, m_run);
+        __stcg(a.part_ml + u * 256 + 128 + qr, l_run);
       }
     }
   }
@@ -413,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the split partials of one (sequence, kv head): 8 query rows per CTA,
-// one thread per (row, 4 output columns).  Pairs whose keys fit one unit were
+// one thread per (row, 4 output columns), partials read 8 splits at a time
+// with an online log-sum-exp rescale.  Pairs whose keys fit one unit were
 // finished by the attention kernel and are skipped.
 __global__ void __launch_bounds__(256)
     attn_combine_kernel(const __grid_constant__ AttnArgs a,
@@ -430,24 +493,44 @@ __global__ void __launch_bounds__(256)
   if (r >= rows_pair) return;
   const size_t base = (size_t)sq.unit_off[b] + (size_t)h * nch;
   grid_dep_wait();
-  float mx = -INFINITY;
-  for (int c = 0; c < nch; ++c) mx = fmaxf(mx, __ldcg(a.part_ml + (base + c) * 256 + r));
-  const float mref = mx == -INFINITY ? 0.f : mx;
+  float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < nch; ++c) {
-    const size_t u = base + c;
-    const float mc = __ldcg(a.part_ml + u * 256 + r);
-    const float lc = __ldcg(a.part_ml + u * 256 + 128 + r);
-    const float4 t = __ldcg(reinterpret_cast<const float4*>(a.part_o + u * 128 * HD) +
-                            c4 * 128 + r);
-    const float f = mc == -INFINITY ? 0.f : fast_exp2(mc - mref);
-    L += f * lc;
-    acc.x += f * t.x;
-    acc.y += f * t.y;
-    acc.z += f * t.z;
-    acc.w += f * t.w;
+  for (int c0 = 0; c0 < nch; c0 += 8) {
+    float mv[8], lv[8];
+    float4 tv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const size_t u = base + c0 + j;
+      if (c0 + j < nch) {
+        mv[j] = __ldcg(a.part_ml + u * 256 + r);
+        lv[j] = __ldcg(a.part_ml + u * 256 + 128 + r);
+        tv[j] = __ldcg(reinterpret_cast<const float4*>(a.part_o + u * 128 * HD) + c4 * 128 + r);
+      } else {
+        mv[j] = -INFINITY;
+        lv[j] = 0.f;
+        tv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float bm = M;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) bm = fmaxf(bm, mv[j]);
+    if (bm == -INFINITY) continue;
+    const float sc = M == -INFINITY ? 0.f : fast_exp2(M - bm);
+    L *= sc;
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float f = mv[j] == -INFINITY ? 0.f : fast_exp2(mv[j] - bm);
+      L += f * lv[j];
+      acc.x += f * tv[j].x;
+      acc.y += f * tv[j].y;
+      acc.z += f * tv[j].z;
+      acc.w += f * tv[j].w;
+    }
+    M = bm;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int gi = r / a.q_len, t = r - gi * a.q_len;
@@ -468,22 +551,27 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                      cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(attn_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_BYTES);
+    cudaFuncSetAttribute(attn_bf16_kernel<false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     attr_done = true;
   }
   if (a.n_units <= 0) return cudaSuccess;
   if (kv_rows_total >= (1LL << 31) || q_rows_total >= (1LL << 31))
     return cudaErrorInvalidValue;
+  const bool dual = a.mode == 0 && a.groups * a.q_len <= 64;
   CUtensorMap mq, mk, mv;
-  if (make_tmap_bf16_rows(&mq, qbuf, q_rows_total, HD, 128) != 0 ||
+  if (make_tmap_bf16_rows(&mq, qbuf, q_rows_total, HD, dual ? 64 : 128) != 0 ||
       make_tmap_bf16_rows(&mk, cache_k, kv_rows_total, HD, 128) != 0 ||
       make_tmap_bf16_rows(&mv, cache_v, kv_rows_total, HD, 128) != 0)
     return cudaErrorInvalidValue;
   static AttnSeqs zero_seqs{};
   const AttnSeqs& sq = seqs ? *seqs : zero_seqs;
-  cudaError_t e = launch_pdl(attn_bf16_kernel, dim3(a.n_units), dim3(kThreads), SMEM_BYTES,
-                             stream, mq, mk, mv, a, sq);
+  cudaError_t e = dual ? launch_pdl(attn_bf16_kernel<true>, dim3(a.n_units), dim3(kThreads),
+                                    SMEM_BYTES, stream, mq, mk, mv, a, sq)
+                       : launch_pdl(attn_bf16_kernel<false>, dim3(a.n_units), dim3(kThreads),
+                                    SMEM_BYTES, stream, mq, mk, mv, a, sq);
   if (e != cudaSuccess || a.mode != 0) return (int)e;
   bool any_split = false;
   for (int b = 0; b < a.batch; ++b) any_split |= sq.n_chunks[b] > 1;

@@ -134,7 +134,7 @@ int run_qkv(dflash_attn* a, const void* noise, int rows_noise, const void* ctx,
   if (a->dt == DFLASH_BF16) {
     int r = ensure_gemm_scratch(a, EPI_QKV, rows_noise, rows_ctx, nqkv, a->H, a->nq * a->d);
     if (r) return r;
-    GemmShape gs{noise, rows_noise, ctx, rows_ctx, &a->tm_qkv, nqkv, a->H,
+    GemmShape gs{noise, rows_noise, ctx, rows_ctx, &a->tm_qkv, &a->tm_qkv256, nqkv, a->H,
                  a->nq * a->d};
     TraceScope tr(a, DFLASH_K_QKV, s);
     DF_CUDA(launch_gemm_bf16(gs, EPI_QKV, nullptr, 0, &o, &st, gemm_scratch(a),
@@ -165,7 +165,7 @@ int run_o_proj(dflash_attn* a, int rows, void* out, cudaStream_t s) {
     int r = ensure_gemm_scratch(a, EPI_BF16, rows, 0, a->H, a->nq * a->d, 0);
     if (r) return r;
     TraceScope tr(a, DFLASH_K_OPROJ, s);
-    GemmShape gs{a->attn_out.p, rows, nullptr, 0, &a->tm_o, a->H, a->nq * a->d, 0};
+    GemmShape gs{a->attn_out.p, rows, nullptr, 0, &a->tm_o, &a->tm_o256, a->H, a->nq * a->d, 0};
     DF_CUDA(launch_gemm_bf16(gs, EPI_BF16, out, a->H, nullptr, nullptr, gemm_scratch(a),
                              a->num_sms, a->err, s),
             "o_proj launch");
@@ -282,7 +282,10 @@ int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const v
   if (bf) {
     if (make_tmap_bf16_rows(&a->tm_qkv, a->w_qkv, (nq + 2 * nkv) * d, (int)H, 128) != 0 ||
         make_tmap_bf16_rows(&a->tm_o, a->w_o, H, (int)(nq * d), 128) != 0 ||
-        (fc_w && make_tmap_bf16_rows(&a->tm_fc, a->w_fc, H, (int)(a->nL * H), 128) != 0))
+        (fc_w && make_tmap_bf16_rows(&a->tm_fc, a->w_fc, H, (int)(a->nL * H), 128) != 0) ||
+        make_tmap_bf16_rows(&a->tm_qkv256, a->w_qkv, (nq + 2 * nkv) * d, (int)H, 256) != 0 ||
+        make_tmap_bf16_rows(&a->tm_o256, a->w_o, H, (int)(nq * d), 256) != 0 ||
+        (fc_w && make_tmap_bf16_rows(&a->tm_fc256, a->w_fc, H, (int)(a->nL * H), 256) != 0))
       return cleanup(fail(DFLASH_ERR_CUDA, "tensor map encoding failed"));
   }
   if ((e = cudaDeviceSynchronize()) != cudaSuccess)
@@ -431,7 +434,7 @@ int dflash_ctx_project(dflash_attn* a, const void* x, int rows, void* y,
   float* z = static_cast<float*>(a->zbuf.p);
   if (a->dt == DFLASH_BF16) {
     if (int r = ensure_gemm_scratch(a, EPI_F32, rows, 0, a->H, K, 0)) return r;
-    GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, a->H, K, 0};
+    GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, &a->tm_fc256, a->H, K, 0};
     TraceScope tr(a, DFLASH_K_FC, s);
     DF_CUDA(launch_gemm_bf16(gs, EPI_F32, z, a->H, nullptr, nullptr, gemm_scratch(a),
                              a->num_sms, a->err, s),

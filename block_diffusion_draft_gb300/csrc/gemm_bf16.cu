@@ -148,6 +148,80 @@ DF_DEV void norm_rope(float* v, const float* w, float eps, const float2* rope_ro
   }
 }
 
+// Final epilogue of one accumulator row: `v` holds 128 columns starting at
+// output column n0 for source row (src, srow).
+template <int EPI>
+DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, float* v,
+                       int src, int srow, int n0) {
+  constexpr int BN = HD;
+  constexpr int C4 = BN / 4;
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
+    if constexpr (EPI == EPI_BF16) {
+      store_bf16(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc + n0, v, BN);
+    } else {
+      float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) +
+                                             (size_t)srow * p.ldc + n0);
+#pragma unroll
+      for (int c4 = 0; c4 < C4; ++c4)
+        d4[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+    }
+  } else {
+    // ---------------- fused QKV epilogue: one head (128 columns) per tile
+    int b, pos_idx, crow, t = 0;
+    if (src == 0) {  // noise (block) row
+      b = srow / st.q_len;
+      t = srow - b * st.q_len;
+      const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
+      pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
+      crow = st.cache_len[b] + nb + t;
+    } else {  // new context row: find its sequence
+      int lo = 0, hi = st.n;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (st.ctx_off[mid] <= srow) lo = mid; else hi = mid;
+      }
+      b = lo;
+      const int rr = srow - st.ctx_off[b];
+      pos_idx = st.ctx_off[b] + b * st.q_len + rr;
+      crow = st.cache_len[b] + rr;
+    }
+    const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
+    if (n0 < q_cols + kv_cols) {
+      const bool is_q = n0 < q_cols;
+      if (!is_q || src == 0) {  // queries exist for block rows only
+        int pos = qo.positions[pos_idx];
+        if (pos < 0 || pos >= qo.max_pos) {
+          record_error(p.err, 2 /* DFLASH_DEV_POSITION */);
+          pos = 0;
+        }
+        const float2* rope_row = qo.rope + (size_t)pos * (HD / 2);
+        if (is_q) {
+          const int hq = n0 / HD;
+          const int h = hq / qo.groups, gi = hq - h * qo.groups;
+          const int nblk = st.q_len / qo.q_block;
+          const int blk = t / qo.q_block, tt = t - blk * qo.q_block;
+          const size_t qrow =
+              ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) *
+                  qo.q_block + tt;
+          norm_rope(v, qo.q_norm, qo.eps, rope_row, qo.q_scale);
+          store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD, v, HD);
+        } else {
+          const int h = (n0 - q_cols) / HD;
+          norm_rope(v, qo.k_norm, qo.eps, rope_row, 1.f);
+          store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
+                         (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
+                     v, HD);
+        }
+      }
+    } else {
+      const int h = (n0 - q_cols - kv_cols) / HD;
+      store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
+                     (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
+                 v, HD);
+    }
+  }
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0,
@@ -348,71 +422,162 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (et == 0) p.counters[tile_id] = 0;
       }
     }
-    if (last && src >= 0) {
-      if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
-        if constexpr (EPI == EPI_BF16) {
-          store_bf16(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc + n0, v, BN);
-        } else {
-          float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) +
-                                                 (size_t)srow * p.ldc + n0);
+    if (last && src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+// ---------------------------------------------------------------- large M
+// Persistent variant for calls with many token rows: one CTA per SM walks
+// its share of 128 x 256 output tiles (round-robin over the grouped order).
+// Two TMEM accumulators (2 x 256 fp32 columns) let the epilogue of one tile
+// run while the MMA warp accumulates the next; 256-wide tiles halve the
+// shared-memory traffic of A per flop.  K is never split.
+constexpr int BNB = 256, STAGES_BIG = 4;
+constexpr uint32_t B_BIG = BNB * BK * 2;  // 32 KB
+constexpr size_t SMEM_BIG = 1024 + STAGES_BIG * (A_FULL + B_BIG) + 512;
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_big_kernel(const __grid_constant__ CUtensorMap tmA0,
+                    const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ Plan p,
+                    const __grid_constant__ QkvOut qo,
+                    const __grid_constant__ SeqTable st) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES_BIG * A_FULL;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES_BIG * B_BIG);
+  uint64_t* empty = full + STAGES_BIG;
+  uint64_t* acc_full = empty + STAGES_BIG;  // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES_BIG; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA0);
+    prefetch_tmap(&tmA1);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
+  grid_dep_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t it = 0;
+      bool alive = true;
+      for (int t = blockIdx.x; t < tiles && alive; t += gridDim.x) {
+        int m, n, sp;
+        decode_unit(p, t, m, n, sp);
+        const bool a0 = m < p.n_m0;
+        const CUtensorMap* ma = a0 ? &tmA0 : &tmA1;
+        const int a_row0 = (a0 ? m : m - p.n_m0) * BM;
+        for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
+          const int s = it % STAGES_BIG;
+          const uint32_t ph = (it / STAGES_BIG) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], A_FULL + B_BIG);
+          tma_load_2d(sA + s * A_FULL, ma, &full[s], kb * BK, a_row0, pol_a);
+          tma_load_2d(sB + s * B_BIG, &tmB, &full[s], kb * BK, n * BNB, pol_w);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BNB, false);
+      uint32_t it = 0, tc = 0;
+      bool alive = true;
+      for (int t = blockIdx.x; t < tiles && alive; t += gridDim.x, ++tc) {
+        const uint32_t buf = tc & 1, use = tc >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * BNB;
+        for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
+          const int s = it % STAGES_BIG;
+          const uint32_t ph = (it / STAGES_BIG) & 1;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * A_FULL);
+          const uint32_t b_base = smem_u32(sB + s * B_BIG);
 #pragma unroll
-          for (int c4 = 0; c4 < C4; ++c4)
-            d4[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(d, sdesc_sw128(a_base + kk * 32, 16, 1024),
+                        sdesc_sw128(b_base + kk * 32, 16, 1024), idesc,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
         }
-      } else {
-        // ---------------- fused QKV epilogue: one head (128 columns) per tile
-        int b, pos_idx, crow, t = 0;
-        if (src == 0) {  // noise (block) row
-          b = srow / st.q_len;
-          t = srow - b * st.q_len;
-          const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
-          pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
-          crow = st.cache_len[b] + nb + t;
-        } else {  // new context row: find its sequence
-          int lo = 0, hi = st.n;
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (st.ctx_off[mid] <= srow) lo = mid; else hi = mid;
-          }
-          b = lo;
-          const int rr = srow - st.ctx_off[b];
-          pos_idx = st.ctx_off[b] + b * st.q_len + rr;
-          crow = st.cache_len[b] + rr;
+        tc_commit(&acc_full[buf]);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+      int m, n, sp;
+      decode_unit(p, t, m, n, sp);
+      const uint32_t buf = tc & 1, use = tc >> 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1, abort_flag, p.err)))
+        break;
+      tc_fence_after();
+      int src, srow;
+      row_source(p, m, r, src, srow);
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
+#pragma unroll 1
+      for (int half = 0; half < BNB / HD; ++half) {
+        float v[HD];
+        uint32_t raw[HD / 32][32];
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) tmem_ld32_nowait(trow + half * HD + c * 32, raw[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(raw[c][i]);
+        if (half == BNB / HD - 1) {
+          // the accumulator is fully read: hand it back to the MMA warp
+          tc_fence_before();
+          mbar_arrive(&acc_empty[buf]);
         }
-        const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
-        if (n0 < q_cols + kv_cols) {
-          const bool is_q = n0 < q_cols;
-          if (!is_q || src == 0) {  // queries exist for block rows only
-            int pos = qo.positions[pos_idx];
-            if (pos < 0 || pos >= qo.max_pos) {
-              record_error(p.err, 2 /* DFLASH_DEV_POSITION */);
-              pos = 0;
-            }
-            const float2* rope_row = qo.rope + (size_t)pos * (HD / 2);
-            if (is_q) {
-              const int hq = n0 / HD;
-              const int h = hq / qo.groups, gi = hq - h * qo.groups;
-              const int nblk = st.q_len / qo.q_block;
-              const int blk = t / qo.q_block, tt = t - blk * qo.q_block;
-              const size_t qrow =
-                  ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) *
-                      qo.q_block + tt;
-              norm_rope(v, qo.q_norm, qo.eps, rope_row, qo.q_scale);
-              store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD, v, HD);
-            } else {
-              const int h = (n0 - q_cols) / HD;
-              norm_rope(v, qo.k_norm, qo.eps, rope_row, 1.f);
-              store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
-                             (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
-                         v, HD);
-            }
-          }
-        } else {
-          const int h = (n0 - q_cols - kv_cols) / HD;
-          store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
-                         (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
-                     v, HD);
-        }
+        if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
       }
     }
   }
@@ -421,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -514,6 +679,15 @@ void set_smem_attr() {
                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
 }
 
+// many token rows and 256-aligned column regions: the persistent kernel
+bool use_big(int rows0, int rows1, int n, int q_cols) {
+  const int m_tiles = (rows0 + BM - 1) / BM + (rows1 + BM - 1) / BM;
+  return m_tiles >= 4 && n % BNB == 0 && q_cols % BNB == 0;
+}
+
+int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
+               const SeqTable* seqs, int num_sms, int* err, cudaStream_t stream);
+
 }  // namespace
 
 int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
@@ -535,6 +709,10 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
 
 size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_cols,
                           int num_sms, int* n_counters) {
+  if (use_big(rows0, rows1, n, q_cols)) {
+    if (n_counters) *n_counters = 0;
+    return 0;
+  }
   Geometry g = geometry(epi, rows0, rows1, n, k, q_cols, num_sms);
   const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
   if (n_counters) *n_counters = dense_tiles;
@@ -554,6 +732,8 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
     attr_done = true;
   }
   if (s.k % BK != 0) return cudaErrorInvalidValue;
+  if (use_big(s.a0_rows, s.a1_rows, s.n, s.q_cols))
+    return launch_big(s, epi, c, ldc, qkv, seqs, num_sms, err, stream);
   Geometry g = geometry(epi, s.a0_rows, s.a1_rows, s.n, s.k, s.q_cols, num_sms);
   if (s.n % g.bn != 0 || s.q_cols % g.bn != 0) return cudaErrorInvalidValue;
   if (g.tiles == 0) return cudaSuccess;
@@ -613,4 +793,66 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   return (int)e;
 }
 
+}  // namespace df
+
+namespace df {
+namespace {
+
+int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
+               const SeqTable* seqs, int num_sms, int* err, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_BIG);
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_BIG);
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_BIG);
+    attr_done = true;
+  }
+  if (s.b_map256 == nullptr) return cudaErrorInvalidValue;
+  Plan p{};
+  p.a0_rows = s.a0_rows;
+  p.a1_rows = s.a1_rows;
+  p.n_m0 = (s.a0_rows + BM - 1) / BM;
+  p.n_m1 = (s.a1_rows + BM - 1) / BM;
+  p.merged = 0;
+  p.box0 = p.box1 = BM;
+  p.n_tiles = s.n / BNB;
+  p.n_q_tiles = s.q_cols / BNB;
+  p.n_kb = s.k / BK;
+  p.splits = 1;
+  p.stages = STAGES_BIG;
+  p.a_bytes = A_FULL;
+  p.units_q = p.n_q_tiles * p.n_m0;
+  p.ldc = ldc;
+  p.c = c;
+  p.err = err;
+  const int tiles = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
+  CUtensorMap ma0, ma1;
+  if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, BM) != 0) return cudaErrorInvalidValue;
+  if (s.a1_rows > 0) {
+    if (make_tmap_bf16_rows(&ma1, s.a1, s.a1_rows, s.k, BM) != 0) return cudaErrorInvalidValue;
+  } else {
+    ma1 = ma0;
+  }
+  static QkvOut zero_q{};
+  static SeqTable zero_st{};
+  const QkvOut& qo = qkv ? *qkv : zero_q;
+  const SeqTable& st = seqs ? *seqs : zero_st;
+  const dim3 grid(std::min(tiles, num_sms)), block(kThreads);
+  cudaError_t e;
+  if (epi == EPI_QKV)
+    e = launch_pdl(gemm_big_kernel<EPI_QKV>, grid, block, SMEM_BIG, stream, ma0, ma1,
+                   *s.b_map256, p, qo, st);
+  else if (epi == EPI_BF16)
+    e = launch_pdl(gemm_big_kernel<EPI_BF16>, grid, block, SMEM_BIG, stream, ma0, ma1,
+                   *s.b_map256, p, qo, st);
+  else
+    e = launch_pdl(gemm_big_kernel<EPI_F32>, grid, block, SMEM_BIG, stream, ma0, ma1,
+                   *s.b_map256, p, qo, st);
+  return (int)e;
+}
+
+}  // namespace
 }  // namespace df

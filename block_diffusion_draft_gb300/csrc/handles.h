@@ -51,7 +51,7 @@ struct dflash_attn {
   float* hidden_norm = nullptr;
   float2* rope = nullptr;
   int* err = nullptr;
-  CUtensorMap tm_qkv, tm_o, tm_fc;
+  CUtensorMap tm_qkv, tm_o, tm_fc, tm_qkv256, tm_o256, tm_fc256;
   // launch trace
   bool trace = false;
   struct Rec { int kind; cudaEvent_t e0, e1; };

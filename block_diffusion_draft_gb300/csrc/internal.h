@@ -65,6 +65,7 @@ struct GemmShape {
   const void* a0; int a0_rows;   // noise rows (or the only source)
   const void* a1; int a1_rows;   // context rows (may be 0)
   const CUtensorMap* b_map;      // weights, 128-row boxes, built at create
+  const CUtensorMap* b_map256;   // the same weights, 256-row boxes
   int n, k;
   int q_cols;                    // leading columns computed from A0 only
 };

@@ -105,7 +105,7 @@ extern "C" int dflash_ctx_project_noalloc(dflash_attn* a, const void* x, int row
     // previous call left, so clear them on this stream first
     e = cudaMemsetAsync(scr.counters, 0, cnt_bytes, s);
     if (e == cudaSuccess) {
-      df::GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, a->H, K, 0};
+      df::GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, &a->tm_fc256, a->H, K, 0};
       e = (cudaError_t)df::launch_gemm_bf16(gs, df::EPI_F32, z, a->H, nullptr, nullptr, scr,
                                             a->num_sms, a->err, s);
     }

@@ -79,12 +79,28 @@ def test_bf16_sliding_window_band():
     T.assert_close(got, ref, "bf16", "band step")
 
 
+def test_bf16_large_batch_persistent_gemm():
+    # 40 sequences: 640 block rows and ~400 context rows take the persistent
+    # 128 x 256-tile projection path
+    sp = small_bf16(batch=40)
+    sc = T.Scenario(sp, seed=12, capacity=256, check=[0, 17, 39])
+    n = [int(x) for x in np.random.default_rng(3).integers(0, 21, size=40)]
+    got, ref = sc.step(n)
+    T.assert_close(got, ref, "bf16", "batch 40")
+    sc.crop(n)
+    got, ref = sc.step([16] * 40)
+    T.assert_close(got, ref, "bf16", "batch 40 step 2")
+    for k, ko, v, vo in sc.compare_cache():
+        T.assert_close(k, ko, "bf16", "cache K")
+        T.assert_close(v, vo, "bf16", "cache V")
+
+
 def test_bf16_ctx_project_matches_oracle():
     sp = small_bf16()
     w = W.weights(sp, 5)
     cfg, lw = T.oracle_layer(sp, w)
     attn = T.gpu_layer(sp, w)
-    for rows in (1, 16, 200):
+    for rows in (1, 16, 200, 600):
         x = W.target_layer_rows(sp, 5, 0, rows, rows)
         y = attn.ctx_project(x.cuda())
         torch.cuda.synchronize()

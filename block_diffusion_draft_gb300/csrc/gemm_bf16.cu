@@ -58,6 +58,9 @@ struct Plan {
   int stages;
   uint32_t a_bytes;    // bytes per A stage (all boxes of one stage)
   int units_q;
+  int stream_k;        // persistent kernel: iteration ranges instead of tiles
+  int grid;            // persistent kernel: CTAs
+  long long iters;     // persistent kernel: tiles * n_kb
   int ldc;
   float* partial;
   int* counters;
@@ -443,6 +446,48 @@ constexpr int BNB = 256, STAGES_BIG = 4;
 constexpr uint32_t B_BIG = BNB * BK * 2;  // 32 KB
 constexpr size_t SMEM_BIG = 1024 + STAGES_BIG * (A_FULL + B_BIG) + 512;
 
+// Work of one persistent CTA as segments (tile, k-blocks [k0, k1)).  Plain
+// mode: whole tiles cta, cta + grid, ...  Stream-K mode: the CTA's share
+// [cta * iters / grid, (cta + 1) * iters / grid) of all (tile, k-block)
+// iterations; its first segment may start inside a tile and its last may
+// end inside one.  `slot` names where a partial segment's sums go (0: the
+// CTA's first segment, 1: a later one).
+struct SegIter {
+  long long pos, end, beg;
+};
+
+DF_DEV SegIter seg_begin(const Plan& p, int cta) {
+  SegIter it;
+  if (p.stream_k) {
+    it.beg = it.pos = (long long)cta * p.iters / p.grid;
+    it.end = (long long)(cta + 1) * p.iters / p.grid;
+  } else {
+    it.beg = it.pos = cta;
+    it.end = 0;
+  }
+  return it;
+}
+
+DF_DEV bool seg_next(const Plan& p, int tiles, SegIter& it, int& t, int& k0, int& k1,
+                     int& slot) {
+  if (p.stream_k) {
+    if (it.pos >= it.end) return false;
+    t = (int)(it.pos / p.n_kb);
+    k0 = (int)(it.pos - (long long)t * p.n_kb);
+    k1 = (int)min((long long)p.n_kb, k0 + (it.end - it.pos));
+    slot = it.pos == it.beg ? 0 : 1;
+    it.pos += k1 - k0;
+  } else {
+    if (it.pos >= tiles) return false;
+    t = (int)it.pos;
+    k0 = 0;
+    k1 = p.n_kb;
+    slot = 0;
+    it.pos += p.grid;
+  }
+  return true;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_big_kernel(const __grid_constant__ CUtensorMap tmA0,
@@ -462,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;       // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
@@ -498,13 +544,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = policy_evict_last();
       uint32_t it = 0;
       bool alive = true;
-      for (int t = blockIdx.x; t < tiles && alive; t += gridDim.x) {
+      SegIter si = seg_begin(p, blockIdx.x);
+      int t, k0, k1, slot;
+      while (alive && seg_next(p, tiles, si, t, k0, k1, slot)) {
         int m, n, sp;
         decode_unit(p, t, m, n, sp);
         const bool a0 = m < p.n_m0;
         const CUtensorMap* ma = a0 ? &tmA0 : &tmA1;
         const int a_row0 = (a0 ? m : m - p.n_m0) * BM;
-        for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
+        for (int kb = k0; kb < k1; ++kb, ++it) {
           const int s = it % STAGES_BIG;
           const uint32_t ph = (it / STAGES_BIG) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) {
@@ -522,12 +570,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(BM, BNB, false);
       uint32_t it = 0, tc = 0;
       bool alive = true;
-      for (int t = blockIdx.x; t < tiles && alive; t += gridDim.x, ++tc) {
+      SegIter si = seg_begin(p, blockIdx.x);
+      int t, k0, k1, slot;
+      for (; alive && seg_next(p, tiles, si, t, k0, k1, slot); ++tc) {
         const uint32_t buf = tc & 1, use = tc >> 1;
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * BNB;
-        for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
+        for (int kb = k0; kb < k1; ++kb, ++it) {
           const int s = it % STAGES_BIG;
           const uint32_t ph = (it / STAGES_BIG) & 1;
           if (!mbar_wait(&full[s], ph, abort_flag, p.err)) {
@@ -541,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_bf16(d, sdesc_sw128(a_base + kk * 32, 16, 1024),
                         sdesc_sw128(b_base + kk * 32, 16, 1024), idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
+                        (kb > k0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[s]);
         }
         tc_commit(&acc_full[buf]);
@@ -550,8 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int et = threadIdx.x - 64;
     uint32_t tc = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+    SegIter si = seg_begin(p, blockIdx.x);
+    int t, k0, k1, slot;
+    for (; seg_next(p, tiles, si, t, k0, k1, slot); ++tc) {
       int m, n, sp;
       decode_unit(p, t, m, n, sp);
       const uint32_t buf = tc & 1, use = tc >> 1;
@@ -561,6 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int src, srow;
       row_source(p, m, r, src, srow);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
+      const bool whole = k0 == 0 && k1 == p.n_kb;
+      // partial segments: sums of the valid rows go to this CTA's slot
+      float* my_part = p.partial + (((size_t)blockIdx.x * 2 + slot) * BM + r) * BNB;
 #pragma unroll 1
       for (int half = 0; half < BNB / HD; ++half) {
         float v[HD];
@@ -577,8 +633,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(&acc_empty[buf]);
         }
-        if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
+        if (whole) {
+          if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
+        } else if (src >= 0) {
+          float4* d4 = reinterpret_cast<float4*>(my_part + half * HD);
+#pragma unroll
+          for (int c4 = 0; c4 < HD / 4; ++c4)
+            __stcg(d4 + c4, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                                        v[4 * c4 + 3]));
+        }
       }
+      if (whole) continue;
+      // the CTA that completes the tile's k-blocks sums every contribution,
+      // in CTA order (deterministic), and runs the epilogue
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (et == 0) {
+        const int old = atomicAdd(p.counters + t, k1 - k0);
+        *last_flag = (old + (k1 - k0) == p.n_kb) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      const bool last = *last_flag != 0;
+      named_bar_sync(1, 128);  // everyone has read the flag before it is reused
+      if (!last) continue;
+      __threadfence();
+      const long long x = (long long)t * p.n_kb, y = x + p.n_kb - 1;
+      const int c_lo = (int)(((x + 1) * p.grid + p.iters - 1) / p.iters) - 1;
+      const int c_hi = (int)(((y + 1) * p.grid + p.iters - 1) / p.iters) - 1;
+#pragma unroll 1
+      for (int half = 0; half < BNB / HD; ++half) {
+        float v[HD];
+#pragma unroll
+        for (int i = 0; i < HD; ++i) v[i] = 0.f;
+        if (src >= 0) {
+          for (int c = c_lo; c <= c_hi; ++c) {
+            const long long bc = (long long)c * p.iters / p.grid;
+            const long long ec = (long long)(c + 1) * p.iters / p.grid;
+            if (bc == ec) continue;
+            const int sl = bc >= x ? 0 : 1;
+            const float4* pc = reinterpret_cast<const float4*>(
+                p.partial + (((size_t)c * 2 + sl) * BM + r) * BNB + half * HD);
+#pragma unroll
+            for (int c4 = 0; c4 < HD / 4; ++c4) {
+              const float4 u = __ldcg(pc + c4);
+              v[4 * c4] += u.x;
+              v[4 * c4 + 1] += u.y;
+              v[4 * c4 + 2] += u.z;
+              v[4 * c4 + 3] += u.w;
+            }
+          }
+          finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
+        }
+      }
+      if (et == 0) p.counters[t] = 0;
     }
   }
 
@@ -685,8 +792,14 @@ bool use_big(int rows0, int rows1, int n, int q_cols) {
   return m_tiles >= 4 && n % BNB == 0 && q_cols % BNB == 0;
 }
 
+int big_tiles(int rows0, int rows1, int n, int q_cols) {
+  const int m0 = (rows0 + BM - 1) / BM, m1 = (rows1 + BM - 1) / BM;
+  return (q_cols / BNB) * m0 + (n / BNB - q_cols / BNB) * (m0 + m1);
+}
+
 int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
-               const SeqTable* seqs, int num_sms, int* err, cudaStream_t stream);
+               const SeqTable* seqs, const GemmScratch& scr, int num_sms, int* err,
+               cudaStream_t stream);
 
 }  // namespace
 
@@ -710,8 +823,10 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
 size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_cols,
                           int num_sms, int* n_counters) {
   if (use_big(rows0, rows1, n, q_cols)) {
-    if (n_counters) *n_counters = 0;
-    return 0;
+    const int tiles = big_tiles(rows0, rows1, n, q_cols);
+    if (n_counters) *n_counters = tiles;
+    if (tiles >= 4 * num_sms) return 0;
+    return (size_t)num_sms * 2 * BM * BNB * sizeof(float);
   }
   Geometry g = geometry(epi, rows0, rows1, n, k, q_cols, num_sms);
   const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
@@ -733,7 +848,7 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   }
   if (s.k % BK != 0) return cudaErrorInvalidValue;
   if (use_big(s.a0_rows, s.a1_rows, s.n, s.q_cols))
-    return launch_big(s, epi, c, ldc, qkv, seqs, num_sms, err, stream);
+    return launch_big(s, epi, c, ldc, qkv, seqs, scr, num_sms, err, stream);
   Geometry g = geometry(epi, s.a0_rows, s.a1_rows, s.n, s.k, s.q_cols, num_sms);
   if (s.n % g.bn != 0 || s.q_cols % g.bn != 0) return cudaErrorInvalidValue;
   if (g.tiles == 0) return cudaSuccess;
@@ -799,7 +914,8 @@ namespace df {
 namespace {
 
 int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
-               const SeqTable* seqs, int num_sms, int* err, cudaStream_t stream) {
+               const SeqTable* seqs, const GemmScratch& scr, int num_sms, int* err,
+               cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaFuncSetAttribute(gemm_big_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -829,6 +945,17 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
   p.c = c;
   p.err = err;
   const int tiles = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
+  // few tiles per SM: balance (tile, k-block) iterations across all SMs
+  p.stream_k = tiles < 4 * num_sms;
+  p.grid = p.stream_k ? num_sms : std::min(tiles, num_sms);
+  p.iters = (long long)tiles * p.n_kb;
+  if (p.stream_k) {
+    if (scr.partial == nullptr || scr.n_counters < tiles ||
+        scr.partial_bytes < (size_t)p.grid * 2 * BM * BNB * sizeof(float))
+      return cudaErrorInvalidValue;
+    p.partial = scr.partial;
+    p.counters = scr.counters;
+  }
   CUtensorMap ma0, ma1;
   if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, BM) != 0) return cudaErrorInvalidValue;
   if (s.a1_rows > 0) {
@@ -840,7 +967,7 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
   static SeqTable zero_st{};
   const QkvOut& qo = qkv ? *qkv : zero_q;
   const SeqTable& st = seqs ? *seqs : zero_st;
-  const dim3 grid(std::min(tiles, num_sms)), block(kThreads);
+  const dim3 grid(p.grid), block(kThreads);
   cudaError_t e;
   if (epi == EPI_QKV)
     e = launch_pdl(gemm_big_kernel<EPI_QKV>, grid, block, SMEM_BIG, stream, ma0, ma1,

@@ -58,9 +58,7 @@ struct Plan {
   int stages;
   uint32_t a_bytes;    // bytes per A stage (all boxes of one stage)
   int units_q;
-  int stream_k;        // persistent kernel: iteration ranges instead of tiles
   int grid;            // persistent kernel: CTAs
-  long long iters;     // persistent kernel: tiles * n_kb
   int ldc;
   float* partial;
   int* counters;
@@ -446,46 +444,15 @@ constexpr int BNB = 256, STAGES_BIG = 4;
 constexpr uint32_t B_BIG = BNB * BK * 2;  // 32 KB
 constexpr size_t SMEM_BIG = 1024 + STAGES_BIG * (A_FULL + B_BIG) + 512;
 
-// Work of one persistent CTA as segments (tile, k-blocks [k0, k1)).  Plain
-// mode: whole tiles cta, cta + grid, ...  Stream-K mode: the CTA's share
-// [cta * iters / grid, (cta + 1) * iters / grid) of all (tile, k-block)
-// iterations; its first segment may start inside a tile and its last may
-// end inside one.  `slot` names where a partial segment's sums go (0: the
-// CTA's first segment, 1: a later one).
-struct SegIter {
-  long long pos, end, beg;
-};
-
-DF_DEV SegIter seg_begin(const Plan& p, int cta) {
-  SegIter it;
-  if (p.stream_k) {
-    it.beg = it.pos = (long long)cta * p.iters / p.grid;
-    it.end = (long long)(cta + 1) * p.iters / p.grid;
-  } else {
-    it.beg = it.pos = cta;
-    it.end = 0;
-  }
-  return it;
-}
-
-DF_DEV bool seg_next(const Plan& p, int tiles, SegIter& it, int& t, int& k0, int& k1,
-                     int& slot) {
-  if (p.stream_k) {
-    if (it.pos >= it.end) return false;
-    t = (int)(it.pos / p.n_kb);
-    k0 = (int)(it.pos - (long long)t * p.n_kb);
-    k1 = (int)min((long long)p.n_kb, k0 + (it.end - it.pos));
-    slot = it.pos == it.beg ? 0 : 1;
-    it.pos += k1 - k0;
-  } else {
-    if (it.pos >= tiles) return false;
-    t = (int)it.pos;
-    k0 = 0;
-    k1 = p.n_kb;
-    slot = 0;
-    it.pos += p.grid;
-  }
-  return true;
+// Work unit u of the persistent kernel: (m, n) tile and split of K.  Units
+// are ordered as in the decode-size kernel (groups of m-tiles, then n, then
+// split, then m), so the CTAs running at the same time share weight tiles.
+DF_DEV void big_unit(const Plan& p, int u, int& m, int& n, int& split, int& k0, int& k1,
+                     int& tile_id) {
+  decode_unit(p, u, m, n, split);
+  k0 = (int)((long long)split * p.n_kb / p.splits);
+  k1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
+  tile_id = n * (p.n_m0 + p.n_m1) + m;
 }
 
 template <int EPI>
@@ -510,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
+  const int units = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1) * p.splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES_BIG; ++s) {
@@ -544,11 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = policy_evict_last();
       uint32_t it = 0;
       bool alive = true;
-      SegIter si = seg_begin(p, blockIdx.x);
-      int t, k0, k1, slot;
-      while (alive && seg_next(p, tiles, si, t, k0, k1, slot)) {
-        int m, n, sp;
-        decode_unit(p, t, m, n, sp);
+      for (int u = blockIdx.x; alive && u < units; u += gridDim.x) {
+        int m, n, sp, k0, k1, tid;
+        big_unit(p, u, m, n, sp, k0, k1, tid);
         const bool a0 = m < p.n_m0;
         const CUtensorMap* ma = a0 ? &tmA0 : &tmA1;
         const int a_row0 = (a0 ? m : m - p.n_m0) * BM;
@@ -570,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(BM, BNB, false);
       uint32_t it = 0, tc = 0;
       bool alive = true;
-      SegIter si = seg_begin(p, blockIdx.x);
-      int t, k0, k1, slot;
-      for (; alive && seg_next(p, tiles, si, t, k0, k1, slot); ++tc) {
+      for (int u = blockIdx.x; alive && u < units; u += gridDim.x, ++tc) {
+        int m, n, sp, k0, k1, tid;
+        big_unit(p, u, m, n, sp, k0, k1, tid);
         const uint32_t buf = tc & 1, use = tc >> 1;
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
@@ -602,11 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     const int et = threadIdx.x - 64;
     uint32_t tc = 0;
-    SegIter si = seg_begin(p, blockIdx.x);
-    int t, k0, k1, slot;
-    for (; seg_next(p, tiles, si, t, k0, k1, slot); ++tc) {
-      int m, n, sp;
-      decode_unit(p, t, m, n, sp);
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
+      int m, n, sp, k0, k1, tid;
+      big_unit(p, u, m, n, sp, k0, k1, tid);
       const uint32_t buf = tc & 1, use = tc >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1, abort_flag, p.err)))
         break;
@@ -614,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int src, srow;
       row_source(p, m, r, src, srow);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
-      const bool whole = k0 == 0 && k1 == p.n_kb;
-      // partial segments: sums of the valid rows go to this CTA's slot
-      float* my_part = p.partial + (((size_t)blockIdx.x * 2 + slot) * BM + r) * BNB;
+      const bool whole = p.splits == 1;
+      // split units: sums of the valid rows go to the (tile, split) slot
+      float* my_part = p.partial + (((size_t)tid * p.splits + sp) * BM + r) * BNB;
 #pragma unroll 1
       for (int half = 0; half < BNB / HD; ++half) {
         float v[HD];
@@ -644,48 +607,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (whole) continue;
-      // the CTA that completes the tile's k-blocks sums every contribution,
-      // in CTA order (deterministic), and runs the epilogue
+      // the CTA that finishes a tile's last split sums every split in order
+      // (deterministic) and runs the epilogue
       __threadfence();
       named_bar_sync(1, 128);
       if (et == 0) {
-        const int old = atomicAdd(p.counters + t, k1 - k0);
-        *last_flag = (old + (k1 - k0) == p.n_kb) ? 1 : 0;
+        const int old = atomicAdd(p.counters + tid, 1);
+        *last_flag = (old == p.splits - 1) ? 1 : 0;
       }
       named_bar_sync(1, 128);
       const bool last = *last_flag != 0;
       named_bar_sync(1, 128);  // everyone has read the flag before it is reused
       if (!last) continue;
       __threadfence();
-      const long long x = (long long)t * p.n_kb, y = x + p.n_kb - 1;
-      const int c_lo = (int)(((x + 1) * p.grid + p.iters - 1) / p.iters) - 1;
-      const int c_hi = (int)(((y + 1) * p.grid + p.iters - 1) / p.iters) - 1;
 #pragma unroll 1
       for (int half = 0; half < BNB / HD; ++half) {
         float v[HD];
 #pragma unroll
         for (int i = 0; i < HD; ++i) v[i] = 0.f;
         if (src >= 0) {
-          for (int c = c_lo; c <= c_hi; ++c) {
-            const long long bc = (long long)c * p.iters / p.grid;
-            const long long ec = (long long)(c + 1) * p.iters / p.grid;
-            if (bc == ec) continue;
-            const int sl = bc >= x ? 0 : 1;
+          for (int c = 0; c < p.splits; ++c) {
             const float4* pc = reinterpret_cast<const float4*>(
-                p.partial + (((size_t)c * 2 + sl) * BM + r) * BNB + half * HD);
+                p.partial + (((size_t)tid * p.splits + c) * BM + r) * BNB + half * HD);
 #pragma unroll
             for (int c4 = 0; c4 < HD / 4; ++c4) {
-              const float4 u = __ldcg(pc + c4);
-              v[4 * c4] += u.x;
-              v[4 * c4 + 1] += u.y;
-              v[4 * c4 + 2] += u.z;
-              v[4 * c4 + 3] += u.w;
+              const float4 w4 = __ldcg(pc + c4);
+              v[4 * c4] += w4.x;
+              v[4 * c4 + 1] += w4.y;
+              v[4 * c4 + 2] += w4.z;
+              v[4 * c4 + 3] += w4.w;
             }
           }
           finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
         }
       }
-      if (et == 0) p.counters[t] = 0;
+      if (et == 0) p.counters[tid] = 0;
     }
   }
 
@@ -797,6 +753,25 @@ int big_tiles(int rows0, int rows1, int n, int q_cols) {
   return (q_cols / BNB) * m0 + (n / BNB - q_cols / BNB) * (m0 + m1);
 }
 
+// Splits of K for the persistent kernel: fill the SMs in whole waves, with
+// a small per-unit cost (no relaunch) plus the partial round trip.
+int big_splits(int tiles, int n_kb, int num_sms) {
+  if (tiles >= 2 * num_sms) return 1;
+  const double c_unit = 2.0, c_part = 4.0;
+  int best = 1;
+  double best_t = 1e30;
+  const int max_s = std::max(1, std::min(8, n_kb / 4));
+  for (int sp = 1; sp <= max_s; ++sp) {
+    const int waves = (tiles * sp + num_sms - 1) / num_sms;
+    const double t = waves * ((double)n_kb / sp + c_unit + (sp > 1 ? c_part : 0.0));
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = sp;
+    }
+  }
+  return best;
+}
+
 int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
                const SeqTable* seqs, const GemmScratch& scr, int num_sms, int* err,
                cudaStream_t stream);
@@ -824,9 +799,11 @@ size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_col
                           int num_sms, int* n_counters) {
   if (use_big(rows0, rows1, n, q_cols)) {
     const int tiles = big_tiles(rows0, rows1, n, q_cols);
-    if (n_counters) *n_counters = tiles;
-    if (tiles >= 4 * num_sms) return 0;
-    return (size_t)num_sms * 2 * BM * BNB * sizeof(float);
+    const int splits = big_splits(tiles, k / BK, num_sms);
+    const int dense = (n / BNB) * ((rows0 + BM - 1) / BM + (rows1 + BM - 1) / BM);
+    if (n_counters) *n_counters = dense;
+    if (splits == 1) return 0;
+    return (size_t)dense * splits * BM * BNB * sizeof(float);
   }
   Geometry g = geometry(epi, rows0, rows1, n, k, q_cols, num_sms);
   const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
@@ -937,21 +914,20 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
   p.n_tiles = s.n / BNB;
   p.n_q_tiles = s.q_cols / BNB;
   p.n_kb = s.k / BK;
-  p.splits = 1;
   p.stages = STAGES_BIG;
   p.a_bytes = A_FULL;
-  p.units_q = p.n_q_tiles * p.n_m0;
   p.ldc = ldc;
   p.c = c;
   p.err = err;
-  const int tiles = p.units_q + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
-  // few tiles per SM: balance (tile, k-block) iterations across all SMs
-  p.stream_k = tiles < 4 * num_sms;
-  p.grid = p.stream_k ? num_sms : std::min(tiles, num_sms);
-  p.iters = (long long)tiles * p.n_kb;
-  if (p.stream_k) {
-    if (scr.partial == nullptr || scr.n_counters < tiles ||
-        scr.partial_bytes < (size_t)p.grid * 2 * BM * BNB * sizeof(float))
+  const int tiles = p.n_q_tiles * p.n_m0 + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
+  p.splits = big_splits(tiles, p.n_kb, num_sms);
+  p.units_q = p.n_q_tiles * p.splits * p.n_m0;
+  const int units = tiles * p.splits;
+  p.grid = std::min(units, num_sms);
+  if (p.splits > 1) {
+    const int dense = p.n_tiles * (p.n_m0 + p.n_m1);
+    if (scr.partial == nullptr || scr.n_counters < dense ||
+        scr.partial_bytes < (size_t)dense * p.splits * BM * BNB * sizeof(float))
       return cudaErrorInvalidValue;
     p.partial = scr.partial;
     p.counters = scr.counters;

@@ -754,13 +754,15 @@ int big_tiles(int rows0, int rows1, int n, int q_cols) {
 }
 
 // Splits of K for the persistent kernel: fill the SMs in whole waves, with
-// a small per-unit cost (no relaunch) plus the partial round trip.
+// a small per-unit cost (no relaunch) plus the partial round trip.  At most
+// two splits: the last CTA of a tile reads every split's 128 KB partial
+// back, which costs more than the balance gains beyond two.
 int big_splits(int tiles, int n_kb, int num_sms) {
   if (tiles >= 2 * num_sms) return 1;
   const double c_unit = 2.0, c_part = 4.0;
   int best = 1;
   double best_t = 1e30;
-  const int max_s = std::max(1, std::min(8, n_kb / 4));
+  const int max_s = std::max(1, std::min(2, n_kb / 4));
   for (int sp = 1; sp <= max_s; ++sp) {
     const int waves = (tiles * sp + num_sms - 1) / num_sms;
     const double t = waves * ((double)n_kb / sp + c_unit + (sp > 1 ? c_part : 0.0));

@@ -93,6 +93,21 @@ DF_DEV void decode_unit(const Plan& p, int u, int& m_tile, int& n_tile, int& spl
   }
 }
 
+// Decode-size kernel: unit u is split (u % splits) of tile (u / splits), so
+// the splits of one tile are consecutive blocks (one cluster); tiles follow
+// the grouped order.
+DF_DEV void decode_tile_split(const Plan& p, int u, int& m_tile, int& n_tile, int& split) {
+  split = u % p.splits;
+  const int t = u / p.splits, tq = p.n_q_tiles * p.n_m0;
+  int dummy;
+  if (t < tq) {
+    decode_region(t, p.n_m0, p.n_q_tiles, 1, m_tile, n_tile, dummy);
+  } else {
+    decode_region(t - tq, p.n_m0 + p.n_m1, p.n_tiles - p.n_q_tiles, 1, m_tile, n_tile, dummy);
+    n_tile += p.n_q_tiles;
+  }
+}
+
 // Which source row accumulator row r of tile m_tile holds: src 0 = A0
 // (block rows), 1 = A1 (context rows), -1 = no row.
 DF_DEV void row_source(const Plan& p, int m_tile, int r, int& src, int& row) {
@@ -246,18 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accb = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int m_tile, n_tile, split;
-  decode_unit(p, blockIdx.x, m_tile, n_tile, split);
+  decode_tile_split(p, blockIdx.x, m_tile, n_tile, split);
   const int kb0 = (int)((long long)split * p.n_kb / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
   const int nkb = kb1 - kb0;
   const bool from_a0 = m_tile < p.n_m0;
   const int a_row0 = (from_a0 ? m_tile : m_tile - p.n_m0) * BM;
   const int n0 = n_tile * BN;
-  const int tile_id = n_tile * (p.n_m0 + p.n_m1) + m_tile;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -334,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const int et = threadIdx.x - 64;  // 0..127 within the epilogue warps
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     int src, srow;
     row_source(p, m_tile, r, src, srow);
@@ -348,82 +360,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[c * 32 + i] = ok ? t[i] : 0.f;
     }
-    bool last = true;
-    if (p.splits > 1) {
-      // valid rows of this split's partial, row-major [row][BN]
-      float* tile_part = p.partial + (size_t)tile_id * p.splits * (BM * BN);
-      if (src >= 0) {
-        float4* mine = reinterpret_cast<float4*>(tile_part + (size_t)split * (BM * BN) +
-                                                 (size_t)r * BN);
+    if (p.splits == 1) {
+      if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
+    } else if (src >= 0) {
+      // park the valid rows in this CTA's (now idle) stage buffers, swizzled
+      float4* red = reinterpret_cast<float4*>(smem);
 #pragma unroll
-        for (int c4 = 0; c4 < C4; ++c4)
-          __stcg(mine + c4, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                                        v[4 * c4 + 3]));
-      }
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (et == 0) {
-        const int old = atomicAdd(p.counters + tile_id, 1);
-        *last_flag = (old == p.splits - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, 128);
-      last = *last_flag != 0;
-      if (last) {
-        // sum the splits in fixed order, 8 row-chunks per thread at a time,
-        // into a swizzled fp32 tile in the (now idle) stage buffers
-        __threadfence();
-        float4* stile = reinterpret_cast<float4*>(smem);
-        constexpr int ITEMS = BM * C4;
-        for (int it0 = et; it0 < ITEMS; it0 += 128 * 8) {
-          float4 acc[8];
-          int rows[8];
-          bool use[8];
+      for (int c4 = 0; c4 < C4; ++c4)
+        red[r * C4 + (c4 ^ (r & (C4 - 1)))] =
+            make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+    }
+  }
+
+  if (p.splits > 1) {
+    // The splits of this tile are one thread-block cluster.  Each CTA sums
+    // every r-th valid row (r % splits == its rank) from all CTAs' shared
+    // memory in rank order, so the result does not depend on timing, and
+    // runs the epilogue for those rows.
+    cluster_sync();
+    if (warp >= 2) {
+      const int r = (warp & 3) * 32 + lane;
+      int src, srow;
+      row_source(p, m_tile, r, src, srow);
+      if (src >= 0 && (uint32_t)(r % p.splits) == cluster_ctarank()) {
+        float v[BN];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int it = it0 + j * 128;
-            rows[j] = it / C4;
-            int sj, rj;
-            row_source(p, m_tile, rows[j], sj, rj);
-            use[j] = it < ITEMS && sj >= 0;
-            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          for (int s2 = 0; s2 < p.splits; ++s2) {
-            const float4* part =
-                reinterpret_cast<const float4*>(tile_part + (size_t)s2 * (BM * BN));
-            float4 t[8];
+        for (int i = 0; i < BN; ++i) v[i] = 0.f;
+        const uint32_t row_addr = smem_u32(smem) + (uint32_t)r * C4 * 16;
+        for (int c = 0; c < p.splits; ++c) {
+          const uint32_t remote = cluster_map(row_addr, (uint32_t)c);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              t[j] = use[j] ? __ldcg(part + it0 + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              acc[j].x += t[j].x;
-              acc[j].y += t[j].y;
-              acc[j].z += t[j].z;
-              acc[j].w += t[j].w;
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int it = it0 + j * 128;
-            if (use[j]) {
-              const int c4 = it - rows[j] * C4;
-              stile[rows[j] * C4 + (c4 ^ (rows[j] & (C4 - 1)))] = acc[j];
-            }
+          for (int c4 = 0; c4 < C4; ++c4) {
+            const float4 t = ld_cluster_f4(remote + (uint32_t)((c4 ^ (r & (C4 - 1))) * 16));
+            v[4 * c4] += t.x;
+            v[4 * c4 + 1] += t.y;
+            v[4 * c4 + 2] += t.z;
+            v[4 * c4 + 3] += t.w;
           }
         }
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int c4 = 0; c4 < C4; ++c4) {
-          const float4 t = stile[r * C4 + (c4 ^ (r & (C4 - 1)))];
-          v[4 * c4] = t.x;
-          v[4 * c4 + 1] = t.y;
-          v[4 * c4 + 2] = t.z;
-          v[4 * c4 + 3] = t.w;
-        }
-        if (et == 0) p.counters[tile_id] = 0;
+        finish_row<EPI>(p, qo, st, v, src, srow, n0);
       }
     }
-    if (last && src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
+    cluster_sync();  // no CTA leaves while the others still read its rows
   }
 
   tc_fence_before();
@@ -673,13 +651,14 @@ EncodeTiledFn encode_fn() {
 }
 
 // Split count minimising (waves) x (per-unit time), per-unit time in
-// k-block units plus a fixed cost per CTA and a cost for the partial tile.
+// k-block units plus a fixed cost per CTA and a cost for the cluster merge.
+// At most 8 splits (a portable cluster).
 int choose_splits(int tiles, int n_kb, int num_sms) {
   if (tiles >= num_sms) return 1;
-  const double c_cta = 6.0, c_part = 3.0;
+  const double c_cta = 6.0, c_part = 2.0;
   int best = 1;
   double best_t = 1e30;
-  const int max_s = std::max(1, std::min(16, n_kb / 2));
+  const int max_s = std::max(1, std::min(8, n_kb / 2));
   for (int s = 1; s <= max_s; ++s) {
     const int waves = (tiles * s + num_sms - 1) / num_sms;
     const double t = waves * ((double)n_kb / s + c_cta + (s > 1 ? c_part : 0.0));
@@ -807,11 +786,11 @@ size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_col
     if (splits == 1) return 0;
     return (size_t)dense * splits * BM * BNB * sizeof(float);
   }
-  Geometry g = geometry(epi, rows0, rows1, n, k, q_cols, num_sms);
-  const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
-  if (n_counters) *n_counters = dense_tiles;
-  if (g.splits <= 1) return 0;
-  return (size_t)dense_tiles * g.splits * BM * g.bn * sizeof(float);
+  // the decode-size kernel merges its splits inside a cluster: no scratch
+  (void)epi;
+  (void)k;
+  if (n_counters) *n_counters = 0;
+  return 0;
 }
 
 int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
@@ -851,12 +830,6 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   p.err = err;
   p.partial = scr.partial;
   p.counters = scr.counters;
-  if (g.splits > 1) {
-    const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * g.bn * 4;
-    if (scr.partial == nullptr || scr.partial_bytes < need ||
-        scr.n_counters < g.n_tiles * (g.n_m0 + g.n_m1))
-      return cudaErrorInvalidValue;
-  }
   CUtensorMap ma0, ma1;
   if (make_tmap_bf16_rows(&ma0, s.a0, s.a0_rows, s.k, g.box0) != 0)
     return cudaErrorInvalidValue;
@@ -873,16 +846,17 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   const dim3 grid(g.tiles * g.splits), block(kThreads);
   const size_t smem = smem_bytes(g);
   cudaError_t e;
+  const unsigned cl = (unsigned)g.splits;
   if (epi == EPI_QKV) {
     if (g.bn != 128) return cudaErrorInvalidValue;
-    e = launch_pdl(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, ma0, ma1,
-                   *s.b_map, p, qo, st);
+    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, cl, ma0,
+                           ma1, *s.b_map, p, qo, st);
   } else if (epi == EPI_BF16) {
-    e = launch_pdl(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream, ma0, ma1,
-                   *s.b_map, p, qo, st);
+    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream, cl, ma0,
+                           ma1, *s.b_map, p, qo, st);
   } else {
-    e = launch_pdl(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream, ma0, ma1,
-                   *s.b_map, p, qo, st);
+    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream, cl, ma0,
+                           ma1, *s.b_map, p, qo, st);
   }
   return (int)e;
 }

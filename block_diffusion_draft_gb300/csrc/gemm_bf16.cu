@@ -723,8 +723,7 @@ void set_smem_attr() {
 
 // many token rows and 256-aligned column regions: the persistent kernel
 bool use_big(int rows0, int rows1, int n, int q_cols) {
-  const int m_tiles = (rows0 + BM - 1) / BM + (rows1 + BM - 1) / BM;
-  return m_tiles >= 4 && n % BNB == 0 && q_cols % BNB == 0;
+  return rows0 + rows1 > BM && n % BNB == 0 && q_cols % BNB == 0;
 }
 
 int big_tiles(int rows0, int rows1, int n, int q_cols) {
@@ -733,18 +732,17 @@ int big_tiles(int rows0, int rows1, int n, int q_cols) {
 }
 
 // Splits of K for the persistent kernel: fill the SMs in whole waves, with
-// a small per-unit cost (no relaunch) plus the partial round trip.  At most
-// two splits: the last CTA of a tile reads every split's 128 KB partial
-// back, which costs more than the balance gains beyond two.
+// a small per-unit cost (no relaunch); the last CTA of a tile reads every
+// split's 128 KB partial back, a cost that grows with the split count.
 int big_splits(int tiles, int n_kb, int num_sms) {
   if (tiles >= 2 * num_sms) return 1;
-  const double c_unit = 2.0, c_part = 4.0;
+  const double c_unit = 2.0, c_merge = 8.0;
   int best = 1;
   double best_t = 1e30;
-  const int max_s = std::max(1, std::min(2, n_kb / 4));
+  const int max_s = std::max(1, std::min(4, n_kb / 4));
   for (int sp = 1; sp <= max_s; ++sp) {
     const int waves = (tiles * sp + num_sms - 1) / num_sms;
-    const double t = waves * ((double)n_kb / sp + c_unit + (sp > 1 ? c_part : 0.0));
+    const double t = waves * ((double)n_kb / sp + c_unit) + (sp > 1 ? c_merge * sp : 0.0);
     if (t < best_t - 1e-9) {
       best_t = t;
       best = sp;

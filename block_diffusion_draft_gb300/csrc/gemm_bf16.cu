@@ -556,8 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_source(p, m, r, src, srow);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
       const bool whole = p.splits == 1;
-      // split units: sums of the valid rows go to the (tile, split) slot
-      float* my_part = p.partial + (((size_t)tid * p.splits + sp) * BM + r) * BNB;
+      // split units: sums of the valid rows go to the (tile, split) slot,
+      // laid out [column chunk of 4][row] so a warp's access is contiguous
+      float4* my_part =
+          reinterpret_cast<float4*>(p.partial) + ((size_t)tid * p.splits + sp) * (BM * BNB / 4);
 #pragma unroll 1
       for (int half = 0; half < BNB / HD; ++half) {
         float v[HD];
@@ -577,11 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (whole) {
           if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
         } else if (src >= 0) {
-          float4* d4 = reinterpret_cast<float4*>(my_part + half * HD);
 #pragma unroll
           for (int c4 = 0; c4 < HD / 4; ++c4)
-            __stcg(d4 + c4, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                                        v[4 * c4 + 3]));
+            __stcg(my_part + (half * (HD / 4) + c4) * BM + r,
+                   make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
         }
       }
       if (whole) continue;
@@ -605,11 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < HD; ++i) v[i] = 0.f;
         if (src >= 0) {
           for (int c = 0; c < p.splits; ++c) {
-            const float4* pc = reinterpret_cast<const float4*>(
-                p.partial + (((size_t)tid * p.splits + c) * BM + r) * BNB + half * HD);
+            const float4* pc = reinterpret_cast<const float4*>(p.partial) +
+                               ((size_t)tid * p.splits + c) * (BM * BNB / 4) +
+                               (size_t)half * (HD / 4) * BM + r;
 #pragma unroll
             for (int c4 = 0; c4 < HD / 4; ++c4) {
-              const float4 w4 = __ldcg(pc + c4);
+              const float4 w4 = __ldcg(pc + c4 * BM);
               v[4 * c4] += w4.x;
               v[4 * c4 + 1] += w4.y;
               v[4 * c4 + 2] += w4.z;

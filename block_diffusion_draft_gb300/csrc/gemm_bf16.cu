@@ -53,6 +53,7 @@ constexpr int M_GROUP = 16;                // m-tiles sharing one pass over N
 struct Plan {
   int a0_rows, a1_rows, n_m0, n_m1;
   int merged;          // 1: one tile holds A0 rows then A1 rows
+  int cluster;         // decode-size kernel: splits merge inside a cluster
   int box0, box1;      // rows of the A0 / A1 boxes
   int n_tiles, n_q_tiles, n_kb, splits;
   int stages;
@@ -261,10 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accb = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int m_tile, n_tile, split;
   decode_tile_split(p, blockIdx.x, m_tile, n_tile, split);
+  const int tile_id = n_tile * (p.n_m0 + p.n_m1) + m_tile;
   const int kb0 = (int)((long long)split * p.n_kb / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
   const int nkb = kb1 - kb0;
@@ -362,6 +365,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (p.splits == 1) {
       if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
+    } else if (!p.cluster) {
+      // global merge: every split writes the valid rows of its fp32 partial
+      // ([row][BN]); the last CTA of the tile (atomic counter) sums them in
+      // split order, spreading the loads over its 128 epilogue threads and
+      // staging the sums through shared memory
+      const int et = threadIdx.x - 64;
+      float* tile_part = p.partial + (size_t)tile_id * p.splits * (BM * BN);
+      if (src >= 0) {
+        float4* mine = reinterpret_cast<float4*>(tile_part + (size_t)split * (BM * BN) +
+                                                 (size_t)r * BN);
+#pragma unroll
+        for (int c4 = 0; c4 < C4; ++c4)
+          __stcg(mine + c4, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                                        v[4 * c4 + 3]));
+      }
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (et == 0) {
+        const int old = atomicAdd(p.counters + tile_id, 1);
+        *last_flag = (old == p.splits - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (*last_flag) {
+        __threadfence();
+        float4* stile = reinterpret_cast<float4*>(smem);
+        constexpr int ITEMS = BM * C4;
+        for (int it0 = et; it0 < ITEMS; it0 += 128 * 8) {
+          float4 acc[8];
+          int rows[8];
+          bool use[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int it = it0 + j * 128;
+            rows[j] = it / C4;
+            int sj, rj;
+            row_source(p, m_tile, rows[j], sj, rj);
+            use[j] = it < ITEMS && sj >= 0;
+            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int s2 = 0; s2 < p.splits; ++s2) {
+            const float4* part =
+                reinterpret_cast<const float4*>(tile_part + (size_t)s2 * (BM * BN));
+            float4 t[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              t[j] = use[j] ? __ldcg(part + it0 + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc[j].x += t[j].x;
+              acc[j].y += t[j].y;
+              acc[j].z += t[j].z;
+              acc[j].w += t[j].w;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int it = it0 + j * 128;
+            if (use[j]) {
+              const int c4 = it - rows[j] * C4;
+              stile[rows[j] * C4 + (c4 ^ (rows[j] & (C4 - 1)))] = acc[j];
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+        if (src >= 0) {
+#pragma unroll
+          for (int c4 = 0; c4 < C4; ++c4) {
+            const float4 t = stile[r * C4 + (c4 ^ (r & (C4 - 1)))];
+            v[4 * c4] = t.x;
+            v[4 * c4 + 1] = t.y;
+            v[4 * c4 + 2] = t.z;
+            v[4 * c4 + 3] = t.w;
+          }
+          finish_row<EPI>(p, qo, st, v, src, srow, n0);
+        }
+        if (et == 0) p.counters[tile_id] = 0;
+      }
     } else if (src >= 0) {
       // park the valid rows in this CTA's (now idle) stage buffers, swizzled
       float4* red = reinterpret_cast<float4*>(smem);
@@ -372,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (p.splits > 1) {
+  if (p.splits > 1 && p.cluster) {
     // The splits of this tile are one thread-block cluster.  Each CTA sums
     // every r-th valid row (r % splits == its rank) from all CTAs' shared
     // memory in rank order, so the result does not depend on timing, and
@@ -786,11 +866,16 @@ size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_col
     if (splits == 1) return 0;
     return (size_t)dense * splits * BM * BNB * sizeof(float);
   }
-  // the decode-size kernel merges its splits inside a cluster: no scratch
-  (void)epi;
-  (void)k;
-  if (n_counters) *n_counters = 0;
-  return 0;
+  // plain epilogues merge their splits inside a cluster (no scratch); the
+  // QKV epilogue merges through global partials
+  Geometry g = geometry(epi, rows0, rows1, n, k, q_cols, num_sms);
+  const int dense_tiles = g.n_tiles * (g.n_m0 + g.n_m1);
+  if (epi != EPI_QKV || g.splits <= 1) {
+    if (n_counters) *n_counters = 0;
+    return 0;
+  }
+  if (n_counters) *n_counters = dense_tiles;
+  return (size_t)dense_tiles * g.splits * BM * g.bn * sizeof(float);
 }
 
 int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
@@ -816,6 +901,16 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   p.n_m0 = g.n_m0;
   p.n_m1 = g.n_m1;
   p.merged = g.merged;
+  // plain epilogues merge splits in a cluster; the QKV epilogue (heavier,
+  // and 3-CTA clusters schedule poorly behind the previous kernel) merges
+  // through global partials
+  p.cluster = epi != EPI_QKV;
+  if (g.splits > 1 && !p.cluster) {
+    const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * g.bn * 4;
+    if (scr.partial == nullptr || scr.partial_bytes < need ||
+        scr.n_counters < g.n_tiles * (g.n_m0 + g.n_m1))
+      return cudaErrorInvalidValue;
+  }
   p.box0 = g.box0;
   p.box1 = g.box1;
   p.n_tiles = g.n_tiles;
@@ -846,7 +941,7 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   const dim3 grid(g.tiles * g.splits), block(kThreads);
   const size_t smem = smem_bytes(g);
   cudaError_t e;
-  const unsigned cl = (unsigned)g.splits;
+  const unsigned cl = p.cluster ? (unsigned)g.splits : 1u;
   if (epi == EPI_QKV) {
     if (g.bn != 128) return cudaErrorInvalidValue;
     e = launch_pdl_cluster(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, cl, ma0,

@@ -475,9 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the split partials of one (sequence, kv head): 8 query rows per CTA,
-// one thread per (row, 4 output columns), partials read 8 splits at a time
-// with an online log-sum-exp rescale.  Pairs whose keys fit one unit were
-// finished by the attention kernel and are skipped.
+// thread t takes output columns 4(t / 8) .. +3 of row t % 8, so a warp reads
+// four 128-byte runs of the [unit][column chunk][row] partials.  Two passes:
+// the largest running max over the splits, then the rescaled sums, each over
+// independent loads.  Pairs whose keys fit one unit were finished by the
+// attention kernel and are skipped.
 __global__ void __launch_bounds__(256)
     attn_combine_kernel(const __grid_constant__ AttnArgs a,
                         const __grid_constant__ AttnSeqs sq) {
@@ -488,49 +490,31 @@ __global__ void __launch_bounds__(256)
   const int b = pair / a.n_kv, h = pair - b * a.n_kv;
   const int nch = sq.n_chunks[b];
   if (nch <= 1) return;
-  const int r = (blockIdx.x - pair * groups_per_pair) * 8 + (threadIdx.x >> 5);
-  const int c4 = threadIdx.x & 31;
+  const int c4 = threadIdx.x >> 3;
+  const int r = (blockIdx.x - pair * groups_per_pair) * 8 + (threadIdx.x & 7);
   if (r >= rows_pair) return;
   const size_t base = (size_t)sq.unit_off[b] + (size_t)h * nch;
+  const float* ml = a.part_ml + base * 256 + r;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + base * 128 * HD) + c4 * 128 + r;
   grid_dep_wait();
-  float M = -INFINITY, L = 0.f;
+  float M = -INFINITY;
+#pragma unroll 8
+  for (int u = 0; u < nch; ++u) M = fmaxf(M, __ldcg(ml + (size_t)u * 256));
+  float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < nch; c0 += 8) {
-    float mv[8], lv[8];
-    float4 tv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const size_t u = base + c0 + j;
-      if (c0 + j < nch) {
-        mv[j] = __ldcg(a.part_ml + u * 256 + r);
-        lv[j] = __ldcg(a.part_ml + u * 256 + 128 + r);
-        tv[j] = __ldcg(reinterpret_cast<const float4*>(a.part_o + u * 128 * HD) + c4 * 128 + r);
-      } else {
-        mv[j] = -INFINITY;
-        lv[j] = 0.f;
-        tv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+  if (M != -INFINITY) {
+#pragma unroll 8
+    for (int u = 0; u < nch; ++u) {
+      const float m = __ldcg(ml + (size_t)u * 256);
+      const float l = __ldcg(ml + (size_t)u * 256 + 128);
+      const float4 t = __ldcg(po + (size_t)u * (128 * HD / 4));
+      const float f = m == -INFINITY ? 0.f : fast_exp2(m - M);
+      L += f * l;
+      acc.x += f * t.x;
+      acc.y += f * t.y;
+      acc.z += f * t.z;
+      acc.w += f * t.w;
     }
-    float bm = M;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) bm = fmaxf(bm, mv[j]);
-    if (bm == -INFINITY) continue;
-    const float sc = M == -INFINITY ? 0.f : fast_exp2(M - bm);
-    L *= sc;
-    acc.x *= sc;
-    acc.y *= sc;
-    acc.z *= sc;
-    acc.w *= sc;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float f = mv[j] == -INFINITY ? 0.f : fast_exp2(mv[j] - bm);
-      L += f * lv[j];
-      acc.x += f * tv[j].x;
-      acc.y += f * tv[j].y;
-      acc.z += f * tv[j].z;
-      acc.w += f * tv[j].w;
-    }
-    M = bm;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int gi = r / a.q_len, t = r - gi * a.q_len;

@@ -43,6 +43,7 @@ namespace df {
 namespace {
 
 constexpr int BM = 128, BK = 64, MAX_STAGES = 32;
+constexpr int MAX_SPLITS = 8;               // K splits of the decode-size kernel
 constexpr int kThreads = 192;
 constexpr uint32_t A_FULL = BM * BK * 2;   // 16 KB: what one MMA reads of A
 constexpr size_t SMEM_LIMIT = 232448;      // per-CTA opt-in maximum
@@ -165,8 +166,78 @@ DF_DEV void norm_rope(float* v, const float* w, float eps, const float2* rope_ro
   }
 }
 
-// Final epilogue of one accumulator row: `v` holds 128 columns starting at
-// output column n0 for source row (src, srow).
+// Where one accumulator row of a QKV tile goes.  kind: 0 = nowhere (a
+// context row of a query tile: queries exist for block rows only), 1 = Q
+// (per-head RMSNorm + RoPE + scale), 2 = K (RMSNorm + RoPE), 3 = V (copy).
+struct QkvTarget {
+  int kind;
+  int pos_idx;             // index into the positions array
+  __nv_bfloat16* dst;      // the 128-value bf16 destination row
+};
+
+DF_DEV QkvTarget qkv_target(const QkvOut& qo, const SeqTable& st, int src, int srow,
+                            int n0) {
+  int b, pos_idx, crow, t = 0;
+  if (src == 0) {  // noise (block) row
+    b = srow / st.q_len;
+    t = srow - b * st.q_len;
+    const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
+    pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
+    crow = st.cache_len[b] + nb + t;
+  } else {  // new context row: find its sequence
+    int lo = 0, hi = st.n;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (st.ctx_off[mid] <= srow) lo = mid; else hi = mid;
+    }
+    b = lo;
+    const int rr = srow - st.ctx_off[b];
+    pos_idx = st.ctx_off[b] + b * st.q_len + rr;
+    crow = st.cache_len[b] + rr;
+  }
+  const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
+  QkvTarget g;
+  g.pos_idx = pos_idx;
+  if (n0 < q_cols) {
+    if (src != 0) {
+      g.kind = 0;
+      g.dst = nullptr;
+      return g;
+    }
+    const int hq = n0 / HD;
+    const int h = hq / qo.groups, gi = hq - h * qo.groups;
+    const int nblk = st.q_len / qo.q_block;
+    const int blk = t / qo.q_block, tt = t - blk * qo.q_block;
+    const size_t qrow =
+        ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) * qo.q_block + tt;
+    g.kind = 1;
+    g.dst = reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD;
+  } else if (n0 < q_cols + kv_cols) {
+    const int h = (n0 - q_cols) / HD;
+    g.kind = 2;
+    g.dst = reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
+            (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD;
+  } else {
+    const int h = (n0 - q_cols - kv_cols) / HD;
+    g.kind = 3;
+    g.dst = reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
+            (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD;
+  }
+  return g;
+}
+
+// the row's rotary position, out-of-range positions reported and read as 0
+DF_DEV int checked_position(const QkvOut& qo, int pos_idx, int* err) {
+  int pos = qo.positions[pos_idx];
+  if (pos < 0 || pos >= qo.max_pos) {
+    record_error(err, 2 /* DFLASH_DEV_POSITION */);
+    pos = 0;
+  }
+  return pos;
+}
+
+// Final epilogue of one accumulator row held by one thread: `v` holds 128
+// columns starting at output column n0 for source row (src, srow).
 template <int EPI>
 DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, float* v,
                        int src, int srow, int n0) {
@@ -183,58 +254,110 @@ DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, floa
         d4[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
     }
   } else {
-    // ---------------- fused QKV epilogue: one head (128 columns) per tile
-    int b, pos_idx, crow, t = 0;
-    if (src == 0) {  // noise (block) row
-      b = srow / st.q_len;
-      t = srow - b * st.q_len;
-      const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
-      pos_idx = st.ctx_off[b + 1] + b * st.q_len + t;
-      crow = st.cache_len[b] + nb + t;
-    } else {  // new context row: find its sequence
-      int lo = 0, hi = st.n;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (st.ctx_off[mid] <= srow) lo = mid; else hi = mid;
-      }
-      b = lo;
-      const int rr = srow - st.ctx_off[b];
-      pos_idx = st.ctx_off[b] + b * st.q_len + rr;
-      crow = st.cache_len[b] + rr;
+    // fused QKV epilogue: one head (128 columns) per tile
+    const QkvTarget g = qkv_target(qo, st, src, srow, n0);
+    if (g.kind == 0) return;
+    if (g.kind != 3) {
+      const int pos = checked_position(qo, g.pos_idx, p.err);
+      norm_rope(v, g.kind == 1 ? qo.q_norm : qo.k_norm, qo.eps,
+                qo.rope + (size_t)pos * (HD / 2), g.kind == 1 ? qo.q_scale : 1.f);
     }
-    const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
-    if (n0 < q_cols + kv_cols) {
-      const bool is_q = n0 < q_cols;
-      if (!is_q || src == 0) {  // queries exist for block rows only
-        int pos = qo.positions[pos_idx];
+    store_bf16(g.dst, v, HD);
+  }
+}
+
+// The same epilogue with one row spread over a warp: lane l holds columns
+// 4l .. 4l+3.  The RMSNorm sum is a butterfly over the warp, and the RoPE
+// partner of column j < 64 (column j + 64) sits 16 lanes away.
+DF_DEV float4 warp_norm_rope(float4 x, float4 w4, float eps, const float2* rope_row,
+                             float scale, int lane) {
+  float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = rsqrtf(ss * (1.f / HD) + eps);
+  x.x *= inv * w4.x;
+  x.y *= inv * w4.y;
+  x.z *= inv * w4.z;
+  x.w *= inv * w4.w;
+  float4 y;
+  y.x = __shfl_xor_sync(0xffffffffu, x.x, 16);
+  y.y = __shfl_xor_sync(0xffffffffu, x.y, 16);
+  y.z = __shfl_xor_sync(0xffffffffu, x.z, 16);
+  y.w = __shfl_xor_sync(0xffffffffu, x.w, 16);
+  // (cos, sin) of pairs 4(l % 16) .. 4(l % 16) + 3
+  const float4* r4 = reinterpret_cast<const float4*>(rope_row) + 2 * (lane & 15);
+  const float4 c0 = __ldg(r4), c1 = __ldg(r4 + 1);
+  // first half: a' = a cos - b sin; second half: b' = b cos + a sin
+  const float sg = lane < 16 ? -1.f : 1.f;
+  float4 o;
+  o.x = (x.x * c0.x + sg * y.x * c0.y) * scale;
+  o.y = (x.y * c0.z + sg * y.y * c0.w) * scale;
+  o.z = (x.z * c1.x + sg * y.z * c1.y) * scale;
+  o.w = (x.w * c1.z + sg * y.w * c1.w) * scale;
+  return o;
+}
+
+// Warp wq of the decode-size kernel's QKV epilogue finishes rows wq, wq + 4,
+// wq + 8 ... of the tile, four at a time so that their loads overlap.  A row
+// is read from the shared-memory tile (one split) or summed over the splits'
+// global partials in split order.  Lane l holds the target of row wq + 4l
+// (`lk` kind, `ld` destination, `lp` position), worked out while the main
+// loop ran; the rows' targets are broadcast from there.
+DF_DEV void qkv_finish_warp(const Plan& p, const QkvOut& qo, int wq, int lane, float4 w4,
+                            int lk, __nv_bfloat16* ld, int lp, const float4* stile,
+                            const float* tile_part) {
+  constexpr int C4 = HD / 4;
+  const int last_j = __reduce_max_sync(0xffffffffu, lk != 0 ? lane : -1);
+  for (int j0 = 0; j0 <= last_j; j0 += 4) {
+    int kind[4];
+    float4 x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rr = wq + 4 * (j0 + i);
+      kind[i] = __shfl_sync(0xffffffffu, lk, (j0 + i) & 31);
+      if (j0 + i >= 32) kind[i] = 0;
+      x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kind[i] != 0 && stile != nullptr) x[i] = stile[rr * C4 + (lane ^ (rr & (C4 - 1)))];
+    }
+    if (stile == nullptr) {
+#pragma unroll
+      for (int sp = 0; sp < MAX_SPLITS; ++sp) {
+        if (sp < p.splits) {
+          const float4* part = reinterpret_cast<const float4*>(tile_part + (size_t)sp * (BM * HD));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (kind[i] != 0) {
+              const float4 t = __ldcg(part + (wq + 4 * (j0 + i)) * C4 + lane);
+              x[i].x += t.x;
+              x[i].y += t.y;
+              x[i].z += t.z;
+              x[i].w += t.w;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int src_lane = (j0 + i) & 31;
+      const int pos_raw = __shfl_sync(0xffffffffu, lp, src_lane);
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(ld), src_lane));
+      if (kind[i] == 0) continue;
+      float4 o = x[i];
+      if (kind[i] != 3) {
+        int pos = pos_raw;
         if (pos < 0 || pos >= qo.max_pos) {
-          record_error(p.err, 2 /* DFLASH_DEV_POSITION */);
+          if (lane == 0) record_error(p.err, 2 /* DFLASH_DEV_POSITION */);
           pos = 0;
         }
-        const float2* rope_row = qo.rope + (size_t)pos * (HD / 2);
-        if (is_q) {
-          const int hq = n0 / HD;
-          const int h = hq / qo.groups, gi = hq - h * qo.groups;
-          const int nblk = st.q_len / qo.q_block;
-          const int blk = t / qo.q_block, tt = t - blk * qo.q_block;
-          const size_t qrow =
-              ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) *
-                  qo.q_block + tt;
-          norm_rope(v, qo.q_norm, qo.eps, rope_row, qo.q_scale);
-          store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD, v, HD);
-        } else {
-          const int h = (n0 - q_cols) / HD;
-          norm_rope(v, qo.k_norm, qo.eps, rope_row, 1.f);
-          store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
-                         (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
-                     v, HD);
-        }
+        o = warp_norm_rope(o, w4, qo.eps, qo.rope + (size_t)pos * (HD / 2),
+                           kind[i] == 1 ? qo.q_scale : 1.f, lane);
       }
-    } else {
-      const int h = (n0 - q_cols - kv_cols) / HD;
-      store_bf16(reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
-                     (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD,
-                 v, HD);
+      uint2 pk;
+      pk.x = pack_bf16x2(o.x, o.y);
+      pk.y = pack_bf16x2(o.z, o.w);
+      reinterpret_cast<uint2*>(dst)[lane] = pk;
     }
   }
 }
@@ -353,102 +476,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     int src, srow;
     row_source(p, m_tile, r, src, srow);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
-    tc_fence_after();
-    float v[BN];
+    if constexpr (EPI == EPI_QKV) {
+      // While the main loop runs: this tile's norm weights into registers,
+      // and lane l looks up the position of row q + 4l (the rows warp q
+      // finishes) and warms L2 with its RoPE row.
+      const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
+      const bool roped = n0 < q_cols + kv_cols;
+      const float4 w4 =
+          roped ? __ldg(reinterpret_cast<const float4*>(n0 < q_cols ? qo.q_norm : qo.k_norm) +
+                        lane)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+      int lane_kind = 0, lane_pos = 0;
+      __nv_bfloat16* lane_dst = nullptr;
+      {
+        int s2, r2;
+        row_source(p, m_tile, q + 4 * lane, s2, r2);
+        if (s2 >= 0) {
+          const QkvTarget g = qkv_target(qo, st, s2, r2, n0);
+          lane_kind = g.kind;
+          lane_dst = g.dst;
+          if (g.kind == 1 || g.kind == 2) {
+            lane_pos = qo.positions[g.pos_idx];
+            if (lane_pos >= 0 && lane_pos < qo.max_pos) {
+              const char* rp = reinterpret_cast<const char*>(qo.rope + (size_t)lane_pos * (HD / 2));
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
-      float t[32];
-      tmem_ld32(trow + c * 32, t);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[c * 32 + i] = ok ? t[i] : 0.f;
-    }
-    if (p.splits == 1) {
-      if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
-    } else if (!p.cluster) {
-      // global merge: every split writes the valid rows of its fp32 partial
-      // ([row][BN]); the last CTA of the tile (atomic counter) sums them in
-      // split order, spreading the loads over its 128 epilogue threads and
-      // staging the sums through shared memory
+              for (int i = 0; i < HD * 4; i += 128) prefetch_l2(rp + i);
+            }
+          }
+        }
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
+      tc_fence_after();
       const int et = threadIdx.x - 64;
-      float* tile_part = p.partial + (size_t)tile_id * p.splits * (BM * BN);
-      if (src >= 0) {
-        float4* mine = reinterpret_cast<float4*>(tile_part + (size_t)split * (BM * BN) +
-                                                 (size_t)r * BN);
+      float* tile_part = p.partial + (size_t)tile_id * p.splits * (BM * HD);
+      float4* stile = reinterpret_cast<float4*>(smem);
+      bool finish = true;
+      if (p.splits == 1) {
+        // accumulator row -> shared tile ([row][column chunk], swizzled)
 #pragma unroll
-        for (int c4 = 0; c4 < C4; ++c4)
-          __stcg(mine + c4, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                                        v[4 * c4 + 3]));
-      }
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (et == 0) {
-        const int old = atomicAdd(p.counters + tile_id, 1);
-        *last_flag = (old == p.splits - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, 128);
-      if (*last_flag) {
-        __threadfence();
-        float4* stile = reinterpret_cast<float4*>(smem);
-        constexpr int ITEMS = BM * C4;
-        for (int it0 = et; it0 < ITEMS; it0 += 128 * 8) {
-          float4 acc[8];
-          int rows[8];
-          bool use[8];
+        for (int c = 0; c < HD / 32; ++c) {
+          float t[32];
+          tmem_ld32(trow + c * 32, t);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int it = it0 + j * 128;
-            rows[j] = it / C4;
-            int sj, rj;
-            row_source(p, m_tile, rows[j], sj, rj);
-            use[j] = it < ITEMS && sj >= 0;
-            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          for (int s2 = 0; s2 < p.splits; ++s2) {
-            const float4* part =
-                reinterpret_cast<const float4*>(tile_part + (size_t)s2 * (BM * BN));
-            float4 t[8];
+          for (int i4 = 0; i4 < 8; ++i4)
+            stile[r * C4 + ((c * 8 + i4) ^ (r & (C4 - 1)))] =
+                ok ? make_float4(t[4 * i4], t[4 * i4 + 1], t[4 * i4 + 2], t[4 * i4 + 3])
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        named_bar_sync(1, 128);
+      } else {
+        // every split writes the valid rows of its fp32 partial ([row][128]);
+        // the last CTA of the tile (atomic counter) sums them in split order
+        // (tcgen05.ld is warp-collective: every lane loads, valid rows store)
+        float4* mine = reinterpret_cast<float4*>(tile_part + (size_t)split * (BM * HD) +
+                                                 (size_t)r * HD);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              t[j] = use[j] ? __ldcg(part + it0 + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < HD / 32; ++c) {
+          float t[32];
+          tmem_ld32(trow + c * 32, t);
+          if (src >= 0) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              acc[j].x += t[j].x;
-              acc[j].y += t[j].y;
-              acc[j].z += t[j].z;
-              acc[j].w += t[j].w;
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int it = it0 + j * 128;
-            if (use[j]) {
-              const int c4 = it - rows[j] * C4;
-              stile[rows[j] * C4 + (c4 ^ (rows[j] & (C4 - 1)))] = acc[j];
-            }
+            for (int i4 = 0; i4 < 8; ++i4)
+              __stcg(mine + c * 8 + i4,
+                     ok ? make_float4(t[4 * i4], t[4 * i4 + 1], t[4 * i4 + 2], t[4 * i4 + 3])
+                        : make_float4(0.f, 0.f, 0.f, 0.f));
           }
         }
         named_bar_sync(1, 128);
-        if (src >= 0) {
-#pragma unroll
-          for (int c4 = 0; c4 < C4; ++c4) {
-            const float4 t = stile[r * C4 + (c4 ^ (r & (C4 - 1)))];
-            v[4 * c4] = t.x;
-            v[4 * c4 + 1] = t.y;
-            v[4 * c4 + 2] = t.z;
-            v[4 * c4 + 3] = t.w;
-          }
-          finish_row<EPI>(p, qo, st, v, src, srow, n0);
+        if (et == 0) {
+          const int old = atomic_add_acq_rel_gpu(p.counters + tile_id, 1);
+          *last_flag = (old == p.splits - 1) ? 1 : 0;
         }
-        if (et == 0) p.counters[tile_id] = 0;
+        named_bar_sync(1, 128);
+        finish = *last_flag != 0;
       }
-    } else if (src >= 0) {
-      // park the valid rows in this CTA's (now idle) stage buffers, swizzled
-      float4* red = reinterpret_cast<float4*>(smem);
+      if (finish) {
+        qkv_finish_warp(p, qo, q, lane, w4, lane_kind, lane_dst, lane_pos,
+                        p.splits == 1 ? stile : nullptr, tile_part);
+        if (p.splits > 1 && et == 0) p.counters[tile_id] = 0;
+      }
+    } else {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
+      tc_fence_after();
+      float v[BN];
 #pragma unroll
-      for (int c4 = 0; c4 < C4; ++c4)
-        red[r * C4 + (c4 ^ (r & (C4 - 1)))] =
-            make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+      for (int c = 0; c < BN / 32; ++c) {
+        float t[32];
+        tmem_ld32(trow + c * 32, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[c * 32 + i] = ok ? t[i] : 0.f;
+      }
+      if (p.splits == 1) {
+        if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
+      } else if (src >= 0) {
+        // park the valid rows in this CTA's (now idle) stage buffers, swizzled
+        float4* red = reinterpret_cast<float4*>(smem);
+#pragma unroll
+        for (int c4 = 0; c4 < C4; ++c4)
+          red[r * C4 + (c4 ^ (r & (C4 - 1)))] =
+              make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+      }
     }
   }
 
@@ -668,17 +795,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (whole) continue;
       // the CTA that finishes a tile's last split sums every split in order
       // (deterministic) and runs the epilogue
-      __threadfence();
       named_bar_sync(1, 128);
       if (et == 0) {
-        const int old = atomicAdd(p.counters + tid, 1);
+        const int old = atomic_add_acq_rel_gpu(p.counters + tid, 1);
         *last_flag = (old == p.splits - 1) ? 1 : 0;
       }
       named_bar_sync(1, 128);
       const bool last = *last_flag != 0;
       named_bar_sync(1, 128);  // everyone has read the flag before it is reused
       if (!last) continue;
-      __threadfence();
 #pragma unroll 1
       for (int half = 0; half < BNB / HD; ++half) {
         float v[HD];

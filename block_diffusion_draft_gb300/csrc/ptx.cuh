@@ -86,6 +86,19 @@ DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
   }
 }
 
+// Arrival counter of a split-K merge: one thread adds 1 with acquire-release
+// semantics at GPU scope and gets the old value.  Preceded by a CTA barrier,
+// the release publishes every store the CTA made before it (cumulativity);
+// followed by one, the acquire orders the CTA's later loads after it.
+DF_DEV int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- TMA
 DF_DEV void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
@@ -101,6 +114,11 @@ DF_DEV uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// hint: bring the 128-byte line holding p into L2
+DF_DEV void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // 2-D tiled load of one box into shared memory; completion is signalled on

@@ -62,6 +62,7 @@ struct Unit {
   int s0_lo, s0_hi, s1_lo, s1_hi;  // key segments
   int blk0;         // packed: first block of the tile
   int direct;       // 1: this unit covers all keys of its rows
+  int len;          // inference: keys of the sequence after this call
 };
 
 DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
@@ -78,8 +79,9 @@ DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
     const int r = u - sq.unit_off[w.b];
     w.h = r / nch;
     const int c = r - w.h * nch;
-    w.s0_lo = sq.lo[w.b] + c * a.chunk;
-    w.s0_hi = min(sq.len[w.b], w.s0_lo + a.chunk);
+    w.len = sq.len[w.b];
+    w.s0_lo = sq.lo[w.b] + c * sq.chunk[w.b];
+    w.s0_hi = min(w.len, w.s0_lo + sq.chunk[w.b]);
     w.s1_lo = w.s1_hi = 0;
     w.q_row0 = (w.b * a.n_kv + w.h) * rows_per_block;
     w.rows = rows_per_block;
@@ -108,6 +110,7 @@ DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
     w.s1_lo = a.seq + w.blk0 * a.q_block;
     w.s1_hi = w.s1_lo + nbt * a.q_block;
     w.direct = 1;
+    w.len = 0;
   }
   w.kv_row0 = ((long long)w.b * a.n_kv + w.h) * a.cap;
   return w;
@@ -122,6 +125,86 @@ DF_DEV int n_tiles_of(const Unit& w) {
 DF_DEV int tile_start(const Unit& w, int j) {
   const int n0 = w.s0_hi > w.s0_lo ? (w.s0_hi - w.s0_lo + BKEY - 1) / BKEY : 0;
   return j < n0 ? w.s0_lo + j * BKEY : w.s1_lo + (j - n0) * BKEY;
+}
+
+// On-chip merge of the key splits of one (sequence, kv head), whose C CTAs
+// form a thread-block cluster.  Query row r belongs to rank r / RPO (RPO =
+// ceil(rows / C)).  After a cluster barrier (every CTA is done with its stage
+// buffers) each CTA stores (O, m, l) of each of its rows into the owner's
+// idle K slots 1-2 (O, [source][row] swizzled) and V slot 0 (m, l); after a
+// second barrier the owner merges its rows from local shared memory: one
+// warp per row, lane l holding columns 4l .. 4l+3, sources in rank order (so
+// the result does not depend on timing), rescaled by the largest running max,
+// written as the normalised bf16 row.
+DF_DEV uint32_t merge_slot(int src, int lr, int rpo) { return (uint32_t)(src * rpo + lr); }
+
+DF_DEV void cluster_push_row(uint8_t* obuf, uint8_t* mlbuf, int C, int qr, int rows,
+                             const float (&o)[HD], float m, float l) {
+  const int rpo = (rows + C - 1) / C;
+  const uint32_t owner = (uint32_t)(qr / rpo);
+  const uint32_t slot = merge_slot((int)cluster_ctarank(), qr % rpo, rpo);
+  const uint32_t ob = cluster_map(smem_u32(obuf), owner);
+  const uint32_t mb = cluster_map(smem_u32(mlbuf), owner);
+#pragma unroll
+  for (int c4 = 0; c4 < HD / 4; ++c4)
+    st_cluster_f4(ob + (slot * 32 + (c4 ^ (slot & 31))) * 16,
+                  make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
+  st_cluster_f32(mb + slot * 4, m);
+  st_cluster_f32(mb + (128 + slot) * 4, l);
+}
+
+template <int C>
+DF_DEV void cluster_merge_rows(const AttnArgs& a, const Unit& w, const uint8_t* obuf,
+                               const uint8_t* mlbuf, int warp, int lane) {
+  const int rpo = (w.rows + C - 1) / C;
+  const int row0 = (int)cluster_ctarank() * rpo;
+  const float4* ob = reinterpret_cast<const float4*>(obuf);
+  const float* mb = reinterpret_cast<const float*>(mlbuf);
+  const int ld_out = a.n_kv * a.groups * HD;
+  for (int lr = warp - 2; lr < rpo && row0 + lr < w.rows; lr += 4) {
+    float m[C], l[C];
+    float4 t[C];
+#pragma unroll
+    for (int k = 0; k < C; ++k) {
+      const uint32_t slot = merge_slot(k, lr, rpo);
+      m[k] = mb[slot];
+      l[k] = mb[128 + slot];
+      t[k] = ob[slot * 32 + (lane ^ (slot & 31))];
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < C; ++k) M = fmaxf(M, m[k]);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < C; ++k) {
+      const float f = m[k] == -INFINITY ? 0.f : fast_exp2(m[k] - M);
+      L += f * l[k];
+      acc.x += f * t[k].x;
+      acc.y += f * t[k].y;
+      acc.z += f * t[k].z;
+      acc.w += f * t[k].w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int row = row0 + lr;
+    const int gi = row / a.q_len, tt = row - gi * a.q_len;
+    const size_t token = (size_t)w.b * a.q_len + tt;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + token * ld_out +
+                              (size_t)(w.h * a.groups + gi) * HD + lane * 4) = pk;
+  }
+}
+
+DF_DEV void cluster_merge(const AttnArgs& a, const Unit& w, const uint8_t* obuf,
+                          const uint8_t* mlbuf, int warp, int lane) {
+  switch (a.cluster) {
+    case 2: cluster_merge_rows<2>(a, w, obuf, mlbuf, warp, lane); break;
+    case 4: cluster_merge_rows<4>(a, w, obuf, mlbuf, warp, lane); break;
+    case 8: cluster_merge_rows<8>(a, w, obuf, mlbuf, warp, lane); break;
+    default: cluster_merge_rows<16>(a, w, obuf, mlbuf, warp, lane); break;
+  }
 }
 
 template <bool DUAL>
@@ -277,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         i1_lo = w.s0_lo;
         i1_hi = w.s0_hi;
         if (a.window > 0) {
-          const int qi = sq.len[w.b] - a.q_len + t;
+          const int qi = w.len - a.q_len + t;
           i1_lo = max(i1_lo, qi - a.window + 1);
           i1_hi = min(i1_hi, qi + a.window);
         }
@@ -453,6 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
           dst[i] = pk;
         }
+      } else if (a.cluster > 1) {
+        // handed to the owner rank below
       } else {
         const size_t u = blockIdx.x;
         float4* po = reinterpret_cast<float4*>(a.part_o + u * 128 * HD);
@@ -464,6 +549,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __stcg(a.part_ml + u * 256 + 128 + qr, l_run);
       }
     }
+    if (a.cluster > 1) {
+      __syncwarp();
+      cluster_sync();  // every CTA of the cluster is done with its stage buffers
+      if (writer) cluster_push_row(sK + TILE_BYTES, sV, a.cluster, qr, w.rows, o, m_run, l_run);
+      __syncwarp();
+      cluster_sync();  // every row has reached its owner
+      cluster_merge(a, w, sK + TILE_BYTES, sV, warp, lane);
+    }
+  }
+  if (warp < 2 && a.cluster > 1) {
+    // the producer and MMA warps take part in both cluster barriers
+    __syncwarp();
+    cluster_sync();
+    cluster_sync();
   }
 
   tc_fence_before();
@@ -529,19 +628,64 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
+namespace {
+
+void set_attn_attrs() {
+  static bool done = false;
+  if (done) return;
+  for (const void* f : {(const void*)attn_bf16_kernel<true>, (const void*)attn_bf16_kernel<false>}) {
+    cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
+  done = true;
+}
+
+// clusters of `c` attention CTAs that can be resident at once (0 if none)
+int max_active_clusters(int c, bool dual) {
+  static int cache[2][17] = {};
+  static bool known[2][17] = {};
+  if (known[dual][c]) return cache[dual][c];
+  set_attn_attrs();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const void* f = dual ? (const void*)attn_bf16_kernel<true> : (const void*)attn_bf16_kernel<false>;
+  if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dual][c] = n;
+  known[dual][c] = true;
+  return n;
+}
+
+}  // namespace
+
+int attn_decode_cluster(int pairs, int num_sms, bool dual) {
+  for (int c = 16; c >= 2; c /= 2) {
+    if ((long long)pairs * c > num_sms) continue;
+    if (max_active_clusters(c, dual) >= pairs) return c;
+  }
+  return 1;
+}
+
 int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                      long long q_rows_total, const void* cache_k,
                      const void* cache_v, long long kv_rows_total,
                      cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(attn_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)SMEM_BYTES);
-    cudaFuncSetAttribute(attn_bf16_kernel<false>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    attr_done = true;
-  }
+  set_attn_attrs();
   if (a.n_units <= 0) return cudaSuccess;
+  if (a.cluster > 1 && (a.mode != 0 || a.cluster > 16 || a.n_units % a.cluster != 0))
+    return cudaErrorInvalidValue;
   if (kv_rows_total >= (1LL << 31) || q_rows_total >= (1LL << 31))
     return cudaErrorInvalidValue;
   const bool dual = a.mode == 0 && a.groups * a.q_len <= 64;
@@ -552,11 +696,13 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
     return cudaErrorInvalidValue;
   static AttnSeqs zero_seqs{};
   const AttnSeqs& sq = seqs ? *seqs : zero_seqs;
-  cudaError_t e = dual ? launch_pdl(attn_bf16_kernel<true>, dim3(a.n_units), dim3(kThreads),
-                                    SMEM_BYTES, stream, mq, mk, mv, a, sq)
-                       : launch_pdl(attn_bf16_kernel<false>, dim3(a.n_units), dim3(kThreads),
-                                    SMEM_BYTES, stream, mq, mk, mv, a, sq);
-  if (e != cudaSuccess || a.mode != 0) return (int)e;
+  const unsigned cl = a.cluster > 1 ? (unsigned)a.cluster : 1u;
+  cudaError_t e =
+      dual ? launch_pdl_cluster(attn_bf16_kernel<true>, dim3(a.n_units), dim3(kThreads),
+                                SMEM_BYTES, stream, cl, mq, mk, mv, a, sq)
+           : launch_pdl_cluster(attn_bf16_kernel<false>, dim3(a.n_units), dim3(kThreads),
+                                SMEM_BYTES, stream, cl, mq, mk, mv, a, sq);
+  if (e != cudaSuccess || a.mode != 0 || a.cluster > 1) return (int)e;
   bool any_split = false;
   for (int b = 0; b < a.batch; ++b) any_split |= sq.n_chunks[b] > 1;
   if (!any_split) return cudaSuccess;

@@ -510,12 +510,25 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
                    : 0;
     total_keys += (long long)a->nkv * (sq.len[b] - sq.lo[b]);
   }
-  // about one key chunk per SM, in whole 128-key tiles, at most 4096 keys
+  // Few (sequence, kv head) pairs: each pair's keys split evenly over the C
+  // CTAs of a thread-block cluster that merge on chip.  Otherwise about one
+  // key chunk per SM, in whole 128-key tiles, at most 4096 keys, merged by a
+  // second kernel.
+  const int cl = a->dt == DFLASH_BF16
+                     ? attn_decode_cluster(batch * a->nkv, a->num_sms, a->g * q_len <= 64)
+                     : 1;
   int chunk = (int)((total_keys + a->num_sms - 1) / a->num_sms);
   chunk = std::min(4096, std::max(128, (chunk + 127) / 128 * 128));
   sq.unit_off[0] = 0;
   for (int b = 0; b < batch; ++b) {
-    sq.n_chunks[b] = std::max(1, (sq.len[b] - sq.lo[b] + chunk - 1) / chunk);
+    const int keys = sq.len[b] - sq.lo[b];
+    if (cl > 1) {
+      sq.chunk[b] = std::max(128, ((keys + cl - 1) / cl + 127) / 128 * 128);
+      sq.n_chunks[b] = cl;
+    } else {
+      sq.chunk[b] = chunk;
+      sq.n_chunks[b] = std::max(1, (keys + chunk - 1) / chunk);
+    }
     sq.unit_off[b + 1] = sq.unit_off[b] + a->nkv * sq.n_chunks[b];
   }
   AttnArgs aa{};
@@ -531,7 +544,7 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
   aa.cap = c->cap;
   aa.window = a->cfg.sliding_window;
   aa.n_units = sq.unit_off[batch];
-  aa.chunk = chunk;
+  aa.cluster = cl;
   aa.out = a->attn_out.p;
   aa.err = a->err;
   if (a->dt == DFLASH_BF16) {

@@ -111,6 +111,7 @@ struct AttnSeqs {
   int len[kMaxBatch];          // keys of the sequence after this call's append
   int lo[kMaxBatch];           // first key any query of the block can see
   int n_chunks[kMaxBatch];     // splits of [lo, len) per kv head
+  int chunk[kMaxBatch];        // keys per split (a multiple of 128)
   int unit_off[kMaxBatch + 1]; // first work unit of the sequence
 };
 
@@ -126,13 +127,19 @@ struct AttnArgs {
   int seq;           // packed: context rows per sequence
   const int* anchors;  // packed: [B][n_blocks]
   int n_units;
-  int chunk;         // inference: keys per split
+  int cluster;       // inference: > 1 = the splits of one (sequence, kv head)
+                     // form a thread-block cluster and merge on chip
   float* part_o;     // [units][128 rows][d] fp32 partial outputs
   float* part_ml;    // [units][2][128] running max (log2 units) and sum
   int* counters;     // [B * n_kv]
   void* out;         // [B*q_len][n_heads*d]
   int* err;
 };
+
+// Splits per (sequence, kv head) for the on-chip merge of a decode step with
+// `pairs` (sequence, kv head) pairs: the largest of 16, 8, 4, 2 whose
+// clusters all fit on the GPU at once, or 1 (separate merge kernel).
+int attn_decode_cluster(int pairs, int num_sms, bool dual);
 
 int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                      long long q_rows_total, const void* cache_k,

@@ -362,6 +362,46 @@ DF_DEV void qkv_finish_warp(const Plan& p, const QkvOut& qo, int wq, int lane, f
   }
 }
 
+// Split-K merge of a plain epilogue inside a thread-block cluster of SPLITS
+// CTAs, each of which parked its fp32 rows in its own shared memory
+// ([row][column chunk], swizzled).  Warp wq of rank c takes the valid rows
+// r = c + SPLITS (wq + 4i); lane l reads columns 4l .. 4l+3 of row r from every
+// rank, sums them in rank order and stores them (coalesced across the warp).
+template <int EPI, int SPLITS>
+DF_DEV void cluster_sum_rows(const Plan& p, int m_tile, int n0, const uint8_t* smem, int wq,
+                             int lane) {
+  constexpr int C4 = HD / 4;
+  const int rank = (int)cluster_ctarank();
+  const uint32_t base = smem_u32(smem);
+  for (int r = rank + SPLITS * wq; r < BM; r += SPLITS * 4) {
+    int src, srow;
+    row_source(p, m_tile, r, src, srow);
+    if (src < 0) continue;
+    const uint32_t off = base + (uint32_t)(r * C4 + (lane ^ (r & (C4 - 1)))) * 16;
+    float4 t[SPLITS];
+#pragma unroll
+    for (int c = 0; c < SPLITS; ++c) t[c] = ld_cluster_f4(cluster_map(off, (uint32_t)c));
+    float4 acc = t[0];
+#pragma unroll
+    for (int c = 1; c < SPLITS; ++c) {
+      acc.x += t[c].x;
+      acc.y += t[c].y;
+      acc.z += t[c].z;
+      acc.w += t[c].w;
+    }
+    if constexpr (EPI == EPI_F32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)srow * p.ldc + n0)[lane] =
+          acc;
+    } else {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc +
+                               n0)[lane] = pk;
+    }
+  }
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0,
@@ -580,32 +620,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (p.splits > 1 && p.cluster) {
-    // The splits of this tile are one thread-block cluster.  Each CTA sums
-    // every r-th valid row (r % splits == its rank) from all CTAs' shared
-    // memory in rank order, so the result does not depend on timing, and
-    // runs the epilogue for those rows.
+    // The splits of this tile are one thread-block cluster.  Rank c sums the
+    // valid rows r with r % splits == c from every rank's shared memory, in
+    // rank order (so the result does not depend on timing), one row per warp.
     cluster_sync();
     if (warp >= 2) {
-      const int r = (warp & 3) * 32 + lane;
-      int src, srow;
-      row_source(p, m_tile, r, src, srow);
-      if (src >= 0 && (uint32_t)(r % p.splits) == cluster_ctarank()) {
-        float v[BN];
-#pragma unroll
-        for (int i = 0; i < BN; ++i) v[i] = 0.f;
-        const uint32_t row_addr = smem_u32(smem) + (uint32_t)r * C4 * 16;
-        for (int c = 0; c < p.splits; ++c) {
-          const uint32_t remote = cluster_map(row_addr, (uint32_t)c);
-#pragma unroll
-          for (int c4 = 0; c4 < C4; ++c4) {
-            const float4 t = ld_cluster_f4(remote + (uint32_t)((c4 ^ (r & (C4 - 1))) * 16));
-            v[4 * c4] += t.x;
-            v[4 * c4 + 1] += t.y;
-            v[4 * c4 + 2] += t.z;
-            v[4 * c4 + 3] += t.w;
-          }
-        }
-        finish_row<EPI>(p, qo, st, v, src, srow, n0);
+      switch (p.splits) {
+        case 2: cluster_sum_rows<EPI, 2>(p, m_tile, n0, smem, warp & 3, lane); break;
+        case 3: cluster_sum_rows<EPI, 3>(p, m_tile, n0, smem, warp & 3, lane); break;
+        case 4: cluster_sum_rows<EPI, 4>(p, m_tile, n0, smem, warp & 3, lane); break;
+        case 5: cluster_sum_rows<EPI, 5>(p, m_tile, n0, smem, warp & 3, lane); break;
+        case 6: cluster_sum_rows<EPI, 6>(p, m_tile, n0, smem, warp & 3, lane); break;
+        case 7: cluster_sum_rows<EPI, 7>(p, m_tile, n0, smem, warp & 3, lane); break;
+        default: cluster_sum_rows<EPI, 8>(p, m_tile, n0, smem, warp & 3, lane); break;
       }
     }
     cluster_sync();  // no CTA leaves while the others still read its rows

@@ -410,9 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) s[c] = -INFINITY;
           }
         }
-        float tmax = -INFINITY;
+        // row max and row sum as 8 interleaved partial chains (a single
+        // chain over NC columns is a latency chain of NC dependent ops)
+        // (three-input max: chain e takes columns e, e+8, e+16, ...)
+        float pmax[8];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) tmax = fmaxf(tmax, s[c]);
+        for (int e = 0; e < 8; ++e) {
+          pmax[e] = s[e];
+#pragma unroll
+          for (int k = 1; k < NC / 8; k += 2)
+            pmax[e] = k + 1 < NC / 8 ? max3f(pmax[e], s[e + 8 * k], s[e + 8 * (k + 1)])
+                                     : fmaxf(pmax[e], s[e + 8 * k]);
+        }
+        const float tmax = fmaxf(fmaxf(fmaxf(pmax[0], pmax[1]), fmaxf(pmax[2], pmax[3])),
+                                 fmaxf(fmaxf(pmax[4], pmax[5]), fmaxf(pmax[6], pmax[7])));
         float m_new = m_run;
         if (m_run == -INFINITY || tmax > m_run + kRescaleThreshold) m_new = fmaxf(m_run, tmax);
         if (m_new != m_run) {
@@ -420,7 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = j > 0;
         }
         const float mm = (m_new == -INFINITY) ? 0.f : m_new;
-        float sum = 0.f;
+        // exponentials with paired fp32 subtract and sum
+        const float2 neg_m = make_float2(-mm, -mm);
+        float2 psum[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) psum[e] = make_float2(0.f, 0.f);
         uint8_t* prow = sK + (j % NST) * TILE_BYTES + r * 128;
         // this thread's NC columns are 16-byte chunks col0/8 .. col0/8+NC/8-1
         // of its P row (one 64-key atom per half); in dual mode the other
@@ -429,9 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < NC / 8; ++cc) {
           float pv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pv[e] = fast_exp2(s[cc * 8 + e] - mm);
-            sum += pv[e];
+          for (int e = 0; e < 4; ++e) {
+            const float2 d =
+                add_f32x2(make_float2(s[cc * 8 + 2 * e], s[cc * 8 + 2 * e + 1]), neg_m);
+            pv[2 * e] = fast_exp2(d.x);
+            pv[2 * e + 1] = fast_exp2(d.y);
+            psum[e] = add_f32x2(psum[e], make_float2(pv[2 * e], pv[2 * e + 1]));
           }
           uint4 pk;
           pk.x = pack_bf16x2(pv[0], pv[1]);
@@ -449,6 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(prow + other * HALF_BYTES + ((cc ^ (r & 7)) * 16)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
+        const float sum = ((psum[0].x + psum[0].y) + (psum[1].x + psum[1].y)) +
+                          ((psum[2].x + psum[2].y) + (psum[3].x + psum[3].y));
         l_run = l_run * alpha + sum;
         m_run = m_new;
       }

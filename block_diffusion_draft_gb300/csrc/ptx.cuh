@@ -344,6 +344,24 @@ DF_DEV float fast_exp2(float x) {
   return y;
 }
 
+// max of three floats in one instruction
+DF_DEV float max3f(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// two fp32 additions in one instruction (round to nearest)
+DF_DEV float2 add_f32x2(float2 a, float2 b) {
+  unsigned long long pa, pb, pc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(pc) : "l"(pa), "l"(pb));
+  float2 c;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c.x), "=f"(c.y) : "l"(pc));
+  return c;
+}
+
 DF_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

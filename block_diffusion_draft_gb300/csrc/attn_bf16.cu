@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_empty = v_full + NST;
   uint64_t* s_full = kv_empty + NST;  // [2]
   uint64_t* p_full = s_full + 2;      // [2]
-  uint64_t* o_done = p_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  uint64_t* o_done = p_full + 2;      // [2]: PV(j) completes o_done[j & 1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -247,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
     }
-    mbar_init(o_done, 1);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmQ);
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_sw128(v_base + kk * 16 * 128, HALF_BYTES, 1024);
           tc_mma_bf16(tmem + O_COL, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(o_done);
+        tc_commit(&o_done[j & 1]);
         tc_commit(&kv_empty[s]);
       }
     }
@@ -472,12 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run = l_run * alpha + sum;
         m_run = m_new;
       }
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, a.err)))
+      // O is touched only to rescale it, and only then must PV(j-1) be
+      // complete.  Having seen S(j) complete, PV(j-2) and everything before
+      // it are (one thread issues all MMAs, in order), so o_done[(j-1) & 1]
+      // has at most the phase of PV(j-1) pending and a parity wait is exact.
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1,
+                                               abort_flag, a.err)))
           break;
         tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? alpha : 1.f;
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
@@ -495,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ finish
     bool have_o = __all_sync(0xffffffffu, T > 0 && !*abort_flag);
     if (have_o) {
-      have_o = __all_sync(0xffffffffu, mbar_wait(o_done, (T - 1) & 1, abort_flag, a.err));
+      have_o = __all_sync(0xffffffffu, mbar_wait(&o_done[(T - 1) & 1], ((T - 1) >> 1) & 1,
+                                                 abort_flag, a.err));
       tc_fence_after();
     }
     float o[HD];

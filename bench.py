@@ -32,6 +32,33 @@ import time
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(ROOT, "block_diffusion_draft_gb300", "csrc")
+
+
+def csrc_digest() -> str:
+    """sha256 over the CUDA sources (names and contents, sorted by name)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    capture in profiles/traffic.json, or None when there is none or the CUDA
+    sources changed since it was taken."""
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tfile):
+        return None
+    tj = json.load(open(tfile))
+    rec = tj.get("kernels", {}).get(f"{workload}:{kernel}")
+    if not rec or tj.get("csrc_sha256") != csrc_digest():
+        return None
+    return rec.get("bytes_per_launch")
 sys.path.insert(0, ROOT)
 
 METRIC = "draft-attn blocks/s per layer; achieved HBM GB/s (or tensor util) vs GB300 peak"
@@ -556,12 +583,7 @@ def main():
         peak = pk["hbm_gbs"]
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak,
                 "unit": "GB/s", "frac": ach / peak, "peak_source": f"{pk['source']} hbm"}
-    roof["traffic"] = None
-    tfile = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tfile):
-        tj = json.load(open(tfile)).get(f"{args.workload}:{dom}")
-        if tj:
-            roof["traffic"] = tj.get("bytes_per_launch")
+    roof["traffic"] = measured_traffic(args.workload, dom)
 
     # ---------------------------------------------------- end to end (host)
     wl.reset()

@@ -598,6 +598,370 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- packed, 2 Q tiles
+// Packed training layout ("nemo_automodel...draft_qwen3", module docstring:
+// a block sees the context strictly before its anchor and its own block).
+// One CTA takes two Q tiles of the same (sequence, kv head) -- 2 x tile_blocks
+// consecutive blocks -- and streams their common key range once:
+// [0, largest anchor of its blocks) and the blocks' own rows.  Each K/V tile
+// then feeds twice the tensor work, and the two softmax warpgroups take
+// turns: while one works on its tile the tensor core runs the other's MMAs.
+//
+//   warp 0      TMA producer: Q0, Q1 once; K and V tiles of 128 keys into a
+//               2-stage ring (K and V slots free separately)
+//   warp 1      TMEM allocator + MMA issuer, per key tile j:
+//                 PV0(j-1), S0(j), PV1(j-1), S1(j) (S_i(j) waits for the
+//                 softmax of tile j-1 of Q tile i; PV_i(j-1) for its P)
+//   warps 2-5   softmax of Q tile 0, one TMEM lane (row) per thread
+//   warps 6-9   softmax of Q tile 1
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).  P_i(j) goes
+// into the first 64 columns of S_i as bf16 pairs (S_i(j) is already in
+// registers) and is the TMEM A operand of PV_i(j).  Because S_i(j+1) is
+// issued after PV_i(j), seeing S_i(j+1) complete means PV_i(j) is complete:
+// a rescale of O_i never waits.
+constexpr int PK_NST = 2;
+constexpr int PK_THREADS = 320;
+constexpr size_t PK_SMEM = 1024 + TILE_BYTES * (2 + 2 * PK_NST) + 512;
+
+struct PkUnit {
+  int b, h, blk0;
+  int rows[2];        // real query rows of Q tile 0 / 1
+  int q_row0;         // first row of Q tile 0 in the Q buffer
+  int s0_hi;          // context keys [0, s0_hi)
+  int s1_lo, s1_hi;   // the blocks' own keys
+  long long kv_row0;
+};
+
+DF_DEV PkUnit pk_decode(const AttnArgs& a, int u) {
+  PkUnit w;
+  const int rpb = a.groups * a.q_block;
+  const int per_unit = 2 * a.tile_blocks;
+  const int n_pu = (a.n_blocks + per_unit - 1) / per_unit;
+  const int per = a.batch * a.n_kv;
+  const int p_rev = u / per;
+  const int rem = u - p_rev * per;
+  w.b = rem / a.n_kv;
+  w.h = rem - w.b * a.n_kv;
+  const int p = n_pu - 1 - p_rev;  // latest anchors (longest key ranges) first
+  w.blk0 = p * per_unit;
+  const int nb = min(per_unit, a.n_blocks - w.blk0);
+  const int nb0 = min(a.tile_blocks, nb);
+  w.rows[0] = nb0 * rpb;
+  w.rows[1] = (nb - nb0) * rpb;
+  w.q_row0 = ((w.b * a.n_kv + w.h) * a.n_blocks + w.blk0) * rpb;
+  int amax = 0;
+  for (int k = 0; k < nb; ++k) {
+    int an = a.anchors[w.b * a.n_blocks + w.blk0 + k];
+    an = min(max(an, 0), a.seq);
+    amax = max(amax, an);
+  }
+  w.s0_hi = amax;
+  w.s1_lo = a.seq + w.blk0 * a.q_block;
+  w.s1_hi = w.s1_lo + nb * a.q_block;
+  w.kv_row0 = ((long long)w.b * a.n_kv + w.h) * a.cap;
+  return w;
+}
+
+DF_DEV int pk_tiles(const PkUnit& w) {
+  return (w.s0_hi + BKEY - 1) / BKEY + (w.s1_hi - w.s1_lo + BKEY - 1) / BKEY;
+}
+
+DF_DEV int pk_tile_start(const PkUnit& w, int j) {
+  const int n0 = (w.s0_hi + BKEY - 1) / BKEY;
+  return j < n0 ? j * BKEY : w.s1_lo + (j - n0) * BKEY;
+}
+
+__global__ void __launch_bounds__(PK_THREADS, 1)
+    attn_pk2_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                              // [2] Q tiles
+  uint8_t* sK = smem + 2 * TILE_BYTES;             // [PK_NST]
+  uint8_t* sV = sK + PK_NST * TILE_BYTES;          // [PK_NST]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + PK_NST * TILE_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* v_full = k_full + PK_NST;
+  uint64_t* k_empty = v_full + PK_NST;
+  uint64_t* v_empty = k_empty + PK_NST;
+  uint64_t* s_full = v_empty + PK_NST;  // [2] per Q tile
+  uint64_t* p_full = s_full + 2;        // [2]
+  uint64_t* o_done = p_full + 2;        // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PkUnit w = pk_decode(a, blockIdx.x);
+  const int T = pk_tiles(w);
+  const int nqt = w.rows[1] > 0 ? 2 : 1;  // Q tiles with rows
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < PK_NST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    grid_dep_wait();
+    if (lane == 0) {
+      const uint64_t pol_kv = policy_evict_last();
+      const uint64_t pol_q = policy_evict_first();
+      mbar_arrive_expect_tx(q_full, (uint32_t)nqt * TILE_BYTES);
+      for (int i = 0; i < nqt; ++i)
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_2d(sQ + i * TILE_BYTES + hf * HALF_BYTES, &tmQ, q_full, 64 * hf,
+                      w.q_row0 + i * a.tile_blocks * a.groups * a.q_block, pol_q);
+      for (int j = 0; j < T; ++j) {
+        const int s = j % PK_NST;
+        const uint32_t ph = ((j / PK_NST) & 1) ^ 1;
+        const int y = (int)(w.kv_row0 + pk_tile_start(w, j));
+        if (!mbar_wait(&k_empty[s], ph, abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
+        tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
+        tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
+        if (!mbar_wait(&v_empty[s], ph, abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
+        tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
+        tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    grid_dep_wait();
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, BKEY, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
+      bool alive = mbar_wait(q_full, 0, abort_flag, a.err);
+      // S_i(j) = Q_i K(j)^T into S_i; the last Q tile's S frees the K slot
+      auto issue_s = [&](int i, int j) {
+        const int s = j % PK_NST;
+        if (!mbar_wait(&k_full[s], (j / PK_NST) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t q_base = smem_u32(sQ + i * TILE_BYTES);
+        const uint32_t k_base = smem_u32(sK + s * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+          tc_mma_bf16(tmem + (uint32_t)(i * BKEY), sdesc_sw128(q_base + off, 16, 1024),
+                      sdesc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[i]);
+        if (i == nqt - 1) tc_commit(&k_empty[s]);
+        return true;
+      };
+      // O_i += P_i(j) V(j), P_i(j) from TMEM; the last Q tile's PV frees V
+      auto issue_pv = [&](int i, int j) {
+        const int s = j % PK_NST;
+        if (!mbar_wait(&p_full[i], j & 1, abort_flag, a.err)) return false;
+        if (!mbar_wait(&v_full[s], (j / PK_NST) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(sV + s * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BKEY / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(v_base + kk * 16 * 128, HALF_BYTES, 1024);
+          tc_mma_bf16_ta(tmem + O_COL + (uint32_t)(i * HD), tmem + (uint32_t)(i * BKEY) + kk * 8,
+                         bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&o_done[i]);
+        if (i == nqt - 1) tc_commit(&v_empty[s]);
+        return true;
+      };
+      for (int i = 0; i < nqt && alive; ++i) alive = issue_s(i, 0);
+      for (int j = 0; j < T && alive; ++j) {
+        for (int i = 0; i < nqt && alive; ++i) {
+          alive = issue_pv(i, j);
+          if (alive && j + 1 < T) alive = issue_s(i, j + 1);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    grid_dep_wait();
+    const int i = (warp - 2) >> 2;  // Q tile of this warpgroup
+    if (i < nqt && T > 0) {
+      const int q = warp & 3;
+      const int r = q * 32 + lane;  // TMEM lane = row of Q tile i
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t s_col = trow + (uint32_t)(i * BKEY);
+      const uint32_t o_col = trow + O_COL + (uint32_t)(i * HD);
+      const bool real = r < w.rows[i];
+      const int rpb = a.groups * a.q_block;
+      const int kb = r / rpb;
+      const int within = r - kb * rpb;
+      const int gi = within / a.q_block;
+      const int t = within - gi * a.q_block;
+      const int blk = w.blk0 + i * a.tile_blocks + kb;
+      int i1_hi = 0, i2_lo = 0, i2_hi = 0;
+      if (real) {
+        int an = a.anchors[w.b * a.n_blocks + blk];
+        if (an < 0 || an > a.seq) {
+          record_error(a.err, 3 /* DFLASH_DEV_ANCHOR */);
+          an = min(max(an, 0), a.seq);
+        }
+        i1_hi = an;
+        i2_lo = a.seq + blk * a.q_block;
+        i2_hi = i2_lo + a.q_block;
+      }
+      const int n_ctx_tiles = (w.s0_hi + BKEY - 1) / BKEY;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < T; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i], j & 1, abort_flag, a.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[BKEY];
+        {
+          uint32_t raw[BKEY / 32][32];
+#pragma unroll
+          for (int c = 0; c < BKEY / 32; ++c) tmem_ld32_nowait(s_col + c * 32, raw[c]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < BKEY / 32; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[c][e]);
+        }
+        // a context tile may run past the context into block rows, which
+        // the own-block tile covers: each tile admits only its segment's keys
+        const int k0 = pk_tile_start(w, j);
+        const bool ctx_tile = j < n_ctx_tiles;
+        const int lo = ctx_tile ? 0 : i2_lo, hi = ctx_tile ? i1_hi : i2_hi;
+        if (!real || !(k0 >= lo && k0 + BKEY <= hi)) {
+#pragma unroll
+          for (int c = 0; c < BKEY; ++c) {
+            const int key = k0 + c;
+            if (!(real && key >= lo && key < hi)) s[c] = -INFINITY;
+          }
+        }
+        // row max as 8 interleaved three-input chains
+        float pmax[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          pmax[e] = s[e];
+#pragma unroll
+          for (int k = 1; k < BKEY / 8; k += 2)
+            pmax[e] = k + 1 < BKEY / 8 ? max3f(pmax[e], s[e + 8 * k], s[e + 8 * (k + 1)])
+                                       : fmaxf(pmax[e], s[e + 8 * k]);
+        }
+        const float tmax = fmaxf(fmaxf(fmaxf(pmax[0], pmax[1]), fmaxf(pmax[2], pmax[3])),
+                                 fmaxf(fmaxf(pmax[4], pmax[5]), fmaxf(pmax[6], pmax[7])));
+        float m_new = m_run, alpha = 1.f;
+        if (m_run == -INFINITY || tmax > m_run + kRescaleThreshold) m_new = fmaxf(m_run, tmax);
+        bool rescale = false;
+        if (m_new != m_run) {
+          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+          rescale = j > 0;
+        }
+        const float mm = (m_new == -INFINITY) ? 0.f : m_new;
+        // P(j) = exp2(S - m) as bf16 pairs over the first 64 columns of S_i
+        const float2 neg_m = make_float2(-mm, -mm);
+        float2 psum[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) psum[e] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p0 = 0; p0 < BKEY; p0 += 64) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = p0 + cc * 8 + 2 * e;
+              const float2 d = add_f32x2(make_float2(s[c], s[c + 1]), neg_m);
+              pv[2 * e] = fast_exp2(d.x);
+              pv[2 * e + 1] = fast_exp2(d.y);
+              psum[e] = add_f32x2(psum[e], make_float2(pv[2 * e], pv[2 * e + 1]));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pw[cc * 4 + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+          }
+          tmem_st32_nowait(s_col + (uint32_t)(p0 / 2), pw);
+        }
+        const float sum = ((psum[0].x + psum[0].y) + (psum[1].x + psum[1].y)) +
+                          ((psum[2].x + psum[2].y) + (psum[3].x + psum[3].y));
+        l_run = l_run * alpha + sum;
+        m_run = m_new;
+        // S_i(j) complete implies PV_i(j-1) complete: O_i may be rescaled
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float o[32];
+            tmem_ld32(o_col + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= f;
+            tmem_st32(o_col + c * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[i]);
+      }
+      // ---------------------------------------------------------- finish
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[i], (T - 1) & 1, abort_flag, a.err));
+      tc_fence_after();
+      // normalised O row, 32 columns at a time (warp-collective loads)
+      const float inv = ok && l_run > 0.f ? 1.f / l_run : 0.f;
+      const int ld_out = a.n_kv * a.groups * HD;
+      const size_t token = (size_t)w.b * a.q_len + (size_t)blk * a.q_block + t;
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                            token * ld_out + (size_t)(w.h * a.groups + gi) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float o[32];
+        tmem_ld32(o_col + c * 32, o);
+        if (real) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 pk;
+            pk.x = pack_bf16x2(o[8 * e] * inv, o[8 * e + 1] * inv);
+            pk.y = pack_bf16x2(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
+            pk.z = pack_bf16x2(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
+            pk.w = pack_bf16x2(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
+            dst[c * 4 + e] = pk;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // Merge the split partials of one (sequence, kv head): 8 query rows per CTA,
 // thread t takes output columns 4(t / 8) .. +3 of row t % 8, so a warp reads
 // four 128-byte runs of the [unit][column chunk][row] partials.  Two passes:
@@ -662,6 +1026,8 @@ void set_attn_attrs() {
     cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
+  cudaFuncSetAttribute(attn_pk2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)PK_SMEM);
   done = true;
 }
 
@@ -713,6 +1079,18 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
     return cudaErrorInvalidValue;
   if (kv_rows_total >= (1LL << 31) || q_rows_total >= (1LL << 31))
     return cudaErrorInvalidValue;
+  if (a.mode == 1) {
+    // packed layout: two Q tiles per CTA sharing one pass over the keys
+    CUtensorMap mq, mk, mv;
+    if (make_tmap_bf16_rows(&mq, qbuf, q_rows_total, HD, 128) != 0 ||
+        make_tmap_bf16_rows(&mk, cache_k, kv_rows_total, HD, 128) != 0 ||
+        make_tmap_bf16_rows(&mv, cache_v, kv_rows_total, HD, 128) != 0)
+      return cudaErrorInvalidValue;
+    const int per_unit = 2 * a.tile_blocks;
+    const int units = a.batch * a.n_kv * ((a.n_blocks + per_unit - 1) / per_unit);
+    return (int)launch_pdl(attn_pk2_kernel, dim3(units), dim3(PK_THREADS), PK_SMEM, stream, mq,
+                           mk, mv, a);
+  }
   const bool dual = a.mode == 0 && a.groups * a.q_len <= 64;
   CUtensorMap mq, mk, mv;
   if (make_tmap_bf16_rows(&mq, qbuf, q_rows_total, HD, dual ? 64 : 128) != 0 ||

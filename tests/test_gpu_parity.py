@@ -119,12 +119,18 @@ def test_fp32_ctx_project_matches_oracle():
     T.assert_close(T.f64(y), O.ctx_project(cfg, lw, T.f64(x)), "fp32", "fp32 ctx_project")
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_packed_training_layout_matches_oracle(dtype):
+# bf16 cases: (query heads, blocks).  A bf16 CTA takes two Q tiles of
+# 128 // (groups * 16) blocks each; the cases end on a unit with one partial
+# Q tile (8, 9), with a full and a partial Q tile (8, 7), with Q tiles of 96
+# rows (6, 7) and with 8-block units (4, 10).
+@pytest.mark.parametrize("dtype,heads,n_blocks", [("bf16", 8, 9), ("bf16", 8, 7),
+                                                  ("bf16", 6, 7), ("bf16", 4, 10),
+                                                  ("fp32", 0, 5)])
+def test_packed_training_layout_matches_oracle(dtype, heads, n_blocks):
     if dtype == "bf16":
-        sp = small_bf16(batch=2, seq=300, n_blocks=9)
+        sp = small_bf16(batch=2, seq=300, n_blocks=n_blocks, n_heads=heads)
     else:
-        sp = W.spec("tiny_fp32", batch=2, seq=100, n_blocks=5)
+        sp = W.spec("tiny_fp32", batch=2, seq=100, n_blocks=n_blocks)
     seed = 7
     w = W.weights(sp, seed)
     cfg, lw = T.oracle_layer(sp, w)

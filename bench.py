@@ -203,6 +203,9 @@ class ServingWorkload:
             if not self.fixed:
                 L = keep
         rows = max(int(sum(st["n_ctx"])) for st in self.steps)
+        # size every scratch buffer for the largest step up front, as a server
+        # does at start-up (a buffer that grows mid-run synchronises the device)
+        self.attn.reserve(B, B * q + rows, self.cap)
         self.th_buf = torch.empty(rows, sp.hidden, dtype=torch.bfloat16, device=device)
         self.out_buf = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16, device=device)
         self.out_h = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()

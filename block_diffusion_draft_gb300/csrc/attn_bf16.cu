@@ -24,14 +24,13 @@
 // takes keys 0..63 and lane r + 64 keys 64..127 of every tile as two
 // independent online-softmax streams (the other half of each P row is zero),
 // and the two are merged at the end.  All four softmax warps work and each
-// thread handles 64 columns per tile.  The packed training layout fills the
-// 128 rows with real queries (two blocks x 4 heads x 16 rows).
+// thread handles 64 columns per tile.  Blocks of more than 64 query rows use
+// the same kernel with one row per lane.  The packed training layout has its
+// own kernel below (attn_pk2_kernel).
 //
-// Masks ("nemo_automodel...draft_qwen3", _sliding_window_mask and the module
-// docstring): every row carries up to two allowed key intervals.
-//   inference, full layer   [unit start, unit end)
-//   inference, band layer   the same, cut to |query index - key| < W
-//   packed training         [0, anchor) and the row's own block
+// Masks ("nemo_automodel...draft_qwen3", _sliding_window_mask): a row's
+// allowed keys are the unit's key range, on a band layer cut to
+// |query index - key| < W.
 // A key range split across CTAs leaves per-split partials (unnormalised O,
 // running max, running sum); attn_combine_kernel merges them with the usual
 // log-sum-exp rescaling, one CTA per 8 query rows of a (sequence, kv head).
@@ -60,58 +59,31 @@ struct Unit {
   int rows;         // real query rows in the tile
   long long kv_row0;  // first K/V storage row of (b, h)
   int s0_lo, s0_hi, s1_lo, s1_hi;  // key segments
-  int blk0;         // packed: first block of the tile
   int direct;       // 1: this unit covers all keys of its rows
   int len;          // inference: keys of the sequence after this call
 };
 
+// Inference work unit u: split c of the keys of (sequence b, kv head h).
 DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
   Unit w;
   const int rows_per_block = a.groups * a.q_block;
-  if (a.mode == 0) {
-    int lo = 0, hi = a.batch;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sq.unit_off[mid] <= u) lo = mid; else hi = mid;
-    }
-    w.b = lo;
-    const int nch = sq.n_chunks[w.b];
-    const int r = u - sq.unit_off[w.b];
-    w.h = r / nch;
-    const int c = r - w.h * nch;
-    w.len = sq.len[w.b];
-    w.s0_lo = sq.lo[w.b] + c * sq.chunk[w.b];
-    w.s0_hi = min(w.len, w.s0_lo + sq.chunk[w.b]);
-    w.s1_lo = w.s1_hi = 0;
-    w.q_row0 = (w.b * a.n_kv + w.h) * rows_per_block;
-    w.rows = rows_per_block;
-    w.blk0 = 0;
-    w.direct = nch == 1;
-  } else {
-    const int n_tiles = (a.n_blocks + a.tile_blocks - 1) / a.tile_blocks;
-    const int per = a.batch * a.n_kv;
-    const int p_rev = u / per;
-    const int rem = u - p_rev * per;
-    w.b = rem / a.n_kv;
-    w.h = rem - w.b * a.n_kv;
-    const int p = n_tiles - 1 - p_rev;  // longest (latest anchors) first
-    w.blk0 = p * a.tile_blocks;
-    const int nbt = min(a.tile_blocks, a.n_blocks - w.blk0);
-    w.rows = nbt * rows_per_block;
-    w.q_row0 = ((w.b * a.n_kv + w.h) * a.n_blocks + w.blk0) * rows_per_block;
-    int amax = 0;
-    for (int k = 0; k < nbt; ++k) {
-      int an = a.anchors[w.b * a.n_blocks + w.blk0 + k];
-      an = min(max(an, 0), a.seq);
-      amax = max(amax, an);
-    }
-    w.s0_lo = 0;
-    w.s0_hi = amax;
-    w.s1_lo = a.seq + w.blk0 * a.q_block;
-    w.s1_hi = w.s1_lo + nbt * a.q_block;
-    w.direct = 1;
-    w.len = 0;
+  int lo = 0, hi = a.batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sq.unit_off[mid] <= u) lo = mid; else hi = mid;
   }
+  w.b = lo;
+  const int nch = sq.n_chunks[w.b];
+  const int r = u - sq.unit_off[w.b];
+  w.h = r / nch;
+  const int c = r - w.h * nch;
+  w.len = sq.len[w.b];
+  w.s0_lo = sq.lo[w.b] + c * sq.chunk[w.b];
+  w.s0_hi = min(w.len, w.s0_lo + sq.chunk[w.b]);
+  w.s1_lo = w.s1_hi = 0;
+  w.q_row0 = (w.b * a.n_kv + w.h) * rows_per_block;
+  w.rows = rows_per_block;
+  w.direct = nch == 1;
   w.kv_row0 = ((long long)w.b * a.n_kv + w.h) * a.cap;
   return w;
 }
@@ -269,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     grid_dep_wait();
     if (lane == 0) {
-      const uint64_t pol_kv = a.mode == 0 ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_first();
       mbar_arrive_expect_tx(q_full, TILE_BYTES);
       if (DUAL) {  // the 64 query rows twice: smem rows 0..63 and 64..127
@@ -346,39 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = DUAL ? (r >> 6) * 64 : 0;  // first S column of this thread
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     const bool real = qr < w.rows;
-    // this row's allowed key intervals
-    int i1_lo = 0, i1_hi = 0, i2_lo = 0, i2_hi = 0;
+    // this row's allowed keys: the unit's range, on a band layer cut to
+    // |query index - key| < W (the query's index is len - q_len + t)
+    int i1_lo = 0, i1_hi = 0;
     int out_token = 0, out_col = 0;
     {
-      const int rows_per_block = a.groups * a.q_block;
-      const int kb = qr / rows_per_block;
-      const int within = qr - kb * rows_per_block;
-      const int gi = within / a.q_block;
-      const int t = within - gi * a.q_block;
+      const int gi = qr / a.q_block;
+      const int t = qr - gi * a.q_block;
       out_col = (w.h * a.groups + gi) * HD;
-      if (a.mode == 0) {
-        out_token = w.b * a.q_len + t;
-        i1_lo = w.s0_lo;
-        i1_hi = w.s0_hi;
-        if (a.window > 0) {
-          const int qi = w.len - a.q_len + t;
-          i1_lo = max(i1_lo, qi - a.window + 1);
-          i1_hi = min(i1_hi, qi + a.window);
-        }
-      } else {
-        const int blk = w.blk0 + kb;
-        out_token = w.b * a.q_len + blk * a.q_block + t;
-        if (real) {
-          int an = a.anchors[w.b * a.n_blocks + blk];
-          if (an < 0 || an > a.seq) {
-            record_error(a.err, 3 /* DFLASH_DEV_ANCHOR */);
-            an = min(max(an, 0), a.seq);
-          }
-          i1_lo = 0;
-          i1_hi = an;
-          i2_lo = a.seq + blk * a.q_block;
-          i2_hi = i2_lo + a.q_block;
-        }
+      out_token = w.b * a.q_len + t;
+      i1_lo = w.s0_lo;
+      i1_hi = w.s0_hi;
+      if (a.window > 0) {
+        const int qi = w.len - a.q_len + t;
+        i1_lo = max(i1_lo, qi - a.window + 1);
+        i1_hi = min(i1_hi, qi + a.window);
       }
     }
     float m_run = -INFINITY, l_run = 0.f;
@@ -407,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             const int key = k0 + c;
-            const bool ok = (key >= i1_lo && key < i1_hi) || (key >= i2_lo && key < i2_hi);
-            if (!ok) s[c] = -INFINITY;
+            if (!(key >= i1_lo && key < i1_hi)) s[c] = -INFINITY;
           }
         }
         // row max and row sum as 8 interleaved partial chains (a single

@@ -197,12 +197,14 @@ class ServingWorkload:
             pos = torch.cat([W.window_positions(L[b], n_ctx[b], q) for b in range(B)])
             keep = [L[b] + n_ctx[b] for b in range(B)] if not self.fixed else list(pre)
             self.steps.append(dict(n_ctx=n_ctx, keep=keep, len_before=list(L),
-                                   x_h=x.pin_memory(), nz_h=nz.pin_memory(),
-                                   pos_h=pos.pin_memory(),
+                                   x_h=x, nz_h=nz, pos_h=pos,
                                    x=x.to(device), nz=nz.to(device), pos=pos.to(device)))
             if not self.fixed:
                 L = keep
         rows = max(int(sum(st["n_ctx"])) for st in self.steps)
+        self.stage = {k: torch.empty(max(st[k + "_h"].numel() for st in self.steps),
+                                     dtype=self.steps[0][k + "_h"].dtype).pin_memory()
+                      for k in ("x", "nz", "pos")}
         # size every scratch buffer for the largest step up front, as a server
         # does at start-up (a buffer that grows mid-run synchronises the device)
         self.attn.reserve(B, B * q + rows, self.cap)
@@ -228,12 +230,22 @@ class ServingWorkload:
         self.attn.forward(self.cache, st["nz"], th, st["n_ctx"], st["pos"], out=self.out_buf)
         self.cache.crop(st["keep"])
 
-    def step_e2e(self, i):
-        """The same step from pinned host buffers, result read back to host."""
+    def stage_e2e(self, i):
+        """Put step i's host inputs into the fixed pinned staging buffers (a
+        server receives each step's inputs into the same pinned memory; this
+        runs before the timed region)."""
         st = self._inputs(i)
-        st["x"].copy_(st["x_h"], non_blocking=True)
-        st["nz"].copy_(st["nz_h"], non_blocking=True)
-        st["pos"].copy_(st["pos_h"], non_blocking=True)
+        for k in ("x", "nz", "pos"):
+            n = st[k + "_h"].numel()
+            self.stage[k][:n].copy_(st[k + "_h"].view(-1))
+
+    def step_e2e(self, i):
+        """The same step from the pinned staging buffers, result read back to
+        host."""
+        st = self._inputs(i)
+        for k in ("x", "nz", "pos"):
+            dst = st[k]
+            dst.view(-1).copy_(self.stage[k][:dst.numel()], non_blocking=True)
         self.step(i)
         self.out_h.copy_(self.out_buf, non_blocking=True)
 
@@ -313,6 +325,9 @@ class PackedWorkload:
 
     def step(self, i):
         self.attn.forward_packed(self.nz, self.th, self.an, self.sp.block_size, out=self.out)
+
+    def stage_e2e(self, i):
+        """Inputs are the same every step and already sit in pinned memory."""
 
     def step_e2e(self, i):
         for d, h in ((self.th, self.th_h), (self.nz, self.nz_h), (self.an, self.an_h)):
@@ -590,11 +605,14 @@ def main():
 
     # ---------------------------------------------------- end to end (host)
     wl.reset()
-    h2d, d2h = wl.io_bytes(0)
+    io = [wl.io_bytes(i) for i in range(K)]
+    h2d = int(round(sum(b[0] for b in io) / K))
+    d2h = int(round(sum(b[1] for b in io) / K))
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(K)]
     torch.cuda.synchronize(device)
     for i in range(K):
+        wl.stage_e2e(i)
         flush.zero_()
         e_ev[i][0].record()
         wl.step_e2e(i)

@@ -94,6 +94,20 @@ int ensure_gemm_scratch(dflash_attn* a, int epi, int rows0, int rows1, int n, in
   return DFLASH_OK;
 }
 
+// Scratch for every GEMM shape with up to max0 / max1 rows.  Split-K scratch
+// is not monotonic in the row count (fewer row tiles take more K splits), so
+// every count of 128-row tiles is tried.
+int reserve_gemm_scratch(dflash_attn* a, int epi, int max0, int max1, int n, int k,
+                         int q_cols) {
+  const int m0 = (max0 + 127) / 128, m1 = (max1 + 127) / 128;
+  for (int i = 1; i <= m0; ++i)
+    for (int j = 0; j <= m1; ++j)
+      if (int r = ensure_gemm_scratch(a, epi, std::min(max0, i * 128), std::min(max1, j * 128),
+                                      n, k, q_cols))
+        return r;
+  return DFLASH_OK;
+}
+
 GemmScratch gemm_scratch(dflash_attn* a) {
   GemmScratch s;
   s.partial = static_cast<float*>(a->gemm_partial.p);
@@ -328,13 +342,19 @@ int dflash_attn_reserve(dflash_attn* a, int max_batch, int max_rows, int max_key
   DF_CUDA(a->attn_out.ensure((size_t)max_rows * qd * es), "scratch allocation");
   if (a->dt == DFLASH_BF16) {
     const int nqkv = (a->nq + 2 * a->nkv) * a->d;
-    if (int r = ensure_gemm_scratch(a, EPI_QKV, max_rows, max_rows, nqkv, a->H, a->nq * a->d))
+    if (int r = reserve_gemm_scratch(a, EPI_QKV, max_rows, max_rows, nqkv, a->H, a->nq * a->d))
       return r;
-    if (int r = ensure_gemm_scratch(a, EPI_BF16, max_rows, 0, a->H, a->nq * a->d, 0)) return r;
+    if (int r = reserve_gemm_scratch(a, EPI_BF16, max_rows, 0, a->H, a->nq * a->d, 0)) return r;
     if (a->nL > 0) {
-      if (int r = ensure_gemm_scratch(a, EPI_F32, max_rows, 0, a->H, a->nL * a->H, 0)) return r;
+      if (int r = reserve_gemm_scratch(a, EPI_F32, max_rows, 0, a->H, a->nL * a->H, 0)) return r;
     }
-    const size_t units = (size_t)max_batch * a->nkv * (max_keys / 256 + 2) + 2 * a->num_sms;
+    // a forward splits each sequence's keys into chunks of at least
+    // max(128, total keys / SMs) and at most 4096 keys: per kv head at most
+    // max(SMs, batch * ceil(keys / 4096)) + batch units
+    const size_t per_head = (size_t)std::max<long long>(
+                                a->num_sms, (long long)max_batch * ((max_keys + 4095) / 4096)) +
+                            max_batch;
+    const size_t units = (size_t)a->nkv * per_head;
     DF_CUDA(a->part_o.ensure(units * 128 * 128 * 4), "scratch allocation");
     DF_CUDA(a->part_ml.ensure(units * 256 * 4), "scratch allocation");
   }

@@ -235,14 +235,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    grid_dep_wait();
+    const uint64_t pol_kv = policy_evict_first();
+    const uint64_t pol_q = policy_evict_first();
+    auto load_kv = [&](int j) {
+      const int s = j % NST;
+      const int y = (int)(w.kv_row0 + tile_start(w, j));
+      mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
+      tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
+      tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
+      mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
+      tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
+      tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+    };
+    // Tiles made only of rows that were in the cache before this call were
+    // written by kernels that have completed (every kernel here starts its
+    // successor only after its own dependency wait): they fill the first
+    // stages while the previous kernel (the one appending this call's rows
+    // and writing Q) finishes.
+    int pre = 0;
     if (lane == 0) {
-      const uint64_t pol_kv = policy_evict_first();
-      const uint64_t pol_q = policy_evict_first();
+      const int first_new = sq.first_new[w.b];
+      for (; pre < T && pre < NST; ++pre) {
+        if (tile_start(w, pre) + BKEY > first_new) break;
+        load_kv(pre);
+      }
+    }
+    grid_dep_sync();
+    if (lane == 0) {
       mbar_arrive_expect_tx(q_full, TILE_BYTES);
       if (DUAL) {  // the 64 query rows twice: smem rows 0..63 and 64..127
         for (int copy = 0; copy < 2; ++copy)
@@ -253,22 +275,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sQ, &tmQ, q_full, 0, w.q_row0, pol_q);
         tma_load_2d(sQ + HALF_BYTES, &tmQ, q_full, 64, w.q_row0, pol_q);
       }
-      for (int j = 0; j < T; ++j) {
+      for (int j = pre; j < T; ++j) {
         const int s = j % NST;
         const uint32_t ph = (j / NST) & 1;
         if (!mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, a.err)) break;
-        const int y = (int)(w.kv_row0 + tile_start(w, j));
-        mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
-        tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
-        tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
-        mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
-        tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
-        tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+        load_kv(j);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    grid_dep_wait();
+    grid_dep_sync();
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, BKEY, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
@@ -311,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    grid_dep_wait();
+    grid_dep_sync();
     const int q = warp & 3;
     const int r = q * 32 + lane;                // TMEM lane (accumulator row)
     const int qr = DUAL ? (r & 63) : r;         // query row of the tile
@@ -679,11 +695,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    grid_dep_wait();
+    grid_dep_sync();
     if (lane == 0) {
       const uint64_t pol_kv = policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
@@ -708,7 +723,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    grid_dep_wait();
+    grid_dep_sync();
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, BKEY, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
@@ -757,7 +772,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    grid_dep_wait();
+    grid_dep_sync();
     const int i = (warp - 2) >> 2;  // Q tile of this warpgroup
     if (i < nqt && T > 0) {
       const int q = warp & 3;
@@ -924,7 +939,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
 __global__ void __launch_bounds__(256)
     attn_combine_kernel(const __grid_constant__ AttnArgs a,
                         const __grid_constant__ AttnSeqs sq) {
-  grid_dep_launch();
   const int rows_pair = a.groups * a.q_len;
   const int groups_per_pair = (rows_pair + 7) / 8;
   const int pair = blockIdx.x / groups_per_pair;
@@ -937,7 +951,7 @@ __global__ void __launch_bounds__(256)
   const size_t base = (size_t)sq.unit_off[b] + (size_t)h * nch;
   const float* ml = a.part_ml + base * 256 + r;
   const float4* po = reinterpret_cast<const float4*>(a.part_o + base * 128 * HD) + c4 * 128 + r;
-  grid_dep_wait();
+  grid_dep_sync();
   float M = -INFINITY;
 #pragma unroll 8
   for (int u = 0; u < nch; ++u) M = fmaxf(M, __ldcg(ml + (size_t)u * 256));

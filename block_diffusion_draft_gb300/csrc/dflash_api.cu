@@ -525,6 +525,7 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
   long long total_keys = 0;
   for (int b = 0; b < batch; ++b) {
     sq.len[b] = c->len[b] + host_n_ctx[b] + q_len;
+    sq.first_new[b] = c->len[b];
     sq.lo[b] = a->cfg.sliding_window > 0
                    ? std::max(0, sq.len[b] - q_len - a->cfg.sliding_window + 1)
                    : 0;

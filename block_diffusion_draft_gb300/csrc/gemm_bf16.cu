@@ -458,7 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -471,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[i], p.a_bytes + B_BYTES);
         tma_load_2d(sB + (size_t)i * B_BYTES, &tmB, &full[i], (kb0 + i) * BK, n0, pol_w);
       }
-      grid_dep_wait();
+      grid_dep_sync();
       for (int i = 0; i < nkb; ++i) {
         const int s = i % S;
         const int kx = (kb0 + i) * BK;
@@ -488,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    grid_dep_wait();
+    grid_dep_sync();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN, false);
       for (int i = 0; i < nkb; ++i) {
@@ -510,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    grid_dep_wait();
+    grid_dep_sync();
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
@@ -714,8 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_launch();
-  grid_dep_wait();
+  grid_dep_sync();
 
   if (warp == 0) {
     if (lane == 0) {

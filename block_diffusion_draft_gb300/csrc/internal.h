@@ -113,6 +113,8 @@ struct AttnSeqs {
   int n_chunks[kMaxBatch];     // splits of [lo, len) per kv head
   int chunk[kMaxBatch];        // keys per split (a multiple of 128)
   int unit_off[kMaxBatch + 1]; // first work unit of the sequence
+  int first_new[kMaxBatch];    // first row this call appends (rows below it
+                               // were written by earlier calls)
 };
 
 struct AttnArgs {

@@ -32,8 +32,7 @@ constexpr int kNormVec = 8;  // cols <= 512 * 4 * 8 = 16384
 __global__ void __launch_bounds__(kNormThreads)
     row_rmsnorm_kernel(const float* z, int cols, const float* w, float eps, void* out,
                        int out_bf16) {
-  grid_dep_launch();
-  grid_dep_wait();
+  grid_dep_sync();
   const float4* zr = reinterpret_cast<const float4*>(z + (size_t)blockIdx.x * cols);
   const int n4 = cols / 4;
   float4 x[kNormVec];

@@ -320,6 +320,16 @@ DF_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory");
 // while this grid finishes; it still waits in grid_dep_wait for our results).
 DF_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Wait for the previous kernel, then let the next one begin launching.  Every
+// kernel of this library triggers its successor only after its own wait, so
+// a kernel that has started knows that the kernel two places before it has
+// completed, and by induction every earlier kernel of the stream: it may read
+// data those kernels wrote (old cache rows) before its own wait.
+DF_DEV void grid_dep_sync() {
+  grid_dep_wait();
+  grid_dep_launch();
+}
+
 // ------------------------------------------------------ thread-block clusters
 DF_DEV uint32_t cluster_ctarank() {
   uint32_t r;

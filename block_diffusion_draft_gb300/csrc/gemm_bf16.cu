@@ -645,6 +645,200 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- swapped operands
+// 129 .. 384 token rows from one source (the context projection and o_proj of
+// mid-size batches).  The MMA takes a 128-row weight tile as A and the token
+// rows as B: N = the rows rounded up to 16, in one or two MMAs of at most 256,
+// so no tensor work goes to padding rows (the persistent kernel would compute
+// whole 128-row tiles).  D^T (weight rows x token rows) accumulates in TMEM.
+// The K splits of a weight tile form one thread-block cluster: each parks D^T
+// in its idle stage buffers as [token][column] rows, and every rank sums a
+// share of the tokens from all ranks, in rank order.
+constexpr int SWAP_MAX_ROWS = 384;
+
+struct SwapPlan {
+  int rows;          // token rows
+  int rb;            // rows rounded up to 16 (the MMA N, both chunks)
+  int xb0, xb1;      // rows of the two X boxes (xb1 = 0: one box)
+  int n_kb, splits, stages;
+  uint32_t x_bytes;  // X bytes per stage
+  uint32_t tmem_cols;
+  int ldc;
+  void* c;
+  int* err;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_swap_kernel(const __grid_constant__ CUtensorMap tmX0,
+                     const __grid_constant__ CUtensorMap tmX1,
+                     const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ SwapPlan p) {
+  constexpr uint32_t W_BYTES = BM * BK * 2;
+  constexpr int C4 = BM / 4;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint8_t* sW = smem;
+  uint8_t* sX = smem + (size_t)S * W_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + (size_t)S * p.x_bytes);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* accb = empty + MAX_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  const int kb0 = (int)((long long)split * p.n_kb / p.splits);
+  const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
+  const int nkb = kb1 - kb0;
+  const int n0 = n_tile * BM;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX0);
+    if (p.xb1 > 0) prefetch_tmap(&tmX1);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      // weights first: they do not depend on the previous kernel
+      const int pre = min(S, nkb);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], W_BYTES + p.x_bytes);
+        tma_load_2d(sW + (size_t)i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pol_w);
+      }
+      grid_dep_sync();
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        const int kx = (kb0 + i) * BK;
+        if (i >= pre) {
+          if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(&full[s], W_BYTES + p.x_bytes);
+          tma_load_2d(sW + (size_t)s * W_BYTES, &tmW, &full[s], kx, n0, pol_w);
+        }
+        uint8_t* x_dst = sX + (size_t)s * p.x_bytes;
+        tma_load_2d(x_dst, &tmX0, &full[s], kx, 0, pol_x);
+        if (p.xb1 > 0) tma_load_2d(x_dst + (size_t)p.xb0 * BK * 2, &tmX1, &full[s], kx, p.xb0, pol_x);
+      }
+    }
+  } else if (warp == 1) {
+    grid_dep_sync();
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_bf16(BM, p.xb0, false);
+      const uint32_t idesc1 = idesc_bf16(BM, p.xb1 > 0 ? p.xb1 : 16, false);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t w_base = smem_u32(sW + (size_t)s * W_BYTES);
+        const uint32_t x_base = smem_u32(sX + (size_t)s * p.x_bytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(w_base + kk * 32, 16, 1024);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tmem, ad, sdesc_sw128(x_base + kk * 32, 16, 1024), idesc0, acc);
+          if (p.xb1 > 0)
+            tc_mma_bf16(tmem + (uint32_t)p.xb0, ad,
+                        sdesc_sw128(x_base + (uint32_t)p.xb0 * BK * 2 + kk * 32, 16, 1024),
+                        idesc1, acc);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(accb);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    grid_dep_sync();
+    const int q = warp & 3;
+    const int j = q * 32 + lane;  // weight row of the tile = output column n0 + j
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
+    tc_fence_after();
+    float* park = reinterpret_cast<float*>(smem);
+    for (int t0 = 0; t0 < p.rb; t0 += 32) {
+      float v[32];
+      tmem_ld32(trow + (uint32_t)t0, v);
+      if (p.splits == 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = t0 + i;
+          if (t >= p.rows) break;
+          const float y = ok ? v[i] : 0.f;
+          if constexpr (EPI == EPI_F32)
+            reinterpret_cast<float*>(p.c)[(size_t)t * p.ldc + n0 + j] = y;
+          else
+            reinterpret_cast<__nv_bfloat16*>(p.c)[(size_t)t * p.ldc + n0 + j] =
+                __float2bfloat16_rn(y);
+        }
+      } else {
+        // token t's row in the park area: 32 float4 chunks, swizzled by t
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = t0 + i;
+          if (t >= p.rb) break;
+          park[(t * C4 + ((j >> 2) ^ (t & (C4 - 1)))) * 4 + (j & 3)] = ok ? v[i] : 0.f;
+        }
+      }
+    }
+  }
+
+  if (p.splits > 1) {
+    cluster_sync();
+    if (warp >= 2) {
+      const int rank = (int)cluster_ctarank();
+      const uint32_t base = smem_u32(smem);
+      for (int t = rank + p.splits * (warp & 3); t < p.rows; t += p.splits * 4) {
+        const uint32_t off = base + (uint32_t)(t * C4 + (lane ^ (t & (C4 - 1)))) * 16;
+        float4 acc = ld_cluster_f4(cluster_map(off, 0u));
+        for (int c = 1; c < p.splits; ++c) {
+          const float4 u = ld_cluster_f4(cluster_map(off, (uint32_t)c));
+          acc.x += u.x;
+          acc.y += u.y;
+          acc.z += u.z;
+          acc.w += u.w;
+        }
+        if constexpr (EPI == EPI_F32) {
+          reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)t * p.ldc + n0)[lane] =
+              acc;
+        } else {
+          uint2 pk;
+          pk.x = pack_bf16x2(acc.x, acc.y);
+          pk.y = pack_bf16x2(acc.z, acc.w);
+          reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)t * p.ldc +
+                                   n0)[lane] = pk;
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while the others still read its rows
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
 // ---------------------------------------------------------------- large M
 // Persistent variant for calls with many token rows: one CTA per SM walks
 // its share of 128 x 256 output tiles (round-robin over the grouped order).
@@ -953,9 +1147,64 @@ void set_smem_attr() {
                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
 }
 
+// one source of 129 .. 384 rows, plain epilogue: the swapped-operand kernel
+bool use_swap(int epi, int rows0, int rows1, int n) {
+  return epi != EPI_QKV && rows1 == 0 && rows0 > BM && rows0 <= SWAP_MAX_ROWS && n % BM == 0;
+}
+
 // many token rows and 256-aligned column regions: the persistent kernel
 bool use_big(int rows0, int rows1, int n, int q_cols) {
   return rows0 + rows1 > BM && n % BNB == 0 && q_cols % BNB == 0;
+}
+
+int launch_swap(const GemmShape& s, int epi, void* c, int ldc, int num_sms, int* err,
+                cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(gemm_swap_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_LIMIT);
+    cudaFuncSetAttribute(gemm_swap_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_LIMIT);
+    attr_done = true;
+  }
+  SwapPlan p{};
+  p.rows = s.a0_rows;
+  p.rb = (s.a0_rows + 15) / 16 * 16;
+  p.xb0 = std::min(p.rb, 256);
+  p.xb1 = p.rb - p.xb0;
+  p.n_kb = s.k / BK;
+  const int tiles = s.n / BM;
+  p.splits = choose_splits(tiles, p.n_kb, num_sms);
+  p.x_bytes = (uint32_t)p.rb * BK * 2;
+  const size_t stage = (size_t)BM * BK * 2 + p.x_bytes;
+  p.stages = (int)std::min<size_t>(MAX_STAGES, (SMEM_LIMIT - SMEM_FIXED) / stage);
+  // the split merge parks [rb][128] fp32 in the stage buffers
+  if (p.stages < 2 || (p.splits > 1 && (size_t)p.stages * stage < (size_t)p.rb * BM * 4))
+    return cudaErrorInvalidValue;
+  p.tmem_cols = p.rb <= 256 ? 256u : 512u;
+  p.ldc = ldc;
+  p.c = c;
+  p.err = err;
+  CUtensorMap mx0, mx1;
+  if (make_tmap_bf16_rows(&mx0, s.a0, s.a0_rows, s.k, p.xb0) != 0)
+    return cudaErrorInvalidValue;
+  if (p.xb1 > 0) {
+    if (make_tmap_bf16_rows(&mx1, s.a0, s.a0_rows, s.k, p.xb1) != 0)
+      return cudaErrorInvalidValue;
+  } else {
+    mx1 = mx0;
+  }
+  const size_t smem = SMEM_FIXED + (size_t)p.stages * stage;
+  const dim3 grid(tiles * p.splits), block(kThreads);
+  const unsigned cl = p.splits > 1 ? (unsigned)p.splits : 1u;
+  cudaError_t e;
+  if (epi == EPI_F32)
+    e = launch_pdl_cluster(gemm_swap_kernel<EPI_F32>, grid, block, smem, stream, cl, mx0, mx1,
+                           *s.b_map, p);
+  else
+    e = launch_pdl_cluster(gemm_swap_kernel<EPI_BF16>, grid, block, smem, stream, cl, mx0, mx1,
+                           *s.b_map, p);
+  return (int)e;
 }
 
 int big_tiles(int rows0, int rows1, int n, int q_cols) {
@@ -1008,6 +1257,10 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
 
 size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_cols,
                           int num_sms, int* n_counters) {
+  if (use_swap(epi, rows0, rows1, n)) {  // cluster merge, no scratch
+    if (n_counters) *n_counters = 0;
+    return 0;
+  }
   if (use_big(rows0, rows1, n, q_cols)) {
     const int tiles = big_tiles(rows0, rows1, n, q_cols);
     const int splits = big_splits(tiles, k / BK, num_sms);
@@ -1040,6 +1293,8 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
     attr_done = true;
   }
   if (s.k % BK != 0) return cudaErrorInvalidValue;
+  if (use_swap(epi, s.a0_rows, s.a1_rows, s.n))
+    return launch_swap(s, epi, c, ldc, num_sms, err, stream);
   if (use_big(s.a0_rows, s.a1_rows, s.n, s.q_cols))
     return launch_big(s, epi, c, ldc, qkv, seqs, scr, num_sms, err, stream);
   Geometry g = geometry(epi, s.a0_rows, s.a1_rows, s.n, s.k, s.q_cols, num_sms);

@@ -95,12 +95,23 @@ def test_bf16_large_batch_persistent_gemm():
         T.assert_close(v, vo, "bf16", "cache V")
 
 
+def test_bf16_mid_batch_swapped_operand_o_proj():
+    # 20 sequences x 16 block rows = 320 o_proj rows: the swapped-operand
+    # projection kernel (two MMA chunks of 256 + 64 token rows)
+    sp = small_bf16(batch=20)
+    sc = T.Scenario(sp, seed=13, capacity=256, check=[0, 9, 19])
+    n = [int(x) for x in np.random.default_rng(5).integers(0, 17, size=20)]
+    got, ref = sc.step(n)
+    T.assert_close(got, ref, "bf16", "batch 20")
+
+
 def test_bf16_ctx_project_matches_oracle():
     sp = small_bf16()
     w = W.weights(sp, 5)
     cfg, lw = T.oracle_layer(sp, w)
     attn = T.gpu_layer(sp, w)
-    for rows in (1, 16, 200, 600):
+    # 129 .. 384 rows take the swapped-operand kernel (one and two MMA chunks)
+    for rows in (1, 16, 129, 200, 384, 600):
         x = W.target_layer_rows(sp, 5, 0, rows, rows)
         y = attn.ctx_project(x.cuda())
         torch.cuda.synchronize()

@@ -280,16 +280,7 @@ class ServingWorkload:
         return {}
 
     def config(self):
-        sp = self.sp
-        c = {"workload": sp.name, "batch": sp.batch, "hidden": sp.hidden,
-             "heads": f"{sp.n_heads}/{sp.n_kv_heads}", "head_dim": sp.head_dim,
-             "block_size": sp.block_size, "fc_in": sp.n_target_layers * sp.hidden,
-             "new_ctx_rows": self.steps[0]["n_ctx"][0] if self.fixed else "U{1..16}",
-             "cached_ctx": sp.prefill if self.fixed else f"U[{sp.prefill_lo},{sp.prefill_hi}]",
-             "sliding_window": sp.sliding_window,
-             "step": "ctx_project + forward + crop",
-             "l2": "flushed (512 MiB write) before every timed step"}
-        return c
+        return spec_config(self.sp)
 
 
 class PackedWorkload:
@@ -355,12 +346,26 @@ class PackedWorkload:
         return {}
 
     def config(self):
-        sp = self.sp
+        return spec_config(self.sp)
+
+
+def spec_config(sp):
+    """The `config` of a workload's bench line (both arms)."""
+    if sp.seq > 0:
         return {"workload": sp.name, "batch": sp.batch, "seq": sp.seq,
                 "n_blocks": sp.n_blocks, "block_size": sp.block_size,
                 "hidden": sp.hidden, "heads": f"{sp.n_heads}/{sp.n_kv_heads}",
                 "head_dim": sp.head_dim, "step": "forward_packed",
                 "l2": "flushed (512 MiB write) before every timed step"}
+    fixed = sp.prefill > 0
+    return {"workload": sp.name, "batch": sp.batch, "hidden": sp.hidden,
+            "heads": f"{sp.n_heads}/{sp.n_kv_heads}", "head_dim": sp.head_dim,
+            "block_size": sp.block_size, "fc_in": sp.n_target_layers * sp.hidden,
+            "new_ctx_rows": sp.n_new if fixed else "U{1..16}",
+            "cached_ctx": sp.prefill if fixed else f"U[{sp.prefill_lo},{sp.prefill_hi}]",
+            "sliding_window": sp.sliding_window,
+            "step": "ctx_project + forward + crop",
+            "l2": "flushed (512 MiB write) before every timed step"}
 
 
 def make_workload(name, seed, device, n_steps):
@@ -472,6 +477,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
+        from block_diffusion_draft_gb300 import workloads as W
         Wm = max(1, args.warmup)
         r = OracleRunner(args.workload, args.seed)
         for _ in range(Wm):
@@ -483,7 +489,10 @@ def main():
                 "ms_per_step": 1000.0 * dt / n, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
-                "config": {"workload": args.workload, "arm": "fp64 CPU oracle"},
+                "config": dict(spec_config(W.SPECS[args.workload]),
+                               parallelism=f"replicas x{world}", timing="host wall clock",
+                               l2="not applicable (host cores)",
+                               arm="fp64 CPU oracle"),
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
                                  "kind": "oracle", "sample": r.sample},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -119,7 +119,7 @@ GemmScratch gemm_scratch(dflash_attn* a) {
 
 QkvOut make_qkv_out(const dflash_attn* a, const int* positions, void* qbuf,
                     void* k, void* v, int cap, int q_block) {
-  QkvOut o;
+  QkvOut o{};
   o.n_heads = a->nq;
   o.n_kv = a->nkv;
   o.groups = a->g;
@@ -586,6 +586,140 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
   }
   if (int r = run_o_proj(a, (int)rows_noise, out, s)) return r;
   for (int b = 0; b < batch; ++b) c->len[b] = sq.len[b];
+  return DFLASH_OK;
+}
+
+int dflash_kv_group_create(dflash_attn* const* layers, int n_layers, dflash_kv_group** out) {
+  if (out == nullptr || layers == nullptr) return fail(DFLASH_ERR_ARG, "null argument");
+  *out = nullptr;
+  if (n_layers < 1 || n_layers > kMaxGroupLayers)
+    return fail(DFLASH_ERR_ARG, "n_layers must be in 1..%d", kMaxGroupLayers);
+  const dflash_attn* a0 = layers[0];
+  if (a0 == nullptr) return fail(DFLASH_ERR_ARG, "null layer handle");
+  if (a0->dt != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "layer groups need bf16 layers");
+  for (int l = 0; l < n_layers; ++l) {
+    const dflash_attn* a = layers[l];
+    if (a == nullptr) return fail(DFLASH_ERR_ARG, "null layer handle %d", l);
+    if (a->dt != a0->dt || a->H != a0->H || a->nkv != a0->nkv || a->d != a0->d ||
+        a->device != a0->device || a->max_pos != a0->max_pos ||
+        a->cfg.rms_eps != a0->cfg.rms_eps || a->cfg.rope_theta != a0->cfg.rope_theta)
+      return fail(DFLASH_ERR_SHAPE,
+                  "layer %d differs from layer 0 (dtype, hidden, kv heads, head_dim, device, "
+                  "max_position, eps or rope_theta)", l);
+  }
+  dflash_kv_group* g = new dflash_kv_group();
+  g->n_layers = n_layers;
+  g->device = a0->device;
+  g->num_sms = a0->num_sms;
+  const size_t kv_rows = 2 * (size_t)a0->nkv * a0->d, H = a0->H;
+  cudaError_t e = cudaMalloc(&g->w_kv, n_layers * kv_rows * H * 2);
+  for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
+    g->layers[l] = layers[l];
+    // K and V rows follow the Q rows in the layer's stacked weight
+    const char* src = static_cast<const char*>(layers[l]->w_qkv) + (size_t)layers[l]->nq *
+                                                                          layers[l]->d * H * 2;
+    e = cudaMemcpy(static_cast<char*>(g->w_kv) + l * kv_rows * H * 2, src, kv_rows * H * 2,
+                   cudaMemcpyDeviceToDevice);
+  }
+  if (e != cudaSuccess) {
+    dflash_kv_group_destroy(g);
+    return cuda_fail(e, "layer group weights");
+  }
+  if (make_tmap_bf16_rows(&g->tm, g->w_kv, n_layers * kv_rows, (int)H, 128) != 0 ||
+      make_tmap_bf16_rows(&g->tm256, g->w_kv, n_layers * kv_rows, (int)H, 256) != 0) {
+    dflash_kv_group_destroy(g);
+    return fail(DFLASH_ERR_CUDA, "tensor map encoding failed");
+  }
+  *out = g;
+  return DFLASH_OK;
+}
+
+int dflash_kv_group_destroy(dflash_kv_group* g) {
+  if (g == nullptr) return DFLASH_OK;
+  cudaDeviceSynchronize();
+  cudaFree(g->w_kv);
+  g->gemm_partial.release();
+  g->gemm_counters.release();
+  delete g;
+  return DFLASH_OK;
+}
+
+int dflash_kv_group_append(dflash_kv_group* g, dflash_cache* const* caches, int batch,
+                           const void* target_hidden, const int32_t* host_n_ctx,
+                           const int32_t* positions, dflash_stream stream) {
+  if (g == nullptr || caches == nullptr || host_n_ctx == nullptr)
+    return fail(DFLASH_ERR_ARG, "null argument");
+  const dflash_attn* a0 = g->layers[0];
+  if (batch <= 0) return fail(DFLASH_ERR_ARG, "batch must be positive");
+  long long rows = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (host_n_ctx[b] < 0) return fail(DFLASH_ERR_ARG, "n_ctx[%d] < 0", b);
+    rows += host_n_ctx[b];
+  }
+  for (int l = 0; l < g->n_layers; ++l) {
+    const dflash_cache* c = caches[l];
+    if (c == nullptr) return fail(DFLASH_ERR_ARG, "null cache %d", l);
+    if (c->batch != batch) return fail(DFLASH_ERR_SHAPE, "cache %d batch differs", l);
+    if (c->nkv != a0->nkv || c->d != a0->d || c->dt != a0->dt)
+      return fail(DFLASH_ERR_SHAPE, "cache %d geometry does not match the layers", l);
+    for (int b = 0; b < batch; ++b) {
+      if (c->len[b] != caches[0]->len[b])
+        return fail(DFLASH_ERR_SHAPE, "caches 0 and %d hold different lengths (sequence %d)", l, b);
+      if ((long long)c->len[b] + host_n_ctx[b] > c->cap)
+        return fail(DFLASH_ERR_CAPACITY, "cache %d sequence %d: %d + %d rows exceed capacity %d",
+                    l, b, c->len[b], host_n_ctx[b], c->cap);
+    }
+  }
+  if (rows == 0) return DFLASH_OK;
+  if (rows > (1LL << 30)) return fail(DFLASH_ERR_SHAPE, "too many rows");
+  if (target_hidden == nullptr || positions == nullptr) return fail(DFLASH_ERR_ARG, "null tensor");
+  if (!aligned16(target_hidden)) return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SeqTable st;
+  st.n = batch;
+  st.q_len = 0;  // context rows only: position index = row index
+  st.ctx_off[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    st.ctx_off[b + 1] = st.ctx_off[b] + host_n_ctx[b];
+    st.cache_len[b] = caches[0]->len[b];
+  }
+  QkvOut o{};
+  o.n_heads = a0->nq;
+  o.n_kv = a0->nkv;
+  o.groups = a0->g;
+  o.q_block = 1;
+  o.max_pos = a0->max_pos;
+  o.eps = a0->cfg.rms_eps;
+  o.q_scale = 1.f;
+  o.positions = positions;
+  o.rope = a0->rope;
+  o.n_layers = g->n_layers;
+  for (int l = 0; l < g->n_layers; ++l) {
+    o.g_cache_k[l] = caches[l]->k;
+    o.g_cache_v[l] = caches[l]->v;
+    o.g_k_norm[l] = g->layers[l]->k_norm;
+    o.g_cap[l] = caches[l]->cap;
+  }
+  const int n = g->n_layers * 2 * a0->nkv * a0->d;
+  int n_counters = 0;
+  const size_t bytes = gemm_scratch_bytes(EPI_QKV, (int)rows, 0, n, a0->H, 0, g->num_sms,
+                                          &n_counters);
+  DF_CUDA(g->gemm_partial.ensure(std::max<size_t>(bytes, 256)), "scratch allocation");
+  DF_CUDA(g->gemm_counters.ensure((size_t)std::max(n_counters, 64) * sizeof(int), true),
+          "scratch allocation");
+  GemmScratch scr;
+  scr.partial = static_cast<float*>(g->gemm_partial.p);
+  scr.partial_bytes = g->gemm_partial.bytes;
+  scr.counters = static_cast<int*>(g->gemm_counters.p);
+  scr.n_counters = (int)(g->gemm_counters.bytes / sizeof(int));
+  GemmShape gs{target_hidden, (int)rows, nullptr, 0, &g->tm, &g->tm256, n, a0->H, 0};
+  {
+    TraceScope tr(g->layers[0], DFLASH_K_QKV, s);
+    DF_CUDA(launch_gemm_bf16(gs, EPI_QKV, nullptr, 0, &o, &st, scr, g->num_sms, a0->err, s),
+            "layer group projection launch");
+  }
+  for (int l = 0; l < g->n_layers; ++l)
+    for (int b = 0; b < batch; ++b) caches[l]->len[b] += host_n_ctx[b];
   return DFLASH_OK;
 }
 

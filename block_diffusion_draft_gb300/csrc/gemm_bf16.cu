@@ -173,12 +173,24 @@ struct QkvTarget {
   int kind;
   int pos_idx;             // index into the positions array
   __nv_bfloat16* dst;      // the 128-value bf16 destination row
+  const float* norm;       // RMSNorm gains of the row's head (null for V)
 };
+
+// RMSNorm gains of the head starting at output column n0 (null for V)
+DF_DEV const float* qkv_col_norm(const QkvOut& qo, int n0) {
+  const int kv_cols = qo.n_kv * HD;
+  if (qo.n_layers > 0) {
+    const int l = n0 / (2 * kv_cols);
+    return n0 - l * 2 * kv_cols < kv_cols ? qo.g_k_norm[l] : nullptr;
+  }
+  const int q_cols = qo.n_heads * HD;
+  return n0 < q_cols ? qo.q_norm : (n0 < q_cols + kv_cols ? qo.k_norm : nullptr);
+}
 
 DF_DEV QkvTarget qkv_target(const QkvOut& qo, const SeqTable& st, int src, int srow,
                             int n0) {
   int b, pos_idx, crow, t = 0;
-  if (src == 0) {  // noise (block) row
+  if (src == 0 && qo.n_layers == 0) {  // noise (block) row
     b = srow / st.q_len;
     t = srow - b * st.q_len;
     const int nb = st.ctx_off[b + 1] - st.ctx_off[b];
@@ -198,6 +210,18 @@ DF_DEV QkvTarget qkv_target(const QkvOut& qo, const SeqTable& st, int src, int s
   const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
   QkvTarget g;
   g.pos_idx = pos_idx;
+  g.norm = qkv_col_norm(qo, n0);
+  if (qo.n_layers > 0) {
+    // layer group: column n0 is K or V head h of layer l
+    const int l = n0 / (2 * kv_cols);
+    const int c = n0 - l * 2 * kv_cols;
+    const bool is_k = c < kv_cols;
+    const int h = (is_k ? c : c - kv_cols) / HD;
+    g.kind = is_k ? 2 : 3;
+    g.dst = reinterpret_cast<__nv_bfloat16*>(is_k ? qo.g_cache_k[l] : qo.g_cache_v[l]) +
+            (((size_t)b * qo.n_kv + h) * qo.g_cap[l] + crow) * HD;
+    return g;
+  }
   if (n0 < q_cols) {
     if (src != 0) {
       g.kind = 0;
@@ -259,7 +283,7 @@ DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, floa
     if (g.kind == 0) return;
     if (g.kind != 3) {
       const int pos = checked_position(qo, g.pos_idx, p.err);
-      norm_rope(v, g.kind == 1 ? qo.q_norm : qo.k_norm, qo.eps,
+      norm_rope(v, g.norm, qo.eps,
                 qo.rope + (size_t)pos * (HD / 2), g.kind == 1 ? qo.q_scale : 1.f);
     }
     store_bf16(g.dst, v, HD);
@@ -519,12 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // While the main loop runs: this tile's norm weights into registers,
       // and lane l looks up the position of row q + 4l (the rows warp q
       // finishes) and warms L2 with its RoPE row.
-      const int q_cols = qo.n_heads * HD, kv_cols = qo.n_kv * HD;
-      const bool roped = n0 < q_cols + kv_cols;
-      const float4 w4 =
-          roped ? __ldg(reinterpret_cast<const float4*>(n0 < q_cols ? qo.q_norm : qo.k_norm) +
-                        lane)
-                : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* norm = qkv_col_norm(qo, n0);
+      const float4 w4 = norm != nullptr ? __ldg(reinterpret_cast<const float4*>(norm) + lane)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
       int lane_kind = 0, lane_pos = 0;
       __nv_bfloat16* lane_dst = nullptr;
       {

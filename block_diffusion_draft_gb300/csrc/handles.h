@@ -62,6 +62,16 @@ struct dflash_attn {
       zbuf, proj_noise, proj_ctx, packed_k, packed_v, packed_pos;
 };
 
+// Context K/V of several layers from one projection: the layers' K and V
+// weights stacked as [layer][K rows | V rows][H] bf16.
+struct dflash_kv_group {
+  int n_layers = 0, device = 0, num_sms = 0;
+  dflash_attn* layers[df::kMaxGroupLayers] = {};
+  void* w_kv = nullptr;
+  CUtensorMap tm, tm256;
+  df::Buf gemm_partial, gemm_counters;
+};
+
 struct dflash_cache {
   int batch = 0, cap = 0, nkv = 0, d = 0, dt = 0, device = 0;
   void* k = nullptr;

@@ -11,6 +11,7 @@
 namespace df {
 
 constexpr int kMaxBatch = 512;
+constexpr int kMaxGroupLayers = 16;  // layers of one context K/V group
 
 // Per-sequence bookkeeping of one forward call, passed to kernels by value.
 struct SeqTable {
@@ -35,6 +36,13 @@ struct QkvOut {
   void* qbuf;              // [B][n_kv][n_blocks][groups][q_block][d]
   void* cache_k;           // [B][n_kv][cap][d]
   void* cache_v;
+  // layer group (context K/V of several layers from one GEMM, no Q columns):
+  // n_layers > 0, columns [layer][K heads | V heads], every row a context row
+  int n_layers;
+  void* g_cache_k[kMaxGroupLayers];
+  void* g_cache_v[kMaxGroupLayers];
+  const float* g_k_norm[kMaxGroupLayers];
+  int g_cap[kMaxGroupLayers];
 };
 
 // Launch with programmatic stream serialization: the kernel may start while

@@ -59,6 +59,10 @@ _SIGNATURES = {
                              POINTER(c_int32), c_void_p, c_void_p, c_void_p], c_int),
     "dflash_attn_forward_packed": ([c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p], c_int),
+    "dflash_kv_group_create": ([POINTER(c_void_p), c_int, POINTER(c_void_p)], c_int),
+    "dflash_kv_group_destroy": ([c_void_p], c_int),
+    "dflash_kv_group_append": ([c_void_p, POINTER(c_void_p), c_int, c_void_p,
+                                POINTER(c_int32), c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
     "dflash_trace_enable": ([c_void_p, c_int], c_int),
     "dflash_trace_read": ([c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int32)],
@@ -260,6 +264,42 @@ class DraftCache:
     def close(self) -> None:
         if getattr(self, "handle", None):
             lib().dflash_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class KVGroup:
+    """Context K/V of several layers from one projection (the layers' K and V
+    weights stacked); see dflash_kv_group_* in include/dflash_attn.h."""
+
+    def __init__(self, layers: Sequence[DFlashAttention]):
+        self.layers = list(layers)
+        self.device = self.layers[0].device
+        arr = (c_void_p * len(self.layers))(*[l.handle.value for l in self.layers])
+        h = c_void_p()
+        with torch.cuda.device(self.device):
+            check(lib().dflash_kv_group_create(arr, len(self.layers), ctypes.byref(h)))
+        self.handle = h
+
+    def append(self, caches: Sequence["DraftCache"], target_hidden: Optional[torch.Tensor],
+               n_ctx: Sequence[int], positions: Optional[torch.Tensor]) -> None:
+        """Append the new context rows' K/V of every layer to its cache."""
+        arr = (c_void_p * len(caches))(*[c.handle.value for c in caches])
+        th = None if target_hidden is None or target_hidden.numel() == 0 else target_hidden
+        with torch.cuda.device(self.device):
+            check(lib().dflash_kv_group_append(self.handle, arr, len(n_ctx), _p(th),
+                                               _int32_array(n_ctx), _p(positions),
+                                               _stream(self.device)))
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            with torch.cuda.device(self.device):
+                lib().dflash_kv_group_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

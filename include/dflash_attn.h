@@ -49,6 +49,7 @@ extern "C" {
 
 typedef struct dflash_attn dflash_attn;   /* one layer: weights + scratch */
 typedef struct dflash_cache dflash_cache; /* one draft KV cache */
+typedef struct dflash_kv_group dflash_kv_group; /* context K/V of several layers */
 typedef void* dflash_stream;              /* a cudaStream_t */
 
 enum {
@@ -224,6 +225,39 @@ int dflash_attn_forward(dflash_attn* attn, dflash_cache* cache, int batch,
                         const void* target_hidden, const int32_t* host_n_ctx,
                         const int32_t* positions, void* out,
                         dflash_stream stream);
+
+/* Context K/V of several draft layers in one projection ([P5]
+ * precompute_and_store_context_kv: the context K/V of all layers come from one
+ * GEMM over their stacked k_proj/v_proj weights, then each layer's k_norm,
+ * RoPE and cache insert).
+ *
+ * dflash_kv_group_create stacks the K and V weights of n_layers (1..16) bf16
+ * layers that share hidden, n_kv_heads, head_dim, device, max_position,
+ * rms_eps and rope_theta (else _SHAPE; fp32 layers _UNSUPPORTED).  The group
+ * owns a copy of those weights; the layers must outlive it.
+ *
+ * dflash_kv_group_append projects the batch's new context rows once for all
+ * layers and appends, for layer l, K = RoPE(k_norm_l(T Wk_l^T)) and
+ * V = T Wv_l^T to caches[l] at its current lengths, exactly as
+ * dflash_attn_forward appends context rows.  Afterwards call each layer's
+ * dflash_attn_forward with host_n_ctx all zero (and positions for the block
+ * rows only): it appends the block rows and attends over every cached row.
+ *   caches          host array of n_layers cache handles (same batch and
+ *                   lengths; geometry of the layers)
+ *   target_hidden   device [sum n_i, H] bf16, sequence-major (may be NULL
+ *                   when every n_i is 0)
+ *   host_n_ctx      host [batch] new context rows per sequence
+ *   positions       device [sum n_i] int32, the context rows' positions
+ * Errors: _ARG (nulls, negative counts), _SHAPE (batch, geometry or lengths
+ * differ between caches), _CAPACITY (a cache would overflow; nothing is
+ * appended). */
+int dflash_kv_group_create(dflash_attn* const* layers, int n_layers,
+                           dflash_kv_group** out);
+int dflash_kv_group_destroy(dflash_kv_group* group);
+int dflash_kv_group_append(dflash_kv_group* group, dflash_cache* const* caches,
+                           int batch, const void* target_hidden,
+                           const int32_t* host_n_ctx, const int32_t* positions,
+                           dflash_stream stream);
 
 /* Training-layout forward with no cache ([P4] module docstring: each block's
  * queries see the context strictly before its anchor plus their own block,

@@ -349,6 +349,126 @@ class PackedWorkload:
         return spec_config(self.sp)
 
 
+class StackWorkload:
+    """A stack of draft layers fed by one projected context per step:
+    ctx_project (layer 0's fc) -> the context K/V of every layer from one
+    grouped projection -> each layer's forward with no context rows -> crop.
+    `per_layer_step` runs the same step with each layer's forward projecting
+    the context rows itself (the plain schedule), timed for comparison."""
+
+    def __init__(self, sp, seed, device, n_steps):
+        import torch
+        from block_diffusion_draft_gb300 import DFlashAttention, DraftCache, KVGroup
+        from block_diffusion_draft_gb300 import workloads as W
+
+        self.sp, self.dev, self.W = sp, device, W
+        L, B, q, pre, n = sp.layers, sp.batch, sp.block_size, sp.prefill, sp.n_new
+        self.layers, self.caches = [], []
+        self.cap = pre + n + 2 * q + 16
+        for l in range(L):
+            w = W.weights(sp, seed, layer=l, with_fc=l == 0)
+            a = DFlashAttention(w, hidden=sp.hidden, n_heads=sp.n_heads,
+                                n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
+                                n_target_layers=sp.n_target_layers if l == 0 else 0,
+                                rms_eps=sp.rms_eps, rope_theta=sp.rope_theta,
+                                sliding_window=sp.sliding_window,
+                                max_position=sp.max_position, device=device)
+            del w
+            c = DraftCache(a, B, self.cap)
+            th = torch.cat([W.hidden_rows(sp, seed, "hidden", 1000, b, pre) for b in range(B)])
+            nz = torch.stack([W.hidden_rows(sp, seed, "noise", 1000 + l, b, q) for b in range(B)])
+            pos = torch.cat([W.window_positions(0, pre, q) for b in range(B)])
+            a.forward(c, nz.to(device), th.to(device), [pre] * B, pos.to(device))
+            c.crop([pre] * B)
+            a.reserve(B, B * q + B * n, self.cap)
+            self.layers.append(a)
+            self.caches.append(c)
+        self.attn = self.layers[0]
+        self.group = KVGroup(self.layers)
+        torch.cuda.synchronize(device)
+        self.x_h = torch.cat([W.target_layer_rows(sp, seed, 0, b, n) for b in range(B)])
+        self.nz_h = torch.stack([torch.stack([W.hidden_rows(sp, seed, "noise", l, b, q)
+                                              for b in range(B)]) for l in range(L)])
+        self.pos_ctx_h = torch.cat([torch.arange(pre, pre + n, dtype=torch.int32)
+                                    for b in range(B)])
+        self.pos_blk_h = torch.cat([W.window_positions(pre + n, 0, q) for b in range(B)])
+        self.pos_full_h = torch.cat([W.window_positions(pre, n, q) for b in range(B)])
+        self.x, self.nz = self.x_h.to(device), self.nz_h.to(device)
+        self.pos_ctx, self.pos_blk = self.pos_ctx_h.to(device), self.pos_blk_h.to(device)
+        self.pos_full = self.pos_full_h.to(device)
+        for t in ("x_h", "nz_h", "pos_ctx_h", "pos_blk_h", "pos_full_h"):
+            setattr(self, t, getattr(self, t).pin_memory())
+        self.th = torch.empty(B * n, sp.hidden, dtype=torch.bfloat16, device=device)
+        self.out = torch.empty(L, B, q, sp.hidden, dtype=torch.bfloat16, device=device)
+        self.out_h = torch.empty(L, B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()
+        self.fixed = True
+        self.blocks_per_step = B * L  # blocks per layer-step summed over the layers
+        self.launches_per_step = 3 + 3 * L
+
+    def handles(self):
+        return self.layers
+
+    def reset(self):
+        pass
+
+    def step(self, i=0):
+        sp, B, n = self.sp, self.sp.batch, self.sp.n_new
+        self.attn.ctx_project(self.x, out=self.th)
+        self.group.append(self.caches, self.th, [n] * B, self.pos_ctx)
+        for l, (a, c) in enumerate(zip(self.layers, self.caches)):
+            a.forward(c, self.nz[l], None, [0] * B, self.pos_blk, out=self.out[l])
+        for c in self.caches:
+            c.crop([sp.prefill] * B)
+
+    def per_layer_step(self, i=0):
+        sp, B, n = self.sp, self.sp.batch, self.sp.n_new
+        self.attn.ctx_project(self.x, out=self.th)
+        for l, (a, c) in enumerate(zip(self.layers, self.caches)):
+            a.forward(c, self.nz[l], self.th, [n] * B, self.pos_full, out=self.out[l])
+        for c in self.caches:
+            c.crop([sp.prefill] * B)
+
+    def stage_e2e(self, i):
+        """Inputs are the same every step and already sit in pinned memory."""
+
+    def step_e2e(self, i):
+        for d, h in ((self.x, self.x_h), (self.nz, self.nz_h), (self.pos_ctx, self.pos_ctx_h),
+                     (self.pos_blk, self.pos_blk_h)):
+            d.copy_(h, non_blocking=True)
+        self.step(i)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+    def io_bytes(self, i):
+        h2d = sum(t.numel() * t.element_size()
+                  for t in (self.x_h, self.nz_h, self.pos_ctx_h, self.pos_blk_h))
+        return h2d, self.out_h.numel() * self.out_h.element_size()
+
+    def kernel_bytes(self, i):
+        """Algorithmic HBM bytes per trace bucket of one grouped step."""
+        sp = self.sp
+        H, d, nq, nkv, q, B, L = (sp.hidden, sp.head_dim, sp.n_heads, sp.n_kv_heads,
+                                  sp.block_size, sp.batch, sp.layers)
+        n = B * sp.n_new
+        K = sp.n_target_layers * H
+        keys = B * (sp.prefill + sp.n_new + q)
+        return {
+            "fc": H * K * 2 + n * K * 2 + n * H * 4,
+            "norm": n * H * 4 + n * H * 2,
+            # grouped K/V projection of the context rows, then each layer's
+            # Q/K/V projection of its block rows
+            "qkv": L * 2 * nkv * d * H * 2 + n * H * 2 + L * n * 2 * nkv * d * 2
+                   + L * ((nq + 2 * nkv) * d * H * 2 + B * q * H * 2 + B * q * (nq + 2 * nkv) * d * 2),
+            "attn": L * (keys * nkv * d * 2 * 2 + 2 * B * q * nq * d * 2),
+            "o_proj": L * (H * nq * d * 2 + B * q * nq * d * 2 + B * q * H * 2),
+        }
+
+    def kernel_flops(self, i):
+        return {}
+
+    def config(self):
+        return spec_config(self.sp)
+
+
 def spec_config(sp):
     """The `config` of a workload's bench line (both arms)."""
     if sp.seq > 0:
@@ -358,6 +478,9 @@ def spec_config(sp):
                 "head_dim": sp.head_dim, "step": "forward_packed",
                 "l2": "flushed (512 MiB write) before every timed step"}
     fixed = sp.prefill > 0
+    extra = {"layers": sp.layers,
+             "step": "ctx_project + grouped context K/V of all layers + per-layer forward "
+                     "(no context rows) + crop"} if sp.layers > 1 else {}
     return {"workload": sp.name, "batch": sp.batch, "hidden": sp.hidden,
             "heads": f"{sp.n_heads}/{sp.n_kv_heads}", "head_dim": sp.head_dim,
             "block_size": sp.block_size, "fc_in": sp.n_target_layers * sp.hidden,
@@ -365,12 +488,14 @@ def spec_config(sp):
             "cached_ctx": sp.prefill if fixed else f"U[{sp.prefill_lo},{sp.prefill_hi}]",
             "sliding_window": sp.sliding_window,
             "step": "ctx_project + forward + crop",
-            "l2": "flushed (512 MiB write) before every timed step"}
+            "l2": "flushed (512 MiB write) before every timed step", **extra}
 
 
 def make_workload(name, seed, device, n_steps):
     from block_diffusion_draft_gb300 import workloads as W
     sp = W.SPECS[name]
+    if sp.layers > 1:
+        return StackWorkload(sp, seed, device, n_steps)
     if sp.seq > 0:
         return PackedWorkload(sp, seed, device, n_steps)
     return ServingWorkload(sp, seed, device, n_steps)
@@ -432,6 +557,21 @@ class OracleRunner:
             self.blocks_per_step = 1
             self.sample = ("ctx_project + forward + crop of one sequence per step "
                            f"({pre} cached rows, {n} new, block {q})")
+            # layer stack: the other layers (own weights and caches), each step
+            # their per-layer forward with the context rows (the definition)
+            self.more = []
+            for l in range(1, sp.layers):
+                wl_ = W.weights(sp, seed, layer=l, with_fc=False)
+                lw = O.LayerWeights(*(f64(wl_[k]) for k in ("wq", "wk", "wv", "wo", "q_norm",
+                                                             "k_norm")))
+                c = O.DraftCache(sp.n_kv_heads, sp.head_dim, 1)
+                O.forward(self.cfg, lw, c, nz[None], [th], [W.window_positions(0, pre, q).numpy()])
+                c.crop([pre])
+                self.more.append((lw, c, f64(W.hidden_rows(sp, seed, "noise", l, 0, q))[None]))
+            if sp.layers > 1:
+                self.blocks_per_step = sp.layers
+                self.sample = (f"ctx_project + {sp.layers} per-layer forwards + crop of one "
+                               f"sequence per step ({pre} cached rows, {n} new, block {q})")
 
     def step(self):
         O, sp = self.O, self.sp
@@ -442,6 +582,9 @@ class OracleRunner:
             t = O.ctx_project(self.cfg, self.lw, self.x)
             O.forward(self.cfg, self.lw, self.cache, self.nzs, [t], [self.pos])
             self.cache.crop([self.pre])
+            for lw, c, nzs in self.more:
+                O.forward(self.cfg, lw, c, nzs, [t], [self.pos])
+                c.crop([self.pre])
 
     def time(self, steps, budget_s):
         t0 = time.perf_counter()
@@ -578,15 +721,47 @@ def main():
         ms = float(t.item())
     value = world * wl.blocks_per_step / (ms / 1000.0)
 
+    # the plain per-layer schedule of a layer stack, same inputs, for comparison
+    per_layer = None
+    if hasattr(wl, "per_layer_step"):
+        g2 = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(device)
+        s2.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s2):
+            wl.per_layer_step(0)
+            torch.cuda.synchronize(device)
+            with torch.cuda.graph(g2, stream=s2):
+                wl.per_layer_step(0)
+        torch.cuda.current_stream(device).wait_stream(s2)
+        torch.cuda.synchronize(device)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            ev2[i][0].record()
+            g2.replay()
+            ev2[i][1].record()
+        torch.cuda.synchronize(device)
+        ms2 = float(np.mean([a.elapsed_time(b) for a, b in ev2]))
+        per_layer = {"ms_per_step": ms2,
+                     "value": world * wl.blocks_per_step / (ms2 / 1000.0),
+                     "step": "ctx_project + per-layer forward with the context rows + crop"}
+
     # ---------------------------------------------------- per-kernel timing
+    handles = wl.handles() if hasattr(wl, "handles") else [wl.attn]
     wl.reset()
-    wl.attn.trace(True)
+    for h in handles:
+        h.trace(True)
     for i in range(K):
         flush.zero_()
         wl.step(i)
     torch.cuda.synchronize(device)
-    tr = wl.attn.trace_read()
-    wl.attn.trace(False)
+    tr = {}
+    for h in handles:
+        for name, (t_ms, n_l) in h.trace_read().items():
+            t0_, n0_ = tr.get(name, (0.0, 0))
+            tr[name] = (t0_ + t_ms, n0_ + n_l)
+        h.trace(False)
     kb = [wl.kernel_bytes(i) for i in range(K)]
     kf = [wl.kernel_flops(i) for i in range(K)]
     per_kernel = {}
@@ -634,7 +809,7 @@ def main():
         e_ms = float(t.item())
     e2e = {"value": world * wl.blocks_per_step / (e_ms / 1000.0), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
-    err = wl.attn.device_error()
+    err = max(h.device_error() for h in handles)
 
     if rank != 0:
         if dist is not None:
@@ -651,6 +826,8 @@ def main():
             "clocks": clocks.summary(t0, t1) if clocks else None,
             "e2e": e2e, "gpu_launches": K * wl.launches_per_step,
             "device_error": err}
+    if per_layer:
+        line["per_layer_schedule"] = per_layer
     step_bytes = sum(kb[0].values()) if kb[0] else None
     if step_bytes:
         line["step_achieved_gbs"] = step_bytes / (ms / 1000.0) / 1e9

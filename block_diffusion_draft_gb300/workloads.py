@@ -54,6 +54,8 @@ class Spec:
     seq: int = 0
     n_blocks: int = 0
     max_position: int = 65536
+    # layer stacks: draft layers sharing the step's projected context
+    layers: int = 1
 
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
@@ -82,6 +84,15 @@ SPECS: Dict[str, Spec] = {
                          n_kv_heads=8, head_dim=128, block_size=16, batch=4,
                          dtype="bf16", prefill=32768, n_new=16,
                          sliding_window=4096),
+    # five Qwen3-8B-shaped draft layers fed by one projected context: 4096
+    # cached rows, then 16 (decode) or 512 (a long accepted run / prefill
+    # chunk) new context rows and one block per layer
+    "stack5_ctx16": Spec("stack5_ctx16", hidden=4096, n_heads=32, n_kv_heads=8,
+                         head_dim=128, block_size=16, batch=1, dtype="bf16",
+                         prefill=4096, n_new=16, layers=5),
+    "stack5_ctx512": Spec("stack5_ctx512", hidden=4096, n_heads=32, n_kv_heads=8,
+                          head_dim=128, block_size=16, batch=1, dtype="bf16",
+                          prefill=4096, n_new=512, layers=5),
     # packed training layout: 2 x 4096 context rows, 256 anchors x 16 rows
     "packed_train": Spec("packed_train", hidden=4096, n_heads=32,
                          n_kv_heads=8, head_dim=128, block_size=16, batch=2,

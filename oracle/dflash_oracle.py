@@ -413,3 +413,58 @@ def forward_packed(cfg: LayerConfig, w: LayerWeights, noise: np.ndarray,
             o = attention(cfg, q, k, v, allowed)
             out[b, rows] = linear(o, w.wo)
     return out
+
+
+# --------------------------------------------------------------------------
+# decoder layer: norms, residuals and the MLP around the attention
+# --------------------------------------------------------------------------
+@dataclass
+class MlpWeights:
+    """The rest of a draft decoder layer.
+
+    [P4] ``Qwen3DFlashDecoderLayer``: ``input_layernorm``, ``self_attn``,
+    ``post_attention_layernorm`` and ``mlp = Qwen3MLP(config)``; [P5] stacks
+    ``gate_proj`` and ``up_proj`` into one ``gate_up_proj``.  nn.Linear
+    layout [out, in]: gate, up [intermediate, hidden]; down [hidden,
+    intermediate]; norm gains [hidden].
+    """
+
+    gate: np.ndarray
+    up: np.ndarray
+    down: np.ndarray
+    input_norm: np.ndarray
+    post_norm: np.ndarray
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU, ``x * sigmoid(x)`` (the Qwen3 MLP activation; reading taken:
+    the pages name Qwen3MLP without printing it)."""
+    return x / (1.0 + np.exp(-x))
+
+
+def mlp(m: MlpWeights, y: np.ndarray) -> np.ndarray:
+    """Qwen3 MLP: ``down(silu(gate(y)) * up(y))``."""
+    return linear(silu(linear(y, m.gate)) * linear(y, m.up), m.down)
+
+
+def decoder_layer(cfg: LayerConfig, w: LayerWeights, m: MlpWeights, cache: DraftCache,
+                  hidden: np.ndarray, residual: Optional[np.ndarray],
+                  target_hidden: Sequence[np.ndarray], positions: Sequence[np.ndarray],
+                  seqs: Optional[Sequence[int]] = None):
+    """One draft decoder layer over a batch of blocks, updating ``cache``.
+
+    Pre-norm residual block in the residual-stream form of [P5]'s draft model
+    (each layer returns ``(hidden_states, residual)``; the next layer adds
+    them):  ``r1 = hidden + residual`` (or ``hidden`` for the first layer),
+    ``r2 = r1 + attn(input_norm(r1))``, output ``(mlp(post_norm(r2)), r2)``.
+    ``hidden`` / ``residual`` [B, q_len, hidden]; the attention takes the
+    normed rows as its noise rows (context K/V from ``target_hidden``).
+    Reading taken: the standard Qwen3 decoder order (the pages list the parts
+    of [P4] ``Qwen3DFlashDecoderLayer`` but not its forward body).
+    """
+    r1 = hidden if residual is None else hidden + residual
+    a = forward(cfg, w, cache, rms_norm(r1, m.input_norm, cfg.rms_eps), target_hidden,
+                positions, seqs=seqs)
+    r2 = r1 + a
+    out = mlp(m, rms_norm(r2, m.post_norm, cfg.rms_eps))
+    return out, r2

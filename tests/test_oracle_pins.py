@@ -475,6 +475,123 @@ def test_ctx_project_is_norm_of_fc_and_checks_width():
 # --------------------------------------------------------------------------
 # the pins catch plausible slips
 # --------------------------------------------------------------------------
+# --------------------------------------------------------------------------
+# decoder layer: SiLU, the Qwen3 MLP, norms and residuals
+# --------------------------------------------------------------------------
+def test_silu_closed_forms():
+    x = np.linspace(-30.0, 30.0, 121)
+    y = O.silu(x)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    # silu(x) - silu(-x) = x (sigmoid(x) + sigmoid(-x) = 1)
+    np.testing.assert_allclose(y - O.silu(-x), x, rtol=0, atol=1e-12)
+    # silu(1) = 1 / (1 + 1/e); large |x|: x and 0
+    assert abs(O.silu(np.array([1.0]))[0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(y[-1] - 30.0) < 1e-11 and abs(y[0]) < 1e-11
+
+
+def tiny_mlp(H, inter, rng, gains=True):
+    g = (lambda n: 1.0 + 0.3 * rng.standard_normal(n)) if gains else np.ones
+    return O.MlpWeights(gate=0.2 * rng.standard_normal((inter, H)),
+                        up=0.2 * rng.standard_normal((inter, H)),
+                        down=0.2 * rng.standard_normal((H, inter)),
+                        input_norm=g(H), post_norm=g(H))
+
+
+def _brute_mlp(m, y):
+    """down(silu(gate y) * up y) with explicit sums and the sigmoid written out."""
+    H, inter = m.gate.shape[1], m.gate.shape[0]
+    out = np.zeros((y.shape[0], H))
+    for r in range(y.shape[0]):
+        act = []
+        for j in range(inter):
+            gj = sum(m.gate[j, k] * y[r, k] for k in range(H))
+            uj = sum(m.up[j, k] * y[r, k] for k in range(H))
+            act.append(gj / (1.0 + math.exp(-gj)) * uj)
+        for i in range(H):
+            out[r, i] = sum(m.down[i, j] * act[j] for j in range(inter))
+    return out
+
+
+def _brute_norm(x, w, eps):
+    out = np.empty_like(x)
+    for r in range(x.shape[0]):
+        ms = sum(float(v) * float(v) for v in x[r]) / x.shape[1]
+        out[r] = [w[i] * x[r, i] / math.sqrt(ms + eps) for i in range(x.shape[1])]
+    return out
+
+
+def test_mlp_matches_explicit_sums():
+    rng = np.random.default_rng(11)
+    m = tiny_mlp(8, 12, rng)
+    y = rng.standard_normal((3, 8))
+    np.testing.assert_allclose(O.mlp(m, y), _brute_mlp(m, y), rtol=1e-12, atol=1e-12)
+
+
+def _decoder_case(seed, zero_wo=False, zero_down=False):
+    rng = np.random.default_rng(seed)
+    cfg = tiny_cfg()
+    w = tiny_weights(cfg, rng)
+    if zero_wo:
+        w.wo = np.zeros_like(w.wo)
+    m = tiny_mlp(cfg.hidden, 24, rng)
+    if zero_down:
+        m.down = np.zeros_like(m.down)
+    q = 4
+    hidden = rng.standard_normal((1, q, cfg.hidden))
+    th = [rng.standard_normal((3, cfg.hidden))]
+    pos = [np.arange(0, 3 + q)]
+    return cfg, w, m, hidden, th, pos, rng
+
+
+def test_decoder_layer_without_attention_is_mlp_of_post_norm():
+    # wo = 0: the attention adds nothing, so r2 = hidden and the output is the
+    # MLP of hidden through the post-attention norm (not the input norm)
+    cfg, w, m, hidden, th, pos, _ = _decoder_case(21, zero_wo=True)
+    out, r2 = O.decoder_layer(cfg, w, m, O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1),
+                              hidden, None, th, pos)
+    np.testing.assert_array_equal(r2, hidden)
+    ref = _brute_mlp(m, _brute_norm(hidden[0], m.post_norm, cfg.rms_eps))
+    np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_decoder_layer_attention_term_reads_input_norm_rows():
+    # down = 0: the MLP adds nothing; r2 - r1 is the attention of the rows
+    # through the input norm (explicit loops), cache appended as by forward
+    cfg, w, m, hidden, th, pos, _ = _decoder_case(22, zero_down=True)
+    c1 = O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1)
+    out, r2 = O.decoder_layer(cfg, w, m, c1, hidden, None, th, pos)
+    assert np.all(out == 0.0)
+    c2 = O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1)
+    normed = _brute_norm(hidden[0], m.input_norm, cfg.rms_eps)[None]
+    a = O.forward(cfg, w, c2, normed, th, pos)
+    np.testing.assert_allclose(r2 - hidden, a, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(c1.k[0], c2.k[0], rtol=1e-10, atol=1e-12)
+
+
+def test_decoder_layer_output_is_mlp_of_post_norm_of_the_residual():
+    # both branches active: the output is the MLP (explicit sums) of the
+    # returned residual r2 (pinned above as r1 + attention) through the
+    # post-attention norm
+    cfg, w, m, hidden, th, pos, _ = _decoder_case(24)
+    out, r2 = O.decoder_layer(cfg, w, m, O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1),
+                              hidden, None, th, pos)
+    assert np.abs(r2 - hidden).max() > 1e-3  # the attention did contribute
+    ref = _brute_mlp(m, _brute_norm(r2[0], m.post_norm, cfg.rms_eps))
+    np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_decoder_layer_residual_stream_form():
+    # (hidden = a, residual = b) is the layer applied to a + b
+    cfg, w, m, hidden, th, pos, rng = _decoder_case(23)
+    res = rng.standard_normal(hidden.shape)
+    o1, r1 = O.decoder_layer(cfg, w, m, O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1),
+                             hidden - res, res, th, pos)
+    o2, r2 = O.decoder_layer(cfg, w, m, O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1),
+                             hidden, None, th, pos)
+    np.testing.assert_allclose(o1, o2, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(r1, r2, rtol=1e-12, atol=1e-12)
+
+
 def test_pins_catch_planted_mistakes(monkeypatch):
     """Plant slips in the oracle (CPU only) and check a pin fails for each."""
     import copy
@@ -514,7 +631,34 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         c2 = copy.copy(cfg); c2.n_kv_heads = cfg.n_heads
         return orig_attention(c2, q, k2, v2, allowed)
 
+    orig_rms_norm = O.rms_norm
+
+    def broke_mlp_swapped(m, y):
+        return O.linear(O.silu(O.linear(y, m.up)) * O.linear(y, m.gate), m.down)
+
+    def broke_silu_sigmoid(x):
+        return 1.0 / (1.0 + np.exp(-x))
+
+    def broke_decoder_post_on_r1(cfg, w, m, cache, hidden, residual, th, pos, seqs=None):
+        r1 = hidden if residual is None else hidden + residual
+        a = O.forward(cfg, w, cache, orig_rms_norm(r1, m.input_norm, cfg.rms_eps), th, pos,
+                      seqs=seqs)
+        return O.mlp(m, orig_rms_norm(r1, m.post_norm, cfg.rms_eps)), r1 + a
+
+    def broke_decoder_input_gains(cfg, w, m, cache, hidden, residual, th, pos, seqs=None):
+        r1 = hidden if residual is None else hidden + residual
+        a = O.forward(cfg, w, cache, orig_rms_norm(r1, m.post_norm, cfg.rms_eps), th, pos,
+                      seqs=seqs)
+        r2 = r1 + a
+        return O.mlp(m, orig_rms_norm(r2, m.post_norm, cfg.rms_eps)), r2
+
     slips = [
+        ("mlp", broke_mlp_swapped, [test_mlp_matches_explicit_sums]),
+        ("silu", broke_silu_sigmoid, [test_silu_closed_forms, test_mlp_matches_explicit_sums]),
+        ("decoder_layer", broke_decoder_post_on_r1,
+         [test_decoder_layer_output_is_mlp_of_post_norm_of_the_residual]),
+        ("decoder_layer", broke_decoder_input_gains,
+         [test_decoder_layer_attention_term_reads_input_norm_rows]),
         ("rope", broke_rope_sign, [test_rope_basis_vectors_rotate_half_pairs]),
         ("rope", broke_rope_interleaved, [test_rope_basis_vectors_rotate_half_pairs]),
         ("rms_norm", broke_norm_no_eps, [test_rms_norm_constant_vector_closed_form]),

@@ -723,6 +723,130 @@ int dflash_kv_group_append(dflash_kv_group* g, dflash_cache* const* caches, int 
   return DFLASH_OK;
 }
 
+int dflash_mlp_create(int hidden, int intermediate, float rms_eps, const void* gate_w,
+                      const void* up_w, const void* down_w, const void* input_norm_w,
+                      const void* post_norm_w, dflash_mlp** out) {
+  if (out == nullptr) return fail(DFLASH_ERR_ARG, "null output handle");
+  *out = nullptr;
+  if (!gate_w || !up_w || !down_w || !input_norm_w || !post_norm_w)
+    return fail(DFLASH_ERR_ARG, "a weight pointer is null");
+  if (hidden <= 0 || hidden % 128 != 0 || hidden > 8192)
+    return fail(DFLASH_ERR_SHAPE, "hidden must be a positive multiple of 128, at most 8192");
+  if (intermediate <= 0 || intermediate % 128 != 0)
+    return fail(DFLASH_ERR_SHAPE, "intermediate must be a positive multiple of 128");
+  if (!(rms_eps >= 0.f)) return fail(DFLASH_ERR_SHAPE, "rms_eps must be >= 0");
+  dflash_mlp* m = new dflash_mlp();
+  m->H = hidden;
+  m->I = intermediate;
+  m->eps = rms_eps;
+  cudaGetDevice(&m->device);
+  cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+  const size_t H = hidden, I = intermediate;
+  cudaError_t e = cudaMalloc(&m->w_gu, 2 * I * H * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&m->w_d, H * I * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&m->in_norm, H * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&m->post_norm, H * 4);
+  // gate rows 64c .. 64c+63 -> rows 128c .., up rows -> rows 128c + 64 ..
+  const size_t chunk = 64 * H * 2;
+  if (e == cudaSuccess)
+    e = cudaMemcpy2D(m->w_gu, 2 * chunk, gate_w, chunk, chunk, I / 64, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2D(static_cast<char*>(m->w_gu) + chunk, 2 * chunk, up_w, chunk, chunk, I / 64,
+                     cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(m->w_d, down_w, H * I * 2, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess) e = (cudaError_t)launch_to_f32(input_norm_w, 1, m->in_norm, H, 0);
+  if (e == cudaSuccess) e = (cudaError_t)launch_to_f32(post_norm_w, 1, m->post_norm, H, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    dflash_mlp_destroy(m);
+    return cuda_fail(e, "mlp weights");
+  }
+  if (make_tmap_bf16_rows(&m->tm_gu, m->w_gu, 2 * I, (int)H, 128) != 0 ||
+      make_tmap_bf16_rows(&m->tm_gu256, m->w_gu, 2 * I, (int)H, 256) != 0 ||
+      make_tmap_bf16_rows(&m->tm_d, m->w_d, H, (int)I, 128) != 0 ||
+      make_tmap_bf16_rows(&m->tm_d256, m->w_d, H, (int)I, 256) != 0) {
+    dflash_mlp_destroy(m);
+    return fail(DFLASH_ERR_CUDA, "tensor map encoding failed");
+  }
+  *out = m;
+  return DFLASH_OK;
+}
+
+int dflash_mlp_destroy(dflash_mlp* m) {
+  if (m == nullptr) return DFLASH_OK;
+  cudaDeviceSynchronize();
+  cudaFree(m->w_gu);
+  cudaFree(m->w_d);
+  cudaFree(m->in_norm);
+  cudaFree(m->post_norm);
+  for (df::Buf* b : {&m->y, &m->attn_out, &m->act, &m->gemm_partial, &m->gemm_counters})
+    b->release();
+  delete m;
+  return DFLASH_OK;
+}
+
+int dflash_decoder_layer_forward(dflash_attn* a, dflash_mlp* m, dflash_cache* c, int batch,
+                                 int q_len, const void* hidden_in, const void* residual_in,
+                                 const void* target_hidden, const int32_t* host_n_ctx,
+                                 const int32_t* positions, void* hidden_out, void* residual_out,
+                                 dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (m == nullptr) return fail(DFLASH_ERR_ARG, "null mlp handle");
+  if (a->dt != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "decoder layers need bf16");
+  if (m->H != a->H) return fail(DFLASH_ERR_SHAPE, "mlp hidden %d differs from the layer's %d",
+                                m->H, a->H);
+  if (hidden_in == nullptr || hidden_out == nullptr || residual_out == nullptr)
+    return fail(DFLASH_ERR_ARG, "null tensor");
+  if (batch <= 0 || q_len <= 0) return fail(DFLASH_ERR_ARG, "batch and q_len must be positive");
+  if (!aligned16(hidden_in) || !aligned16(hidden_out) || !aligned16(residual_out) ||
+      (residual_in && !aligned16(residual_in)))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rows = batch * q_len;
+  const size_t H = m->H, I = m->I;
+  DF_CUDA(m->y.ensure((size_t)rows * H * 2), "scratch allocation");
+  DF_CUDA(m->attn_out.ensure((size_t)rows * H * 2), "scratch allocation");
+  DF_CUDA(m->act.ensure((size_t)rows * I * 2), "scratch allocation");
+  int n_counters = 0;
+  size_t bytes = std::max(
+      gemm_scratch_bytes(EPI_SWIGLU, rows, 0, (int)(2 * I), (int)H, 0, m->num_sms, &n_counters),
+      gemm_scratch_bytes(EPI_BF16, rows, 0, (int)H, (int)I, 0, m->num_sms, nullptr));
+  int n2 = 0;
+  gemm_scratch_bytes(EPI_BF16, rows, 0, (int)H, (int)I, 0, m->num_sms, &n2);
+  DF_CUDA(m->gemm_partial.ensure(std::max<size_t>(bytes, 256)), "scratch allocation");
+  DF_CUDA(m->gemm_counters.ensure((size_t)std::max({n_counters, n2, 64}) * sizeof(int), true),
+          "scratch allocation");
+  GemmScratch scr;
+  scr.partial = static_cast<float*>(m->gemm_partial.p);
+  scr.partial_bytes = m->gemm_partial.bytes;
+  scr.counters = static_cast<int*>(m->gemm_counters.p);
+  scr.n_counters = (int)(m->gemm_counters.bytes / sizeof(int));
+  // r1 = hidden (+ residual) -> residual_out; y = input_norm(r1)
+  {
+    TraceScope tr(a, DFLASH_K_MLP, s);
+    DF_CUDA(launch_add_rmsnorm(hidden_in, residual_in, rows, (int)H, m->in_norm, m->eps,
+                               residual_out, m->y.p, s),
+            "add + norm launch");
+  }
+  if (int r = dflash_attn_forward(a, c, batch, q_len, m->y.p, target_hidden, host_n_ctx,
+                                  positions, m->attn_out.p, stream))
+    return r;
+  // r2 = r1 + attention -> residual_out; y = post_norm(r2); out = mlp(y)
+  TraceScope tr(a, DFLASH_K_MLP, s);
+  DF_CUDA(launch_add_rmsnorm(residual_out, m->attn_out.p, rows, (int)H, m->post_norm, m->eps,
+                             residual_out, m->y.p, s),
+          "add + norm launch");
+  GemmShape g1{m->y.p, rows, nullptr, 0, &m->tm_gu, &m->tm_gu256, (int)(2 * I), (int)H, 0};
+  DF_CUDA(launch_gemm_bf16(g1, EPI_SWIGLU, m->act.p, (int)I, nullptr, nullptr, scr, m->num_sms,
+                           a->err, s),
+          "gate/up projection launch");
+  GemmShape g2{m->act.p, rows, nullptr, 0, &m->tm_d, &m->tm_d256, (int)H, (int)I, 0};
+  DF_CUDA(launch_gemm_bf16(g2, EPI_BF16, hidden_out, (int)H, nullptr, nullptr, scr, m->num_sms,
+                           a->err, s),
+          "down projection launch");
+  return DFLASH_OK;
+}
+
 int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
                                int block_size, const void* noise, const void* target_hidden,
                                const int32_t* anchors, void* out, dflash_stream stream) {

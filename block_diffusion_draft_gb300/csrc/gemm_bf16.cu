@@ -267,7 +267,17 @@ DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, floa
                        int src, int srow, int n0) {
   constexpr int BN = HD;
   constexpr int C4 = BN / 4;
-  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
+  if constexpr (EPI == EPI_SWIGLU) {
+    // columns 0..63 gate, 64..127 up of the same 64 outputs
+    float act[HD / 2];
+#pragma unroll
+    for (int c = 0; c < HD / 2; ++c) {
+      const float gt = v[c];
+      act[c] = gt / (1.f + __expf(-gt)) * v[HD / 2 + c];
+    }
+    store_bf16(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc + n0 / 2, act,
+               HD / 2);
+  } else if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
     if constexpr (EPI == EPI_BF16) {
       store_bf16(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc + n0, v, BN);
     } else {
@@ -416,6 +426,22 @@ DF_DEV void cluster_sum_rows(const Plan& p, int m_tile, int n0, const uint8_t* s
     if constexpr (EPI == EPI_F32) {
       reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + (size_t)srow * p.ldc + n0)[lane] =
           acc;
+    } else if constexpr (EPI == EPI_SWIGLU) {
+      // lanes 0..15 hold gate columns 4l.., lanes 16..31 the matching up columns
+      float4 up;
+      up.x = __shfl_down_sync(0xffffffffu, acc.x, 16);
+      up.y = __shfl_down_sync(0xffffffffu, acc.y, 16);
+      up.z = __shfl_down_sync(0xffffffffu, acc.z, 16);
+      up.w = __shfl_down_sync(0xffffffffu, acc.w, 16);
+      if (lane < 16) {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x / (1.f + __expf(-acc.x)) * up.x,
+                           acc.y / (1.f + __expf(-acc.y)) * up.y);
+        pk.y = pack_bf16x2(acc.z / (1.f + __expf(-acc.z)) * up.z,
+                           acc.w / (1.f + __expf(-acc.w)) * up.w);
+        reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc +
+                                 n0 / 2)[lane] = pk;
+      }
     } else {
       uint2 pk;
       pk.x = pack_bf16x2(acc.x, acc.y);
@@ -1170,7 +1196,8 @@ void set_smem_attr() {
 
 // one source of 129 .. 384 rows, plain epilogue: the swapped-operand kernel
 bool use_swap(int epi, int rows0, int rows1, int n) {
-  return epi != EPI_QKV && rows1 == 0 && rows0 > BM && rows0 <= SWAP_MAX_ROWS && n % BM == 0;
+  return (epi == EPI_F32 || epi == EPI_BF16) && rows1 == 0 && rows0 > BM &&
+         rows0 <= SWAP_MAX_ROWS && n % BM == 0;
 }
 
 // many token rows and 256-aligned column regions: the persistent kernel
@@ -1311,6 +1338,7 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
     set_smem_attr<EPI_BF16, 128>();
     set_smem_attr<EPI_F32, 128>();
     set_smem_attr<EPI_QKV, 128>();
+    set_smem_attr<EPI_SWIGLU, 128>();
     attr_done = true;
   }
   if (s.k % BK != 0) return cudaErrorInvalidValue;
@@ -1375,6 +1403,9 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   } else if (epi == EPI_BF16) {
     e = launch_pdl_cluster(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream, cl, ma0,
                            ma1, *s.b_map, p, qo, st);
+  } else if (epi == EPI_SWIGLU) {
+    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_SWIGLU, 128>, grid, block, smem, stream, cl,
+                           ma0, ma1, *s.b_map, p, qo, st);
   } else {
     e = launch_pdl_cluster(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream, cl, ma0,
                            ma1, *s.b_map, p, qo, st);
@@ -1398,6 +1429,8 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
                          (int)SMEM_BIG);
     cudaFuncSetAttribute(gemm_big_kernel<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_BIG);
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_SWIGLU>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BIG);
     attr_done = true;
   }
   if (s.b_map256 == nullptr) return cudaErrorInvalidValue;
@@ -1447,6 +1480,9 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
                    *s.b_map256, p, qo, st);
   else if (epi == EPI_BF16)
     e = launch_pdl(gemm_big_kernel<EPI_BF16>, grid, block, SMEM_BIG, stream, ma0, ma1,
+                   *s.b_map256, p, qo, st);
+  else if (epi == EPI_SWIGLU)
+    e = launch_pdl(gemm_big_kernel<EPI_SWIGLU>, grid, block, SMEM_BIG, stream, ma0, ma1,
                    *s.b_map256, p, qo, st);
   else
     e = launch_pdl(gemm_big_kernel<EPI_F32>, grid, block, SMEM_BIG, stream, ma0, ma1,

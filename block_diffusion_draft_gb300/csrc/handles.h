@@ -72,6 +72,20 @@ struct dflash_kv_group {
   df::Buf gemm_partial, gemm_counters;
 };
 
+// The rest of a draft decoder layer: norms and the Qwen3 MLP.  gate and up
+// rows interleaved in 64-row chunks ([g 0..63][u 0..63][g 64..127]...), so
+// one 128-row weight tile feeds 64 SwiGLU outputs.
+struct dflash_mlp {
+  int H = 0, I = 0, device = 0, num_sms = 0;
+  float eps = 0.f;
+  void* w_gu = nullptr;  // [2I][H] bf16
+  void* w_d = nullptr;   // [H][I] bf16
+  float* in_norm = nullptr;
+  float* post_norm = nullptr;
+  CUtensorMap tm_gu, tm_gu256, tm_d, tm_d256;
+  df::Buf y, attn_out, act, gemm_partial, gemm_counters;
+};
+
 struct dflash_cache {
   int batch = 0, cap = 0, nkv = 0, d = 0, dt = 0, device = 0;
   void* k = nullptr;

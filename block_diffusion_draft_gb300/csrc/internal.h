@@ -88,7 +88,10 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 // ----------------------------------------------------------- bf16 GEMM
 // C = A * B^T with A [rows, K] (token rows; two sources A0 then A1) and B
 // [N, K] (weights), both bf16 K-contiguous; fp32 accumulation on tcgen05.
-enum GemmEpi { EPI_BF16 = 0, EPI_F32 = 1, EPI_QKV = 2 };
+// EPI_SWIGLU: the weight rows are gate and up rows interleaved in 64-row
+// chunks; each 128-column tile yields 64 outputs silu(gate) * up, bf16, at
+// column n0 / 2
+enum GemmEpi { EPI_BF16 = 0, EPI_F32 = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
 
 struct GemmShape {
   const void* a0; int a0_rows;   // noise rows (or the only source)
@@ -163,6 +166,10 @@ int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
                        float eps, void* out, int out_bf16, cudaStream_t st);
 int launch_to_f32(const void* src, int src_bf16, float* dst, size_t n,
                   cudaStream_t st);
+// sum_out = a + b (b may be null), norm_out = w * sum / rms(sum); bf16 rows,
+// cols % 8 == 0, cols <= 8192; w fp32
+int launch_add_rmsnorm(const void* a, const void* b, int rows, int cols, const float* w,
+                       float eps, void* sum_out, void* norm_out, cudaStream_t st);
 int launch_packed_positions(const int* anchors, int batch, int seq,
                             int n_blocks, int block_size, int* pos, int* err,
                             cudaStream_t st);

@@ -70,6 +70,81 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
+// Residual add + RMSNorm of a decoder layer, one CTA per row: r = a (+ b),
+// (sum_out may alias a or b: each element is read before it is written, by
+// the same thread)
+// stored bf16 (the residual stream), and w * r / sqrt(mean(r^2) + eps) of the
+// stored (bf16) r, also bf16.  Each thread holds up to kAddNormVec groups of 8
+// columns.
+constexpr int kAddNormThreads = 256;
+constexpr int kAddNormVec = 4;  // cols <= 256 * 8 * 4 = 8192
+
+__global__ void __launch_bounds__(kAddNormThreads)
+    add_rmsnorm_kernel(const uint4* a, const uint4* b, int cols,
+                       const float* __restrict__ w, float eps, uint4* sum_out,
+                       uint4* __restrict__ norm_out) {
+  grid_dep_sync();
+  const int n8 = cols / 8;
+  const size_t row = (size_t)blockIdx.x * n8;
+  float x[kAddNormVec][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kAddNormVec; ++i) {
+    const int c = threadIdx.x + i * kAddNormThreads;
+    if (c < n8) {
+      uint4 va = a[row + c];
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&va);
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        f[2 * e] = __low2float(pa[e]);
+        f[2 * e + 1] = __high2float(pa[e]);
+      }
+      if (b != nullptr) {
+        uint4 vb = b[row + c];
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&vb);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          f[2 * e] += __low2float(pb[e]);
+          f[2 * e + 1] += __high2float(pb[e]);
+        }
+      }
+      uint4 vr;
+      uint32_t* pr = reinterpret_cast<uint32_t*>(&vr);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pr[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&pr[e]);
+        x[i][2 * e] = __low2float(h);
+        x[i][2 * e + 1] = __high2float(h);
+        ss += x[i][2 * e] * x[i][2 * e] + x[i][2 * e + 1] * x[i][2 * e + 1];
+      }
+      sum_out[row + c] = vr;
+    }
+  }
+  __shared__ float red[kAddNormThreads / 32];
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kAddNormThreads / 32; ++i) tot += red[i];
+  const float inv = rsqrtf(tot / cols + eps);
+#pragma unroll
+  for (int i = 0; i < kAddNormVec; ++i) {
+    const int c = threadIdx.x + i * kAddNormThreads;
+    if (c >= n8) break;
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * c);
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * c + 1);
+    uint4 vo;
+    vo.x = pack_bf16x2(x[i][0] * inv * g0.x, x[i][1] * inv * g0.y);
+    vo.y = pack_bf16x2(x[i][2] * inv * g0.z, x[i][3] * inv * g0.w);
+    vo.z = pack_bf16x2(x[i][4] * inv * g1.x, x[i][5] * inv * g1.y);
+    vo.w = pack_bf16x2(x[i][6] * inv * g1.z, x[i][7] * inv * g1.w);
+    norm_out[row + c] = vo;
+  }
+}
+
 __global__ void to_f32_kernel(const void* src, int src_bf16, float* dst, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x)
@@ -130,6 +205,15 @@ int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
   if (cols % 4 != 0 || cols > kNormThreads * 4 * kNormVec) return cudaErrorInvalidValue;
   return launch_pdl(row_rmsnorm_kernel, dim3(rows), dim3(kNormThreads), 0, st, z, cols, w,
                     eps, out, out_bf16);
+}
+
+int launch_add_rmsnorm(const void* a, const void* b, int rows, int cols, const float* w,
+                       float eps, void* sum_out, void* norm_out, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (cols % 8 != 0 || cols > kAddNormThreads * 8 * kAddNormVec) return cudaErrorInvalidValue;
+  return launch_pdl(add_rmsnorm_kernel, dim3(rows), dim3(kAddNormThreads), 0, st,
+                    static_cast<const uint4*>(a), static_cast<const uint4*>(b), cols, w, eps,
+                    static_cast<uint4*>(sum_out), static_cast<uint4*>(norm_out));
 }
 
 int launch_to_f32(const void* src, int src_bf16, float* dst, size_t n,

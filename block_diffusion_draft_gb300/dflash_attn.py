@@ -63,13 +63,19 @@ _SIGNATURES = {
     "dflash_kv_group_destroy": ([c_void_p], c_int),
     "dflash_kv_group_append": ([c_void_p, POINTER(c_void_p), c_int, c_void_p,
                                 POINTER(c_int32), c_void_p, c_void_p], c_int),
+    "dflash_mlp_create": ([c_int, c_int, c_float] + [c_void_p] * 5 + [POINTER(c_void_p)],
+                          c_int),
+    "dflash_mlp_destroy": ([c_void_p], c_int),
+    "dflash_decoder_layer_forward": ([c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p,
+                                      c_void_p, c_void_p, POINTER(c_int32), c_void_p,
+                                      c_void_p, c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
     "dflash_trace_enable": ([c_void_p, c_int], c_int),
     "dflash_trace_read": ([c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int32)],
                           c_int),
 }
 
-KERNEL_KINDS = {"fc": 0, "norm": 1, "qkv": 2, "attn": 3, "o_proj": 4, "misc": 5}
+KERNEL_KINDS = {"fc": 0, "norm": 1, "qkv": 2, "attn": 3, "o_proj": 4, "misc": 5, "mlp": 6}
 
 
 def declared_functions() -> list:
@@ -300,6 +306,54 @@ class KVGroup:
         if getattr(self, "handle", None):
             with torch.cuda.device(self.device):
                 lib().dflash_kv_group_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class DecoderMLP:
+    """Norms and Qwen3 MLP of a draft decoder layer (dflash_mlp_*): weights
+    ``gate``, ``up`` [intermediate, hidden], ``down`` [hidden, intermediate],
+    ``input_norm``, ``post_norm`` [hidden], all bf16."""
+
+    def __init__(self, w: dict, hidden: int, intermediate: int, rms_eps: float = 1e-6,
+                 device="cuda"):
+        self.device = torch.device(device)
+        self.hidden, self.intermediate = hidden, intermediate
+        with torch.cuda.device(self.device):
+            self._w = {k: w[k].to(self.device, torch.bfloat16).contiguous()
+                       for k in ("gate", "up", "down", "input_norm", "post_norm")}
+            h = c_void_p()
+            check(lib().dflash_mlp_create(hidden, intermediate, rms_eps,
+                                          *[_p(self._w[k]) for k in ("gate", "up", "down",
+                                                                      "input_norm", "post_norm")],
+                                          ctypes.byref(h)))
+        self._w = None  # the library holds copies
+        self.handle = h
+
+    def layer_forward(self, attn: DFlashAttention, cache: "DraftCache", hidden: torch.Tensor,
+                      residual: Optional[torch.Tensor], target_hidden: Optional[torch.Tensor],
+                      n_ctx: Sequence[int], positions: torch.Tensor):
+        """One decoder layer; returns (hidden_out, residual_out)."""
+        B, q_len, _ = hidden.shape
+        out = torch.empty_like(hidden)
+        res = torch.empty_like(hidden)
+        th = None if target_hidden is None or target_hidden.numel() == 0 else target_hidden
+        with torch.cuda.device(self.device):
+            check(lib().dflash_decoder_layer_forward(
+                attn.handle, self.handle, cache.handle, B, q_len, _p(hidden), _p(residual),
+                _p(th), _int32_array(n_ctx), _p(positions), _p(out), _p(res),
+                _stream(self.device)))
+        return out, res
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            with torch.cuda.device(self.device):
+                lib().dflash_mlp_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

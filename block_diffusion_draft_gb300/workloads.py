@@ -159,6 +159,24 @@ def weights(sp: Spec, seed: int = 0, layer: int = 0,
 # --------------------------------------------------------------------------
 # activations
 # --------------------------------------------------------------------------
+def mlp_weights(sp: Spec, seed: int, intermediate: int, layer: int = 0,
+                random_gains: bool = False) -> Dict[str, torch.Tensor]:
+    """Decoder-layer MLP and norm weights: gate, up [intermediate, hidden],
+    down [hidden, intermediate] N(0, 0.02); norm gains 1 (or 1 + N(0, 0.1))."""
+    dt = sp.torch_dtype()
+    H = sp.hidden
+    w = {"gate": _normal(_rng(seed, "weight", layer, 5), (intermediate, H), 0.02, dt),
+         "up": _normal(_rng(seed, "weight", layer, 6), (intermediate, H), 0.02, dt),
+         "down": _normal(_rng(seed, "weight", layer, 7), (H, intermediate), 0.02, dt)}
+    for i, name in enumerate(("input_norm", "post_norm")):
+        if random_gains:
+            g = 1.0 + 0.1 * _rng(seed, "gain", layer, 3 + i).standard_normal(H, dtype=np.float32)
+            w[name] = torch.from_numpy(g).to(dt)
+        else:
+            w[name] = torch.ones(H, dtype=dt)
+    return w
+
+
 def hidden_rows(sp: Spec, seed: int, kind: str, step: int, seq: int,
                 rows: int) -> torch.Tensor:
     """N(0,1) rows of width hidden: ``kind`` is "hidden" (projected context,

@@ -50,6 +50,7 @@ extern "C" {
 typedef struct dflash_attn dflash_attn;   /* one layer: weights + scratch */
 typedef struct dflash_cache dflash_cache; /* one draft KV cache */
 typedef struct dflash_kv_group dflash_kv_group; /* context K/V of several layers */
+typedef struct dflash_mlp dflash_mlp;     /* norms + MLP of a decoder layer */
 typedef void* dflash_stream;              /* a cudaStream_t */
 
 enum {
@@ -259,6 +260,38 @@ int dflash_kv_group_append(dflash_kv_group* group, dflash_cache* const* caches,
                            const int32_t* host_n_ctx, const int32_t* positions,
                            dflash_stream stream);
 
+/* The rest of a draft decoder layer ([P4] Qwen3DFlashDecoderLayer:
+ * input_layernorm, self_attn, post_attention_layernorm, mlp = Qwen3MLP; [P5]
+ * stacks gate_proj/up_proj into gate_up_proj).  Reading taken (the pages name
+ * Qwen3MLP without printing it): mlp(y) = down(silu(gate(y)) * up(y)).
+ * Weights bf16 device, nn.Linear layout: gate_w, up_w [intermediate, hidden],
+ * down_w [hidden, intermediate]; input_norm_w, post_norm_w [hidden] bf16.
+ * hidden % 128 == 0 (<= 8192), intermediate % 128 == 0, else _SHAPE.  The
+ * handle owns copies of the weights. */
+int dflash_mlp_create(int hidden, int intermediate, float rms_eps,
+                      const void* gate_w, const void* up_w, const void* down_w,
+                      const void* input_norm_w, const void* post_norm_w,
+                      dflash_mlp** out);
+int dflash_mlp_destroy(dflash_mlp* mlp);
+
+/* One draft decoder layer in the residual-stream form of [P5]'s draft model
+ * (each layer returns (hidden_states, residual); the next one adds them):
+ *   r1 = hidden_in + residual_in   (residual_in NULL: r1 = hidden_in)
+ *   r2 = r1 + attn(input_norm(r1))   -- dflash_attn_forward on the normed rows
+ *   hidden_out = mlp(post_norm(r2)),  residual_out = r2
+ * hidden_in, residual_in, hidden_out, residual_out: device bf16
+ * [batch, q_len, hidden] (residual_out may alias residual_in); the other
+ * arguments and the cache update are those of dflash_attn_forward.  bf16
+ * layers only (_UNSUPPORTED otherwise); the MLP's hidden must equal the
+ * layer's (_SHAPE). */
+int dflash_decoder_layer_forward(dflash_attn* attn, dflash_mlp* mlp,
+                                 dflash_cache* cache, int batch, int q_len,
+                                 const void* hidden_in, const void* residual_in,
+                                 const void* target_hidden,
+                                 const int32_t* host_n_ctx,
+                                 const int32_t* positions, void* hidden_out,
+                                 void* residual_out, dflash_stream stream);
+
 /* Training-layout forward with no cache ([P4] module docstring: each block's
  * queries see the context strictly before its anchor plus their own block,
  * bidirectionally; training is one forward with no cache).
@@ -285,7 +318,8 @@ enum {
   DFLASH_K_ATTN = 3,   /* attention (with the split merge)                */
   DFLASH_K_OPROJ = 4,  /* o_proj GEMM                                     */
   DFLASH_K_MISC = 5,   /* packed-layout positions                         */
-  DFLASH_K_COUNT = 6
+  DFLASH_K_MLP = 6,    /* decoder layer: add+norm kernels and MLP GEMMs    */
+  DFLASH_K_COUNT = 7
 };
 
 /* Launch tracing for measurement: while enabled, every kernel launch of the

@@ -171,6 +171,11 @@ class ServingWorkload:
                                     sliding_window=sp.sliding_window,
                                     max_position=sp.max_position, device=device)
         del w
+        self.mlp = None
+        if sp.intermediate > 0:
+            from block_diffusion_draft_gb300 import DecoderMLP
+            self.mlp = DecoderMLP(W.mlp_weights(sp, seed, sp.intermediate), sp.hidden,
+                                  sp.intermediate, sp.rms_eps, device=device)
         self.fixed = sp.prefill > 0  # every step identical (crop back each time)
         sched = W.serving_schedule(sp, seed, steps=1 if self.fixed else n_steps)
         self.sched = sched
@@ -210,9 +215,10 @@ class ServingWorkload:
         self.attn.reserve(B, B * q + rows, self.cap)
         self.th_buf = torch.empty(rows, sp.hidden, dtype=torch.bfloat16, device=device)
         self.out_buf = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16, device=device)
+        self.res_buf = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16, device=device)
         self.out_h = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()
         self.blocks_per_step = B
-        self.launches_per_step = 5
+        self.launches_per_step = 5 if self.mlp is None else 9
 
     def _inputs(self, i):
         return self.steps[i % len(self.steps)]
@@ -227,7 +233,12 @@ class ServingWorkload:
         n = int(sum(st["n_ctx"]))
         th = self.th_buf[:n]
         self.attn.ctx_project(st["x"], out=th)
-        self.attn.forward(self.cache, st["nz"], th, st["n_ctx"], st["pos"], out=self.out_buf)
+        if self.mlp is None:
+            self.attn.forward(self.cache, st["nz"], th, st["n_ctx"], st["pos"],
+                              out=self.out_buf)
+        else:
+            self.mlp.layer_forward_into(self.attn, self.cache, st["nz"], None, th,
+                                        st["n_ctx"], st["pos"], self.out_buf, self.res_buf)
         self.cache.crop(st["keep"])
 
     def stage_e2e(self, i):
@@ -274,6 +285,9 @@ class ServingWorkload:
                    + B * q * nq * d * 2 + (B * q + n) * 2 * nkv * d * 2,
             "attn": keys * nkv * d * 2 * 2 + 2 * B * q * nq * d * 2,
             "o_proj": H * nq * d * 2 + B * q * nq * d * 2 + B * q * H * 2,
+            # two add+norm passes (read 2 rows, write 2) and the SwiGLU MLP
+            "mlp": (2 * 4 * B * q * H * 2 + 3 * sp.intermediate * H * 2
+                    + B * q * (H + 2 * sp.intermediate + H) * 2) if sp.intermediate else 0,
         }
 
     def kernel_flops(self, i):
@@ -481,6 +495,10 @@ def spec_config(sp):
     extra = {"layers": sp.layers,
              "step": "ctx_project + grouped context K/V of all layers + per-layer forward "
                      "(no context rows) + crop"} if sp.layers > 1 else {}
+    if sp.intermediate > 0:
+        extra = {"intermediate": sp.intermediate,
+                 "step": "ctx_project + decoder layer (input norm, attention, residual, "
+                         "post norm, SwiGLU MLP) + crop"}
     return {"workload": sp.name, "batch": sp.batch, "hidden": sp.hidden,
             "heads": f"{sp.n_heads}/{sp.n_kv_heads}", "head_dim": sp.head_dim,
             "block_size": sp.block_size, "fc_in": sp.n_target_layers * sp.hidden,
@@ -557,6 +575,13 @@ class OracleRunner:
             self.blocks_per_step = 1
             self.sample = ("ctx_project + forward + crop of one sequence per step "
                            f"({pre} cached rows, {n} new, block {q})")
+            self.om = None
+            if sp.intermediate > 0:
+                mw = W.mlp_weights(sp, seed, sp.intermediate)
+                self.om = O.MlpWeights(*(f64(mw[k]) for k in ("gate", "up", "down",
+                                                               "input_norm", "post_norm")))
+                self.sample = ("ctx_project + decoder layer + crop of one sequence per step "
+                               f"({pre} cached rows, {n} new, block {q}, MLP {sp.intermediate})")
             # layer stack: the other layers (own weights and caches), each step
             # their per-layer forward with the context rows (the definition)
             self.more = []
@@ -580,7 +605,11 @@ class OracleRunner:
                              sp.block_size, seqs=[0], blocks=self.blocks)
         else:
             t = O.ctx_project(self.cfg, self.lw, self.x)
-            O.forward(self.cfg, self.lw, self.cache, self.nzs, [t], [self.pos])
+            if self.om is None:
+                O.forward(self.cfg, self.lw, self.cache, self.nzs, [t], [self.pos])
+            else:
+                O.decoder_layer(self.cfg, self.lw, self.om, self.cache, self.nzs, None, [t],
+                                [self.pos])
             self.cache.crop([self.pre])
             for lw, c, nzs in self.more:
                 O.forward(self.cfg, lw, c, nzs, [t], [self.pos])

@@ -350,6 +350,20 @@ class DecoderMLP:
                 _stream(self.device)))
         return out, res
 
+    def layer_forward_into(self, attn: DFlashAttention, cache: "DraftCache",
+                           hidden: torch.Tensor, residual: Optional[torch.Tensor],
+                           target_hidden: Optional[torch.Tensor], n_ctx: Sequence[int],
+                           positions: torch.Tensor, out: torch.Tensor,
+                           residual_out: torch.Tensor) -> None:
+        """layer_forward writing into caller-owned output tensors."""
+        B, q_len, _ = hidden.shape
+        th = None if target_hidden is None or target_hidden.numel() == 0 else target_hidden
+        with torch.cuda.device(self.device):
+            check(lib().dflash_decoder_layer_forward(
+                attn.handle, self.handle, cache.handle, B, q_len, _p(hidden), _p(residual),
+                _p(th), _int32_array(n_ctx), _p(positions), _p(out), _p(residual_out),
+                _stream(self.device)))
+
     def close(self) -> None:
         if getattr(self, "handle", None):
             with torch.cuda.device(self.device):

@@ -56,6 +56,8 @@ class Spec:
     max_position: int = 65536
     # layer stacks: draft layers sharing the step's projected context
     layers: int = 1
+    # > 0: the whole decoder layer (norms, residual, MLP of this width)
+    intermediate: int = 0
 
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
@@ -84,6 +86,11 @@ SPECS: Dict[str, Spec] = {
                          n_kv_heads=8, head_dim=128, block_size=16, batch=4,
                          dtype="bf16", prefill=32768, n_new=16,
                          sliding_window=4096),
+    # the whole Qwen3-8B-shaped decoder layer (attention + SwiGLU MLP of
+    # width 12288), one sequence: 4096 cached + 16 new ctx + 16 block
+    "decoder_8b_single": Spec("decoder_8b_single", hidden=4096, n_heads=32,
+                              n_kv_heads=8, head_dim=128, block_size=16, batch=1,
+                              dtype="bf16", prefill=4096, n_new=16, intermediate=12288),
     # five Qwen3-8B-shaped draft layers fed by one projected context: 4096
     # cached rows, then 16 (decode) or 512 (a long accepted run / prefill
     # chunk) new context rows and one block per layer

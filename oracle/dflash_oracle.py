@@ -67,6 +67,9 @@ class LayerConfig:
     rope_theta: float = 1e6
     sliding_window: int = 0
     n_target_layers: int = 0
+    # [P5] _dflash_layer_causal / _resolve_layer_attention: some checkpoints
+    # make a layer causal (the sliding-attention layers, or all of them)
+    causal: bool = False
 
     def __post_init__(self):
         if self.head_dim == 0:
@@ -213,6 +216,17 @@ def band_mask(q_len: int, k_len: int, window: int) -> np.ndarray:
     qi = (k_len - q_len + np.arange(q_len))[:, None]
     kj = np.arange(k_len)[None, :]
     return np.abs(qi - kj) < window
+
+
+def causal_mask(q_len: int, k_len: int) -> np.ndarray:
+    """Causal layers ([P5] ``_dflash_layer_causal``): query row i, at key index
+    ``k_len - q_len + i``, sees the keys at or before that index -- every
+    cached and context row and the block rows up to its own.  Reading taken:
+    the pages resolve which layers are causal but do not print the mask; this
+    is the plain causal rule over the [cache | context | block] key axis."""
+    qi = (k_len - q_len + np.arange(q_len))[:, None]
+    kj = np.arange(k_len)[None, :]
+    return kj <= qi
 
 
 def anchor_mask(seq: int, anchors: Sequence[int], block_size: int) -> np.ndarray:
@@ -368,6 +382,8 @@ def forward(cfg: LayerConfig, w: LayerWeights, cache: DraftCache,
             allowed = band_mask(q_len, k_len, cfg.sliding_window)
         else:
             allowed = full_mask(q_len, k_len)
+        if cfg.causal:
+            allowed = allowed & causal_mask(q_len, k_len)
         o = attention(cfg, q, cache.k[b], cache.v[b], allowed)
         out[b] = linear(o, w.wo)
     return out

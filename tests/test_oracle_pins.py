@@ -476,6 +476,57 @@ def test_ctx_project_is_norm_of_fc_and_checks_width():
 # the pins catch plausible slips
 # --------------------------------------------------------------------------
 # --------------------------------------------------------------------------
+# causal layers
+# --------------------------------------------------------------------------
+def test_causal_mask_elementwise_rule():
+    m = O.causal_mask(3, 7)
+    for i in range(3):
+        for j in range(7):
+            assert m[i, j] == (j <= 4 + i)
+
+
+def test_causal_empty_context_is_library_causal_sdpa():
+    # no cached rows: a causal layer is textbook causal SDPA over the block
+    cfg = tiny_cfg(causal=True)
+    rng = np.random.default_rng(41)
+    w = tiny_weights(cfg, rng)
+    q_len = 6
+    noise = rng.standard_normal((1, q_len, cfg.hidden))
+    pos = np.arange(q_len)
+    out = O.forward(cfg, w, O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1), noise,
+                    [np.zeros((0, cfg.hidden))], [pos])
+    f = O.rope_frequencies(cfg.head_dim, cfg.rope_theta)
+    d, g = cfg.head_dim, cfg.groups
+    def heads(wm, n, gains):
+        x = (noise[0] @ wm.T).reshape(q_len, n, d).transpose(1, 0, 2)
+        return np.stack([O.rope(O.rms_norm(x[h], gains, cfg.rms_eps), pos, f) for h in range(n)])
+    qh = torch.from_numpy(heads(w.wq, cfg.n_heads, w.q_norm))
+    kh = torch.from_numpy(heads(w.wk, cfg.n_kv_heads, w.k_norm)).repeat_interleave(g, 0)
+    vh = torch.from_numpy((noise[0] @ w.wv.T).reshape(q_len, cfg.n_kv_heads, d)
+                          .transpose(1, 0, 2)).repeat_interleave(g, 0)
+    o = torch.nn.functional.scaled_dot_product_attention(qh[None], kh[None], vh[None],
+                                                         is_causal=True)[0]
+    ref = o.numpy().transpose(1, 0, 2).reshape(q_len, -1) @ w.wo.T
+    np.testing.assert_allclose(out[0], ref, rtol=1e-9, atol=1e-11)
+
+
+def test_causal_last_block_row_equals_non_causal():
+    # the last block row sees every key either way; the first row does not
+    rng = np.random.default_rng(42)
+    outs = []
+    for causal in (False, True):
+        cfg = tiny_cfg(causal=causal)
+        w = tiny_weights(cfg, np.random.default_rng(7))
+        c = O.DraftCache(cfg.n_kv_heads, cfg.head_dim, 1)
+        r = np.random.default_rng(8)
+        th = [r.standard_normal((5, cfg.hidden))]
+        noise = r.standard_normal((1, 4, cfg.hidden))
+        outs.append(O.forward(cfg, w, c, noise, th, [np.arange(9)]))
+    np.testing.assert_allclose(outs[0][0, -1], outs[1][0, -1], rtol=1e-12, atol=1e-13)
+    assert np.abs(outs[0][0, 0] - outs[1][0, 0]).max() > 1e-6
+
+
+# --------------------------------------------------------------------------
 # decoder layer: SiLU, the Qwen3 MLP, norms and residuals
 # --------------------------------------------------------------------------
 def test_silu_closed_forms():
@@ -652,7 +703,12 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         r2 = r1 + a
         return O.mlp(m, orig_rms_norm(r2, m.post_norm, cfg.rms_eps)), r2
 
+    def broke_causal_strict(q_len, k_len):
+        qi = (k_len - q_len + np.arange(q_len))[:, None]
+        return np.arange(k_len)[None, :] < qi
+
     slips = [
+        ("causal_mask", broke_causal_strict, [test_causal_mask_elementwise_rule]),
         ("mlp", broke_mlp_swapped, [test_mlp_matches_explicit_sums]),
         ("silu", broke_silu_sigmoid, [test_silu_closed_forms, test_mlp_matches_explicit_sums]),
         ("decoder_layer", broke_decoder_post_on_r1,

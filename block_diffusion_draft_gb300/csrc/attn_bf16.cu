@@ -335,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     const bool real = qr < w.rows;
     // this row's allowed keys: the unit's range, on a band layer cut to
-    // |query index - key| < W (the query's index is len - q_len + t)
+    // |query index - key| < W, on a causal layer to keys <= the query index
+    // (the query's index is len - q_len + t)
     int i1_lo = 0, i1_hi = 0;
     int out_token = 0, out_col = 0;
     {
@@ -345,11 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       out_token = w.b * a.q_len + t;
       i1_lo = w.s0_lo;
       i1_hi = w.s0_hi;
+      const int qi = w.len - a.q_len + t;  // the row's own key index
       if (a.window > 0) {
-        const int qi = w.len - a.q_len + t;
         i1_lo = max(i1_lo, qi - a.window + 1);
         i1_hi = min(i1_hi, qi + a.window);
       }
+      if (a.causal) i1_hi = min(i1_hi, qi + 1);
     }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {

@@ -204,7 +204,7 @@ extern "C" {
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
 
-int dflash_abi_version(void) { return 100; }
+int dflash_abi_version(void) { return 101; }
 
 int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const void* wk,
                        const void* wv, const void* wo, const void* q_norm_w,
@@ -224,6 +224,7 @@ int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const v
       cfg.n_target_layers < 0 || cfg.sliding_window < 0 || cfg.max_position < 0 ||
       !(cfg.rms_eps >= 0.f) || !(cfg.rope_theta > 0.f))
     return fail(DFLASH_ERR_SHAPE, "non-positive or invalid layer scalar");
+  if (cfg.causal != 0 && cfg.causal != 1) return fail(DFLASH_ERR_SHAPE, "causal must be 0 or 1");
   if (cfg.head_dim == 0) cfg.head_dim = cfg.hidden / cfg.n_heads;
   if (cfg.max_position == 0) cfg.max_position = 131072;
   if (cfg.n_heads % cfg.n_kv_heads != 0)
@@ -564,6 +565,7 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
   aa.tile_blocks = 1;
   aa.cap = c->cap;
   aa.window = a->cfg.sliding_window;
+  aa.causal = a->cfg.causal != 0;
   aa.n_units = sq.unit_off[batch];
   aa.cluster = cl;
   aa.out = a->attn_out.p;
@@ -858,6 +860,7 @@ int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
   if (batch > kMaxBatch) return fail(DFLASH_ERR_SHAPE, "batch above %d", kMaxBatch);
   if (a->cfg.sliding_window > 0)
     return fail(DFLASH_ERR_UNSUPPORTED, "packed layout on a sliding-window layer");
+  if (a->cfg.causal) return fail(DFLASH_ERR_UNSUPPORTED, "packed layout on a causal layer");
   if (a->dt == DFLASH_BF16 && a->g * block_size > 128)
     return fail(DFLASH_ERR_UNSUPPORTED, "groups * block_size = %d above 128",
                 a->g * block_size);

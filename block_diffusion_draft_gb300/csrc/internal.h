@@ -137,6 +137,7 @@ struct AttnArgs {
   int tile_blocks;   // blocks per 128-row Q tile
   int cap;           // key rows per (sequence, head) in the K/V storage
   int window;        // sliding window (0 = full)
+  int causal;        // inference: block row t sees keys up to its own index
   int seq;           // packed: context rows per sequence
   const int* anchors;  // packed: [B][n_blocks]
   int n_units;

@@ -145,11 +145,12 @@ __global__ void attn_f32_kernel(const AttnArgs a, const AttnSeqs sq,
     const int len = sq.len[b];
     lo1 = 0;
     hi1 = len;
+    const int qi = len - a.q_len + tg;  // the row's own key index
     if (a.window > 0) {
-      const int qi = len - a.q_len + tg;
       lo1 = max(0, qi - a.window + 1);
       hi1 = min(len, qi + a.window);
     }
+    if (a.causal) hi1 = min(hi1, qi + 1);
   } else {
     int an = a.anchors[b * a.n_blocks + blk];
     if (an < 0 || an > a.seq) {

@@ -29,7 +29,7 @@ class Config(ctypes.Structure):
                 ("n_kv_heads", c_int32), ("head_dim", c_int32),
                 ("n_target_layers", c_int32), ("rms_eps", c_float),
                 ("rope_theta", c_float), ("sliding_window", c_int32),
-                ("max_position", c_int32), ("dtype", c_int32)]
+                ("max_position", c_int32), ("dtype", c_int32), ("causal", c_int32)]
 
 
 class DFlashError(RuntimeError):
@@ -133,7 +133,7 @@ class DFlashAttention:
                  n_target_layers: int = 0, rms_eps: float = 1e-6,
                  rope_theta: float = 1e6, sliding_window: int = 0,
                  max_position: int = 0, dtype: torch.dtype = torch.bfloat16,
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, causal: bool = False):
         self.device = torch.device(device or "cuda")
         if self.device.type != "cuda":
             raise ValueError("the library runs on CUDA devices only")
@@ -145,7 +145,8 @@ class DFlashAttention:
         self.cfg = Config(hidden, n_heads, n_kv_heads, self.head_dim,
                           n_target_layers, rms_eps, rope_theta, sliding_window,
                           max_position,
-                          DFLASH_BF16 if dtype == torch.bfloat16 else DFLASH_FP32)
+                          DFLASH_BF16 if dtype == torch.bfloat16 else DFLASH_FP32,
+                          1 if causal else 0)
         dev_w = {k: v.to(self.device, dtype).contiguous() for k, v in weights.items()}
         fc = dev_w.get("fc") if n_target_layers > 0 else None
         hn = dev_w.get("hidden_norm") if n_target_layers > 0 else None

@@ -58,6 +58,8 @@ class Spec:
     layers: int = 1
     # > 0: the whole decoder layer (norms, residual, MLP of this width)
     intermediate: int = 0
+    # causal attention layer (block row t sees keys up to its own index)
+    causal: bool = False
 
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32

@@ -94,6 +94,13 @@ typedef struct {
   int32_t max_position;    /* positions must lie in [0, max_position);
                               0 -> 131072                                    */
   int32_t dtype;           /* DFLASH_BF16 or DFLASH_FP32                     */
+  int32_t causal;          /* 1: block row t sees the keys at or before its
+                              own key index (every cached and context row,
+                              block rows 0..t), with the band on sliding
+                              layers ([P5] _dflash_layer_causal); 0: the
+                              block is bidirectional.  Inference only: the
+                              packed training forward is _UNSUPPORTED on a
+                              causal layer                                   */
 } dflash_attn_config;
 
 /* Message for the last failed call on this thread ("" if none). */

@@ -28,7 +28,7 @@ def oracle_layer(sp: W.Spec, w: Dict[str, torch.Tensor]):
                         n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
                         rms_eps=sp.rms_eps, rope_theta=sp.rope_theta,
                         sliding_window=sp.sliding_window,
-                        n_target_layers=sp.n_target_layers)
+                        n_target_layers=sp.n_target_layers, causal=sp.causal)
     lw = O.LayerWeights(wq=f64(w["wq"]), wk=f64(w["wk"]), wv=f64(w["wv"]),
                         wo=f64(w["wo"]), q_norm=f64(w["q_norm"]),
                         k_norm=f64(w["k_norm"]),
@@ -44,7 +44,7 @@ def gpu_layer(sp: W.Spec, w: Dict[str, torch.Tensor], device="cuda") -> DFlashAt
                            rms_eps=sp.rms_eps, rope_theta=sp.rope_theta,
                            sliding_window=sp.sliding_window,
                            max_position=sp.max_position, dtype=sp.torch_dtype(),
-                           device=device)
+                           device=device, causal=sp.causal)
 
 
 def errors(gpu: np.ndarray, ref: np.ndarray):

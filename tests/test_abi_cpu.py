@@ -26,7 +26,7 @@ def test_every_declared_function_is_exported(L):
 
 
 def test_abi_version(L):
-    assert L.dflash_abi_version() == 100
+    assert L.dflash_abi_version() == 101
 
 
 def test_create_rejects_null_config(L):
@@ -44,7 +44,7 @@ def test_create_rejects_bad_shapes_before_touching_the_device(L):
     def create(**kw):
         base = dict(hidden=256, n_heads=4, n_kv_heads=2, head_dim=0, n_target_layers=0,
                     rms_eps=1e-6, rope_theta=1e6, sliding_window=0, max_position=0,
-                    dtype=0)
+                    dtype=0, causal=0)
         base.update(kw)
         cfg = D.Config(*[base[f] for f, _ in D.Config._fields_])
         return L.dflash_attn_create(ctypes.byref(cfg), fake, fake, fake, fake, fake,
@@ -56,6 +56,7 @@ def test_create_rejects_bad_shapes_before_touching_the_device(L):
     assert create(head_dim=64) == -2                      # bf16 needs head_dim 128
     assert create(n_target_layers=2) == -2                # fc missing
     assert create(dtype=1, head_dim=512, hidden=2048) == -2  # fp32 head_dim limit
+    assert create(causal=2) == -2                         # causal is 0 or 1
 
 
 def test_calls_reject_null_handles(L):

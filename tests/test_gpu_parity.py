@@ -69,6 +69,26 @@ def test_bf16_full_q_tile_groups8():
     T.assert_close(got, ref, "bf16", "g8")
 
 
+@pytest.mark.parametrize("window", [0, 100])
+def test_bf16_causal_layer(window):
+    # causal layers ("vllm...qwen3_dflash", _dflash_layer_causal), full and
+    # banded: a long prefill step split across CTAs, a crop, then a short step
+    sp = small_bf16(sliding_window=window, causal=True, batch=2)
+    sc = T.Scenario(sp, seed=14, capacity=1024)
+    got, ref = sc.step([50, 400])
+    T.assert_close(got, ref, "bf16", "causal prefill")
+    sc.crop([50, 400])
+    got, ref = sc.step([16, 3])
+    T.assert_close(got, ref, "bf16", "causal step")
+
+
+def test_fp32_causal_layer():
+    sp = W.spec("tiny_fp32", causal=True)
+    sc = T.Scenario(sp, seed=15, capacity=256)
+    got, ref = sc.step([sp.prefill])
+    T.assert_close(got, ref, "fp32", "fp32 causal")
+
+
 def test_bf16_sliding_window_band():
     sp = small_bf16(sliding_window=100, batch=2)
     sc = T.Scenario(sp, seed=4, capacity=1024)

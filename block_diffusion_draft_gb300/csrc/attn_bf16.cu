@@ -242,13 +242,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_q = policy_evict_first();
     auto load_kv = [&](int j) {
       const int s = j % NST;
-      const int y = (int)(w.kv_row0 + tile_start(w, j));
+      const int k0 = tile_start(w, j);
       mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
-      tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
-      tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
       mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
-      tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
-      tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+      if (a.block_table == nullptr) {
+        const int y = (int)(w.kv_row0 + k0);
+        tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
+        tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
+        tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
+        tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+      } else {
+        // paged: the tile's 128 / P pages, each a P-row box per half (an
+        // entry past the sequence or out of range reads page 0: masked keys)
+        const int P = a.page_size;
+        const int* bt = a.block_table + (size_t)w.b * a.bt_stride;
+        for (int i = 0; i < BKEY / P; ++i) {
+          const int slot = k0 / P + i;
+          int page = slot < a.bt_stride ? bt[slot] : 0;
+          if (page < 0 || page >= a.n_pages) page = 0;
+          const int y = (page * a.n_kv + w.h) * P;
+          const uint32_t off = (uint32_t)(i * P * 128);
+          tma_load_2d(sK + s * TILE_BYTES + off, &tmK, &k_full[s], 0, y, pol_kv);
+          tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES + off, &tmK, &k_full[s], 64, y, pol_kv);
+          tma_load_2d(sV + s * TILE_BYTES + off, &tmV, &v_full[s], 0, y, pol_kv);
+          tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES + off, &tmV, &v_full[s], 64, y, pol_kv);
+        }
+      }
     };
     // Tiles made only of rows that were in the cache before this call were
     // written by kernels that have completed (every kernel here starts its
@@ -1061,10 +1080,13 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                            mk, mv, a);
   }
   const bool dual = a.mode == 0 && a.groups * a.q_len <= 64;
+  const int kv_box = a.block_table != nullptr ? a.page_size : 128;
+  if (a.block_table != nullptr && (kv_box < 16 || kv_box > 128 || (kv_box & (kv_box - 1)) != 0))
+    return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv;
   if (make_tmap_bf16_rows(&mq, qbuf, q_rows_total, HD, dual ? 64 : 128) != 0 ||
-      make_tmap_bf16_rows(&mk, cache_k, kv_rows_total, HD, 128) != 0 ||
-      make_tmap_bf16_rows(&mv, cache_v, kv_rows_total, HD, 128) != 0)
+      make_tmap_bf16_rows(&mk, cache_k, kv_rows_total, HD, kv_box) != 0 ||
+      make_tmap_bf16_rows(&mv, cache_v, kv_rows_total, HD, kv_box) != 0)
     return cudaErrorInvalidValue;
   static AttnSeqs zero_seqs{};
   const AttnSeqs& sq = seqs ? *seqs : zero_seqs;

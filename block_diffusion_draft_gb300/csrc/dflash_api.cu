@@ -195,6 +195,132 @@ int run_o_proj(dflash_attn* a, int rows, void* out, cudaStream_t s) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The cache a forward appends to and reads: contiguous ([B][n_kv][cap][d])
+// or paged ([n_pages][n_kv][P][d] with the caller's slots and block table).
+struct KvView {
+  void* k = nullptr;
+  void* v = nullptr;
+  int cap = 0;
+  long long rows_total = 0;  // rows of the K (and V) storage
+  const int* slot_mapping = nullptr;
+  const int* block_table = nullptr;
+  int bt_stride = 0, page_size = 0, n_pages = 0;
+  static KvView of(const dflash_cache* c) {
+    KvView v;
+    v.k = c->k;
+    v.v = c->v;
+    v.cap = c->cap;
+    v.rows_total = (long long)c->batch * c->nkv * c->cap;
+    return v;
+  }
+};
+
+// Projections, attention and o_proj of one forward (arguments checked by the
+// caller); the caller updates its own lengths.
+int forward_core(dflash_attn* a, const KvView& kv, int batch, int q_len, const void* noise,
+                 const void* target_hidden, const int32_t* host_n_ctx, const int* len_before,
+                 const int32_t* positions, void* out, dflash_stream stream) {
+  const long long rows_noise = (long long)batch * q_len;
+  long long total_ctx = 0;
+  for (int b = 0; b < batch; ++b) total_ctx += host_n_ctx[b];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t es = dtype_size(a->dt);
+  const size_t qd = (size_t)a->nq * a->d;
+
+  SeqTable st;
+  st.n = batch;
+  st.q_len = q_len;
+  st.ctx_off[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    st.ctx_off[b + 1] = st.ctx_off[b] + host_n_ctx[b];
+    st.cache_len[b] = len_before[b];
+  }
+  DF_CUDA(a->qbuf.ensure(rows_noise * qd * es), "scratch allocation");
+  DF_CUDA(a->attn_out.ensure(rows_noise * qd * es), "scratch allocation");
+  QkvOut o = make_qkv_out(a, positions, a->qbuf.p, kv.k, kv.v, kv.cap, q_len);
+  o.slot_mapping = kv.slot_mapping;
+  o.page_size = kv.page_size;
+  o.n_pages = kv.n_pages;
+  o.err = a->err;
+  if (int r = run_qkv(a, noise, (int)rows_noise, target_hidden, (int)total_ctx, o, st, s))
+    return r;
+
+  // attention work list: per sequence the visible key range, split in chunks
+  AttnSeqs sq;
+  long long total_keys = 0;
+  for (int b = 0; b < batch; ++b) {
+    sq.len[b] = len_before[b] + host_n_ctx[b] + q_len;
+    sq.first_new[b] = len_before[b];
+    sq.lo[b] = a->cfg.sliding_window > 0
+                   ? std::max(0, sq.len[b] - q_len - a->cfg.sliding_window + 1)
+                   : 0;
+    // paged tiles gather whole pages: start the range on a tile boundary
+    // (the band still cuts each row's keys)
+    if (kv.block_table != nullptr) sq.lo[b] = sq.lo[b] / 128 * 128;
+    total_keys += (long long)a->nkv * (sq.len[b] - sq.lo[b]);
+  }
+  // Few (sequence, kv head) pairs: each pair's keys split evenly over the C
+  // CTAs of a thread-block cluster that merge on chip.  Otherwise about one
+  // key chunk per SM, in whole 128-key tiles, at most 4096 keys, merged by a
+  // second kernel.
+  const int cl = a->dt == DFLASH_BF16
+                     ? attn_decode_cluster(batch * a->nkv, a->num_sms, a->g * q_len <= 64)
+                     : 1;
+  int chunk = (int)((total_keys + a->num_sms - 1) / a->num_sms);
+  chunk = std::min(4096, std::max(128, (chunk + 127) / 128 * 128));
+  sq.unit_off[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int keys = sq.len[b] - sq.lo[b];
+    if (cl > 1) {
+      sq.chunk[b] = std::max(128, ((keys + cl - 1) / cl + 127) / 128 * 128);
+      sq.n_chunks[b] = cl;
+    } else {
+      sq.chunk[b] = chunk;
+      sq.n_chunks[b] = std::max(1, (keys + chunk - 1) / chunk);
+    }
+    sq.unit_off[b + 1] = sq.unit_off[b] + a->nkv * sq.n_chunks[b];
+  }
+  AttnArgs aa{};
+  aa.mode = 0;
+  aa.batch = batch;
+  aa.n_kv = a->nkv;
+  aa.groups = a->g;
+  aa.head_dim = a->d;
+  aa.q_len = q_len;
+  aa.q_block = q_len;
+  aa.n_blocks = 1;
+  aa.tile_blocks = 1;
+  aa.cap = kv.cap;
+  aa.block_table = kv.block_table;
+  aa.bt_stride = kv.bt_stride;
+  aa.page_size = kv.page_size;
+  aa.n_pages = kv.n_pages;
+  aa.window = a->cfg.sliding_window;
+  aa.causal = a->cfg.causal != 0;
+  aa.n_units = sq.unit_off[batch];
+  aa.cluster = cl;
+  aa.out = a->attn_out.p;
+  aa.err = a->err;
+  if (a->dt == DFLASH_BF16) {
+    DF_CUDA(a->part_o.ensure((size_t)aa.n_units * 128 * 128 * 4), "scratch allocation");
+    DF_CUDA(a->part_ml.ensure((size_t)aa.n_units * 256 * 4), "scratch allocation");
+    aa.part_o = static_cast<float*>(a->part_o.p);
+    aa.part_ml = static_cast<float*>(a->part_ml.p);
+    TraceScope tr(a, DFLASH_K_ATTN, s);
+    DF_CUDA(launch_attn_bf16(aa, &sq, a->qbuf.p, rows_noise * a->nq, kv.k, kv.v,
+                             kv.rows_total, s),
+            "attention launch");
+  } else {
+    TraceScope tr(a, DFLASH_K_ATTN, s);
+    DF_CUDA(launch_attn_f32(aa, &sq, static_cast<const float*>(a->qbuf.p),
+                            static_cast<const float*>(kv.k), static_cast<const float*>(kv.v),
+                            s),
+            "fp32 attention launch");
+  }
+  return run_o_proj(a, (int)rows_noise, out, s);
+}
+
+
 }  // namespace
 
 // error reporting for the allocation-free entry point (noalloc.cu)
@@ -204,7 +330,7 @@ extern "C" {
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
 
-int dflash_abi_version(void) { return 101; }
+int dflash_abi_version(void) { return 102; }
 
 int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const void* wk,
                        const void* wv, const void* wo, const void* q_norm_w,
@@ -503,92 +629,126 @@ int dflash_attn_forward(dflash_attn* a, dflash_cache* c, int batch, int q_len,
   if (a->dt == DFLASH_BF16 &&
       (!aligned16(noise) || !aligned16(out) || (total_ctx > 0 && !aligned16(target_hidden))))
     return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t es = dtype_size(a->dt);
-  const size_t qd = (size_t)a->nq * a->d;
-
-  SeqTable st;
-  st.n = batch;
-  st.q_len = q_len;
-  st.ctx_off[0] = 0;
-  for (int b = 0; b < batch; ++b) {
-    st.ctx_off[b + 1] = st.ctx_off[b] + host_n_ctx[b];
-    st.cache_len[b] = c->len[b];
-  }
-  DF_CUDA(a->qbuf.ensure(rows_noise * qd * es), "scratch allocation");
-  DF_CUDA(a->attn_out.ensure(rows_noise * qd * es), "scratch allocation");
-  QkvOut o = make_qkv_out(a, positions, a->qbuf.p, c->k, c->v, c->cap, q_len);
-  if (int r = run_qkv(a, noise, (int)rows_noise, target_hidden, (int)total_ctx, o, st, s))
-    return r;
-
-  // attention work list: per sequence the visible key range, split in chunks
-  AttnSeqs sq;
-  long long total_keys = 0;
-  for (int b = 0; b < batch; ++b) {
-    sq.len[b] = c->len[b] + host_n_ctx[b] + q_len;
-    sq.first_new[b] = c->len[b];
-    sq.lo[b] = a->cfg.sliding_window > 0
-                   ? std::max(0, sq.len[b] - q_len - a->cfg.sliding_window + 1)
-                   : 0;
-    total_keys += (long long)a->nkv * (sq.len[b] - sq.lo[b]);
-  }
-  // Few (sequence, kv head) pairs: each pair's keys split evenly over the C
-  // CTAs of a thread-block cluster that merge on chip.  Otherwise about one
-  // key chunk per SM, in whole 128-key tiles, at most 4096 keys, merged by a
-  // second kernel.
-  const int cl = a->dt == DFLASH_BF16
-                     ? attn_decode_cluster(batch * a->nkv, a->num_sms, a->g * q_len <= 64)
-                     : 1;
-  int chunk = (int)((total_keys + a->num_sms - 1) / a->num_sms);
-  chunk = std::min(4096, std::max(128, (chunk + 127) / 128 * 128));
-  sq.unit_off[0] = 0;
-  for (int b = 0; b < batch; ++b) {
-    const int keys = sq.len[b] - sq.lo[b];
-    if (cl > 1) {
-      sq.chunk[b] = std::max(128, ((keys + cl - 1) / cl + 127) / 128 * 128);
-      sq.n_chunks[b] = cl;
-    } else {
-      sq.chunk[b] = chunk;
-      sq.n_chunks[b] = std::max(1, (keys + chunk - 1) / chunk);
-    }
-    sq.unit_off[b + 1] = sq.unit_off[b] + a->nkv * sq.n_chunks[b];
-  }
-  AttnArgs aa{};
-  aa.mode = 0;
-  aa.batch = batch;
-  aa.n_kv = a->nkv;
-  aa.groups = a->g;
-  aa.head_dim = a->d;
-  aa.q_len = q_len;
-  aa.q_block = q_len;
-  aa.n_blocks = 1;
-  aa.tile_blocks = 1;
-  aa.cap = c->cap;
-  aa.window = a->cfg.sliding_window;
-  aa.causal = a->cfg.causal != 0;
-  aa.n_units = sq.unit_off[batch];
-  aa.cluster = cl;
-  aa.out = a->attn_out.p;
-  aa.err = a->err;
-  if (a->dt == DFLASH_BF16) {
-    DF_CUDA(a->part_o.ensure((size_t)aa.n_units * 128 * 128 * 4), "scratch allocation");
-    DF_CUDA(a->part_ml.ensure((size_t)aa.n_units * 256 * 4), "scratch allocation");
-    aa.part_o = static_cast<float*>(a->part_o.p);
-    aa.part_ml = static_cast<float*>(a->part_ml.p);
-    TraceScope tr(a, DFLASH_K_ATTN, s);
-    DF_CUDA(launch_attn_bf16(aa, &sq, a->qbuf.p, rows_noise * a->nq, c->k, c->v,
-                             (long long)batch * a->nkv * c->cap, s),
-            "attention launch");
-  } else {
-    TraceScope tr(a, DFLASH_K_ATTN, s);
-    DF_CUDA(launch_attn_f32(aa, &sq, static_cast<const float*>(a->qbuf.p),
-                            static_cast<const float*>(c->k), static_cast<const float*>(c->v),
-                            s),
-            "fp32 attention launch");
-  }
-  if (int r = run_o_proj(a, (int)rows_noise, out, s)) return r;
-  for (int b = 0; b < batch; ++b) c->len[b] = sq.len[b];
+  const int rc = forward_core(a, KvView::of(c), batch, q_len, noise, target_hidden, host_n_ctx,
+                              c->len.data(), positions, out, stream);
+  if (rc != DFLASH_OK) return rc;
+  for (int b = 0; b < batch; ++b) c->len[b] += host_n_ctx[b] + q_len;
   return DFLASH_OK;
+}
+
+int dflash_paged_cache_create(const dflash_attn* a, int n_pages, int page_size,
+                              dflash_paged_cache** out) {
+  if (out == nullptr) return fail(DFLASH_ERR_ARG, "out is null");
+  *out = nullptr;
+  if (int r = check_attn(a)) return r;
+  if (a->dt != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "paged caches need a bf16 layer");
+  if (n_pages <= 0) return fail(DFLASH_ERR_ARG, "n_pages must be positive");
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return fail(DFLASH_ERR_ARG, "page_size must be 16, 32, 64 or 128");
+  if ((long long)n_pages * a->nkv * page_size >= (1LL << 31))
+    return fail(DFLASH_ERR_SHAPE, "too many cache rows");
+  dflash_paged_cache* c = new dflash_paged_cache();
+  c->n_pages = n_pages;
+  c->page_size = page_size;
+  c->nkv = a->nkv;
+  c->d = a->d;
+  c->dt = a->dt;
+  c->device = a->device;
+  const size_t bytes = (size_t)n_pages * a->nkv * page_size * a->d * dtype_size(a->dt);
+  cudaError_t e = cudaMalloc(&c->k, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&c->v, bytes);
+  // zeroed: keys past a sequence's end in its last tile are read (and masked)
+  if (e == cudaSuccess) e = cudaMemset(c->k, 0, bytes);
+  if (e == cudaSuccess) e = cudaMemset(c->v, 0, bytes);
+  if (e != cudaSuccess) {
+    dflash_paged_cache_destroy(c);
+    return cuda_fail(e, "paged cache allocation");
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+int dflash_paged_cache_destroy(dflash_paged_cache* c) {
+  if (c == nullptr) return DFLASH_OK;
+  cudaDeviceSynchronize();
+  cudaFree(c->k);
+  cudaFree(c->v);
+  delete c;
+  return DFLASH_OK;
+}
+
+int dflash_paged_cache_data(const dflash_paged_cache* c, void** k, void** v, int32_t* n_pages,
+                            int32_t* n_kv_heads, int32_t* page_size, int32_t* head_dim) {
+  if (c == nullptr) return fail(DFLASH_ERR_ARG, "null cache");
+  if (k) *k = c->k;
+  if (v) *v = c->v;
+  if (n_pages) *n_pages = c->n_pages;
+  if (n_kv_heads) *n_kv_heads = c->nkv;
+  if (page_size) *page_size = c->page_size;
+  if (head_dim) *head_dim = c->d;
+  return DFLASH_OK;
+}
+
+int dflash_paged_cache_read(const dflash_paged_cache* c, void* k_dst, void* v_dst,
+                            dflash_stream stream) {
+  if (c == nullptr || k_dst == nullptr || v_dst == nullptr)
+    return fail(DFLASH_ERR_ARG, "null argument");
+  const size_t bytes = (size_t)c->n_pages * c->nkv * c->page_size * c->d * dtype_size(c->dt);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DF_CUDA(cudaMemcpyAsync(k_dst, c->k, bytes, cudaMemcpyDeviceToDevice, s), "cache copy");
+  DF_CUDA(cudaMemcpyAsync(v_dst, c->v, bytes, cudaMemcpyDeviceToDevice, s), "cache copy");
+  return DFLASH_OK;
+}
+
+int dflash_attn_forward_paged(dflash_attn* a, dflash_paged_cache* c, int batch, int q_len,
+                              const void* noise, const void* target_hidden,
+                              const int32_t* host_n_ctx, const int32_t* host_len_before,
+                              const int32_t* positions, const int32_t* slot_mapping,
+                              const int32_t* block_table, int bt_stride, void* out,
+                              dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (c == nullptr) return fail(DFLASH_ERR_ARG, "null cache");
+  if (noise == nullptr || host_n_ctx == nullptr || host_len_before == nullptr ||
+      positions == nullptr || slot_mapping == nullptr || block_table == nullptr ||
+      out == nullptr)
+    return fail(DFLASH_ERR_ARG, "null tensor");
+  if (batch <= 0 || q_len <= 0) return fail(DFLASH_ERR_ARG, "batch and q_len must be positive");
+  if (batch > kMaxBatch) return fail(DFLASH_ERR_SHAPE, "batch above %d", kMaxBatch);
+  if (c->nkv != a->nkv || c->d != a->d || c->dt != a->dt || c->device != a->device)
+    return fail(DFLASH_ERR_SHAPE, "cache geometry does not match the layer");
+  if (a->g * q_len > 128)
+    return fail(DFLASH_ERR_UNSUPPORTED, "groups * q_len = %d above 128", a->g * q_len);
+  if (bt_stride <= 0) return fail(DFLASH_ERR_ARG, "bt_stride must be positive");
+  long long total_ctx = 0;
+  std::vector<int> len_before(batch);
+  for (int b = 0; b < batch; ++b) {
+    if (host_n_ctx[b] < 0) return fail(DFLASH_ERR_ARG, "n_ctx[%d] < 0", b);
+    if (host_len_before[b] < 0) return fail(DFLASH_ERR_ARG, "len_before[%d] < 0", b);
+    total_ctx += host_n_ctx[b];
+    const long long len = (long long)host_len_before[b] + host_n_ctx[b] + q_len;
+    if (len > (long long)bt_stride * c->page_size)
+      return fail(DFLASH_ERR_CAPACITY, "sequence %d: %lld rows exceed %d block-table pages",
+                  b, len, bt_stride);
+    len_before[b] = host_len_before[b];
+  }
+  if (total_ctx > 0 && target_hidden == nullptr)
+    return fail(DFLASH_ERR_ARG, "target_hidden is null but n_ctx is not all zero");
+  const long long rows_noise = (long long)batch * q_len;
+  if (rows_noise + total_ctx > (1LL << 30)) return fail(DFLASH_ERR_SHAPE, "too many rows");
+  if (!aligned16(noise) || !aligned16(out) || (total_ctx > 0 && !aligned16(target_hidden)))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  KvView kv;
+  kv.k = c->k;
+  kv.v = c->v;
+  kv.cap = c->page_size;
+  kv.rows_total = (long long)c->n_pages * c->nkv * c->page_size;
+  kv.slot_mapping = slot_mapping;
+  kv.block_table = block_table;
+  kv.bt_stride = bt_stride;
+  kv.page_size = c->page_size;
+  kv.n_pages = c->n_pages;
+  return forward_core(a, kv, batch, q_len, noise, target_hidden, host_n_ctx, len_before.data(),
+                      positions, out, stream);
 }
 
 int dflash_kv_group_create(dflash_attn* const* layers, int n_layers, dflash_kv_group** out) {

@@ -236,16 +236,23 @@ DF_DEV QkvTarget qkv_target(const QkvOut& qo, const SeqTable& st, int src, int s
         ((((size_t)b * qo.n_kv + h) * nblk + blk) * qo.groups + gi) * qo.q_block + tt;
     g.kind = 1;
     g.dst = reinterpret_cast<__nv_bfloat16*>(qo.qbuf) + qrow * HD;
-  } else if (n0 < q_cols + kv_cols) {
-    const int h = (n0 - q_cols) / HD;
-    g.kind = 2;
-    g.dst = reinterpret_cast<__nv_bfloat16*>(qo.cache_k) +
-            (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD;
   } else {
-    const int h = (n0 - q_cols - kv_cols) / HD;
-    g.kind = 3;
-    g.dst = reinterpret_cast<__nv_bfloat16*>(qo.cache_v) +
-            (((size_t)b * qo.n_kv + h) * qo.cap + crow) * HD;
+    const bool is_k = n0 < q_cols + kv_cols;
+    const int h = (n0 - q_cols - (is_k ? 0 : kv_cols)) / HD;
+    size_t row = ((size_t)b * qo.n_kv + h) * qo.cap + crow;
+    if (qo.slot_mapping != nullptr) {  // paged cache: the caller's slot for the row
+      const int sl = qo.slot_mapping[pos_idx];
+      const int page = sl >= 0 ? sl / qo.page_size : -1;
+      if (page < 0 || page >= qo.n_pages) {
+        record_error(qo.err, 4 /* DFLASH_DEV_SLOT */);
+        g.kind = 0;
+        g.dst = nullptr;
+        return g;
+      }
+      row = ((size_t)page * qo.n_kv + h) * qo.page_size + (sl - page * qo.page_size);
+    }
+    g.kind = is_k ? 2 : 3;
+    g.dst = reinterpret_cast<__nv_bfloat16*>(is_k ? qo.cache_k : qo.cache_v) + row * HD;
   }
   return g;
 }

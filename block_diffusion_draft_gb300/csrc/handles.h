@@ -92,3 +92,12 @@ struct dflash_cache {
   void* v = nullptr;
   std::vector<int> len;
 };
+
+// Paged draft KV cache: pages of page_size rows, K and V each
+// [n_pages][nkv][page_size][d] bf16; lengths, slots and block tables belong
+// to the caller.
+struct dflash_paged_cache {
+  int n_pages = 0, page_size = 0, nkv = 0, d = 0, dt = 0, device = 0;
+  void* k = nullptr;
+  void* v = nullptr;
+};

@@ -36,6 +36,13 @@ struct QkvOut {
   void* qbuf;              // [B][n_kv][n_blocks][groups][q_block][d]
   void* cache_k;           // [B][n_kv][cap][d]
   void* cache_v;
+  // paged cache: the row at positions index i goes to slot slot_mapping[i]
+  // (page slot / P, row slot % P) of storage [n_pages][n_kv][P][d]; null:
+  // contiguous cache
+  const int* slot_mapping;
+  int page_size;
+  int n_pages;
+  int* err;
   // layer group (context K/V of several layers from one GEMM, no Q columns):
   // n_layers > 0, columns [layer][K heads | V heads], every row a context row
   int n_layers;
@@ -138,6 +145,13 @@ struct AttnArgs {
   int cap;           // key rows per (sequence, head) in the K/V storage
   int window;        // sliding window (0 = full)
   int causal;        // inference: block row t sees keys up to its own index
+  // paged cache: a sequence's key row k lives in page block_table[b][k / P]
+  // at offset k % P of storage [n_pages][n_kv][P][d] (cap = P); null:
+  // contiguous [B][n_kv][cap][d]
+  const int* block_table;
+  int bt_stride;     // entries per sequence in block_table
+  int page_size;     // P (16, 32, 64 or 128; a power of two)
+  int n_pages;
   int seq;           // packed: context rows per sequence
   const int* anchors;  // packed: [B][n_blocks]
   int n_units;

@@ -59,6 +59,14 @@ _SIGNATURES = {
                              POINTER(c_int32), c_void_p, c_void_p, c_void_p], c_int),
     "dflash_attn_forward_packed": ([c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p], c_int),
+    "dflash_paged_cache_create": ([c_void_p, c_int, c_int, POINTER(c_void_p)], c_int),
+    "dflash_paged_cache_destroy": ([c_void_p], c_int),
+    "dflash_paged_cache_data": ([c_void_p, POINTER(c_void_p), POINTER(c_void_p)] +
+                                [POINTER(c_int32)] * 4, c_int),
+    "dflash_paged_cache_read": ([c_void_p, c_void_p, c_void_p, c_void_p], c_int),
+    "dflash_attn_forward_paged": ([c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
+                                   POINTER(c_int32), POINTER(c_int32), c_void_p, c_void_p,
+                                   c_void_p, c_int, c_void_p, c_void_p], c_int),
     "dflash_kv_group_create": ([POINTER(c_void_p), c_int, POINTER(c_void_p)], c_int),
     "dflash_kv_group_destroy": ([c_void_p], c_int),
     "dflash_kv_group_append": ([c_void_p, POINTER(c_void_p), c_int, c_void_p,
@@ -187,6 +195,26 @@ class DFlashAttention:
                 _int32_array(n_ctx), _p(positions), _p(out), _stream(self.device)))
         return out
 
+    def forward_paged(self, cache: "PagedCache", noise: torch.Tensor,
+                      target_hidden: Optional[torch.Tensor], n_ctx: Sequence[int],
+                      len_before: Sequence[int], positions: torch.Tensor,
+                      slot_mapping: torch.Tensor, block_table: torch.Tensor,
+                      out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """forward() over a paged cache: new rows go to slot_mapping's slots
+        (int32, in positions order), keys are read through block_table
+        (int32 [batch, bt_stride])."""
+        B, q_len, _ = noise.shape
+        if out is None:
+            out = torch.empty_like(noise)
+        th = None if target_hidden is None or target_hidden.numel() == 0 else target_hidden
+        bt = block_table.contiguous()
+        with torch.cuda.device(self.device):
+            check(lib().dflash_attn_forward_paged(
+                self.handle, cache.handle, B, q_len, _p(noise), _p(th),
+                _int32_array(n_ctx), _int32_array(len_before), _p(positions),
+                _p(slot_mapping), _p(bt), bt.shape[1], _p(out), _stream(self.device)))
+        return out
+
     def forward_packed(self, noise: torch.Tensor, target_hidden: torch.Tensor,
                        anchors: torch.Tensor, block_size: int,
                        out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -271,6 +299,41 @@ class DraftCache:
     def close(self) -> None:
         if getattr(self, "handle", None):
             lib().dflash_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class PagedCache:
+    """Paged KV storage held by the library ([n_pages][n_kv][page_size]
+    [head_dim] for K and for V); lengths and page tables are the caller's."""
+
+    def __init__(self, attn: DFlashAttention, n_pages: int, page_size: int):
+        self.attn = attn
+        self.n_pages, self.page_size = n_pages, page_size
+        h = c_void_p()
+        with torch.cuda.device(attn.device):
+            check(lib().dflash_paged_cache_create(attn.handle, n_pages, page_size,
+                                                  ctypes.byref(h)))
+        self.handle = h
+
+    def read(self):
+        """Copies of the K and V storage as [n_pages, n_kv, page_size, head_dim]."""
+        a = self.attn
+        shape = (self.n_pages, a.n_kv_heads, self.page_size, a.head_dim)
+        k = torch.empty(shape, device=a.device, dtype=a.dtype)
+        v = torch.empty(shape, device=a.device, dtype=a.dtype)
+        with torch.cuda.device(a.device):
+            check(lib().dflash_paged_cache_read(self.handle, _p(k), _p(v), _stream(a.device)))
+        return k, v
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            lib().dflash_paged_cache_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -51,6 +51,7 @@ typedef struct dflash_attn dflash_attn;   /* one layer: weights + scratch */
 typedef struct dflash_cache dflash_cache; /* one draft KV cache */
 typedef struct dflash_kv_group dflash_kv_group; /* context K/V of several layers */
 typedef struct dflash_mlp dflash_mlp;     /* norms + MLP of a decoder layer */
+typedef struct dflash_paged_cache dflash_paged_cache; /* paged KV storage */
 typedef void* dflash_stream;              /* a cudaStream_t */
 
 enum {
@@ -72,7 +73,9 @@ enum {
   DFLASH_DEV_OK = 0,
   DFLASH_DEV_WAIT_TIMEOUT = 1, /* a pipeline wait gave up (kernel returned)  */
   DFLASH_DEV_POSITION = 2,     /* position outside [0, max_position)         */
-  DFLASH_DEV_ANCHOR = 3        /* anchor outside [0, seq]                    */
+  DFLASH_DEV_ANCHOR = 3,       /* anchor outside [0, seq]                    */
+  DFLASH_DEV_SLOT = 4          /* paged cache: a slot outside the cache (the
+                                  row was not written)                        */
 };
 
 /* Layer scalars.  [P3] step 1: head_dim is the explicit value, else
@@ -233,6 +236,55 @@ int dflash_attn_forward(dflash_attn* attn, dflash_cache* cache, int batch,
                         const void* target_hidden, const int32_t* host_n_ctx,
                         const int32_t* positions, void* out,
                         dflash_stream stream);
+
+/* Paged draft KV cache ([P5] precompute_and_store_context_kv: the context
+ * K/V go into the layer's paged cache through do_kv_cache_update with a
+ * slot_mapping; the draft's attention reads the pages through the batch's
+ * block table).  Storage: K and V each [n_pages][n_kv_heads][page_size]
+ * [head_dim] bf16, zeroed at creation; page p row r is slot p*page_size + r.
+ * page_size is 16, 32, 64 or 128.  The cache holds no lengths: which pages
+ * belong to which sequence, their order and each sequence's length are the
+ * caller's (block table, slot mapping, host_len_before), so crop and
+ * reuse are the caller's bookkeeping.  bf16 layers only (else _UNSUPPORTED).
+ * dflash_paged_cache_data returns the storage and its geometry (for
+ * inspection and tests; writing through it is the caller's risk);
+ * dflash_paged_cache_read copies the whole K and V storage into caller
+ * device buffers of n_pages*n_kv_heads*page_size*head_dim elements each, on
+ * `stream`. */
+int dflash_paged_cache_create(const dflash_attn* attn, int n_pages,
+                              int page_size, dflash_paged_cache** out);
+int dflash_paged_cache_destroy(dflash_paged_cache* cache);
+int dflash_paged_cache_data(const dflash_paged_cache* cache, void** k,
+                            void** v, int32_t* n_pages, int32_t* n_kv_heads,
+                            int32_t* page_size, int32_t* head_dim);
+int dflash_paged_cache_read(const dflash_paged_cache* cache, void* k_dst,
+                            void* v_dst, dflash_stream stream);
+
+/* dflash_attn_forward over a paged cache.  Arguments, outputs and errors are
+ * those of dflash_attn_forward, with the cache replaced by:
+ *   host_len_before host   [batch]: rows each sequence already holds
+ *   slot_mapping    device [sum_b (n_ctx[b] + q_len)]: the slot each new
+ *                   row's K and V are written to, in the order of positions
+ *   block_table     device [batch][bt_stride]: sequence b's key row k lives
+ *                   in page block_table[b][k / page_size], row k % page_size
+ * The new rows of sequence b take key indices len_before[b] .. len_before[b]
+ * + n_ctx[b] + q_len - 1; the call attends over indices 0 .. that end
+ * through the block table.  The slots must be the ones the block table gives
+ * for those indices (the kernels trust it).  A slot outside the cache skips
+ * that row's write and records DFLASH_DEV_SLOT; a block-table entry outside
+ * the cache reads page 0 in its place.  Block-table entries past a sequence's
+ * last row may hold anything.
+ * Errors: _ARG, _SHAPE, _UNSUPPORTED, _CAPACITY (a sequence's rows exceed
+ * bt_stride pages), _CUDA. */
+int dflash_attn_forward_paged(dflash_attn* attn, dflash_paged_cache* cache,
+                              int batch, int q_len, const void* noise_hidden,
+                              const void* target_hidden,
+                              const int32_t* host_n_ctx,
+                              const int32_t* host_len_before,
+                              const int32_t* positions,
+                              const int32_t* slot_mapping,
+                              const int32_t* block_table, int bt_stride,
+                              void* out, dflash_stream stream);
 
 /* Context K/V of several draft layers in one projection ([P5]
  * precompute_and_store_context_kv: the context K/V of all layers come from one

@@ -183,13 +183,32 @@ class ServingWorkload:
         pre = sched.prefill
         grow = 0 if self.fixed else sum(max(s.n_ctx) for s in sched.steps)
         self.cap = max(pre) + grow + 2 * (q + sp.block_size) + 16
-        self.cache = DraftCache(self.attn, B, self.cap)
+        self.paged = sp.page_size > 0
+        if self.paged:
+            # every sequence's pages for the whole run, from a shuffled free
+            # list; one block table serves every step (entries past a
+            # sequence's end are not read)
+            from block_diffusion_draft_gb300 import PagedCache
+            P = sp.page_size
+            per_seq = (self.cap + P - 1) // P
+            free = np.random.default_rng(seed + 7).permutation(B * per_seq)
+            self.pages = free.reshape(B, per_seq).astype(np.int32)
+            self.cache = PagedCache(self.attn, B * per_seq, P)
+            self.bt_h = torch.from_numpy(self.pages.copy())
+            self.bt = self.bt_h.to(device)
+        else:
+            self.cache = DraftCache(self.attn, B, self.cap)
         # prefill: context rows at positions 0.., one block, then crop
         th = torch.cat([W.hidden_rows(sp, seed, "hidden", 1000, b, pre[b]) for b in range(B)])
         nz = torch.stack([W.hidden_rows(sp, seed, "noise", 1000, b, q) for b in range(B)])
         pos = torch.cat([W.window_positions(0, pre[b], q) for b in range(B)])
-        self.attn.forward(self.cache, nz.to(device), th.to(device), pre, pos.to(device))
-        self.cache.crop(pre)
+        if self.paged:
+            sl = self._slots([0] * B, [pre[b] + q for b in range(B)])
+            self.attn.forward_paged(self.cache, nz.to(device), th.to(device), pre, [0] * B,
+                                    pos.to(device), sl.to(device), self.bt)
+        else:
+            self.attn.forward(self.cache, nz.to(device), th.to(device), pre, pos.to(device))
+            self.cache.crop(pre)
         del th
         torch.cuda.synchronize(device)
         # per-step inputs (host copies kept pinned for the end-to-end leg)
@@ -201,15 +220,21 @@ class ServingWorkload:
             nz = torch.stack([W.hidden_rows(sp, seed, "noise", s, b, q) for b in range(B)])
             pos = torch.cat([W.window_positions(L[b], n_ctx[b], q) for b in range(B)])
             keep = [L[b] + n_ctx[b] for b in range(B)] if not self.fixed else list(pre)
-            self.steps.append(dict(n_ctx=n_ctx, keep=keep, len_before=list(L),
-                                   x_h=x, nz_h=nz, pos_h=pos,
-                                   x=x.to(device), nz=nz.to(device), pos=pos.to(device)))
+            st = dict(n_ctx=n_ctx, keep=keep, len_before=list(L), x_h=x, nz_h=nz, pos_h=pos,
+                      x=x.to(device), nz=nz.to(device), pos=pos.to(device))
+            if self.paged:
+                sl = self._slots(L, [n_ctx[b] + q for b in range(B)])
+                st.update(sl_h=sl, sl=sl.to(device))
+            self.steps.append(st)
             if not self.fixed:
                 L = keep
         rows = max(int(sum(st["n_ctx"])) for st in self.steps)
+        self.io_keys = ("x", "nz", "pos") + (("sl",) if self.paged else ())
         self.stage = {k: torch.empty(max(st[k + "_h"].numel() for st in self.steps),
                                      dtype=self.steps[0][k + "_h"].dtype).pin_memory()
-                      for k in ("x", "nz", "pos")}
+                      for k in self.io_keys}
+        if self.paged:
+            self.stage["bt"] = self.bt_h.clone().pin_memory()
         # size every scratch buffer for the largest step up front, as a server
         # does at start-up (a buffer that grows mid-run synchronises the device)
         self.attn.reserve(B, B * q + rows, self.cap)
@@ -218,14 +243,25 @@ class ServingWorkload:
         self.res_buf = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16, device=device)
         self.out_h = torch.empty(B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()
         self.blocks_per_step = B
-        self.launches_per_step = 5 if self.mlp is None else 9
+
+    def _slots(self, start, count):
+        """Paged cache: slots of rows start[b] .. start[b] + count[b] - 1 of
+        every sequence, sequence-major (the order of the positions)."""
+        import torch
+        P = self.sp.page_size
+        out = []
+        for b, (s0, n) in enumerate(zip(start, count)):
+            k = np.arange(s0, s0 + n)
+            out.append(self.pages[b][k // P] * P + k % P)
+        return torch.from_numpy(np.concatenate(out).astype(np.int32))
 
     def _inputs(self, i):
         return self.steps[i % len(self.steps)]
 
     def reset(self):
-        """Back to the post-prefill cache state (fixed workloads stay there)."""
-        if not self.fixed:
+        """Back to the post-prefill cache state (fixed workloads stay there;
+        a paged cache's lengths are the schedule's)."""
+        if not self.fixed and not self.paged:
             self.cache.crop(self.sched.prefill)
 
     def step(self, i):
@@ -233,6 +269,10 @@ class ServingWorkload:
         n = int(sum(st["n_ctx"]))
         th = self.th_buf[:n]
         self.attn.ctx_project(st["x"], out=th)
+        if self.paged:
+            self.attn.forward_paged(self.cache, st["nz"], th, st["n_ctx"], st["len_before"],
+                                    st["pos"], st["sl"], self.bt, out=self.out_buf)
+            return
         if self.mlp is None:
             self.attn.forward(self.cache, st["nz"], th, st["n_ctx"], st["pos"],
                               out=self.out_buf)
@@ -246,7 +286,7 @@ class ServingWorkload:
         server receives each step's inputs into the same pinned memory; this
         runs before the timed region)."""
         st = self._inputs(i)
-        for k in ("x", "nz", "pos"):
+        for k in self.io_keys:
             n = st[k + "_h"].numel()
             self.stage[k][:n].copy_(st[k + "_h"].view(-1))
 
@@ -254,15 +294,19 @@ class ServingWorkload:
         """The same step from the pinned staging buffers, result read back to
         host."""
         st = self._inputs(i)
-        for k in ("x", "nz", "pos"):
+        for k in self.io_keys:
             dst = st[k]
             dst.view(-1).copy_(self.stage[k][:dst.numel()], non_blocking=True)
+        if self.paged:
+            self.bt.copy_(self.stage["bt"], non_blocking=True)
         self.step(i)
         self.out_h.copy_(self.out_buf, non_blocking=True)
 
     def io_bytes(self, i):
         st = self._inputs(i)
-        h2d = sum(t.numel() * t.element_size() for t in (st["x_h"], st["nz_h"], st["pos_h"]))
+        h2d = sum(st[k + "_h"].numel() * st[k + "_h"].element_size() for k in self.io_keys)
+        if self.paged:
+            h2d += self.bt_h.numel() * self.bt_h.element_size()
         return h2d, self.out_h.numel() * self.out_h.element_size()
 
     def kernel_bytes(self, i):
@@ -283,7 +327,8 @@ class ServingWorkload:
             "norm": n * H * 4 + n * H * 2,
             "qkv": (nq + 2 * nkv) * d * H * 2 + (B * q + n) * H * 2
                    + B * q * nq * d * 2 + (B * q + n) * 2 * nkv * d * 2,
-            "attn": keys * nkv * d * 2 * 2 + 2 * B * q * nq * d * 2,
+            "attn": keys * nkv * d * 2 * 2 + 2 * B * q * nq * d * 2
+                    + (keys // sp.page_size * 4 if sp.page_size else 0),
             "o_proj": H * nq * d * 2 + B * q * nq * d * 2 + B * q * H * 2,
             # two add+norm passes (read 2 rows, write 2) and the SwiGLU MLP
             "mlp": (2 * 4 * B * q * H * 2 + 3 * sp.intermediate * H * 2
@@ -321,7 +366,6 @@ class PackedWorkload:
         self.out = torch.empty_like(self.nz)
         self.out_h = torch.empty_like(self.nz_h).pin_memory()
         self.blocks_per_step = B * nb
-        self.launches_per_step = 5
         self.anchors_np = an.numpy()
         self.fixed = True
 
@@ -417,7 +461,6 @@ class StackWorkload:
         self.out_h = torch.empty(L, B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()
         self.fixed = True
         self.blocks_per_step = B * L  # blocks per layer-step summed over the layers
-        self.launches_per_step = 3 + 3 * L
 
     def handles(self):
         return self.layers
@@ -506,6 +549,9 @@ def spec_config(sp):
             "cached_ctx": sp.prefill if fixed else f"U[{sp.prefill_lo},{sp.prefill_hi}]",
             "sliding_window": sp.sliding_window,
             "step": "ctx_project + forward + crop",
+            **({"cache": f"paged, {sp.page_size}-row pages in shuffled order",
+                "step": "ctx_project + forward over the paged cache (slot mapping and "
+                        "block table per step)"} if sp.page_size else {}),
             "l2": "flushed (512 MiB write) before every timed step", **extra}
 
 
@@ -696,6 +742,7 @@ def main():
     wl = make_workload(args.workload, args.seed + (rank if world > 1 else 0), device, K + Wm)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
+    from block_diffusion_draft_gb300.dflash_attn import kernel_launches
     # warm-up (also sizes every scratch buffer)
     for i in range(Wm):
         wl.step(i)
@@ -708,8 +755,10 @@ def main():
         with torch.cuda.stream(s):
             wl.step(0)
             torch.cuda.synchronize(device)
+            n_cap = kernel_launches()
             with torch.cuda.graph(graph, stream=s):
                 wl.step(0)
+            graph_kernels = kernel_launches() - n_cap
         torch.cuda.current_stream(device).wait_stream(s)
         run = lambda i: graph.replay()
     else:
@@ -730,6 +779,7 @@ def main():
     wl.reset()
     barrier()
     torch.cuda.synchronize(device)
+    n_launch0 = kernel_launches()
     t0 = time.time()
     for i in range(K):
         flush.zero_()
@@ -739,6 +789,9 @@ def main():
     torch.cuda.synchronize(device)
     barrier()
     t1 = time.time()
+    # the library's own count of the kernels it launched in the timed region
+    # (a graph replays the kernels launched while it was captured)
+    gpu_launches = graph_kernels * K if wl.fixed else kernel_launches() - n_launch0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = float(np.mean(step_ms))
     if clocks:
@@ -853,7 +906,7 @@ def main():
                            timing="CUDA graph of one step" if wl.fixed else "eager"),
             "roofline": roof, "kernels": per_kernel,
             "clocks": clocks.summary(t0, t1) if clocks else None,
-            "e2e": e2e, "gpu_launches": K * wl.launches_per_step,
+            "e2e": e2e, "gpu_launches": gpu_launches,
             "device_error": err}
     if per_layer:
         line["per_layer_schedule"] = per_layer

@@ -240,42 +240,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_first();
+    // The whole warp runs the loop: lane 0 takes the waits and issues the
+    // contiguous tile's boxes; on a paged cache lane i < 128 / P issues the
+    // boxes of the tile's i-th page, its block-table entry read by the warp
+    // 32 entries at a time (entries past the sequence or out of range read
+    // page 0: keys the masks drop).
+    const int P = a.page_size;
+    const int npt = a.block_table != nullptr ? BKEY / P : 0;  // pages per tile
+    const int* bt = a.block_table != nullptr ? a.block_table + (size_t)w.b * a.bt_stride
+                                             : nullptr;
+    int bt_base = -(1 << 30), my_page = 0;  // lane l holds entry bt_base + l
     auto load_kv = [&](int j) {
       const int s = j % NST;
       const int k0 = tile_start(w, j);
-      mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
-      mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
-      if (a.block_table == nullptr) {
-        const int y = (int)(w.kv_row0 + k0);
-        tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
-        tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
-        tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
-        tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
-      } else {
-        // paged: the tile's 128 / P pages, each a P-row box per half (an
-        // entry past the sequence or out of range reads page 0: masked keys)
-        const int P = a.page_size;
-        const int* bt = a.block_table + (size_t)w.b * a.bt_stride;
-        for (int i = 0; i < BKEY / P; ++i) {
-          const int slot = k0 / P + i;
-          int page = slot < a.bt_stride ? bt[slot] : 0;
-          if (page < 0 || page >= a.n_pages) page = 0;
-          const int y = (page * a.n_kv + w.h) * P;
-          const uint32_t off = (uint32_t)(i * P * 128);
-          tma_load_2d(sK + s * TILE_BYTES + off, &tmK, &k_full[s], 0, y, pol_kv);
-          tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES + off, &tmK, &k_full[s], 64, y, pol_kv);
-          tma_load_2d(sV + s * TILE_BYTES + off, &tmV, &v_full[s], 0, y, pol_kv);
-          tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES + off, &tmV, &v_full[s], 64, y, pol_kv);
+      int page = 0;
+      if (bt != nullptr) {
+        const int slot0 = k0 / P;
+        if (slot0 < bt_base || slot0 + npt > bt_base + 32) {
+          bt_base = slot0;
+          const int e = bt_base + lane;
+          my_page = e < a.bt_stride ? __ldg(bt + e) : 0;
+          if (my_page < 0 || my_page >= a.n_pages) my_page = 0;
         }
+        page = __shfl_sync(0xffffffffu, my_page, min(slot0 - bt_base + lane, 31));
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
+        mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
+      }
+      __syncwarp();
+      if (bt == nullptr) {
+        if (lane == 0) {
+          const int y = (int)(w.kv_row0 + k0);
+          tma_load_2d(sK + s * TILE_BYTES, &tmK, &k_full[s], 0, y, pol_kv);
+          tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tmK, &k_full[s], 64, y, pol_kv);
+          tma_load_2d(sV + s * TILE_BYTES, &tmV, &v_full[s], 0, y, pol_kv);
+          tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tmV, &v_full[s], 64, y, pol_kv);
+        }
+      } else if (lane < npt) {
+        const int y = (page * a.n_kv + w.h) * P;
+        const uint32_t off = (uint32_t)(lane * P * 128);
+        tma_load_2d(sK + s * TILE_BYTES + off, &tmK, &k_full[s], 0, y, pol_kv);
+        tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES + off, &tmK, &k_full[s], 64, y, pol_kv);
+        tma_load_2d(sV + s * TILE_BYTES + off, &tmV, &v_full[s], 0, y, pol_kv);
+        tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES + off, &tmV, &v_full[s], 64, y, pol_kv);
       }
     };
     // Tiles made only of rows that were in the cache before this call were
     // written by kernels that have completed (every kernel here starts its
     // successor only after its own dependency wait): they fill the first
     // stages while the previous kernel (the one appending this call's rows
-    // and writing Q) finishes.
+    // and writing Q) finishes.  The block table is the caller's input, in
+    // place before the first kernel of the call.
     int pre = 0;
-    if (lane == 0) {
+    {
       const int first_new = sq.first_new[w.b];
       for (; pre < T && pre < NST; ++pre) {
         if (tile_start(w, pre) + BKEY > first_new) break;
@@ -294,12 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sQ, &tmQ, q_full, 0, w.q_row0, pol_q);
         tma_load_2d(sQ + HALF_BYTES, &tmQ, q_full, 64, w.q_row0, pol_q);
       }
-      for (int j = pre; j < T; ++j) {
-        const int s = j % NST;
-        const uint32_t ph = (j / NST) & 1;
-        if (!mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, a.err)) break;
-        load_kv(j);
-      }
+    }
+    for (int j = pre; j < T; ++j) {
+      const int s = j % NST;
+      const uint32_t ph = (j / NST) & 1;
+      const bool ok = lane == 0 ? mbar_wait(&kv_empty[s], ph ^ 1, abort_flag, a.err) : true;
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      load_kv(j);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

@@ -14,6 +14,10 @@
 
 using namespace df;
 
+namespace df {
+std::atomic<unsigned long long> g_kernel_launches{0};
+}  // namespace df
+
 namespace {
 
 thread_local std::string g_err;
@@ -1082,6 +1086,12 @@ int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
             "fp32 attention launch");
   }
   return run_o_proj(a, (int)rows_noise, out, s);
+}
+
+int dflash_kernel_launches(uint64_t* count) {
+  if (count == nullptr) return fail(DFLASH_ERR_ARG, "count is null");
+  *count = df::g_kernel_launches.load(std::memory_order_relaxed);
+  return DFLASH_OK;
 }
 
 int dflash_trace_enable(dflash_attn* a, int enable) {

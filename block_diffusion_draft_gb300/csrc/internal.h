@@ -2,6 +2,7 @@
 // host-side launchers each kernel file exports.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,6 +53,11 @@ struct QkvOut {
   int g_cap[kMaxGroupLayers];
 };
 
+// Kernels this library has launched in this process (every launch site
+// counts itself; read through dflash_kernel_launches).
+extern std::atomic<unsigned long long> g_kernel_launches;
+inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
+
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel of the stream finishes; it must call grid_dep_wait()
 // before touching memory that kernel writes or reads.
@@ -68,6 +74,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
@@ -89,6 +96,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

@@ -191,6 +191,7 @@ int launch_rope_table(float2* tab, int max_pos, int half, float theta,
   if (e != cudaSuccess) return e;
   e = cudaMemcpy(d_f, h_f, half * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) {
+    count_launch();
     rope_table_kernel<<<1024, 256, 0, st>>>(tab, max_pos, half, d_f);
     e = cudaGetLastError();
   }
@@ -219,6 +220,7 @@ int launch_add_rmsnorm(const void* a, const void* b, int rows, int cols, const f
 int launch_to_f32(const void* src, int src_bf16, float* dst, size_t n,
                   cudaStream_t st) {
   if (n == 0) return cudaSuccess;
+  count_launch();
   to_f32_kernel<<<(unsigned)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(
       src, src_bf16, dst, n);
   return cudaGetLastError();
@@ -228,6 +230,7 @@ int launch_packed_positions(const int* anchors, int batch, int seq, int n_blocks
                             int block_size, int* pos, int* err, cudaStream_t st) {
   const int per = seq + n_blocks * block_size;
   dim3 grid((per + 255) / 256, batch);
+  count_launch();
   packed_positions_kernel<<<grid, 256, 0, st>>>(anchors, seq, n_blocks, block_size,
                                                 pos, err);
   return cudaGetLastError();

@@ -214,6 +214,7 @@ int launch_gemm_f32(const float* a, int rows, const float* b, int n, int k,
                     float* c, int ldc, cudaStream_t st) {
   if (rows <= 0 || n <= 0) return cudaSuccess;
   dim3 grid((n + TS - 1) / TS, (rows + TS - 1) / TS), block(TS, TS);
+  count_launch();
   gemm_f32_kernel<<<grid, block, 0, st>>>(a, rows, b, n, k, c, ldc);
   return cudaGetLastError();
 }
@@ -224,6 +225,7 @@ int launch_qkv_post_f32(const float* qkv_noise, int rows_noise, const float* kv_
   const int rows = rows_noise + rows_ctx;
   if (rows <= 0) return cudaSuccess;
   dim3 grid(rows, o.n_heads + 2 * o.n_kv);
+  count_launch();
   qkv_post_f32_kernel<<<grid, 128, head_dim * sizeof(float), st>>>(
       qkv_noise, rows_noise, kv_ctx, o, *seqs, head_dim, err);
   return cudaGetLastError();
@@ -235,6 +237,7 @@ int launch_attn_f32(const AttnArgs& a, const AttnSeqs* seqs, const float* qbuf,
   const int total = a.batch * a.n_kv * a.groups * a.q_len;
   if (total == 0) return cudaSuccess;
   static AttnSeqs zero_seqs{};
+  count_launch();
   attn_f32_kernel<<<(total + 3) / 4, 128, 0, st>>>(a, seqs ? *seqs : zero_seqs, qbuf,
                                                   k, v);
   return cudaGetLastError();

@@ -78,6 +78,7 @@ _SIGNATURES = {
                                       c_void_p, c_void_p, POINTER(c_int32), c_void_p,
                                       c_void_p, c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
+    "dflash_kernel_launches": ([POINTER(ctypes.c_uint64)], c_int),
     "dflash_trace_enable": ([c_void_p, c_int], c_int),
     "dflash_trace_read": ([c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int32)],
                           c_int),
@@ -113,6 +114,13 @@ def lib():
 def check(rc: int) -> None:
     if rc != 0:
         raise DFlashError(rc, lib().dflash_last_error().decode())
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    n = ctypes.c_uint64(0)
+    check(lib().dflash_kernel_launches(ctypes.byref(n)))
+    return n.value
 
 
 def _p(t: Optional[torch.Tensor]):

@@ -60,6 +60,8 @@ class Spec:
     intermediate: int = 0
     # causal attention layer (block row t sees keys up to its own index)
     causal: bool = False
+    # > 0: paged KV cache of pages of this many rows, handed out shuffled
+    page_size: int = 0
 
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
@@ -79,6 +81,11 @@ SPECS: Dict[str, Spec] = {
     "serving_b32": Spec("serving_b32", hidden=4096, n_heads=32, n_kv_heads=8,
                         head_dim=128, block_size=16, batch=32, dtype="bf16",
                         prefill_lo=512, prefill_hi=8192, n_new=16, steps=64),
+    # the same batch over a paged cache (16-row pages in shuffled order)
+    "serving_b32_paged": Spec("serving_b32_paged", hidden=4096, n_heads=32,
+                              n_kv_heads=8, head_dim=128, block_size=16, batch=32,
+                              dtype="bf16", prefill_lo=512, prefill_hi=8192, n_new=16,
+                              steps=64, page_size=16),
     # long context: 32768 cached + 16 new + 16 block, full layer
     "long_ctx_full": Spec("long_ctx_full", hidden=4096, n_heads=32,
                           n_kv_heads=8, head_dim=128, block_size=16, batch=4,

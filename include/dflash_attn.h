@@ -381,6 +381,11 @@ enum {
   DFLASH_K_COUNT = 7
 };
 
+/* Kernels this library has launched in this process so far, over every
+ * layer, cache and device (a launch that returned an error counts too).  A
+ * caller reads it before and after a region to count that region's kernels. */
+int dflash_kernel_launches(uint64_t* count);
+
 /* Launch tracing for measurement: while enabled, every kernel launch of the
  * layer is bracketed by two CUDA events recorded on its own stream.
  * dflash_trace_enable(attn, 1) starts a fresh trace, (attn, 0) stops it.

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from block_diffusion_draft_gb300 import workloads as W
-from block_diffusion_draft_gb300.dflash_attn import DFlashError, PagedCache
+from block_diffusion_draft_gb300.dflash_attn import DFlashError, PagedCache, kernel_launches
 from oracle import dflash_oracle as O
 import helpers as T
 
@@ -126,8 +126,12 @@ def test_paged_bad_slot_is_reported():
     pos = torch.cat([W.window_positions(0, 0, q) for _ in range(B)]).cuda()
     slots = list(range(0, 16)) + list(range(48, 64))
     slots[5] = 8 * 16  # one past the last slot: that row is skipped
-    attn.forward_paged(cache, nz, None, [0, 0], [0, 0], pos,
-                       torch.tensor(slots, dtype=torch.int32).cuda(), bt)
+    sl = torch.tensor(slots, dtype=torch.int32).cuda()
+    n0 = kernel_launches()
+    attn.forward_paged(cache, nz, None, [0, 0], [0, 0], pos, sl, bt)
+    # no context rows: the QKV projection, the attention (no split at 16
+    # keys) and o_proj
+    assert kernel_launches() - n0 == 3
     torch.cuda.synchronize()
     assert attn.device_error() == 4  # DFLASH_DEV_SLOT
     # host-side checks: a sequence longer than its block-table row

@@ -432,6 +432,92 @@ def forward_packed(cfg: LayerConfig, w: LayerWeights, noise: np.ndarray,
 
 
 # --------------------------------------------------------------------------
+# packed training layout: attention core forward and backward
+# --------------------------------------------------------------------------
+def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, allowed: np.ndarray,
+                   scaling: float):
+    """One head of masked softmax attention, also returning the log-sum-exp.
+
+    ``q`` [q_len, d], ``k``/``v`` [k_len, d], ``allowed`` [q_len, k_len]
+    (every row must allow at least one key).  Scores ``scaling * q.k``
+    ([P4] ``scaling = head_dim ** -0.5``); ``lse`` [q_len] is the natural log
+    of the row's normaliser, ``log(sum over allowed keys of exp(score))``.
+    """
+    s = scaling * (q @ k.T)
+    s = np.where(allowed, s, -np.inf)
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    l = np.sum(e, axis=-1, keepdims=True)
+    o = (e / l) @ v
+    return o, (m + np.log(l))[:, 0]
+
+
+def attention_core_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                            allowed: np.ndarray, scaling: float, d_o: np.ndarray):
+    """Gradients of one head's ``o = softmax(scaling * q k^T, masked) v`` with
+    respect to q, k and v, given the gradient ``d_o`` of o.
+
+    The chain rule written out step by step (the pages train the draft through
+    autograd of this forward, [P4] module docstring): with P the softmax
+    probabilities (0 where masked), ``dV = P^T dO``, ``dP = dO V^T``, each
+    softmax row's Jacobian gives ``dS = P * (dP - rowsum(P * dP))``, and
+    through ``S = scaling * q k^T``: ``dQ = scaling dS K``,
+    ``dK = scaling dS^T Q``.
+    """
+    s = scaling * (q @ k.T)
+    s = np.where(allowed, s, -np.inf)
+    e = np.exp(s - np.max(s, axis=-1, keepdims=True))
+    p = e / np.sum(e, axis=-1, keepdims=True)
+    dv = p.T @ d_o
+    dp = d_o @ v.T
+    ds = p * (dp - np.sum(p * dp, axis=-1, keepdims=True))
+    dq = scaling * (ds @ k)
+    dk = scaling * (ds.T @ q)
+    return dq, dk, dv
+
+
+def packed_core(cfg: LayerConfig, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                anchors: Sequence[int], seq: int, block_size: int):
+    """Attention core of one sequence in the packed training layout.
+
+    ``q`` [n_heads, nb*bs, d] (the blocks' rows in block order), ``k``/``v``
+    [n_kv, seq + nb*bs, d] (context rows, then every block's rows); block k's
+    queries see context rows before ``anchors[k]`` and their own block
+    (``anchor_mask``, [P4] module docstring).  Query head h reads KV head
+    ``h // groups``.  Returns ``o`` [n_heads, nb*bs, d] and ``lse``
+    [n_heads, nb*bs].
+    """
+    allowed = anchor_mask(seq, anchors, block_size)
+    o = np.empty(q.shape)
+    lse = np.empty(q.shape[:2])
+    for h in range(cfg.n_heads):
+        o[h], lse[h] = attention_core(q[h], k[h // cfg.groups], v[h // cfg.groups],
+                                      allowed, cfg.scaling)
+    return o, lse
+
+
+def packed_core_backward(cfg: LayerConfig, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                         anchors: Sequence[int], seq: int, block_size: int,
+                         d_o: np.ndarray):
+    """Gradients of ``packed_core``'s output with respect to q, k and v.
+
+    ``d_o`` [n_heads, nb*bs, d].  A KV head's gradients sum over the query
+    heads that read it (GQA).  Returns ``dq`` like q, ``dk``/``dv`` like k/v.
+    """
+    allowed = anchor_mask(seq, anchors, block_size)
+    dq = np.empty(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for h in range(cfg.n_heads):
+        kv = h // cfg.groups
+        dq[h], dkh, dvh = attention_core_backward(q[h], k[kv], v[kv], allowed, cfg.scaling,
+                                                  d_o[h])
+        dk[kv] += dkh
+        dv[kv] += dvh
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
 # decoder layer: norms, residuals and the MLP around the attention
 # --------------------------------------------------------------------------
 @dataclass

@@ -643,6 +643,92 @@ def test_decoder_layer_residual_stream_form():
     np.testing.assert_allclose(r1, r2, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- packed backward
+def packed_core_case(seed=7, S=7, nb=3, bs=2, d=4, heads=4, kv=2):
+    rng = np.random.default_rng(seed)
+    cfg = tiny_cfg(n_heads=heads, n_kv_heads=kv, head_dim=d, hidden=heads * d)
+    # anchors 0 (no context) and S (all of it) included
+    anchors = np.array([0, S] + list(rng.integers(1, S, nb - 2)))[:nb]
+    T = nb * bs
+    q = rng.standard_normal((heads, T, d))
+    k = rng.standard_normal((kv, S + T, d))
+    v = rng.standard_normal((kv, S + T, d))
+    d_o = rng.standard_normal((heads, T, d))
+    return cfg, anchors, S, bs, q, k, v, d_o
+
+
+def test_packed_core_backward_matches_finite_differences():
+    """Central differences of L = sum(o * dO) in every element of q, k, v."""
+    cfg, anchors, S, bs, q, k, v, d_o = packed_core_case()
+    dq, dk, dv = O.packed_core_backward(cfg, q, k, v, anchors, S, bs, d_o)
+
+    def loss(q_, k_, v_):
+        return float(np.sum(O.packed_core(cfg, q_, k_, v_, anchors, S, bs)[0] * d_o))
+
+    eps = 1e-6
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.empty_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which], args_m[which] = xp, xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-7)
+
+
+def test_packed_core_matches_torch_autograd():
+    """Forward, log-sum-exp and gradients against torch SDPA + autograd in
+    float64, with the anchor rule built here from its statement."""
+    cfg, anchors, S, bs, q, k, v, d_o = packed_core_case(seed=11, S=40, nb=4, bs=4, d=16,
+                                                         heads=4, kv=2)
+    T = q.shape[1]
+    allowed = torch.zeros(T, S + T, dtype=torch.bool)
+    for r in range(T):
+        blk = r // bs
+        allowed[r, :min(int(anchors[blk]), S)] = True
+        allowed[r, S + blk * bs:S + (blk + 1) * bs] = True
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    g = cfg.n_heads // cfg.n_kv_heads
+    K, V = tk.repeat_interleave(g, 0), tv.repeat_interleave(g, 0)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq[None], K[None], V[None], attn_mask=allowed, scale=cfg.scaling)[0]
+    scores = (tq @ K.transpose(1, 2)) * cfg.scaling
+    lse = torch.logsumexp(scores.masked_fill(~allowed, -math.inf), -1)
+    o.backward(torch.tensor(d_o))
+    o_ref, lse_ref = O.packed_core(cfg, q, k, v, anchors, S, bs)
+    dq, dk, dv = O.packed_core_backward(cfg, q, k, v, anchors, S, bs, d_o)
+    np.testing.assert_allclose(o_ref, o.detach().numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse_ref, lse.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_packed_core_backward_invariants():
+    cfg, anchors, S, bs, q, k, v, d_o = packed_core_case(seed=3, S=9, nb=3, bs=3)
+    g = cfg.groups
+    dq, dk, dv = O.packed_core_backward(cfg, q, k, v, anchors, S, bs, d_o)
+    # softmax rows sum to one: a KV head's dV summed over keys is its query
+    # heads' dO summed over rows
+    for kv in range(cfg.n_kv_heads):
+        np.testing.assert_allclose(dv[kv].sum(0), d_o[kv * g:(kv + 1) * g].sum((0, 1)),
+                                   rtol=1e-12, atol=1e-12)
+    # equal keys: every row's scores are constant, dS rows sum to zero, dQ = 0
+    k_eq = np.broadcast_to(k[:, :1], k.shape).copy()
+    dq0, _, _ = O.packed_core_backward(cfg, q, k_eq, v, anchors, S, bs, d_o)
+    np.testing.assert_allclose(dq0, 0.0, atol=1e-12)
+    # the log-sum-exp of one row by an explicit loop over its keys
+    o, lse = O.packed_core(cfg, q, k, v, anchors, S, bs)
+    r, h = 4, 1
+    blk = r // bs
+    keys = list(range(min(int(anchors[blk]), S))) + list(range(S + blk * bs, S + (blk + 1) * bs))
+    tot = sum(math.exp(cfg.scaling * float(q[h, r] @ k[h // g, j])) for j in keys)
+    assert abs(lse[h, r] - math.log(tot)) < 1e-12
+
+
 def test_pins_catch_planted_mistakes(monkeypatch):
     """Plant slips in the oracle (CPU only) and check a pin fails for each."""
     import copy
@@ -707,7 +793,31 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         qi = (k_len - q_len + np.arange(q_len))[:, None]
         return np.arange(k_len)[None, :] < qi
 
+    def broke_bwd_no_rowsum(q, k, v, allowed, scaling, d_o):
+        s = np.where(allowed, scaling * (q @ k.T), -np.inf)
+        p = np.exp(s - s.max(-1, keepdims=True))
+        p /= p.sum(-1, keepdims=True)
+        ds = p * (d_o @ v.T)
+        return scaling * (ds @ k), scaling * (ds.T @ q), p.T @ d_o
+
+    def broke_bwd_dk_unscaled(q, k, v, allowed, scaling, d_o):
+        dq, dk, dv = orig_core_bwd(q, k, v, allowed, scaling, d_o)
+        return dq, dk / scaling, dv
+
+    def broke_bwd_unmasked(q, k, v, allowed, scaling, d_o):
+        return orig_core_bwd(q, k, v, np.ones_like(allowed), scaling, d_o)
+
+    orig_core_bwd = O.attention_core_backward
+
     slips = [
+        ("attention_core_backward", broke_bwd_no_rowsum,
+         [test_packed_core_backward_matches_finite_differences,
+          test_packed_core_matches_torch_autograd]),
+        ("attention_core_backward", broke_bwd_dk_unscaled,
+         [test_packed_core_backward_matches_finite_differences]),
+        ("attention_core_backward", broke_bwd_unmasked,
+         [test_packed_core_backward_matches_finite_differences,
+          test_packed_core_matches_torch_autograd]),
         ("causal_mask", broke_causal_strict, [test_causal_mask_elementwise_rule]),
         ("mlp", broke_mlp_swapped, [test_mlp_matches_explicit_sums]),
         ("silu", broke_silu_sigmoid, [test_silu_closed_forms, test_mlp_matches_explicit_sums]),

@@ -941,6 +941,9 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       const float inv = ok && l_run > 0.f ? 1.f / l_run : 0.f;
       const int ld_out = a.n_kv * a.groups * HD;
       const size_t token = (size_t)w.b * a.q_len + (size_t)blk * a.q_block + t;
+      if (a.lse != nullptr && real)  // natural log of the row's normaliser (S in log2 units)
+        a.lse[token * (a.n_kv * a.groups) + w.h * a.groups + gi] =
+            ok && l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
                                             token * ld_out + (size_t)(w.h * a.groups + gi) * HD);
 #pragma unroll

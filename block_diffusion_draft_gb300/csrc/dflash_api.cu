@@ -334,7 +334,7 @@ extern "C" {
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
 
-int dflash_abi_version(void) { return 102; }
+int dflash_abi_version(void) { return 103; }
 
 int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const void* wk,
                        const void* wv, const void* wo, const void* q_norm_w,
@@ -457,7 +457,7 @@ int dflash_attn_destroy(dflash_attn* a) {
   for (cudaEvent_t e : a->event_pool) cudaEventDestroy(e);
   for (Buf* b : {&a->qbuf, &a->attn_out, &a->gemm_partial, &a->gemm_counters, &a->part_o,
                  &a->part_ml, &a->attn_counters, &a->zbuf, &a->proj_noise, &a->proj_ctx,
-                 &a->packed_k, &a->packed_v, &a->packed_pos})
+                 &a->packed_k, &a->packed_v, &a->packed_pos, &a->bwd_do, &a->bwd_stats})
     b->release();
   delete a;
   return DFLASH_OK;
@@ -1086,6 +1086,128 @@ int dflash_attn_forward_packed(dflash_attn* a, int batch, int seq, int n_blocks,
             "fp32 attention launch");
   }
   return run_o_proj(a, (int)rows_noise, out, s);
+}
+
+namespace {
+
+// shared checks of the packed attention core entry points
+int check_packed_core(const dflash_attn* a, int batch, int seq, int n_blocks, int block_size) {
+  if (a->dt != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "packed core needs a bf16 layer");
+  if (a->cfg.sliding_window > 0 || a->cfg.causal)
+    return fail(DFLASH_ERR_UNSUPPORTED, "packed core on a sliding-window or causal layer");
+  if (batch <= 0 || seq <= 0 || n_blocks <= 0 || block_size <= 0)
+    return fail(DFLASH_ERR_ARG, "sizes must be positive");
+  if (a->g * block_size != 64)
+    return fail(DFLASH_ERR_UNSUPPORTED, "packed core needs groups * block_size = 64 (got %d)",
+                a->g * block_size);
+  const long long per = seq + (long long)n_blocks * block_size;
+  if ((long long)batch * a->nkv * per > (1LL << 30) ||
+      (long long)batch * n_blocks * block_size * a->nq > (1LL << 30))
+    return fail(DFLASH_ERR_SHAPE, "too many rows");
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_packed_attn_core(dflash_attn* a, int batch, int seq, int n_blocks, int block_size,
+                            const void* q, const void* k, const void* v, const int32_t* anchors,
+                            void* out, float* lse, dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (q == nullptr || k == nullptr || v == nullptr || anchors == nullptr || out == nullptr ||
+      lse == nullptr)
+    return fail(DFLASH_ERR_ARG, "null tensor");
+  if (int r = check_packed_core(a, batch, seq, n_blocks, block_size)) return r;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long q_len = (long long)n_blocks * block_size;
+  const long long per = seq + q_len;
+  const long long q_rows = batch * q_len * a->nq;
+  DF_CUDA(a->qbuf.ensure((size_t)q_rows * a->d * 2), "scratch allocation");
+  const float c = (float)(1.0 / std::sqrt((double)a->d) * 1.4426950408889634);
+  {
+    TraceScope tr(a, DFLASH_K_MISC, s);
+    DF_CUDA(launch_packed_prep(q, nullptr, nullptr, nullptr, batch, n_blocks, block_size, a->nkv,
+                               a->g, c, a->qbuf.p, nullptr, nullptr, nullptr, s),
+            "packed prep launch");
+  }
+  AttnArgs aa{};
+  aa.mode = 1;
+  aa.batch = batch;
+  aa.n_kv = a->nkv;
+  aa.groups = a->g;
+  aa.head_dim = a->d;
+  aa.q_len = (int)q_len;
+  aa.q_block = block_size;
+  aa.n_blocks = n_blocks;
+  aa.tile_blocks = 128 / (a->g * block_size);
+  aa.cap = (int)per;
+  aa.seq = seq;
+  aa.anchors = anchors;
+  aa.out = out;
+  aa.lse = lse;
+  aa.err = a->err;
+  aa.n_units = batch * a->nkv * ((n_blocks + aa.tile_blocks - 1) / aa.tile_blocks);
+  TraceScope tr(a, DFLASH_K_ATTN, s);
+  DF_CUDA(launch_attn_bf16(aa, nullptr, a->qbuf.p, q_rows, k, v, (long long)batch * a->nkv * per,
+                           s),
+          "attention launch");
+  return DFLASH_OK;
+}
+
+int dflash_packed_attn_core_backward(dflash_attn* a, int batch, int seq, int n_blocks,
+                                     int block_size, const void* q, const void* k, const void* v,
+                                     const void* out, const float* lse, const void* d_out,
+                                     const int32_t* anchors, void* dq, void* dk, void* dv,
+                                     dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
+      d_out == nullptr || anchors == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return fail(DFLASH_ERR_ARG, "null tensor");
+  if (int r = check_packed_core(a, batch, seq, n_blocks, block_size)) return r;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(d_out) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long q_len = (long long)n_blocks * block_size;
+  const long long per = seq + q_len;
+  const long long q_rows = batch * q_len * a->nq;
+  DF_CUDA(a->qbuf.ensure((size_t)q_rows * a->d * 2), "scratch allocation");
+  DF_CUDA(a->bwd_do.ensure((size_t)q_rows * a->d * 2), "scratch allocation");
+  DF_CUDA(a->bwd_stats.ensure((size_t)q_rows * 2 * sizeof(float)), "scratch allocation");
+  float* lse2 = static_cast<float*>(a->bwd_stats.p);
+  float* dsum = lse2 + q_rows;
+  const double scale = 1.0 / std::sqrt((double)a->d);
+  {
+    TraceScope tr(a, DFLASH_K_MISC, s);
+    DF_CUDA(launch_packed_prep(q, d_out, out, lse, batch, n_blocks, block_size, a->nkv, a->g,
+                               (float)(scale * 1.4426950408889634), a->qbuf.p, a->bwd_do.p, dsum,
+                               lse2, s),
+            "packed prep launch");
+  }
+  PackedBwdArgs ba{};
+  ba.batch = batch;
+  ba.seq = seq;
+  ba.n_blocks = n_blocks;
+  ba.block_size = block_size;
+  ba.n_kv = a->nkv;
+  ba.groups = a->g;
+  ba.per = (int)per;
+  ba.anchors = anchors;
+  ba.lse2 = lse2;
+  ba.dsum = dsum;
+  ba.dq = dq;
+  ba.dk = dk;
+  ba.dv = dv;
+  ba.dq_scale = (float)scale;
+  const int pairs = batch * a->nkv;
+  ba.n_kv_ctx_units = pairs * ((seq + 127) / 128);
+  ba.n_q_units = pairs * ((n_blocks + 1) / 2);
+  ba.n_kv_own_units = pairs * (int)((q_len + 127) / 128);
+  ba.err = a->err;
+  TraceScope tr(a, DFLASH_K_ATTN, s);
+  DF_CUDA(launch_packed_bwd(ba, a->qbuf.p, a->bwd_do.p, k, v, s), "backward launch");
+  return DFLASH_OK;
 }
 
 int dflash_kernel_launches(uint64_t* count) {

@@ -59,7 +59,7 @@ struct dflash_attn {
   std::vector<cudaEvent_t> event_pool;
   // scratch
   df::Buf qbuf, attn_out, gemm_partial, gemm_counters, part_o, part_ml, attn_counters,
-      zbuf, proj_noise, proj_ctx, packed_k, packed_v, packed_pos;
+      zbuf, proj_noise, proj_ctx, packed_k, packed_v, packed_pos, bwd_do, bwd_stats;
 };
 
 // Context K/V of several layers from one projection: the layers' K and V

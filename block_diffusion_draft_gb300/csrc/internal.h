@@ -160,6 +160,7 @@ struct AttnArgs {
   int bt_stride;     // entries per sequence in block_table
   int page_size;     // P (16, 32, 64 or 128; a power of two)
   int n_pages;
+  float* lse;        // packed core: per query row log-sum-exp (natural log), or null
   int seq;           // packed: context rows per sequence
   const int* anchors;  // packed: [B][n_blocks]
   int n_units;
@@ -206,5 +207,36 @@ int launch_qkv_post_f32(const float* qkv_noise, int rows_noise,
                         cudaStream_t st);
 int launch_attn_f32(const AttnArgs& a, const AttnSeqs* seqs, const float* qbuf,
                     const float* k, const float* v, cudaStream_t st);
+
+// Packed-layout attention backward (attn_bwd.cu).  Query-side tensors are
+// in the tile layout [B][n_kv][n_blocks][groups][block][d] (one block = 64
+// rows), K/V and their gradients [B][n_kv][per][d] (context rows, then every
+// block's rows).
+struct PackedBwdArgs {
+  int batch, seq, n_blocks, block_size, n_kv, groups;
+  int per;                 // key rows per (sequence, kv head)
+  const int* anchors;      // [B][n_blocks]
+  const float* lse2;       // tile rows: log-sum-exp in log2 units
+  const float* dsum;       // tile rows: rowsum(dO * O)
+  void* dq;                // [B][n_blocks * block][n_heads][d] bf16
+  void* dk;
+  void* dv;
+  float dq_scale;          // softmax scale
+  int n_kv_ctx_units;      // dK/dV units over context key tiles
+  int n_q_units;           // dQ units
+  int n_kv_own_units;      // dK/dV units over the blocks' own keys
+  int* err;
+};
+
+// q (token-major [B][T][n_heads][d]) -> qs (tile layout, times c); with d_o
+// and o: d_o -> do_tile, rowsum(d_o * o) -> dsum, lse * log2(e) -> lse2
+// (tile rows).  Any of d_o / o / lse / outputs may be null together.
+cudaError_t launch_packed_prep(const void* q, const void* d_o, const void* o, const float* lse,
+                               int batch, int n_blocks, int block_size, int n_kv, int groups,
+                               float c, void* qs, void* do_tile, float* dsum, float* lse2,
+                               cudaStream_t stream);
+// dK/dV and dQ in one launch (units of both kinds); tensors as in PackedBwdArgs
+cudaError_t launch_packed_bwd(const PackedBwdArgs& a, const void* qs, const void* do_tile,
+                              const void* k, const void* v, cudaStream_t stream);
 
 }  // namespace df

@@ -132,6 +132,16 @@ DF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
       : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// into shared memory, completion signalled on `bar` as transaction bytes
+DF_DEV void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // make generic-proxy writes to shared memory visible to the async proxy
 // (tensor core reads of operands written by threads)
 DF_DEV void fence_proxy_async_smem() {

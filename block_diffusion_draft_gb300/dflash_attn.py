@@ -79,6 +79,9 @@ _SIGNATURES = {
                                       c_void_p, c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
     "dflash_kernel_launches": ([POINTER(ctypes.c_uint64)], c_int),
+    "dflash_packed_attn_core": ([c_void_p, c_int, c_int, c_int, c_int] + [c_void_p] * 7, c_int),
+    "dflash_packed_attn_core_backward": ([c_void_p, c_int, c_int, c_int, c_int] +
+                                         [c_void_p] * 11, c_int),
     "dflash_trace_enable": ([c_void_p, c_int], c_int),
     "dflash_trace_read": ([c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int32)],
                           c_int),
@@ -236,6 +239,32 @@ class DFlashAttention:
                 self.handle, B, seq, nb, block_size, _p(noise), _p(target_hidden),
                 _p(anchors), _p(out), _stream(self.device)))
         return out
+
+    def packed_core(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    anchors: torch.Tensor, seq: int, block_size: int):
+        """Packed-layout attention core: q [B, T, n_heads, d], k/v
+        [B, n_kv, seq + T, d] bf16, anchors [B, n_blocks] int32.  Returns
+        (out like q, lse [B, T, n_heads] fp32)."""
+        B, T = q.shape[0], q.shape[1]
+        out = torch.empty_like(q)
+        lse = torch.empty(B, T, q.shape[2], device=q.device, dtype=torch.float32)
+        with torch.cuda.device(self.device):
+            check(lib().dflash_packed_attn_core(
+                self.handle, B, seq, T // block_size, block_size, _p(q), _p(k), _p(v),
+                _p(anchors), _p(out), _p(lse), _stream(self.device)))
+        return out, lse
+
+    def packed_core_backward(self, q, k, v, out, lse, d_out, anchors, seq: int,
+                             block_size: int):
+        """Gradients (dq, dk, dv) of packed_core's output given d_out."""
+        B, T = q.shape[0], q.shape[1]
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        with torch.cuda.device(self.device):
+            check(lib().dflash_packed_attn_core_backward(
+                self.handle, B, seq, T // block_size, block_size, _p(q), _p(k), _p(v),
+                _p(out), _p(lse), _p(d_out), _p(anchors), _p(dq), _p(dk), _p(dv),
+                _stream(self.device)))
+        return dq, dk, dv
 
     def trace(self, enable: bool) -> None:
         """Start (fresh) or stop recording CUDA events around each launch."""

@@ -124,7 +124,7 @@ def spec(name: str, **overrides) -> Spec:
 # random streams
 # --------------------------------------------------------------------------
 _KIND = {"weight": 1, "hidden": 2, "noise": 3, "layers": 4, "lengths": 5,
-         "accept": 6, "anchors": 7, "gain": 8}
+         "accept": 6, "anchors": 7, "gain": 8, "core": 9}
 
 
 def _rng(seed: int, kind: str, *keys: int) -> np.random.Generator:
@@ -268,3 +268,19 @@ def anchors(sp: Spec, seed: int = 0) -> torch.Tensor:
                         size=sp.n_blocks, replace=False)
         out[b] = np.sort(pick)
     return torch.from_numpy(out)
+
+
+def core_tensors(sp: Spec, seed: int = 0) -> Dict[str, torch.Tensor]:
+    """Inputs of the packed attention core and its backward, N(0,1): q and
+    the output gradient d_out [B, nb*bs, n_heads, d] (per-head RMSNorm makes
+    q and k unit-RMS per head, RoPE keeps that), k and v
+    [B, n_kv, seq + nb*bs, d]."""
+    T = sp.n_blocks * sp.block_size
+    per = sp.seq + T
+    shapes = {"q": (sp.batch, T, sp.n_heads, sp.head_dim),
+              "k": (sp.batch, sp.n_kv_heads, per, sp.head_dim),
+              "v": (sp.batch, sp.n_kv_heads, per, sp.head_dim),
+              "d_out": (sp.batch, T, sp.n_heads, sp.head_dim)}
+    return {name: _normal(_rng(seed, "core", i), shape, 1.0, sp.torch_dtype())
+            for i, (name, shape) in enumerate(shapes.items())}
+

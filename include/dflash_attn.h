@@ -381,6 +381,46 @@ enum {
   DFLASH_K_COUNT = 7
 };
 
+/* Attention core of the packed training layout, forward and backward
+ * ([P4] module docstring: block k's queries see the context strictly before
+ * anchors[k] and their own block; the draft is trained by backpropagation
+ * through that masked attention).  These take Q, K and V directly (after
+ * the projections, norms and RoPE), so a training framework can run its own
+ * projections and autograd around them.  The layer handle supplies
+ * n_heads, n_kv_heads, head_dim and scratch; its weights are not used.
+ *   q, out, d_out, dq  device [batch][n_blocks*block_size][n_heads][head_dim]
+ *                      bf16 (block k's rows at k*block_size ..)
+ *   k, v, dk, dv       device [batch][n_kv_heads][seq + n_blocks*block_size]
+ *                      [head_dim] bf16: per (sequence, kv head) the seq
+ *                      context rows, then every block's rows in block order
+ *   lse                device [batch][n_blocks*block_size][n_heads] fp32:
+ *                      natural log of each query row's softmax normaliser,
+ *                      log(sum over visible keys of exp(q.k / sqrt(head_dim)))
+ *   anchors            device [batch][n_blocks] int32 in [0, seq]
+ * dflash_packed_attn_core writes out = softmax(q k^T / sqrt(d), masked) v and
+ * lse.  dflash_packed_attn_core_backward takes the forward's q, k, v, out,
+ * lse and the output gradient d_out and writes the gradients dq, dk, dv
+ * (each KV head's gradient sums over the query heads that read it; key rows
+ * no query sees get 0).  Every output element is written exactly once (no
+ * atomics; reruns are bitwise identical).
+ * Requires a bf16 layer without sliding window or causal flag, and
+ * (n_heads / n_kv_heads) * block_size == 64.  An anchor outside [0, seq] is
+ * clamped and recorded (DFLASH_DEV_ANCHOR) by the forward.
+ * Errors: _ARG, _SHAPE, _UNSUPPORTED, _CUDA. */
+int dflash_packed_attn_core(dflash_attn* attn, int batch, int seq,
+                            int n_blocks, int block_size, const void* q,
+                            const void* k, const void* v,
+                            const int32_t* anchors, void* out, float* lse,
+                            dflash_stream stream);
+int dflash_packed_attn_core_backward(dflash_attn* attn, int batch, int seq,
+                                     int n_blocks, int block_size,
+                                     const void* q, const void* k,
+                                     const void* v, const void* out,
+                                     const float* lse, const void* d_out,
+                                     const int32_t* anchors, void* dq,
+                                     void* dk, void* dv,
+                                     dflash_stream stream);
+
 /* Kernels this library has launched in this process so far, over every
  * layer, cache and device (a launch that returned an error counts too).  A
  * caller reads it before and after a region to count that region's kernels. */

@@ -26,7 +26,7 @@ def test_every_declared_function_is_exported(L):
 
 
 def test_abi_version(L):
-    assert L.dflash_abi_version() == 102
+    assert L.dflash_abi_version() == 103
 
 
 def test_create_rejects_null_config(L):

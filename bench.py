@@ -407,6 +407,78 @@ class PackedWorkload:
         return spec_config(self.sp)
 
 
+class PackedBwdWorkload:
+    """Attention core of the packed training layout, forward (with the
+    log-sum-exp) then backward (dQ, dK, dV), on Q/K/V/dO already resident."""
+
+    def __init__(self, sp, seed, device, n_steps):
+        import torch
+        from block_diffusion_draft_gb300 import DFlashAttention
+        from block_diffusion_draft_gb300 import workloads as W
+
+        self.sp, self.dev = sp, device
+        w = W.weights(sp, seed, with_fc=False)
+        self.attn = DFlashAttention(w, hidden=sp.hidden, n_heads=sp.n_heads,
+                                    n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
+                                    n_target_layers=0, rms_eps=sp.rms_eps,
+                                    rope_theta=sp.rope_theta,
+                                    max_position=sp.max_position, device=device)
+        del w
+        x = W.core_tensors(sp, seed)
+        an = W.anchors(sp, seed)
+        self.h = {k: t.pin_memory() for k, t in x.items()}
+        self.h["anchors"] = an.pin_memory()
+        self.d = {k: t.to(device) for k, t in self.h.items()}
+        self.out = torch.empty_like(self.d["q"])
+        self.grads_h = {k: torch.empty_like(self.h[k]).pin_memory() for k in ("q", "k", "v")}
+        self.blocks_per_step = sp.batch * sp.n_blocks
+        self.anchors_np = an.numpy()
+        self.fixed = True
+        self.last = None
+
+    def reset(self):
+        pass
+
+    def step(self, i):
+        d, sp = self.d, self.sp
+        out, lse = self.attn.packed_core(d["q"], d["k"], d["v"], d["anchors"], sp.seq,
+                                         sp.block_size)
+        self.last = self.attn.packed_core_backward(d["q"], d["k"], d["v"], out, lse,
+                                                   d["d_out"], d["anchors"], sp.seq,
+                                                   sp.block_size)
+
+    def stage_e2e(self, i):
+        """Inputs are the same every step and already sit in pinned memory."""
+
+    def step_e2e(self, i):
+        for k, t in self.d.items():
+            t.copy_(self.h[k], non_blocking=True)
+        self.step(i)
+        for g, k in zip(self.last, ("q", "k", "v")):
+            self.grads_h[k].copy_(g, non_blocking=True)
+
+    def io_bytes(self, i):
+        h2d = sum(t.numel() * t.element_size() for t in self.h.values())
+        return h2d, sum(t.numel() * t.element_size() for t in self.grads_h.values())
+
+    def kernel_flops(self, i):
+        """Forward attention 4 d flops per visible (query, key) pair; the
+        backward's five products (S, dP, dV, dQ, dK) 10 d per pair (masked
+        work and the recomputation of S and dP by the dQ CTAs not counted)."""
+        sp = self.sp
+        pairs = 0
+        for b in range(sp.batch):
+            for a in self.anchors_np[b]:
+                pairs += sp.n_heads * sp.block_size * (min(int(a), sp.seq) + sp.block_size)
+        return {"attn": 4 * sp.head_dim * pairs, "bwd": 10 * sp.head_dim * pairs}
+
+    def kernel_bytes(self, i):
+        return {}
+
+    def config(self):
+        return spec_config(self.sp)
+
+
 class StackWorkload:
     """A stack of draft layers fed by one projected context per step:
     ctx_project (layer 0's fc) -> the context K/V of every layer from one
@@ -532,7 +604,9 @@ def spec_config(sp):
         return {"workload": sp.name, "batch": sp.batch, "seq": sp.seq,
                 "n_blocks": sp.n_blocks, "block_size": sp.block_size,
                 "hidden": sp.hidden, "heads": f"{sp.n_heads}/{sp.n_kv_heads}",
-                "head_dim": sp.head_dim, "step": "forward_packed",
+                "head_dim": sp.head_dim,
+                "step": ("packed attention core forward (with log-sum-exp) + backward "
+                         "(dQ, dK, dV)") if sp.backward else "forward_packed",
                 "l2": "flushed (512 MiB write) before every timed step"}
     fixed = sp.prefill > 0
     extra = {"layers": sp.layers,
@@ -560,6 +634,8 @@ def make_workload(name, seed, device, n_steps):
     sp = W.SPECS[name]
     if sp.layers > 1:
         return StackWorkload(sp, seed, device, n_steps)
+    if sp.backward:
+        return PackedBwdWorkload(sp, seed, device, n_steps)
     if sp.seq > 0:
         return PackedWorkload(sp, seed, device, n_steps)
     return ServingWorkload(sp, seed, device, n_steps)
@@ -597,7 +673,23 @@ class OracleRunner:
             hidden_norm=f64(w["hidden_norm"]) if "fc" in w else None)
         del w
         q = sp.block_size
-        if sp.seq > 0:
+        if sp.backward:
+            # one (sequence, kv head) group: its query heads over all blocks
+            x = W.core_tensors(sp, seed)
+            g = sp.n_heads // sp.n_kv_heads
+            self.core_cfg = O.LayerConfig(hidden=sp.hidden, n_heads=g, n_kv_heads=1,
+                                          head_dim=sp.head_dim, rms_eps=sp.rms_eps,
+                                          rope_theta=sp.rope_theta, n_target_layers=0)
+            self.cq = f64(x["q"][0, :, :g]).transpose(1, 0, 2)
+            self.ck = f64(x["k"][0, :1])
+            self.cv = f64(x["v"][0, :1])
+            self.cdo = f64(x["d_out"][0, :, :g]).transpose(1, 0, 2)
+            self.an = W.anchors(sp, seed).numpy()[0]
+            self.blocks_per_step = sp.n_blocks / sp.n_kv_heads
+            self.sample = (f"packed core forward + backward of sequence 0, kv head 0 ({g} query "
+                           f"heads, {sp.n_blocks} blocks) per step = 1/{sp.n_kv_heads} of a "
+                           "sequence's blocks")
+        elif sp.seq > 0:
             self.an = W.anchors(sp, seed).numpy()[:1]
             self.th = f64(W.hidden_rows(sp, seed, "hidden", 0, 0, sp.seq))[None]
             self.nz = f64(W.hidden_rows(sp, seed, "noise", 0, 0, sp.n_blocks * q))[None]
@@ -646,7 +738,12 @@ class OracleRunner:
 
     def step(self):
         O, sp = self.O, self.sp
-        if sp.seq > 0:
+        if sp.backward:
+            O.packed_core(self.core_cfg, self.cq, self.ck, self.cv, self.an, sp.seq,
+                          sp.block_size)
+            O.packed_core_backward(self.core_cfg, self.cq, self.ck, self.cv, self.an, sp.seq,
+                                   sp.block_size, self.cdo)
+        elif sp.seq > 0:
             O.forward_packed(self.cfg, self.lw, self.nz, self.th, self.an,
                              sp.block_size, seqs=[0], blocks=self.blocks)
         else:

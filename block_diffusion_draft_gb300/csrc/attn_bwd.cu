@@ -17,9 +17,10 @@
 //  - one launch holds two kinds of CTA.  dK/dV CTAs keep a 128-key tile of K
 //    and V in shared memory and stream the blocks that see it, 64 query rows
 //    at a time: S^T = K Q'^T and dP^T = V dO^T (M 128 keys, N 64 queries) into
-//    TMEM, the four compute warps (one key row per thread) turn them into
-//    P^T and dS^T as bf16 pairs written back over the first 32 columns, and
-//    dV += P^T dO, dK += dS^T Q' run with A read from TMEM.  dQ CTAs keep two
+//    TMEM, eight compute warps (two per TMEM lane quarter, one key row and 32
+//    query columns per thread) turn them into P^T and dS^T as bf16 pairs
+//    written back over the first 16 of their columns, and dV += P^T dO,
+//    dK += dS^T Q' run with A read from TMEM.  dQ CTAs keep two
 //    blocks' Q' and dO (128 query rows) and stream the keys those blocks see,
 //    64 at a time: S = Q' K^T, dP = dO V^T, dS in TMEM, dQ += dS K.  S/dP
 //    buffers are double-buffered, so the tensor core computes step i+1 while
@@ -38,7 +39,8 @@ constexpr int QB = 64;               // query rows of one block (groups x block)
 constexpr int KT = 128;              // key rows of a dK/dV CTA
 constexpr int KS = 64;               // key rows of a dQ step
 constexpr int NST = 4;               // pipeline stages
-constexpr int kThreads = 192;        // producer, MMA issuer, four compute warps
+constexpr int kThreads = 320;        // producer, MMA issuer, eight compute warps
+constexpr int kCompute = 256;        // two warps per TMEM lane quarter, 32 columns each
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -107,9 +109,9 @@ __global__ void __launch_bounds__(256)
   float s = d0.x * o0.x + d0.y * o0.y + d1.x * o1.x + d1.y * o1.y;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) {
-    dsum[trow] = s;
-    lse2[trow] = lse[row] * kLog2e;
+  if (lane == 0) {  // negated: the compute warps add them
+    dsum[trow] = -s;
+    lse2[trow] = -lse[row] * kLog2e;
   }
 }
 
@@ -179,7 +181,7 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], kCompute);
     }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
@@ -264,13 +266,15 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
         const uint32_t q_base = smem_u32(sQ + s * T64), do_base = smem_u32(sDO + s * T64);
         const uint32_t cs = tmem + ((i & 1) ? C_S1 : C_S0);
         const uint32_t cdp = tmem + ((i & 1) ? C_DP1 : C_DP0);
-        // dV += P^T dO and dK += dS^T Q' (A from TMEM: 64 queries = 32 columns)
+        // dV += P^T dO and dK += dS^T Q' (A from TMEM: the pairs of queries
+        // 0..31 in columns 0..15, of queries 32..63 in columns 32..47)
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16_ta(tmem + C_ACC0, cs + kk * 8,
+          const uint32_t ac = kk * 8 + (kk >= 2 ? 16 : 0);
+          tc_mma_bf16_ta(tmem + C_ACC0, cs + ac,
                          sdesc_sw128(do_base + kk * 16 * 128, T64 / 2, 1024), idesc_acc, acc);
-          tc_mma_bf16_ta(tmem + C_ACC1, cdp + kk * 8,
+          tc_mma_bf16_ta(tmem + C_ACC1, cdp + ac,
                          sdesc_sw128(q_base + kk * 16 * 128, T64 / 2, 1024), idesc_acc, acc);
         }
         tc_commit(&q_empty[s]);
@@ -282,6 +286,7 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
   } else {
     // ------------------------------------------------------- compute warps
     const int qd = warp & 3;                   // TMEM lane quarter
+    const int hf = (warp - 2) >> 2;            // half: query columns hf*32 .. +31
     const int r = qd * 32 + lane;              // key row of the tile
     const uint32_t lrow = tmem + ((uint32_t)(qd * 32) << 16);
     const int key = w.k0 + r;                  // key index in the (sequence, head)
@@ -297,67 +302,66 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
       tc_fence_after();
       const bool vis = w.own ? (brow < a.n_blocks * a.block_size && brow / a.block_size == k)
                              : key < clamp_anchor(a, w.b, k);
-      const uint32_t cs = lrow + ((i & 1) ? C_S1 : C_S0);
-      const uint32_t cdp = lrow + ((i & 1) ? C_DP1 : C_DP0);
-      const float* st = sStat + s * 2 * QB;  // lse2[64] | dsum[64] of the block's rows
-      uint32_t pw[32], dw[32];
+      const uint32_t cs = lrow + ((i & 1) ? C_S1 : C_S0) + hf * 32;
+      const uint32_t cdp = lrow + ((i & 1) ? C_DP1 : C_DP0) + hf * 32;
+      // -lse2 and -rowsum(dO*O) of this half's 32 query rows
+      const float2* nl = reinterpret_cast<const float2*>(sStat + s * 2 * QB + hf * 32);
+      const float2* nd = reinterpret_cast<const float2*>(sStat + s * 2 * QB + QB + hf * 32);
+      uint32_t rs[32], rd[32];
+      tmem_ld32_nowait(cs, rs);
+      tmem_ld32_nowait(cdp, rd);
+      tmem_ld_wait();
+      uint32_t pw[16], dw[16];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32_nowait(cs + ch * 32, rs);
-        tmem_ld32_nowait(cdp + ch * 32, rd);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = ch * 32 + 2 * e;
-          float p0 = 0.f, p1 = 0.f, g0 = 0.f, g1 = 0.f;
-          if (vis) {
-            p0 = fast_exp2(__uint_as_float(rs[2 * e]) - st[c0]);
-            p1 = fast_exp2(__uint_as_float(rs[2 * e + 1]) - st[c0 + 1]);
-            g0 = p0 * (__uint_as_float(rd[2 * e]) - st[QB + c0]);
-            g1 = p1 * (__uint_as_float(rd[2 * e + 1]) - st[QB + c0 + 1]);
-          }
-          pw[ch * 16 + e] = pack_bf16x2(p0, p1);
-          dw[ch * 16 + e] = pack_bf16x2(g0, g1);
+      for (int e = 0; e < 16; ++e) {
+        float2 p = make_float2(0.f, 0.f), g = make_float2(0.f, 0.f);
+        if (vis) {
+          const float2 x = add_f32x2(
+              make_float2(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), nl[e]);
+          p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          g = mul_f32x2(p, add_f32x2(make_float2(__uint_as_float(rd[2 * e]),
+                                                 __uint_as_float(rd[2 * e + 1])),
+                                     nd[e]));
         }
+        pw[e] = pack_bf16x2(p.x, p.y);
+        dw[e] = pack_bf16x2(g.x, g.y);
       }
-      tmem_st32_nowait(cs, pw);
-      tmem_st32_nowait(cdp, dw);
+      // over the first 16 of this half's columns (already read)
+      tmem_st16_nowait(cs, pw);
+      tmem_st16_nowait(cdp, dw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[i & 1]);
     }
-    // ---------------------------------------------------------- epilogue
+    // ------------------------------------------------ epilogue (half 0: dV,
+    // half 1: dK = ln2 * dS^T Q', Q' carrying scale * log2 e)
     const bool have = ok && i > 0;
     bool done = false;
     if (have) done = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag, a.err));
     tc_fence_after();
     const bool row_ok = r < w.rows_valid;
     const size_t grow = ((size_t)w.b * a.n_kv + w.h) * a.per + w.k0 + r;
+    const float f = hf == 0 ? 1.f : kLn2;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(hf == 0 ? a.dv : a.dk) +
+                                          grow * HD);
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const float f = g == 0 ? 1.f : kLn2;  // dK = ln2 * dS^T Q' (Q' carries scale * log2 e)
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g == 0 ? a.dv : a.dk) +
-                                            grow * HD);
+    for (int c = 0; c < HD / 32; ++c) {
+      float o[32];
+      if (done) {
+        tmem_ld32(lrow + (hf == 0 ? C_ACC0 : C_ACC1) + c * 32, o);
+      } else {
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float o[32];
-        if (done) {
-          tmem_ld32(lrow + (g == 0 ? C_ACC0 : C_ACC1) + c * 32, o);
-        } else {
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
-        }
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 pk;
-            pk.x = pack_bf16x2(o[8 * e] * f, o[8 * e + 1] * f);
-            pk.y = pack_bf16x2(o[8 * e + 2] * f, o[8 * e + 3] * f);
-            pk.z = pack_bf16x2(o[8 * e + 4] * f, o[8 * e + 5] * f);
-            pk.w = pack_bf16x2(o[8 * e + 6] * f, o[8 * e + 7] * f);
-            dst[c * 4 + e] = pk;
-          }
+        for (int e = 0; e < 4; ++e) {
+          uint4 pk;
+          pk.x = pack_bf16x2(o[8 * e] * f, o[8 * e + 1] * f);
+          pk.y = pack_bf16x2(o[8 * e + 2] * f, o[8 * e + 3] * f);
+          pk.z = pack_bf16x2(o[8 * e + 4] * f, o[8 * e + 5] * f);
+          pk.w = pack_bf16x2(o[8 * e + 6] * f, o[8 * e + 7] * f);
+          dst[c * 4 + e] = pk;
         }
       }
     }
@@ -408,7 +412,7 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], kCompute);
     }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
@@ -493,10 +497,11 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
         const int s = j % NST;
         const uint32_t k_base = smem_u32(sK + s * T64);
         const uint32_t cdp = tmem + ((j & 1) ? C_DP1 : C_DP0);
-        // dQ += dS K (A from TMEM: 64 keys = 32 columns; K as MN-major B)
+        // dQ += dS K (A from TMEM: the pairs of keys 0..31 in columns 0..15,
+        // of keys 32..63 in columns 32..47; K as MN-major B)
 #pragma unroll
         for (int kk = 0; kk < KS / 16; ++kk)
-          tc_mma_bf16_ta(tmem + C_ACC0, cdp + kk * 8,
+          tc_mma_bf16_ta(tmem + C_ACC0, cdp + kk * 8 + (kk >= 2 ? 16 : 0),
                          sdesc_sw128(k_base + kk * 16 * 128, T64 / 2, 1024), idesc_acc,
                          (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&kv_empty[s]);
@@ -506,7 +511,8 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
   } else {
     // ------------------------------------------------------- compute warps
     const int qd = warp & 3;
-    const int r = qd * 32 + lane;  // query row of the tile
+    const int hf = (warp - 2) >> 2;  // half: key columns hf*32 .. +31
+    const int r = qd * 32 + lane;    // query row of the tile
     const uint32_t lrow = tmem + ((uint32_t)(qd * 32) << 16);
     const bool real = r < rows;
     const int kl = r / QB;
@@ -516,8 +522,9 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
     const int t = within - gi * a.block_size;
     const int an = real ? clamp_anchor(a, b, blk) : 0;
     const int own_lo = a.seq + blk * a.block_size, own_hi = own_lo + a.block_size;
-    const float lse2 = real ? a.lse2[q_row0 + r] : 0.f;
-    const float dsum = real ? a.dsum[q_row0 + r] : 0.f;
+    const float nl = real ? a.lse2[q_row0 + r] : 0.f;   // -lse2
+    const float nd = real ? a.dsum[q_row0 + r] : 0.f;   // -rowsum(dO*O)
+    const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, a.err))) {
@@ -525,52 +532,52 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
         break;
       }
       tc_fence_after();
-      const int k0 = key0(j);
+      const int k0 = key0(j) + hf * 32;
       const bool ctx = j < n_ctx;
       const int lo = ctx ? 0 : own_lo, hi = ctx ? an : own_hi;
-      const bool all_vis = real && k0 >= lo && k0 + KS <= hi;
-      const uint32_t cs = lrow + ((j & 1) ? C_S1 : C_S0);
-      const uint32_t cdp = lrow + ((j & 1) ? C_DP1 : C_DP0);
-      uint32_t dw[32];
+      const bool all_vis = real && k0 >= lo && k0 + 32 <= hi;
+      const uint32_t cs = lrow + ((j & 1) ? C_S1 : C_S0) + hf * 32;
+      const uint32_t cdp = lrow + ((j & 1) ? C_DP1 : C_DP0) + hf * 32;
+      uint32_t rs[32], rd[32];
+      tmem_ld32_nowait(cs, rs);
+      tmem_ld32_nowait(cdp, rd);
+      tmem_ld_wait();
+      uint32_t dw[16];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32_nowait(cs + ch * 32, rs);
-        tmem_ld32_nowait(cdp + ch * 32, rd);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = ch * 32 + 2 * e;
-          float g[2];
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int key = k0 + c0 + x;
-            const bool vis = all_vis || (real && key >= lo && key < hi);
-            const float p = vis ? fast_exp2(__uint_as_float(rs[2 * e + x]) - lse2) : 0.f;
-            g[x] = p * (__uint_as_float(rd[2 * e + x]) - dsum);
-          }
-          dw[ch * 16 + e] = pack_bf16x2(g[0], g[1]);
+      for (int e = 0; e < 16; ++e) {
+        const float2 x = add_f32x2(
+            make_float2(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), nl2);
+        float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        if (!all_vis) {
+          const int key = k0 + 2 * e;
+          if (!(real && key >= lo && key < hi)) p.x = 0.f;
+          if (!(real && key + 1 >= lo && key + 1 < hi)) p.y = 0.f;
         }
+        const float2 g = mul_f32x2(
+            p, add_f32x2(make_float2(__uint_as_float(rd[2 * e]), __uint_as_float(rd[2 * e + 1])),
+                         nd2));
+        dw[e] = pack_bf16x2(g.x, g.y);
       }
-      tmem_st32_nowait(cdp, dw);
+      tmem_st16_nowait(cdp, dw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[j & 1]);
     }
-    // ---------------------------------------------------------- epilogue
+    // ------------------------------------- epilogue (half h: columns 64h..)
     bool done = false;
     if (ok && T > 0) done = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag, a.err));
     tc_fence_after();
     const int nq = a.n_kv * a.groups;
     const size_t token = (size_t)b * a.n_blocks * a.block_size + (size_t)blk * a.block_size + t;
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) +
-                                          (token * nq + (size_t)h * a.groups + gi) * HD);
+                                          (token * nq + (size_t)h * a.groups + gi) * HD) +
+                 hf * 8;
     const float f = a.dq_scale;
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
+    for (int c = 0; c < 2; ++c) {
       float o[32];
       if (done) {
-        tmem_ld32(lrow + C_ACC0 + c * 32, o);
+        tmem_ld32(lrow + C_ACC0 + hf * 64 + c * 32, o);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0.f;

@@ -1205,7 +1205,7 @@ int dflash_packed_attn_core_backward(dflash_attn* a, int batch, int seq, int n_b
   ba.n_q_units = pairs * ((n_blocks + 1) / 2);
   ba.n_kv_own_units = pairs * (int)((q_len + 127) / 128);
   ba.err = a->err;
-  TraceScope tr(a, DFLASH_K_ATTN, s);
+  TraceScope tr(a, DFLASH_K_BWD, s);
   DF_CUDA(launch_packed_bwd(ba, a->qbuf.p, a->bwd_do.p, k, v, s), "backward launch");
   return DFLASH_OK;
 }

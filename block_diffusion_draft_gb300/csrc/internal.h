@@ -216,8 +216,8 @@ struct PackedBwdArgs {
   int batch, seq, n_blocks, block_size, n_kv, groups;
   int per;                 // key rows per (sequence, kv head)
   const int* anchors;      // [B][n_blocks]
-  const float* lse2;       // tile rows: log-sum-exp in log2 units
-  const float* dsum;       // tile rows: rowsum(dO * O)
+  const float* lse2;       // tile rows: minus the log-sum-exp in log2 units
+  const float* dsum;       // tile rows: minus rowsum(dO * O)
   void* dq;                // [B][n_blocks * block][n_heads][d] bf16
   void* dk;
   void* dv;
@@ -229,8 +229,8 @@ struct PackedBwdArgs {
 };
 
 // q (token-major [B][T][n_heads][d]) -> qs (tile layout, times c); with d_o
-// and o: d_o -> do_tile, rowsum(d_o * o) -> dsum, lse * log2(e) -> lse2
-// (tile rows).  Any of d_o / o / lse / outputs may be null together.
+// and o: d_o -> do_tile, -rowsum(d_o * o) -> dsum, -lse * log2(e) -> lse2
+// (tile rows).  d_o, o, lse and their outputs are null together.
 cudaError_t launch_packed_prep(const void* q, const void* d_o, const void* o, const float* lse,
                                int batch, int n_blocks, int block_size, int n_kv, int groups,
                                float c, void* qs, void* do_tile, float* dsum, float* lse2,

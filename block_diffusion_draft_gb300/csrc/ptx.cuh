@@ -318,6 +318,17 @@ DF_DEV void tmem_st32_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
       : "memory");
 }
 
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
+DF_DEV void tmem_st16_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+      "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+      "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 DF_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------ programmatic launch
@@ -408,6 +419,17 @@ DF_DEV float2 add_f32x2(float2 a, float2 b) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
   asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(pc) : "l"(pa), "l"(pb));
+  float2 c;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c.x), "=f"(c.y) : "l"(pc));
+  return c;
+}
+
+// two fp32 multiplications in one instruction (round to nearest)
+DF_DEV float2 mul_f32x2(float2 a, float2 b) {
+  unsigned long long pa, pb, pc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(pc) : "l"(pa), "l"(pb));
   float2 c;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(c.x), "=f"(c.y) : "l"(pc));
   return c;

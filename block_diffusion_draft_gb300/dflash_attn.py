@@ -87,7 +87,8 @@ _SIGNATURES = {
                           c_int),
 }
 
-KERNEL_KINDS = {"fc": 0, "norm": 1, "qkv": 2, "attn": 3, "o_proj": 4, "misc": 5, "mlp": 6}
+KERNEL_KINDS = {"fc": 0, "norm": 1, "qkv": 2, "attn": 3, "o_proj": 4, "misc": 5, "mlp": 6,
+                "bwd": 7}
 
 
 def declared_functions() -> list:

@@ -62,6 +62,9 @@ class Spec:
     causal: bool = False
     # > 0: paged KV cache of pages of this many rows, handed out shuffled
     page_size: int = 0
+    # packed layout: attention core forward + backward (training step of the
+    # attention) instead of the layer forward
+    backward: bool = False
 
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
@@ -113,6 +116,11 @@ SPECS: Dict[str, Spec] = {
     "packed_train": Spec("packed_train", hidden=4096, n_heads=32,
                          n_kv_heads=8, head_dim=128, block_size=16, batch=2,
                          dtype="bf16", seq=4096, n_blocks=256),
+    # the same shape through the attention core forward and its backward
+    # (dQ, dK, dV through the anchor mask)
+    "packed_train_bwd": Spec("packed_train_bwd", hidden=4096, n_heads=32,
+                             n_kv_heads=8, head_dim=128, block_size=16, batch=2,
+                             dtype="bf16", seq=4096, n_blocks=256, backward=True),
 }
 
 

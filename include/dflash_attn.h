@@ -378,7 +378,8 @@ enum {
   DFLASH_K_OPROJ = 4,  /* o_proj GEMM                                     */
   DFLASH_K_MISC = 5,   /* packed-layout positions                         */
   DFLASH_K_MLP = 6,    /* decoder layer: add+norm kernels and MLP GEMMs    */
-  DFLASH_K_COUNT = 7
+  DFLASH_K_BWD = 7,    /* packed attention core backward (dK/dV and dQ)   */
+  DFLASH_K_COUNT = 8
 };
 
 /* Attention core of the packed training layout, forward and backward

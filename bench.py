@@ -950,7 +950,9 @@ def main():
             per_kernel[name]["gbs"] = sum(k[name] for k in kb) / (tot_ms / 1000.0) / 1e9
         if kf[0].get(name):
             per_kernel[name]["tflops"] = sum(k[name] for k in kf) / (tot_ms / 1000.0) / 1e12
-    dom = max(tr, key=lambda k: tr[k][0])
+    # the longest-running bucket that has a roofline model (flops or bytes)
+    modelled = [k for k in tr if kf[0].get(k) or kb[0].get(k)] or list(tr)
+    dom = max(modelled, key=lambda k: tr[k][0])
     pk = peaks()
     tot_ms, n = tr[dom]
     if kf[0].get(dom):

@@ -21,8 +21,9 @@
 //    query columns per thread) turn them into P^T and dS^T as bf16 pairs
 //    written back over the first 16 of their columns, and dV += P^T dO,
 //    dK += dS^T Q' run with A read from TMEM.  dQ CTAs keep two
-//    blocks' Q' and dO (128 query rows) and stream the keys those blocks see,
-//    64 at a time: S = Q' K^T, dP = dO V^T, dS in TMEM, dQ += dS K.  S/dP
+//    blocks' Q' and dO (128 query rows) in TMEM as the A operands and stream
+//    the keys those blocks see, 64 at a time: S = Q' K^T, dP = dO V^T, dS in
+//    TMEM, dQ += dS K.  S/dP
 //    buffers are double-buffered, so the tensor core computes step i+1 while
 //    the compute warps work on step i.  No atomics: every output row is
 //    written by exactly one CTA.
@@ -48,15 +49,24 @@ constexpr float kLn2 = 0.6931471805599453f;
 // shared memory (both CTA kinds use the same size):
 //   dK/dV: K 32 KB | V 32 KB | Q' stages 4 x 16 KB | dO stages 4 x 16 KB |
 //          stats stages 4 x 512 B | barriers
-//   dQ:    Q' 32 KB | dO 32 KB | K stages 4 x 16 KB | V stages 4 x 16 KB |
-//          barriers
+//   dQ:    K stages 6 x 16 KB | V stages 6 x 16 KB | barriers (Q' and dO
+//          live in TMEM)
 constexpr uint32_t T128 = 128 * HD * 2;  // 32 KB: 128 rows
 constexpr uint32_t T64 = 64 * HD * 2;    // 16 KB: 64 rows
 constexpr uint32_t STATS_BYTES = 2 * QB * 4;
 constexpr size_t SMEM_BYTES = 1024 + 2 * T128 + 2 * NST * T64 + NST * STATS_BYTES + 512;
 
-// TMEM columns
+// TMEM columns (dK/dV CTAs)
 constexpr uint32_t C_S0 = 0, C_DP0 = 64, C_S1 = 128, C_DP1 = 192, C_ACC0 = 256, C_ACC1 = 384;
+// TMEM columns (dQ CTAs): Q' and dO rows as bf16 pairs (the A operands of
+// S and dP), double-buffered S / dP, the dQ accumulator
+constexpr uint32_t Q_QA = 0, Q_DOA = 64, Q_S0 = 128, Q_DP0 = 192, Q_S1 = 256, Q_DP1 = 320,
+                   Q_ACC = 384;
+constexpr int NKS = 6;               // dQ CTAs: K/V stages of 64 rows
+
+// a shared-memory descriptor moved `bytes` further (the start address field
+// holds address / 16 in its low 14 bits; no carry within one operand tile)
+DF_DEV uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 DF_DEV int clamp_anchor(const PackedBwdArgs& a, int b, int k) {
   int an = a.anchors[b * a.n_blocks + k];
@@ -233,24 +243,24 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, QB, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, HD, true);
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+      const uint64_t d_k = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t d_v = sdesc_sw128(smem_u32(sV), 16, 1024);
       bool alive = mbar_wait(kv_full, 0, abort_flag, a.err);
       // S^T = K Q'^T and dP^T = V dO^T of step i into buffer i & 1
       auto issue_s = [&](int i) {
         const int s = i % NST;
         if (!mbar_wait(&q_full[s], (i / NST) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
-        const uint32_t q_base = smem_u32(sQ + s * T64), do_base = smem_u32(sDO + s * T64);
+        const uint64_t d_q = sdesc_sw128(smem_u32(sQ + s * T64), 16, 1024);
+        const uint64_t d_do = sdesc_sw128(smem_u32(sDO + s * T64), 16, 1024);
         const uint32_t cs = tmem + ((i & 1) ? C_S1 : C_S0);
         const uint32_t cdp = tmem + ((i & 1) ? C_DP1 : C_DP0);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * (T128 / 2) + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * (T64 / 2) + (kk & 3) * 32;
-          tc_mma_bf16(cs, sdesc_sw128(k_base + oa, 16, 1024), sdesc_sw128(q_base + ob, 16, 1024),
-                      idesc_s, kk > 0 ? 1u : 0u);
-          tc_mma_bf16(cdp, sdesc_sw128(v_base + oa, 16, 1024),
-                      sdesc_sw128(do_base + ob, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(cs, desc_add(d_k, oa), desc_add(d_q, ob), idesc_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(cdp, desc_add(d_v, oa), desc_add(d_do, ob), idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[i & 1]);
         return true;
@@ -263,7 +273,8 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
         if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
         tc_fence_after();
         const int s = i % NST;
-        const uint32_t q_base = smem_u32(sQ + s * T64), do_base = smem_u32(sDO + s * T64);
+        const uint64_t m_q = sdesc_sw128(smem_u32(sQ + s * T64), T64 / 2, 1024);
+        const uint64_t m_do = sdesc_sw128(smem_u32(sDO + s * T64), T64 / 2, 1024);
         const uint32_t cs = tmem + ((i & 1) ? C_S1 : C_S0);
         const uint32_t cdp = tmem + ((i & 1) ? C_DP1 : C_DP0);
         // dV += P^T dO and dK += dS^T Q' (A from TMEM: the pairs of queries
@@ -272,10 +283,8 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
         for (int kk = 0; kk < QB / 16; ++kk) {
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
           const uint32_t ac = kk * 8 + (kk >= 2 ? 16 : 0);
-          tc_mma_bf16_ta(tmem + C_ACC0, cs + ac,
-                         sdesc_sw128(do_base + kk * 16 * 128, T64 / 2, 1024), idesc_acc, acc);
-          tc_mma_bf16_ta(tmem + C_ACC1, cdp + ac,
-                         sdesc_sw128(q_base + kk * 16 * 128, T64 / 2, 1024), idesc_acc, acc);
+          tc_mma_bf16_ta(tmem + C_ACC0, cs + ac, desc_add(m_do, kk * 16 * 128), idesc_acc, acc);
+          tc_mma_bf16_ta(tmem + C_ACC1, cdp + ac, desc_add(m_q, kk * 16 * 128), idesc_acc, acc);
         }
         tc_commit(&q_empty[s]);
         k = kn;
@@ -375,18 +384,15 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
 }
 
 // ---------------------------------------------------------------- dQ CTA
-DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tmDO,
-                    const CUtensorMap* tmK, const CUtensorMap* tmV, const PackedBwdArgs& a,
-                    int u) {
-  uint8_t* sQ = smem;              // Q' of two blocks (128 rows)
-  uint8_t* sDO = sQ + T128;
-  uint8_t* sK = sDO + T128;        // [NST] 64 key rows
-  uint8_t* sV = sK + NST * T64;    // [NST]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * T64);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = q_full + 1;     // [NST]
-  uint64_t* kv_empty = kv_full + NST;  // [NST]
-  uint64_t* s_full = kv_empty + NST;  // [2]
+DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                    const PackedBwdArgs& a, int u) {
+  uint8_t* sK = smem;              // [NKS] 64 key rows
+  uint8_t* sV = sK + NKS * T64;    // [NKS]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NKS * T64);
+  uint64_t* q_full = bars;            // Q' and dO rows in TMEM (compute warps)
+  uint64_t* kv_full = q_full + 1;     // [NKS]
+  uint64_t* kv_empty = kv_full + NKS;  // [NKS]
+  uint64_t* s_full = kv_empty + NKS;  // [2]
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* acc_done = p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
@@ -405,8 +411,8 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
   const int rows = nbk * QB;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < NST; ++s) {
+    mbar_init(q_full, kCompute);
+    for (int s = 0; s < NKS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
@@ -417,8 +423,6 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(tmQ);
-    prefetch_tmap(tmDO);
     prefetch_tmap(tmK);
     prefetch_tmap(tmV);
   }
@@ -444,16 +448,10 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(q_full, 2 * T128);
-      tma_load_2d(sQ, tmQ, q_full, 0, (int)q_row0, pol);
-      tma_load_2d(sQ + T128 / 2, tmQ, q_full, 64, (int)q_row0, pol);
-      tma_load_2d(sDO, tmDO, q_full, 0, (int)q_row0, pol);
-      tma_load_2d(sDO + T128 / 2, tmDO, q_full, 64, (int)q_row0, pol);
       const uint64_t pol_kv = policy_evict_last();  // context rows serve many CTAs
       for (int j = 0; j < T; ++j) {
-        const int s = j % NST;
-        if (!mbar_wait(&kv_empty[s], ((j / NST) & 1) ^ 1, abort_flag, a.err)) break;
+        const int s = j % NKS;
+        if (!mbar_wait(&kv_empty[s], ((j / NKS) & 1) ^ 1, abort_flag, a.err)) break;
         const int y = (int)(kv_pair + key0(j));
         mbar_arrive_expect_tx(&kv_full[s], 2 * T64);
         tma_load_2d(sK + s * T64, tmK, &kv_full[s], 0, y, pol_kv);
@@ -467,24 +465,23 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, KS, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, HD, true);
-      const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO);
       bool alive = mbar_wait(q_full, 0, abort_flag, a.err);
-      // S = Q' K^T and dP = dO V^T of step j into buffer j & 1
+      tc_fence_after();
+      // S = Q' K^T and dP = dO V^T of step j into buffer j & 1 (A from TMEM:
+      // a K step of 16 head-dim elements is 8 columns)
       auto issue_s = [&](int j) {
-        const int s = j % NST;
-        if (!mbar_wait(&kv_full[s], (j / NST) & 1, abort_flag, a.err)) return false;
+        const int s = j % NKS;
+        if (!mbar_wait(&kv_full[s], (j / NKS) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
-        const uint32_t k_base = smem_u32(sK + s * T64), v_base = smem_u32(sV + s * T64);
-        const uint32_t cs = tmem + ((j & 1) ? C_S1 : C_S0);
-        const uint32_t cdp = tmem + ((j & 1) ? C_DP1 : C_DP0);
+        const uint64_t d_k = sdesc_sw128(smem_u32(sK + s * T64), 16, 1024);
+        const uint64_t d_v = sdesc_sw128(smem_u32(sV + s * T64), 16, 1024);
+        const uint32_t cs = tmem + ((j & 1) ? Q_S1 : Q_S0);
+        const uint32_t cdp = tmem + ((j & 1) ? Q_DP1 : Q_DP0);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * (T128 / 2) + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * (T64 / 2) + (kk & 3) * 32;
-          tc_mma_bf16(cs, sdesc_sw128(q_base + oa, 16, 1024), sdesc_sw128(k_base + ob, 16, 1024),
-                      idesc_s, kk > 0 ? 1u : 0u);
-          tc_mma_bf16(cdp, sdesc_sw128(do_base + oa, 16, 1024),
-                      sdesc_sw128(v_base + ob, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16_ta(cs, tmem + Q_QA + kk * 8, desc_add(d_k, ob), idesc_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16_ta(cdp, tmem + Q_DOA + kk * 8, desc_add(d_v, ob), idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[j & 1]);
         return true;
@@ -494,15 +491,15 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
         if (j + 1 < T && !issue_s(j + 1)) break;
         if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, a.err)) break;
         tc_fence_after();
-        const int s = j % NST;
-        const uint32_t k_base = smem_u32(sK + s * T64);
-        const uint32_t cdp = tmem + ((j & 1) ? C_DP1 : C_DP0);
+        const int s = j % NKS;
+        const uint64_t m_k = sdesc_sw128(smem_u32(sK + s * T64), T64 / 2, 1024);
+        const uint32_t cdp = tmem + ((j & 1) ? Q_DP1 : Q_DP0);
         // dQ += dS K (A from TMEM: the pairs of keys 0..31 in columns 0..15,
         // of keys 32..63 in columns 32..47; K as MN-major B)
 #pragma unroll
         for (int kk = 0; kk < KS / 16; ++kk)
-          tc_mma_bf16_ta(tmem + C_ACC0, cdp + kk * 8 + (kk >= 2 ? 16 : 0),
-                         sdesc_sw128(k_base + kk * 16 * 128, T64 / 2, 1024), idesc_acc,
+          tc_mma_bf16_ta(tmem + Q_ACC, cdp + kk * 8 + (kk >= 2 ? 16 : 0),
+                         desc_add(m_k, kk * 16 * 128), idesc_acc,
                          (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&kv_empty[s]);
       }
@@ -525,6 +522,29 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
     const float nl = real ? a.lse2[q_row0 + r] : 0.f;   // -lse2
     const float nd = real ? a.dsum[q_row0 + r] : 0.f;   // -rowsum(dO*O)
     const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
+    {
+      // this row of Q' (half 0) or dO (half 1) into TMEM: the A operand of S
+      // or dP, the row's 128 elements as 64 bf16 pairs (zeros past the rows)
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(hf == 0 ? a.qs : a.do_tile) +
+          (size_t)(q_row0 + (real ? r : 0)) * HD);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t wv[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 x = real ? __ldg(src + c * 8 + e) : make_uint4(0u, 0u, 0u, 0u);
+          wv[4 * e] = x.x;
+          wv[4 * e + 1] = x.y;
+          wv[4 * e + 2] = x.z;
+          wv[4 * e + 3] = x.w;
+        }
+        tmem_st32_nowait(lrow + (hf == 0 ? Q_QA : Q_DOA) + c * 32, wv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(q_full);
+    }
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, a.err))) {
@@ -536,8 +556,8 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
       const bool ctx = j < n_ctx;
       const int lo = ctx ? 0 : own_lo, hi = ctx ? an : own_hi;
       const bool all_vis = real && k0 >= lo && k0 + 32 <= hi;
-      const uint32_t cs = lrow + ((j & 1) ? C_S1 : C_S0) + hf * 32;
-      const uint32_t cdp = lrow + ((j & 1) ? C_DP1 : C_DP0) + hf * 32;
+      const uint32_t cs = lrow + ((j & 1) ? Q_S1 : Q_S0) + hf * 32;
+      const uint32_t cdp = lrow + ((j & 1) ? Q_DP1 : Q_DP0) + hf * 32;
       uint32_t rs[32], rd[32];
       tmem_ld32_nowait(cs, rs);
       tmem_ld32_nowait(cdp, rd);
@@ -577,7 +597,7 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
     for (int c = 0; c < 2; ++c) {
       float o[32];
       if (done) {
-        tmem_ld32(lrow + C_ACC0 + hf * 64 + c * 32, o);
+        tmem_ld32(lrow + Q_ACC + hf * 64 + c * 32, o);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0.f;
@@ -609,8 +629,6 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* tm
 __global__ void __launch_bounds__(kThreads, 1)
     packed_bwd_kernel(const __grid_constant__ CUtensorMap tmQ64,
                       const __grid_constant__ CUtensorMap tmDO64,
-                      const __grid_constant__ CUtensorMap tmQ128,
-                      const __grid_constant__ CUtensorMap tmDO128,
                       const __grid_constant__ CUtensorMap tmK128,
                       const __grid_constant__ CUtensorMap tmV128,
                       const __grid_constant__ CUtensorMap tmK64,
@@ -623,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u < a.n_kv_ctx_units)
     dkdv_body(smem, &tmQ64, &tmDO64, &tmK128, &tmV128, a, kv_unit(a, u, false));
   else if (u < a.n_kv_ctx_units + a.n_q_units)
-    dq_body(smem, &tmQ128, &tmDO128, &tmK64, &tmV64, a, u - a.n_kv_ctx_units);
+    dq_body(smem, &tmK64, &tmV64, a, u - a.n_kv_ctx_units);
   else
     dkdv_body(smem, &tmQ64, &tmDO64, &tmK128, &tmV128, a,
               kv_unit(a, u - a.n_kv_ctx_units - a.n_q_units, true));
@@ -657,11 +675,9 @@ cudaError_t launch_packed_bwd(const PackedBwdArgs& a, const void* qs, const void
   }
   const long long q_rows = (long long)a.batch * a.n_kv * a.n_blocks * QB;
   const long long kv_rows = (long long)a.batch * a.n_kv * a.per;
-  CUtensorMap mq64, mdo64, mq128, mdo128, mk128, mv128, mk64, mv64;
+  CUtensorMap mq64, mdo64, mk128, mv128, mk64, mv64;
   if (make_tmap_bf16_rows(&mq64, qs, q_rows, HD, 64) != 0 ||
       make_tmap_bf16_rows(&mdo64, do_tile, q_rows, HD, 64) != 0 ||
-      make_tmap_bf16_rows(&mq128, qs, q_rows, HD, 128) != 0 ||
-      make_tmap_bf16_rows(&mdo128, do_tile, q_rows, HD, 128) != 0 ||
       make_tmap_bf16_rows(&mk128, k, kv_rows, HD, 128) != 0 ||
       make_tmap_bf16_rows(&mv128, v, kv_rows, HD, 128) != 0 ||
       make_tmap_bf16_rows(&mk64, k, kv_rows, HD, 64) != 0 ||
@@ -669,8 +685,11 @@ cudaError_t launch_packed_bwd(const PackedBwdArgs& a, const void* qs, const void
     return cudaErrorInvalidValue;
   const int units = a.n_kv_ctx_units + a.n_q_units + a.n_kv_own_units;
   if (units <= 0) return cudaSuccess;
+  PackedBwdArgs args = a;
+  args.qs = qs;
+  args.do_tile = do_tile;
   return launch_pdl(packed_bwd_kernel, dim3(units), dim3(kThreads), SMEM_BYTES, stream, mq64,
-                    mdo64, mq128, mdo128, mk128, mv128, mk64, mv64, a);
+                    mdo64, mk128, mv128, mk64, mv64, args);
 }
 
 }  // namespace df

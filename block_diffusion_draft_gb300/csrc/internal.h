@@ -222,6 +222,8 @@ struct PackedBwdArgs {
   void* dk;
   void* dv;
   float dq_scale;          // softmax scale
+  const void* qs;          // Q' (tile layout, bf16)
+  const void* do_tile;     // dO (tile layout, bf16)
   int n_kv_ctx_units;      // dK/dV units over context key tiles
   int n_q_units;           // dQ units
   int n_kv_own_units;      // dK/dV units over the blocks' own keys

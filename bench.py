@@ -781,13 +781,42 @@ def oracle_baseline(name, seed, budget_s):
 
 
 # --------------------------------------------------------------------------
+# replicas (one process per GPU; sequences are independent, no collective on
+# the data path: only the timing is reduced)
+# --------------------------------------------------------------------------
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_seed(seed, rank, world):
+    """Each replica draws its own sequences (weak scaling)."""
+    return seed + (rank if world > 1 else 0)
+
+
+def max_over_ranks(x, dist, device):
+    """The slowest rank's value (the job finishes with it)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, units_per_step, ms):
+    """Whole-job throughput: the units all ranks processed per second of the
+    slowest rank's step time."""
+    return world * units_per_step / (ms / 1000.0)
+
+
+# --------------------------------------------------------------------------
 # main
 # --------------------------------------------------------------------------
 def main():
     args = parse()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
 
     if args.impl == "reference":
         if rank != 0:
@@ -836,7 +865,7 @@ def main():
             dist.barrier()
 
     K, Wm = args.steps, max(3, args.warmup)
-    wl = make_workload(args.workload, args.seed + (rank if world > 1 else 0), device, K + Wm)
+    wl = make_workload(args.workload, replica_seed(args.seed, rank, world), device, K + Wm)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     from block_diffusion_draft_gb300.dflash_attn import kernel_launches
@@ -894,11 +923,8 @@ def main():
     if clocks:
         time.sleep(0.1)
         clocks.stop()
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * wl.blocks_per_step / (ms / 1000.0)
+    ms = max_over_ranks(ms, dist, device)
+    value = job_value(world, wl.blocks_per_step, ms)
 
     # the plain per-layer schedule of a layer stack, same inputs, for comparison
     per_layer = None
@@ -984,11 +1010,8 @@ def main():
         e_ev[i][1].record()
     torch.cuda.synchronize(device)
     e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
-    if dist is not None:
-        t = torch.tensor([e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e = {"value": world * wl.blocks_per_step / (e_ms / 1000.0), "unit": UNIT,
+    e_ms = max_over_ranks(e_ms, dist, device)
+    e2e = {"value": job_value(world, wl.blocks_per_step, e_ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
     err = max(h.device_error() for h in handles)
 

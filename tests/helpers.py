@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 from block_diffusion_draft_gb300 import workloads as W
-from block_diffusion_draft_gb300.dflash_attn import DFlashAttention, DraftCache
+from block_diffusion_draft_gb300.dflash_attn import DFlashAttention, DraftCache, PagedCache
 from oracle import dflash_oracle as O
 
 # tolerances: bf16 paths max-abs and relative L2; fp32 paths relative L2
@@ -77,6 +77,45 @@ def assert_close(gpu, ref, dtype: str, what: str = ""):
     return max_abs, rel
 
 
+def assert_close_stream(gpu, ref, what):
+    """The bf16 tolerance for outputs that are long sums (the residual stream,
+    the MLP output): values reach several units (one bf16 ulp is 2^-5 at
+    |r| >= 4), and every element carries the propagated rounding of the bf16
+    intermediates it sums, whose size follows the output's RMS, not the
+    element's own value.  So the max-abs bound applies per element relative to
+    max(1, |ref|, rms(ref)); the relative L2 bound is unchanged."""
+    gpu, ref = np.asarray(gpu, np.float64), np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(gpu))
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    scaled = float(np.max(np.abs(gpu - ref) / np.maximum(max(1.0, rms), np.abs(ref))))
+    rel = float(np.linalg.norm(gpu - ref) / np.linalg.norm(ref))
+    _log(what, "bf16", scaled, rel)
+    assert scaled <= BF16_MAX_ABS and rel <= BF16_REL_L2, \
+        f"{what}: scaled max={scaled:.3e} rel_l2={rel:.3e}"
+
+
+# The decoder-layer MLP output passes three bf16 roundings in series (the
+# post-norm input, the SwiGLU activation, the output) and the gate x up
+# product doubles the first: with independent roundings (relative RMS
+# 2^-9/sqrt(3) each) that is 2^-9/sqrt(3) * sqrt(4 + 1 + 1) ~ 2.8e-3, and the
+# SiLU gate correlates them (measured 4.2e-3 .. 4.9e-3 against the fp64
+# oracle; 1.7e-3 against the oracle with y and the activation rounded to
+# bf16).  Bounds for it: relative L2 7.5e-3, max-abs 3e-2 scaled as in
+# assert_close_stream.
+MLP_MAX_ABS, MLP_REL_L2 = 3e-2, 7.5e-3
+
+
+def assert_close_mlp(gpu, ref, what):
+    gpu, ref = np.asarray(gpu, np.float64), np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(gpu))
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    scaled = float(np.max(np.abs(gpu - ref) / np.maximum(max(1.0, rms), np.abs(ref))))
+    rel = float(np.linalg.norm(gpu - ref) / np.linalg.norm(ref))
+    _log(what, "bf16-mlp", scaled, rel)
+    assert scaled <= MLP_MAX_ABS and rel <= MLP_REL_L2, \
+        f"{what}: scaled max={scaled:.3e} rel_l2={rel:.3e}"
+
+
 class Scenario:
     """Drive one layer through inference steps on the GPU and in the oracle.
 
@@ -86,12 +125,24 @@ class Scenario:
 
     def __init__(self, sp: W.Spec, seed: int, capacity: int,
                  check: Optional[Sequence[int]] = None, random_gains=False,
-                 layer: int = 0, device="cuda"):
+                 layer: int = 0, device="cuda", page_size: int = 0):
         self.sp, self.seed, self.device = sp, seed, device
         self.w = W.weights(sp, seed, layer=layer, random_gains=random_gains)
         self.cfg, self.lw = oracle_layer(sp, self.w)
         self.attn = gpu_layer(sp, self.w, device)
-        self.cache = DraftCache(self.attn, sp.batch, capacity)
+        self.page_size = page_size
+        if page_size:
+            # the caller's bookkeeping of a paged cache: every sequence's pages
+            # from a shuffled free list, lengths on the host
+            per_seq = (capacity + page_size - 1) // page_size
+            rng = np.random.default_rng(seed + 99)
+            self.pages = rng.permutation(sp.batch * per_seq).reshape(sp.batch, per_seq)
+            self.pages = self.pages.astype(np.int32)
+            self.cache = PagedCache(self.attn, sp.batch * per_seq, page_size)
+            self.bt = torch.from_numpy(self.pages).to(device)
+            self.lens = [0] * sp.batch
+        else:
+            self.cache = DraftCache(self.attn, sp.batch, capacity)
         self.check = list(range(sp.batch)) if check is None else list(check)
         self.ocache = O.DraftCache(sp.n_kv_heads, sp.head_dim, sp.batch)
         self.step_no = 0
@@ -103,7 +154,7 @@ class Scenario:
         q_len = sp.block_size if q_len is None else q_len
         s = self.step_no
         self.step_no += 1
-        L = self.cache.lengths()
+        L = self.lengths()
         th = [W.hidden_rows(sp, self.seed, "hidden", s, b, n_ctx[b]) for b in range(sp.batch)]
         nz = [W.hidden_rows(sp, self.seed, "noise", s, b, q_len) for b in range(sp.batch)]
         pos = [W.window_positions(L[b], n_ctx[b], q_len) for b in range(sp.batch)]
@@ -111,7 +162,16 @@ class Scenario:
         noise = torch.stack(nz).to(dev)
         target = torch.cat(th).to(dev) if sum(n_ctx) > 0 else None
         positions = torch.cat(pos).to(dev)
-        out = self.attn.forward(self.cache, noise, target, n_ctx, positions)
+        if self.page_size:
+            P = self.page_size
+            slots = np.concatenate([self.pages[b][k // P] * P + k % P for b in range(sp.batch)
+                                    for k in [np.arange(L[b], L[b] + n_ctx[b] + q_len)]])
+            out = self.attn.forward_paged(self.cache, noise, target, n_ctx, L, positions,
+                                          torch.from_numpy(slots.astype(np.int32)).to(dev),
+                                          self.bt)
+            self.lens = [L[b] + n_ctx[b] + q_len for b in range(sp.batch)]
+        else:
+            out = self.attn.forward(self.cache, noise, target, n_ctx, positions)
         torch.cuda.synchronize()
         # only the followed sequences are widened to fp64 for the oracle
         ref = O.forward(self.cfg, self.lw, self.ocache,
@@ -121,8 +181,14 @@ class Scenario:
         got = out.to("cpu", torch.float64).numpy()
         return got[self.check], ref[self.check]
 
+    def lengths(self) -> List[int]:
+        return list(self.lens) if self.page_size else self.cache.lengths()
+
     def crop(self, keep: List[int]):
-        self.cache.crop(keep)
+        if self.page_size:
+            self.lens = list(keep)
+        else:
+            self.cache.crop(keep)
         okeep = [keep[b] if b in self.check else 0 for b in range(self.sp.batch)]
         self.ocache.crop(okeep)
 
@@ -135,6 +201,11 @@ class Scenario:
         for b in self.check:
             n = self.ocache.k[b].shape[1]
             sl = slice(0, n) if rows is None else slice(max(0, n - rows), n)
-            res.append((k[b][:, sl], self.ocache.k[b][:, sl],
-                        v[b][:, sl], self.ocache.v[b][:, sl]))
+            if self.page_size:  # gather the sequence's rows through its pages
+                P, idx = self.page_size, np.arange(n)[sl]
+                kb = np.stack([k[self.pages[b][i // P], :, i % P] for i in idx], axis=1)
+                vb = np.stack([v[self.pages[b][i // P], :, i % P] for i in idx], axis=1)
+            else:
+                kb, vb = k[b][:, sl], v[b][:, sl]
+            res.append((kb, self.ocache.k[b][:, sl], vb, self.ocache.v[b][:, sl]))
         return res

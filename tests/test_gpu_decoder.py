@@ -21,17 +21,7 @@ def small_bf16(**kw):
     return W.spec("qwen3_8b_single", **base)
 
 
-def assert_close_stream(gpu, ref, what):
-    """The bf16 tolerance for the residual stream: values are sums of unit-
-    scale terms (|r| up to ~6) stored in bf16 (one ulp is 2^-5 at |r| >= 4),
-    so the max-abs bound applies per element relative to max(1, |ref|); the
-    relative L2 bound is unchanged."""
-    gpu, ref = np.asarray(gpu, np.float64), np.asarray(ref, np.float64)
-    assert np.all(np.isfinite(gpu))
-    scaled = float(np.max(np.abs(gpu - ref) / np.maximum(1.0, np.abs(ref))))
-    rel = float(np.linalg.norm(gpu - ref) / np.linalg.norm(ref))
-    assert scaled <= T.BF16_MAX_ABS and rel <= T.BF16_REL_L2, \
-        f"{what}: scaled max={scaled:.3e} rel_l2={rel:.3e}"
+assert_close_stream = T.assert_close_stream
 
 
 def oracle_mlp(w):
@@ -70,7 +60,7 @@ def test_decoder_layer_matches_oracle(batch, steps):
                                            None if residual is None else T.f64(residual),
                                            [T.f64(x) for x in th], [p.numpy() for p in pos])
         assert_close_stream(res.to("cpu", torch.float64).numpy(), ref_res, f"residual {s}")
-        T.assert_close(out.to("cpu", torch.float64).numpy(), ref_out, "bf16", f"mlp out {s}")
+        T.assert_close_mlp(out.to("cpu", torch.float64).numpy(), ref_out, f"mlp out {s}")
         k, v = cache.read()
         k = k.to("cpu", torch.float64).numpy()
         for b in range(B):

@@ -19,7 +19,7 @@ def _serving(name, check, steps, cap_extra=64):
     sched = W.serving_schedule(sp, 0, steps=steps)
     pre = sched.prefill
     cap = max(pre) + sum(max(s.n_ctx) for s in sched.steps) + 2 * sp.block_size + cap_extra
-    sc = T.Scenario(sp, seed=0, capacity=cap, check=check)
+    sc = T.Scenario(sp, seed=0, capacity=cap, check=check, page_size=sp.page_size)
     # prefill: all cached rows through one forward, then crop to them
     got, ref = sc.step(pre)
     T.assert_close(got, ref, "bf16", f"{name} prefill")
@@ -28,11 +28,10 @@ def _serving(name, check, steps, cap_extra=64):
     for s, st in enumerate(sched.steps):
         got, ref = sc.step(st.n_ctx)
         T.assert_close(got, ref, "bf16", f"{name} step {s}")
-        assert sc.cache.lengths() == [L[b] + st.n_ctx[b] + sp.block_size
-                                      for b in range(sp.batch)]
+        assert sc.lengths() == [L[b] + st.n_ctx[b] + sp.block_size for b in range(sp.batch)]
         L = [L[b] + st.n_ctx[b] for b in range(sp.batch)]
         sc.crop(L)
-        assert sc.cache.lengths() == L
+        assert sc.lengths() == L
     # cached rows of the last step (context rows; the block was cropped)
     for k, ko, v, vo in sc.compare_cache(rows=64):
         T.assert_close(k, ko, "bf16", f"{name} cache K")
@@ -49,6 +48,14 @@ def test_serving_batch_32_ragged():
     pre = W.serving_schedule(sp, 0, steps=1).prefill
     check = [int(np.argmax(pre)), int(np.argmin(pre)), 5]
     _serving("serving_b32", check=check, steps=3)
+
+
+def test_serving_batch_32_paged():
+    # the same batch over 16-row pages handed out in shuffled order
+    sp = W.SPECS["serving_b32_paged"]
+    pre = W.serving_schedule(sp, 0, steps=1).prefill
+    check = [int(np.argmax(pre)), int(np.argmin(pre)), 11]
+    _serving("serving_b32_paged", check=check, steps=2)
 
 
 @pytest.mark.parametrize("name", ["long_ctx_full", "long_ctx_swa"])
@@ -89,3 +96,41 @@ def test_ctx_project_full_size():
         torch.cuda.synchronize()
         T.assert_close(T.f64(y), O.ctx_project(cfg, lw, T.f64(x)), "bf16",
                        f"ctx_project rows={rows}")
+
+
+def test_decoder_layer_full_size():
+    # the whole 8B-shaped decoder layer (SwiGLU MLP of width 12288), one
+    # sequence: 4096 cached rows, then a step of 16 new context rows and a
+    # block with an incoming residual stream
+    from block_diffusion_draft_gb300.dflash_attn import DecoderMLP
+    sp = W.SPECS["decoder_8b_single"]
+    seed, q, inter = 0, sp.block_size, sp.intermediate
+    w = W.weights(sp, seed)
+    mw = W.mlp_weights(sp, seed, inter)
+    cfg, lw = T.oracle_layer(sp, w)
+    om = O.MlpWeights(*(T.f64(mw[k]) for k in ("gate", "up", "down", "input_norm",
+                                                 "post_norm")))
+    attn = T.gpu_layer(sp, w)
+    mlp = DecoderMLP(mw, sp.hidden, inter, sp.rms_eps)
+    cache = T.DraftCache(attn, 1, sp.prefill + 64)
+    ocache = O.DraftCache(sp.n_kv_heads, sp.head_dim, 1)
+    residual = None
+    for s, n_ctx in enumerate([sp.prefill, sp.n_new]):
+        L0 = cache.lengths()[0]
+        th = W.hidden_rows(sp, seed, "hidden", s, 0, n_ctx)
+        hid = W.hidden_rows(sp, seed, "noise", s, 0, q)[None]
+        pos = W.window_positions(L0, n_ctx, q)
+        out, res = mlp.layer_forward(attn, cache, hid.cuda(),
+                                     None if residual is None else residual.cuda(), th.cuda(),
+                                     [n_ctx], pos.cuda())
+        torch.cuda.synchronize()
+        ref_out, ref_res = O.decoder_layer(cfg, lw, om, ocache, T.f64(hid),
+                                           None if residual is None else T.f64(residual),
+                                           [T.f64(th)], [pos.numpy()])
+        T.assert_close_stream(res.to("cpu", torch.float64).numpy(), ref_res, f"residual {s}")
+        T.assert_close_mlp(out.to("cpu", torch.float64).numpy(), ref_out, f"mlp out {s}")
+        cache.crop([L0 + n_ctx])
+        ocache.crop([L0 + n_ctx])
+        residual = W.hidden_rows(sp, seed, "hidden", 50 + s, 0, q)[None]
+    assert attn.device_error() == 0
+

@@ -260,7 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bt_base = slot0;
           const int e = bt_base + lane;
           my_page = e < a.bt_stride ? __ldg(bt + e) : 0;
-          if (my_page < 0 || my_page >= a.n_pages) my_page = 0;
+          if (my_page < 0 || my_page >= a.n_pages) {
+            // a page holding keys of the sequence must be a page of the cache
+            if (e * P < w.len && e < a.bt_stride) record_error(a.err, 4 /* DFLASH_DEV_SLOT */);
+            my_page = 0;
+          }
         }
         page = __shfl_sync(0xffffffffu, my_page, min(slot0 - bt_base + lane, 31));
       }

@@ -75,7 +75,9 @@ enum {
   DFLASH_DEV_POSITION = 2,     /* position outside [0, max_position)         */
   DFLASH_DEV_ANCHOR = 3,       /* anchor outside [0, seq]                    */
   DFLASH_DEV_SLOT = 4          /* paged cache: a slot outside the cache (the
-                                  row was not written)                        */
+                                  row was not written), or a block-table entry
+                                  of a page holding the sequence's keys outside
+                                  the cache (page 0 read in its place)        */
 };
 
 /* Layer scalars.  [P3] step 1: head_dim is the explicit value, else
@@ -272,7 +274,8 @@ int dflash_paged_cache_read(const dflash_paged_cache* cache, void* k_dst,
  * through the block table.  The slots must be the ones the block table gives
  * for those indices (the kernels trust it).  A slot outside the cache skips
  * that row's write and records DFLASH_DEV_SLOT; a block-table entry outside
- * the cache reads page 0 in its place.  Block-table entries past a sequence's
+ * the cache for a page that holds keys of the sequence reads page 0 in its
+ * place and records DFLASH_DEV_SLOT.  Block-table entries past a sequence's
  * last row may hold anything.
  * Errors: _ARG, _SHAPE, _UNSUPPORTED, _CAPACITY (a sequence's rows exceed
  * bt_stride pages), _CUDA. */

@@ -134,6 +134,19 @@ def test_paged_bad_slot_is_reported():
     assert kernel_launches() - n0 == 3
     torch.cuda.synchronize()
     assert attn.device_error() == 4  # DFLASH_DEV_SLOT
+    # a block-table entry outside the cache for a page holding keys: read as
+    # page 0 and reported
+    slots_ok = list(range(0, 16)) + list(range(48, 64))
+    bt_bad = torch.tensor([[99, 1, 2, -1], [3, 4, 5, -1]], dtype=torch.int32).cuda()
+    attn.forward_paged(cache, nz, None, [0, 0], [0, 0], pos,
+                       torch.tensor(slots_ok, dtype=torch.int32).cuda(), bt_bad)
+    torch.cuda.synchronize()
+    assert attn.device_error() == 4
+    # entries past the sequences' pages may hold anything
+    attn.forward_paged(cache, nz, None, [0, 0], [0, 0], pos,
+                       torch.tensor(slots_ok, dtype=torch.int32).cuda(), bt)
+    torch.cuda.synchronize()
+    assert attn.device_error() == 0
     # host-side checks: a sequence longer than its block-table row
     with pytest.raises(DFlashError):
         attn.forward_paged(cache, nz, None, [0, 0], [60, 0], pos,

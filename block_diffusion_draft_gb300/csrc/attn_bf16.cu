@@ -1034,15 +1034,15 @@ __global__ void __launch_bounds__(256)
 namespace {
 
 void set_attn_attrs() {
-  static bool done = false;
-  if (done) return;
+  static std::atomic<unsigned long long> done{0};
+  if (done_on_device(done)) return;
   for (const void* f : {(const void*)attn_bf16_kernel<true>, (const void*)attn_bf16_kernel<false>}) {
     cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
   cudaFuncSetAttribute(attn_pk2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)PK_SMEM);
-  done = true;
+  mark_device(done);
 }
 
 // clusters of `c` attention CTAs that can be resident at once (0 if none)

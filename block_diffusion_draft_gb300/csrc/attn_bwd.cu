@@ -665,13 +665,13 @@ cudaError_t launch_packed_prep(const void* q, const void* d_o, const void* o, co
 
 cudaError_t launch_packed_bwd(const PackedBwdArgs& a, const void* qs, const void* do_tile,
                               const void* k, const void* v, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<unsigned long long> attr_set{0};
+  if (!done_on_device(attr_set)) {
     cudaError_t e = cudaFuncSetAttribute(packed_bwd_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    mark_device(attr_set);
   }
   const long long q_rows = (long long)a.batch * a.n_kv * a.n_blocks * QB;
   const long long kv_rows = (long long)a.batch * a.n_kv * a.per;

@@ -1214,13 +1214,13 @@ bool use_big(int rows0, int rows1, int n, int q_cols) {
 
 int launch_swap(const GemmShape& s, int epi, void* c, int ldc, int num_sms, int* err,
                 cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!done_on_device(attr_done)) {
     cudaFuncSetAttribute(gemm_swap_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_LIMIT);
     cudaFuncSetAttribute(gemm_swap_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_LIMIT);
-    attr_done = true;
+    mark_device(attr_done);
   }
   SwapPlan p{};
   p.rows = s.a0_rows;
@@ -1340,13 +1340,13 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
                      const QkvOut* qkv, const SeqTable* seqs,
                      const GemmScratch& scr, int num_sms, int* err,
                      cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!done_on_device(attr_done)) {
     set_smem_attr<EPI_BF16, 128>();
     set_smem_attr<EPI_F32, 128>();
     set_smem_attr<EPI_QKV, 128>();
     set_smem_attr<EPI_SWIGLU, 128>();
-    attr_done = true;
+    mark_device(attr_done);
   }
   if (s.k % BK != 0) return cudaErrorInvalidValue;
   if (use_swap(epi, s.a0_rows, s.a1_rows, s.n))
@@ -1428,8 +1428,8 @@ namespace {
 int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
                const SeqTable* seqs, const GemmScratch& scr, int num_sms, int* err,
                cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!done_on_device(attr_done)) {
     cudaFuncSetAttribute(gemm_big_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_BIG);
     cudaFuncSetAttribute(gemm_big_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1438,7 +1438,7 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
                          (int)SMEM_BIG);
     cudaFuncSetAttribute(gemm_big_kernel<EPI_SWIGLU>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BIG);
-    attr_done = true;
+    mark_device(attr_done);
   }
   if (s.b_map256 == nullptr) return cudaErrorInvalidValue;
   Plan p{};

@@ -53,6 +53,19 @@ struct QkvOut {
   int g_cap[kMaxGroupLayers];
 };
 
+// Per-device one-time set-up (kernel attributes): bit d of `mask` is set once
+// the set-up has run on device d.
+inline bool done_on_device(const std::atomic<unsigned long long>& mask) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (mask.load(std::memory_order_acquire) >> (dev & 63)) & 1ull;
+}
+inline void mark_device(std::atomic<unsigned long long>& mask) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  mask.fetch_or(1ull << (dev & 63), std::memory_order_release);
+}
+
 // Kernels this library has launched in this process (every launch site
 // counts itself; read through dflash_kernel_launches).
 extern std::atomic<unsigned long long> g_kernel_launches;

@@ -153,6 +153,55 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # workloads
 # --------------------------------------------------------------------------
+class PackedIO:
+    """A step's inputs packed into one pinned host buffer and one device
+    buffer (256-byte aligned slots of fixed offsets), so the step's
+    host-to-device transfer is one copy, as a server that receives a request
+    into one pinned region would make it."""
+
+    def __init__(self, slots, device):
+        import torch
+        self.off, self.dt, off = {}, {}, 0
+        for name, (numel, dt) in slots.items():
+            self.off[name], self.dt[name] = off, dt
+            off += (numel * torch.empty(0, dtype=dt).element_size() + 255) // 256 * 256
+        self.host = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        self.used = 0
+        self.read = None  # event: the last upload from this buffer has run
+
+    def stage(self, tensors):
+        """Host copies of the step's inputs into the pinned buffer (before the
+        timed region), once the previous upload from it has been read."""
+        if self.read is not None:
+            self.read.synchronize()
+        end = 0
+        for name, t in tensors.items():
+            b = t.contiguous().view(-1).view(torch_uint8())
+            o = self.off[name]
+            self.host[o:o + b.numel()].copy_(b)
+            end = max(end, o + b.numel())
+        self.used = end
+
+    def upload(self, record=True):
+        import torch
+        self.dev[:self.used].copy_(self.host[:self.used], non_blocking=True)
+        if record:
+            self.read = torch.cuda.Event()
+            self.read.record()
+
+    def view(self, name, shape):
+        import torch
+        n = int(np.prod(shape)) * torch.empty(0, dtype=self.dt[name]).element_size()
+        o = self.off[name]
+        return self.dev[o:o + n].view(self.dt[name]).view(*shape)
+
+
+def torch_uint8():
+    import torch
+    return torch.uint8
+
+
 class ServingWorkload:
     """Inference steps of one layer: ctx_project -> forward -> crop."""
 
@@ -229,12 +278,18 @@ class ServingWorkload:
             if not self.fixed:
                 L = keep
         rows = max(int(sum(st["n_ctx"])) for st in self.steps)
-        self.io_keys = ("x", "nz", "pos") + (("sl",) if self.paged else ())
-        self.stage = {k: torch.empty(max(st[k + "_h"].numel() for st in self.steps),
-                                     dtype=self.steps[0][k + "_h"].dtype).pin_memory()
-                      for k in self.io_keys}
+        # the context rows vary most in size from step to step: their slot
+        # goes last so a step uploads only the bytes it uses
+        self.io_keys = ("nz", "pos") + (("sl",) if self.paged else ()) + ("x",)
+        slots = {}
         if self.paged:
-            self.stage["bt"] = self.bt_h.clone().pin_memory()
+            slots["bt"] = (self.bt_h.numel(), self.bt_h.dtype)
+        slots.update({k: (max(st[k + "_h"].numel() for st in self.steps),
+                          self.steps[0][k + "_h"].dtype) for k in self.io_keys})
+        # two upload buffers taken in turn, so the host stages step i + 1
+        # while step i may still be copying (eager steps); graph-replayed
+        # (identical) steps use the first
+        self.pios = [PackedIO(slots, device), PackedIO(slots, device)]
         # size every scratch buffer for the largest step up front, as a server
         # does at start-up (a buffer that grows mid-run synchronises the device)
         self.attn.reserve(B, B * q + rows, self.cap)
@@ -264,42 +319,52 @@ class ServingWorkload:
         if not self.fixed and not self.paged:
             self.cache.crop(self.sched.prefill)
 
-    def step(self, i):
+    def step(self, i, inputs=None):
+        """Step i from its resident device inputs (or from `inputs`, the same
+        tensors as views into the packed upload buffer)."""
         st = self._inputs(i)
+        d = st if inputs is None else inputs
+        bt = None
+        if self.paged:
+            bt = self.bt if inputs is None else inputs["bt"]
         n = int(sum(st["n_ctx"]))
         th = self.th_buf[:n]
-        self.attn.ctx_project(st["x"], out=th)
+        self.attn.ctx_project(d["x"], out=th)
         if self.paged:
-            self.attn.forward_paged(self.cache, st["nz"], th, st["n_ctx"], st["len_before"],
-                                    st["pos"], st["sl"], self.bt, out=self.out_buf)
+            self.attn.forward_paged(self.cache, d["nz"], th, st["n_ctx"], st["len_before"],
+                                    d["pos"], d["sl"], bt, out=self.out_buf)
             return
         if self.mlp is None:
-            self.attn.forward(self.cache, st["nz"], th, st["n_ctx"], st["pos"],
+            self.attn.forward(self.cache, d["nz"], th, st["n_ctx"], d["pos"],
                               out=self.out_buf)
         else:
-            self.mlp.layer_forward_into(self.attn, self.cache, st["nz"], None, th,
-                                        st["n_ctx"], st["pos"], self.out_buf, self.res_buf)
+            self.mlp.layer_forward_into(self.attn, self.cache, d["nz"], None, th,
+                                        st["n_ctx"], d["pos"], self.out_buf, self.res_buf)
         self.cache.crop(st["keep"])
 
     def stage_e2e(self, i):
-        """Put step i's host inputs into the fixed pinned staging buffers (a
-        server receives each step's inputs into the same pinned memory; this
-        runs before the timed region)."""
+        """Put step i's host inputs into the pinned upload buffer (a server
+        receives each step's inputs into the same pinned memory; this runs
+        before the timed region)."""
         st = self._inputs(i)
-        for k in self.io_keys:
-            n = st[k + "_h"].numel()
-            self.stage[k][:n].copy_(st[k + "_h"].view(-1))
+        t = {k: st[k + "_h"] for k in self.io_keys}
+        if self.paged:
+            t["bt"] = self.bt_h
+        self._pio(i).stage(t)
+
+    def _pio(self, i):
+        return self.pios[0 if self.fixed else i % 2]
 
     def step_e2e(self, i):
-        """The same step from the pinned staging buffers, result read back to
-        host."""
+        """The same step from the pinned upload buffer (one copy), result
+        read back to host."""
         st = self._inputs(i)
-        for k in self.io_keys:
-            dst = st[k]
-            dst.view(-1).copy_(self.stage[k][:dst.numel()], non_blocking=True)
+        pio = self._pio(i)
+        pio.upload(record=not self.fixed)
+        views = {k: pio.view(k, tuple(st[k + "_h"].shape)) for k in self.io_keys}
         if self.paged:
-            self.bt.copy_(self.stage["bt"], non_blocking=True)
-        self.step(i)
+            views["bt"] = pio.view("bt", tuple(self.bt_h.shape))
+        self.step(i, views)
         self.out_h.copy_(self.out_buf, non_blocking=True)
 
     def io_bytes(self, i):
@@ -368,20 +433,24 @@ class PackedWorkload:
         self.blocks_per_step = B * nb
         self.anchors_np = an.numpy()
         self.fixed = True
+        self.pio = PackedIO({"th": (th.numel(), th.dtype), "nz": (nz.numel(), nz.dtype),
+                             "an": (an.numel(), an.dtype)}, device)
 
     def reset(self):
         pass
 
-    def step(self, i):
-        self.attn.forward_packed(self.nz, self.th, self.an, self.sp.block_size, out=self.out)
+    def step(self, i, inputs=None):
+        nz, th, an = (self.nz, self.th, self.an) if inputs is None else \
+            (inputs["nz"], inputs["th"], inputs["an"])
+        self.attn.forward_packed(nz, th, an, self.sp.block_size, out=self.out)
 
     def stage_e2e(self, i):
-        """Inputs are the same every step and already sit in pinned memory."""
+        self.pio.stage({"th": self.th_h, "nz": self.nz_h, "an": self.an_h})
 
     def step_e2e(self, i):
-        for d, h in ((self.th, self.th_h), (self.nz, self.nz_h), (self.an, self.an_h)):
-            d.copy_(h, non_blocking=True)
-        self.step(i)
+        self.pio.upload(record=False)
+        self.step(i, {k: self.pio.view(k, tuple(h.shape))
+                      for k, h in (("th", self.th_h), ("nz", self.nz_h), ("an", self.an_h))})
         self.out_h.copy_(self.out, non_blocking=True)
 
     def io_bytes(self, i):
@@ -435,12 +504,13 @@ class PackedBwdWorkload:
         self.anchors_np = an.numpy()
         self.fixed = True
         self.last = None
+        self.pio = PackedIO({k: (t.numel(), t.dtype) for k, t in self.h.items()}, device)
 
     def reset(self):
         pass
 
-    def step(self, i):
-        d, sp = self.d, self.sp
+    def step(self, i, inputs=None):
+        d, sp = (self.d if inputs is None else inputs), self.sp
         out, lse = self.attn.packed_core(d["q"], d["k"], d["v"], d["anchors"], sp.seq,
                                          sp.block_size)
         self.last = self.attn.packed_core_backward(d["q"], d["k"], d["v"], out, lse,
@@ -448,12 +518,11 @@ class PackedBwdWorkload:
                                                    sp.block_size)
 
     def stage_e2e(self, i):
-        """Inputs are the same every step and already sit in pinned memory."""
+        self.pio.stage(self.h)
 
     def step_e2e(self, i):
-        for k, t in self.d.items():
-            t.copy_(self.h[k], non_blocking=True)
-        self.step(i)
+        self.pio.upload(record=False)
+        self.step(i, {k: self.pio.view(k, tuple(t.shape)) for k, t in self.h.items()})
         for g, k in zip(self.last, ("q", "k", "v")):
             self.grads_h[k].copy_(g, non_blocking=True)
 
@@ -533,6 +602,9 @@ class StackWorkload:
         self.out_h = torch.empty(L, B, q, sp.hidden, dtype=torch.bfloat16).pin_memory()
         self.fixed = True
         self.blocks_per_step = B * L  # blocks per layer-step summed over the layers
+        self.io_h = {"x": self.x_h, "nz": self.nz_h, "pos_ctx": self.pos_ctx_h,
+                     "pos_blk": self.pos_blk_h}
+        self.pio = PackedIO({k: (t.numel(), t.dtype) for k, t in self.io_h.items()}, device)
 
     def handles(self):
         return self.layers
@@ -540,12 +612,15 @@ class StackWorkload:
     def reset(self):
         pass
 
-    def step(self, i=0):
+    def step(self, i=0, inputs=None):
         sp, B, n = self.sp, self.sp.batch, self.sp.n_new
-        self.attn.ctx_project(self.x, out=self.th)
-        self.group.append(self.caches, self.th, [n] * B, self.pos_ctx)
+        x, nz, pos_ctx, pos_blk = (self.x, self.nz, self.pos_ctx, self.pos_blk) \
+            if inputs is None else (inputs["x"], inputs["nz"], inputs["pos_ctx"],
+                                    inputs["pos_blk"])
+        self.attn.ctx_project(x, out=self.th)
+        self.group.append(self.caches, self.th, [n] * B, pos_ctx)
         for l, (a, c) in enumerate(zip(self.layers, self.caches)):
-            a.forward(c, self.nz[l], None, [0] * B, self.pos_blk, out=self.out[l])
+            a.forward(c, nz[l], None, [0] * B, pos_blk, out=self.out[l])
         for c in self.caches:
             c.crop([sp.prefill] * B)
 
@@ -558,13 +633,11 @@ class StackWorkload:
             c.crop([sp.prefill] * B)
 
     def stage_e2e(self, i):
-        """Inputs are the same every step and already sit in pinned memory."""
+        self.pio.stage(self.io_h)
 
     def step_e2e(self, i):
-        for d, h in ((self.x, self.x_h), (self.nz, self.nz_h), (self.pos_ctx, self.pos_ctx_h),
-                     (self.pos_blk, self.pos_blk_h)):
-            d.copy_(h, non_blocking=True)
-        self.step(i)
+        self.pio.upload(record=False)
+        self.step(i, {k: self.pio.view(k, tuple(t.shape)) for k, t in self.io_h.items()})
         self.out_h.copy_(self.out, non_blocking=True)
 
     def io_bytes(self, i):
@@ -1001,13 +1074,33 @@ def main():
     d2h = int(round(sum(b[1] for b in io) / K))
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(K)]
+    run_e2e = wl.step_e2e
+    if wl.fixed:
+        # identical steps: the copies and the library calls of one step in a
+        # CUDA graph (the copies read the fixed pinned staging buffers)
+        g3 = torch.cuda.CUDAGraph()
+        s3 = torch.cuda.Stream(device)
+        s3.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s3):
+            wl.stage_e2e(0)
+            wl.step_e2e(0)
+            torch.cuda.synchronize(device)
+            with torch.cuda.graph(g3, stream=s3):
+                wl.step_e2e(0)
+        torch.cuda.current_stream(device).wait_stream(s3)
+        run_e2e = lambda i: g3.replay()
+    wl.reset()
     torch.cuda.synchronize(device)
     for i in range(K):
         wl.stage_e2e(i)
         flush.zero_()
         e_ev[i][0].record()
-        wl.step_e2e(i)
+        run_e2e(i)
         e_ev[i][1].record()
+        if wl.fixed:
+            # one staging buffer (captured in the graph): refilled for the
+            # next step only after this step's copy has read it
+            e_ev[i][1].synchronize()
     torch.cuda.synchronize(device)
     e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
     e_ms = max_over_ranks(e_ms, dist, device)

@@ -62,7 +62,7 @@ enum {
   DFLASH_ERR_RANGE = -4,       /* crop length above the current length, ...  */
   DFLASH_ERR_CUDA = -5,        /* a CUDA runtime call failed                 */
   DFLASH_ERR_DEVICE = -6,      /* a kernel recorded a device-side fault      */
-  DFLASH_ERR_UNSUPPORTED = -7, /* valid request this build does not handle   */
+  DFLASH_ERR_UNSUPPORTED = -7, /* valid request the library does not handle */
   DFLASH_ERR_MEMORY = -8       /* device allocation failed                   */
 };
 

@@ -729,6 +729,36 @@ def test_packed_core_backward_invariants():
     assert abs(lse[h, r] - math.log(tot)) < 1e-12
 
 
+# ---------------------------------------------------------------- golden fixtures
+GOLDEN = __import__("os").path.join(__import__("os").path.dirname(__file__), "golden")
+
+
+def load_golden_matrix(name):
+    rows = [ln.split() for ln in open(f"{GOLDEN}/{name}") if ln.strip() and ln[0] != "#"]
+    return np.array([[int(x) for x in r] for r in rows], dtype=bool)
+
+
+def test_band_mask_matches_hand_written_fixture():
+    np.testing.assert_array_equal(O.band_mask(3, 7, 2),
+                                  load_golden_matrix("band_mask_q3_k7_w2.txt"))
+
+
+def test_anchor_mask_matches_hand_written_fixture():
+    np.testing.assert_array_equal(O.anchor_mask(5, [2, 5], 2),
+                                  load_golden_matrix("anchor_mask_s5_anchors_2_5_bs2.txt"))
+
+
+def test_oracle_forward_matches_stored_fixture():
+    """Guards the oracle against unintended changes of its arithmetic."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("make_oracle_golden",
+                                                  f"{GOLDEN}/make_oracle_golden.py")
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    stored = np.loadtxt(f"{GOLDEN}/oracle_forward_tiny.txt", comments="#")
+    np.testing.assert_allclose(mod.compute(), stored, rtol=1e-12, atol=1e-15)
+
+
 def test_pins_catch_planted_mistakes(monkeypatch):
     """Plant slips in the oracle (CPU only) and check a pin fails for each."""
     import copy
@@ -809,6 +839,18 @@ def test_pins_catch_planted_mistakes(monkeypatch):
 
     orig_core_bwd = O.attention_core_backward
 
+    def broke_band_inclusive(q_len, k_len, window):
+        qi = (k_len - q_len + np.arange(q_len))[:, None]
+        return np.abs(qi - np.arange(k_len)[None, :]) <= window
+
+    def broke_anchor_inclusive(seq, anchors, block_size):
+        m = np.zeros((len(anchors) * block_size, seq + len(anchors) * block_size), bool)
+        for b, a in enumerate(anchors):
+            rows = slice(b * block_size, (b + 1) * block_size)
+            m[rows, :min(int(a) + 1, seq)] = True
+            m[rows, seq + b * block_size: seq + (b + 1) * block_size] = True
+        return m
+
     slips = [
         ("attention_core_backward", broke_bwd_no_rowsum,
          [test_packed_core_backward_matches_finite_differences,
@@ -819,6 +861,9 @@ def test_pins_catch_planted_mistakes(monkeypatch):
          [test_packed_core_backward_matches_finite_differences,
           test_packed_core_matches_torch_autograd]),
         ("causal_mask", broke_causal_strict, [test_causal_mask_elementwise_rule]),
+        ("band_mask", broke_band_inclusive, [test_band_mask_matches_hand_written_fixture]),
+        ("anchor_mask", broke_anchor_inclusive,
+         [test_anchor_mask_matches_hand_written_fixture]),
         ("mlp", broke_mlp_swapped, [test_mlp_matches_explicit_sums]),
         ("silu", broke_silu_sigmoid, [test_silu_closed_forms, test_mlp_matches_explicit_sums]),
         ("decoder_layer", broke_decoder_post_on_r1,

@@ -47,16 +47,35 @@ def csrc_digest() -> str:
     return h.hexdigest()
 
 
+def source_digests() -> dict:
+    """sha256 of each CUDA source file."""
+    import hashlib
+    out = {}
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                out[name] = hashlib.sha256(f.read()).hexdigest()
+    return out
+
+
 def measured_traffic(workload: str, kernel: str):
     """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
-    capture in profiles/traffic.json, or None when there is none or the CUDA
-    sources changed since it was taken."""
+    capture in profiles/traffic.json, or None when there is none or a source
+    file of that kernel (its own file, the shared headers, the launch logic)
+    changed since it was taken."""
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(tfile):
         return None
     tj = json.load(open(tfile))
     rec = tj.get("kernels", {}).get(f"{workload}:{kernel}")
-    if not rec or tj.get("csrc_sha256") != csrc_digest():
+    if not rec:
+        return None
+    then, now = tj.get("file_sha256", {}), source_digests()
+    srcs = rec.get("sources")
+    if srcs is None:  # no per-file record: every source must match
+        if tj.get("csrc_sha256") != csrc_digest():
+            return None
+    elif any(then.get(f) is None or then.get(f) != now.get(f) for f in srcs):
         return None
     return rec.get("bytes_per_launch")
 sys.path.insert(0, ROOT)

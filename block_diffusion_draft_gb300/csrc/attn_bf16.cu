@@ -1047,9 +1047,9 @@ void set_attn_attrs() {
 
 // clusters of `c` attention CTAs that can be resident at once (0 if none)
 int max_active_clusters(int c, bool dual) {
-  static int cache[2][17] = {};
-  static bool known[2][17] = {};
-  if (known[dual][c]) return cache[dual][c];
+  static std::atomic<int> cache[2][17];  // the count + 1; 0: not asked yet
+  const int known = cache[dual][c].load(std::memory_order_acquire);
+  if (known != 0) return known - 1;
   set_attn_attrs();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c);
@@ -1068,8 +1068,7 @@ int max_active_clusters(int c, bool dual) {
     cudaGetLastError();
     n = 0;
   }
-  cache[dual][c] = n;
-  known[dual][c] = true;
+  cache[dual][c].store(n + 1, std::memory_order_release);
   return n;
 }
 

@@ -8,7 +8,11 @@
  * followed by the block, per-head q/k RMSNorm, RoPE over the
  * [context | block] window, grouped KV heads, non-causal softmax (optionally
  * a symmetric sliding-window band), o_proj, and a draft KV cache that is
- * cropped back to the accepted prefix after verification.
+ * cropped back to the accepted prefix after verification.  Around it: the
+ * context K/V of several layers from one projection, the rest of the draft
+ * decoder layer (norms, residual stream, SwiGLU MLP), a paged cache with a
+ * slot mapping and block tables, causal layers, and the attention core of
+ * the packed training layout with its backward.
  *
  * Page citations name the page by title and the section or symbol on it:
  *   [P3] "DFlash源码导读（二）：Qwen3DFlashAttention注意力实现全解析"
@@ -34,9 +38,10 @@
  *    handle and per cache at a time.  One layer's calls share its scratch, so
  *    calls of one layer must not run concurrently on different streams.
  *  - Faults found on the device (a position outside [0, max_position), an
- *    anchor outside [0, seq], a bounded wait that ran out) do not stop the
- *    kernels: the offending value is clamped, a code is recorded in the
- *    layer's device error word, and dflash_device_error() reports it.
+ *    anchor outside [0, seq], a paged-cache slot or block-table entry outside
+ *    the cache, a bounded wait that ran out) do not stop the kernels: the
+ *    offending value is clamped or the access skipped, a code is recorded in
+ *    the layer's device error word, and dflash_device_error() reports it.
  */
 #ifndef DFLASH_ATTN_H
 #define DFLASH_ATTN_H

@@ -134,3 +134,45 @@ def test_decoder_layer_full_size():
         residual = W.hidden_rows(sp, seed, "hidden", 50 + s, 0, q)[None]
     assert attn.device_error() == 0
 
+
+def test_layer_group_full_size():
+    # five 8B-shaped layers fed by one projected context (the bench's
+    # stack5_ctx512 step): 4096 cached rows per layer, then 512 new context
+    # rows appended to all five caches by one grouped projection, and each
+    # layer's block; against the oracle's per-layer forward with those rows
+    from block_diffusion_draft_gb300.dflash_attn import KVGroup
+    sp = W.SPECS["stack5_ctx512"]
+    seed, q, pre, n = 0, sp.block_size, sp.prefill, sp.n_new
+    ws = [W.weights(sp, seed, layer=l, with_fc=False) for l in range(sp.layers)]
+    layers = [T.gpu_layer(sp, w) for w in ws]
+    refs = [T.oracle_layer(sp, w) for w in ws]
+    caches = [T.DraftCache(a, 1, pre + n + 2 * q) for a in layers]
+    ocaches = [O.DraftCache(sp.n_kv_heads, sp.head_dim, 1) for _ in layers]
+    th0 = W.hidden_rows(sp, seed, "hidden", 1000, 0, pre)
+    for l, (a, c) in enumerate(zip(layers, caches)):
+        nz = W.hidden_rows(sp, seed, "noise", 1000 + l, 0, q)[None]
+        pos = W.window_positions(0, pre, q)
+        a.forward(c, nz.cuda(), th0.cuda(), [pre], pos.cuda())
+        cfg, lw = refs[l]
+        O.forward(cfg, lw, ocaches[l], T.f64(nz), [T.f64(th0)], [pos.numpy()])
+        c.crop([pre])
+        ocaches[l].crop([pre])
+    th = W.hidden_rows(sp, seed, "hidden", 0, 0, n)
+    group = KVGroup(layers)
+    group.append(caches, th.cuda(), [n], torch.arange(pre, pre + n, dtype=torch.int32).cuda())
+    for l, (a, c) in enumerate(zip(layers, caches)):
+        nz = W.hidden_rows(sp, seed, "noise", l, 0, q)[None]
+        out = a.forward(c, nz.cuda(), None, [0], W.window_positions(pre + n, 0, q).cuda())
+        torch.cuda.synchronize()
+        cfg, lw = refs[l]
+        ref = O.forward(cfg, lw, ocaches[l], T.f64(nz), [T.f64(th)],
+                        [W.window_positions(pre, n, q).numpy()])
+        T.assert_close(out.to("cpu", torch.float64).numpy(), ref, "bf16", f"layer {l}")
+        k, v = c.read()
+        m = ocaches[l].k[0].shape[1]
+        T.assert_close(T.f64(k[0][:, m - n - q:m]), ocaches[l].k[0][:, m - n - q:m], "bf16",
+                       f"layer {l} K")
+        T.assert_close(T.f64(v[0][:, m - n - q:m]), ocaches[l].v[0][:, m - n - q:m], "bf16",
+                       f"layer {l} V")
+        assert a.device_error() == 0
+

@@ -70,6 +70,33 @@ def test_calls_reject_null_handles(L):
     assert L.dflash_cache_destroy(None) == 0
 
 
+def test_later_entry_points_reject_null_arguments(L):
+    # layer groups, decoder layer, paged cache, packed core: every call checks
+    # its arguments on the host before any CUDA work
+    out = ctypes.c_void_p()
+    assert L.dflash_kv_group_create(None, 2, ctypes.byref(out)) == -1
+    assert L.dflash_kv_group_append(None, None, 1, None, None, None, None) == -1
+    assert L.dflash_kv_group_destroy(None) == 0
+    assert L.dflash_mlp_create(4096, 12288, 1e-6, None, None, None, None, None,
+                               ctypes.byref(out)) == -1
+    assert L.dflash_mlp_destroy(None) == 0
+    assert L.dflash_decoder_layer_forward(None, None, None, 1, 16, None, None, None, None,
+                                          None, None, None, None) == -1
+    assert L.dflash_paged_cache_create(None, 8, 16, ctypes.byref(out)) == -1
+    assert L.dflash_paged_cache_destroy(None) == 0
+    assert L.dflash_paged_cache_data(None, None, None, None, None, None, None) == -1
+    assert L.dflash_paged_cache_read(None, None, None, None) == -1
+    assert L.dflash_attn_forward_paged(None, None, 1, 16, None, None, None, None, None, None,
+                                       None, 4, None, None) == -1
+    assert L.dflash_packed_attn_core(None, 1, 64, 2, 16, None, None, None, None, None, None,
+                                     None) == -1
+    assert L.dflash_packed_attn_core_backward(None, 1, 64, 2, 16, None, None, None, None, None,
+                                              None, None, None, None, None, None) == -1
+    assert L.dflash_kernel_launches(None) == -1
+    n = ctypes.c_uint64(0)
+    assert L.dflash_kernel_launches(ctypes.byref(n)) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(D, "_LIB", None)
     monkeypatch.setattr(D, "LIB_PATH", str(tmp_path / "missing.so"))

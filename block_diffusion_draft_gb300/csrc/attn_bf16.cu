@@ -305,7 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     grid_dep_sync();
-    if (lane == 0) {
+    // A unit with no keys loads no Q either: nothing would wait for the copy,
+    // and its softmax warps reuse the Q tile's shared memory to hand over
+    // their (empty) row statistics, which a late TMA write would overwrite.
+    if (lane == 0 && T > 0) {
       mbar_arrive_expect_tx(q_full, TILE_BYTES);
       if (DUAL) {  // the 64 query rows twice: smem rows 0..63 and 64..127
         for (int copy = 0; copy < 2; ++copy)

@@ -27,7 +27,12 @@ struct Buf {
     cudaError_t e = cudaMalloc(&p, need);
     if (e != cudaSuccess) return e;
     bytes = need;
-    if (zero) e = cudaMemset(p, 0, need);
+    if (zero) {
+      // the memset runs on the legacy default stream, which a non-blocking
+      // caller stream does not wait for: finish it before any launch
+      e = cudaMemset(p, 0, need);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    }
     return e;
   }
   void release() {

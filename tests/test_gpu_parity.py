@@ -229,6 +229,38 @@ def test_crop_is_exact_and_rerun_reproduces_cache_bitwise():
         T.assert_close(T.f64(v3[b, :, :n]), T.f64(v1[b, :, :n]), "bf16", "re-append V")
 
 
+def test_first_call_of_fresh_layers_equals_rerun_bitwise():
+    # A fresh layer's first forward (scratch allocated during the call) and
+    # the identical step after crop(0), enqueued back to back with no host
+    # synchronisation between them, give the same output and cache bits, on
+    # 20 layers in turn.  Most CTAs of the short sequences' key clusters have
+    # no keys, so this also covers the empty-unit path of the attention.
+    sp = small_bf16(batch=2)
+    for it in range(20):
+        sc = T.Scenario(sp, seed=100 + it, capacity=512)
+        n_ctx = [100, 37] if it % 2 == 0 else [3 + it, 200 - it]
+        th = torch.cat([W.hidden_rows(sp, 100 + it, "hidden", 0, b, n)
+                        for b, n in enumerate(n_ctx)]).cuda()
+        nz = torch.stack([W.hidden_rows(sp, 100 + it, "noise", 0, b, 16)
+                          for b in range(2)]).cuda()
+        pos = torch.cat([W.window_positions(0, n, 16) for n in n_ctx]).cuda()
+        out1 = sc.attn.forward(sc.cache, nz, th, n_ctx, pos)
+        k1, v1 = sc.cache.read()
+        sc.cache.crop([0, 0])
+        out2 = sc.attn.forward(sc.cache, nz, th, n_ctx, pos)
+        k2, v2 = sc.cache.read()
+        torch.cuda.synchronize()
+        diff = (out1.float() - out2.float()).abs()
+        assert torch.equal(out1, out2), \
+            f"layer {it}: {int((diff > 0).sum())} elements differ, max {float(diff.max()):.3e}"
+        for b, n in enumerate(n_ctx):
+            assert torch.equal(k1[b, :, :n + 16], k2[b, :, :n + 16])
+            assert torch.equal(v1[b, :, :n + 16], v2[b, :, :n + 16])
+        assert sc.attn.device_error() == 0
+        sc.cache.close()
+        sc.attn.close()
+
+
 def test_bad_position_is_reported_not_faulted():
     sp = small_bf16(batch=1)
     sc = T.Scenario(sp, seed=10, capacity=64)

@@ -334,7 +334,7 @@ extern "C" {
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
 
-int dflash_abi_version(void) { return 103; }
+int dflash_abi_version(void) { return 104; }
 
 int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const void* wk,
                        const void* wv, const void* wo, const void* q_norm_w,
@@ -1207,6 +1207,17 @@ int dflash_packed_attn_core_backward(dflash_attn* a, int batch, int seq, int n_b
   ba.err = a->err;
   TraceScope tr(a, DFLASH_K_BWD, s);
   DF_CUDA(launch_packed_bwd(ba, a->qbuf.p, a->bwd_do.p, k, v, s), "backward launch");
+  return DFLASH_OK;
+}
+
+int dflash_wait_probe(dflash_attn* a, int64_t limit_ns, int arrive, dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (limit_ns < 1000 || limit_ns > 100000000)
+    return fail(DFLASH_ERR_ARG, "limit_ns must be in [1e3, 1e8] (got %lld)", (long long)limit_ns);
+  if (arrive != 0 && arrive != 1) return fail(DFLASH_ERR_ARG, "arrive must be 0 or 1");
+  DF_CUDA(launch_wait_probe(a->err, (unsigned long long)limit_ns, arrive,
+                            static_cast<cudaStream_t>(stream)),
+          "wait probe launch");
   return DFLASH_OK;
 }
 

@@ -211,6 +211,10 @@ int launch_packed_positions(const int* anchors, int batch, int seq,
                             int n_blocks, int block_size, int* pos, int* err,
                             cudaStream_t st);
 
+// one thread waits on an mbarrier for at most limit_ns (a never-completed
+// barrier unless `arrive`); on expiry DFLASH_DEV_WAIT_TIMEOUT goes to `err`
+int launch_wait_probe(int* err, unsigned long long limit_ns, int arrive, cudaStream_t st);
+
 // ----------------------------------------------------------- fp32 path
 int launch_gemm_f32(const float* a, int rows, const float* b, int n, int k,
                     float* c, int ldc, cudaStream_t st);

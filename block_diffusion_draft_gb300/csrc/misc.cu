@@ -177,6 +177,27 @@ __global__ void packed_positions_kernel(const int* anchors, int seq, int n_block
   }
 }
 
+// Check of the bounded pipeline wait: one thread waits on an mbarrier with
+// the same wait routine every kernel uses, for at most limit_ns.  With
+// `arrive` set, the barrier's one expected arrival is made first and the wait
+// returns at once; without it nothing ever arrives, so the wait runs out,
+// records DFLASH_DEV_WAIT_TIMEOUT in `err` and the kernel returns normally.
+__global__ void wait_probe_kernel(int* err, unsigned long long limit_ns, int arrive) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (arrive) mbar_arrive(&bar);
+    mbar_wait_for(&bar, 0, &abort_flag, err, limit_ns);
+  }
+  __syncthreads();
+}
+
 }  // namespace
 
 int launch_rope_table(float2* tab, int max_pos, int half, float theta,
@@ -233,6 +254,12 @@ int launch_packed_positions(const int* anchors, int batch, int seq, int n_blocks
   count_launch();
   packed_positions_kernel<<<grid, 256, 0, st>>>(anchors, seq, n_blocks, block_size,
                                                 pos, err);
+  return cudaGetLastError();
+}
+
+int launch_wait_probe(int* err, unsigned long long limit_ns, int arrive, cudaStream_t st) {
+  count_launch();
+  wait_probe_kernel<<<1, 32, 0, st>>>(err, limit_ns, arrive);
   return cudaGetLastError();
 }
 

@@ -70,20 +70,24 @@ DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  `abort` is a
 // CTA-wide flag in shared memory: once any thread gives up, the others stop
 // waiting too and the kernel winds down.
-DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                      int* err) {
+DF_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                          uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort = 1;
       record_error(err, 1 /* DFLASH_DEV_WAIT_TIMEOUT */);
       return false;
     }
   }
+}
+
+DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  return mbar_wait_for(bar, parity, abort, err, kWaitLimitNs);
 }
 
 // Arrival counter of a split-K merge: one thread adds 1 with acquire-release

@@ -78,6 +78,7 @@ _SIGNATURES = {
                                       c_void_p, c_void_p, POINTER(c_int32), c_void_p,
                                       c_void_p, c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
+    "dflash_wait_probe": ([c_void_p, ctypes.c_int64, c_int, c_void_p], c_int),
     "dflash_kernel_launches": ([POINTER(ctypes.c_uint64)], c_int),
     "dflash_packed_attn_core": ([c_void_p, c_int, c_int, c_int, c_int] + [c_void_p] * 7, c_int),
     "dflash_packed_attn_core_backward": ([c_void_p, c_int, c_int, c_int, c_int] +
@@ -291,6 +292,14 @@ class DFlashAttention:
         if rc not in (0, -6):
             check(rc)
         return code.value
+
+    def wait_probe(self, limit_ns: int, arrive: bool) -> None:
+        """One bounded device wait of at most limit_ns on the current stream
+        (arrive=False: a barrier nothing completes, so the wait runs out and
+        records DFLASH_DEV_WAIT_TIMEOUT; read it with device_error())."""
+        with torch.cuda.device(self.device):
+            check(lib().dflash_wait_probe(self.handle, int(limit_ns), int(bool(arrive)),
+                                          _stream(self.device)))
 
     def close(self) -> None:
         if getattr(self, "handle", None):

@@ -116,7 +116,7 @@ typedef struct {
 /* Message for the last failed call on this thread ("" if none). */
 const char* dflash_last_error(void);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 104. */
 int dflash_abi_version(void);
 
 /* Create one layer on the current CUDA device.
@@ -194,18 +194,21 @@ int dflash_ctx_project(dflash_attn* attn, const void* target_layers, int rows,
 /* The same context projection as dflash_ctx_project, for callers that must
  * not have device memory allocated on their behalf.  The pages have no
  * counterpart: this is a property of this library, not of the method.
- * Who needs it: code that issues the call while a stream is being captured
- * into a CUDA graph (cudaMalloc/cudaFree are not permitted then), serving
- * processes that fix all device memory at start-up and treat any later
- * allocation as a failure, and hosts whose memory pool must be the only
- * allocator on the GPU.  dflash_ctx_project may grow layer-owned scratch
- * with cudaMalloc; this entry point never allocates and never frees.
+ * Who needs it: serving processes that fix all device memory at start-up
+ * and treat any later allocation as a failure, and hosts whose memory pool
+ * must be the only allocator on the GPU.  dflash_ctx_project may grow
+ * layer-owned scratch with cudaMalloc; this entry point never allocates and
+ * never frees.
  * Its scratch (the fp32 fc output, the split-K partial tiles and their
  * counters) lives in one fixed 16 MiB array inside the library's device
  * image, present on every GPU that loads the library until the process
- * exits.  A request whose scratch would exceed 16 MiB (about rows * H * 4
- * bytes plus the split-K tiles; e.g. up to 128 rows at H = 4096) is rejected
- * with DFLASH_ERR_CAPACITY and enqueues nothing.
+ * exits.  The scratch a request needs is rows * H * 4 bytes for the fc
+ * output plus the split-K tiles of the projection kernel the row count
+ * selects: up to 384 rows that kernel needs no split-K tiles, from 385 rows
+ * the persistent kernel may split K and then needs 128 KB per (tile, split).
+ * At H = 4096 (fc 20480 -> 4096) that admits up to 384 rows and rejects
+ * 385 and more.  A request above 16 MiB is rejected with
+ * DFLASH_ERR_CAPACITY and enqueues nothing.
  * The first call on a device looks up the array's device address (which may
  * load the library's device code on that device): make that first call
  * before any stream capture.  Every call on a device shares the one array
@@ -448,6 +451,21 @@ int dflash_trace_read(dflash_attn* attn, int kind, double* total_ms,
 /* Wait for the device, then report and clear the layer's device error word
  * (DFLASH_DEV_*).  Returns DFLASH_ERR_DEVICE when the word was non-zero. */
 int dflash_device_error(dflash_attn* attn, int32_t* code);
+
+/* Check of the bounded device waits (no counterpart on the pages: failure
+ * handling of this library).  Enqueues one kernel on `stream` in which one
+ * thread waits on a shared-memory mbarrier with the same routine every
+ * pipeline wait of the library uses, but for at most limit_ns nanoseconds of
+ * GPU global time instead of the pipelines' 2 s.
+ *   arrive = 1: the barrier's one expected arrival is made first; the wait
+ *               completes at once and nothing is recorded.
+ *   arrive = 0: nothing ever arrives; the wait runs out, records
+ *               DFLASH_DEV_WAIT_TIMEOUT in the layer's device error word and
+ *               the kernel returns normally (no trap, no fault): the context
+ *               stays usable and dflash_device_error() reports the code.
+ * limit_ns must lie in [1e3, 1e8].  Errors: _ARG, _CUDA. */
+int dflash_wait_probe(dflash_attn* attn, int64_t limit_ns, int arrive,
+                      dflash_stream stream);
 
 #ifdef __cplusplus
 }

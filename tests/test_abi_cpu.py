@@ -26,7 +26,7 @@ def test_every_declared_function_is_exported(L):
 
 
 def test_abi_version(L):
-    assert L.dflash_abi_version() == 103
+    assert L.dflash_abi_version() == 104
 
 
 def test_create_rejects_null_config(L):
@@ -102,3 +102,9 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(D, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         D.lib()
+
+
+def test_wait_probe_checks_arguments_on_the_host(L):
+    stream = ctypes.c_void_p(0)
+    assert L.dflash_wait_probe(None, 1_000_000, 0, stream) == -1
+    assert b"null" in L.dflash_last_error()

@@ -2,14 +2,13 @@
 //
 // dflash_ctx_project() grows layer-owned scratch buffers with cudaMalloc the
 // first time it meets a larger request.  Some callers cannot allow that:
-// code that runs while a stream is being captured into a CUDA graph (where
-// cudaMalloc and cudaFree are not permitted), serving processes that plan
-// all device memory at start-up and treat any later allocation as a fault,
-// and hosts that hand the GPU to a custom pool and must not see a library
-// take memory behind its back.  dflash_ctx_project_noalloc() gives them the
-// same computation with its scratch (the fp32 fc output, the split-K partial
-// tiles and their counters) carved from one fixed array in the library's
-// device image, sized kScratchBytes.  The array exists on every GPU that
+// serving processes that plan all device memory at start-up and treat any
+// later allocation as a fault, and hosts that hand the GPU to a custom pool
+// and must not see a library take memory behind its back.
+// dflash_ctx_project_noalloc() gives them the same computation with its
+// scratch (the fp32 fc output, the split-K partial tiles and their counters)
+// carved from one fixed array in the library's device image, sized
+// kScratchBytes.  The array exists on every GPU that
 // loads the library, for the life of the process.
 #include <algorithm>
 #include <cstdio>
@@ -31,8 +30,9 @@ std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scratch on `dev` (the current device), looked up once
-// per device.  The first lookup may load the library's device code on that
-// device, which is why the first call should happen before any capture.
+// per device, at the first call on that device.  The first lookup may load
+// the library's device code on that device, which is why that first call
+// should come before any stream capture.
 cudaError_t scratch_address(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_scratch_addr[dev] == nullptr) {

@@ -6,8 +6,12 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   -> forward (QKV projection + q/k norm + RoPE + cache append, split-KV
      attention, o_proj)
   -> crop (back to the accepted prefix).
-The default workload is the Qwen3-8B-shaped single-sequence draft layer:
-4096 cached rows, 16 new context rows, a 16-row block, fc 20480 -> 4096.
+The default workload is the serving batch of Qwen3-8B-shaped draft layers:
+32 sequences with cached lengths uniform in [512, 8192], each step appending
+the previous step's accepted tokens as context rows (16 at the first step)
+plus a 16-row block, then cropping back to an accepted prefix of 1..16 block
+rows; fc 20480 -> 4096 over the step's new context rows.  This is the
+KV-read-bound configuration; `--workload` selects the others.
 The metric is draft-attention blocks/s per layer (one block = one sequence's
 block through one layer).  Inputs are synthetic, seeded, N(0,1) hidden
 states and N(0,0.02) weights.
@@ -91,7 +95,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen3_8b_single")
+    ap.add_argument("--workload", default="serving_b32")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the timed oracle sample")
@@ -862,12 +866,31 @@ class OracleRunner:
         return n, dt
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def oracle_baseline(name, seed, budget_s):
     r = OracleRunner(name, seed)
     r.step()  # warm-up
     n, dt = r.time(10 ** 6, budget_s)
     return {"value": n * r.blocks_per_step / dt, "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle",
+            "cpu_model": host_cpu_model(), "kind": "oracle",
             "sample": f"{n} oracle steps in {dt:.1f} s: {r.sample}; fp64 numpy, BLAS "
                       "threads = all host cores"}
 
@@ -930,7 +953,8 @@ def main():
                                l2="not applicable (host cores)",
                                arm="fp64 CPU oracle"),
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
-                                 "kind": "oracle", "sample": r.sample},
+                                 "cpu_model": host_cpu_model(), "kind": "oracle",
+                                 "sample": r.sample},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -1134,7 +1158,7 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.sp.dtype_name(),
             "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
             "config": dict(wl.config(), parallelism=f"replicas x{world}",
                            timing="CUDA graph of one step" if wl.fixed else "eager"),
@@ -1144,7 +1168,8 @@ def main():
             "device_error": err}
     if per_layer:
         line["per_layer_schedule"] = per_layer
-    step_bytes = sum(kb[0].values()) if kb[0] else None
+    # algorithmic bytes of the average step (serving steps differ in length)
+    step_bytes = float(np.mean([sum(k.values()) for k in kb])) if kb[0] else None
     if step_bytes:
         line["step_achieved_gbs"] = step_bytes / (ms / 1000.0) / 1e9
     if not args.no_cpu_baseline:

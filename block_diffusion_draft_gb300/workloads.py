@@ -69,6 +69,10 @@ class Spec:
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
 
+    def dtype_name(self) -> str:
+        """The arithmetic type of the path, as a bench line states it."""
+        return "bf16" if self.dtype == "bf16" else "f32"
+
 
 SPECS: Dict[str, Spec] = {
     # tiny fp32 single layer: 112 rows prefilled, then 16 new ctx + 16 block

@@ -1,6 +1,7 @@
 // attn_bf16.cu -- non-causal GQA attention of the draft layer on tcgen05.
 //
-// One CTA owns one work unit: a (sequence, kv head) pair and a range of keys.
+// One CTA owns one work unit: a (sequence, kv head) pair and a range of its
+// 128-key tiles.
 // Its Q tile stacks every query head of the KV group times the block rows
 // (groups * q_len rows), so each K/V row is read once for all heads of the
 // group ("DFlash源码导读（二）" step 1: GQA with num_key_value_groups).
@@ -31,10 +32,21 @@
 // Masks ("nemo_automodel...draft_qwen3", _sliding_window_mask): a row's
 // allowed keys are the unit's key range, on a band layer cut to
 // |query index - key| < W.
-// A key range split across CTAs leaves per-split partials (unnormalised O,
-// running max, running sum); attn_combine_kernel merges them with the usual
-// log-sum-exp rescaling, one CTA per 8 query rows of a (sequence, kv head).
+// Work split (plan_decode_attention): with many (sequence, kv head) pairs,
+// every pair's tiles are split into units of near-equal size, dispatched
+// largest first, so that the SMs finish together; with few pairs, C splits of
+// a pair form a thread-block cluster and k clusters share a pair, so that
+// every SM gets a unit.  A split leaves an unnormalised partial (O, running
+// max, running sum) in its slot in L2; the split that finishes a pair last
+// (an arrival counter) merges the pair's partials with the log-sum-exp
+// rescaling, in split order.  In a cluster, one cluster barrier orders the
+// partials and each rank merges a share of the rows; the clusters' merged row
+// blocks are merged the same way by the last cluster to finish.
 #include <algorithm>
+#include <atomic>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -55,128 +67,134 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 struct Unit {
   int b, h;
-  int q_row0;       // first row of the Q tile in the Q buffer
-  int rows;         // real query rows in the tile
+  int q_row0;         // first row of the Q tile in the Q buffer
+  int rows;           // real query rows in the tile
   long long kv_row0;  // first K/V storage row of (b, h)
-  int s0_lo, s0_hi, s1_lo, s1_hi;  // key segments
-  int direct;       // 1: this unit covers all keys of its rows
-  int len;          // inference: keys of the sequence after this call
+  int s0_lo, s0_hi;   // the unit's keys
+  int len;            // keys of the sequence after this call
+  int ns, c;          // splits of the (sequence, kv head) pair, this unit's split
+  int pair_unit0;     // unit of the pair's split 0 (its units are consecutive)
 };
 
-// Inference work unit u: split c of the keys of (sequence b, kv head h).
+// Inference work unit u: split c of the key tiles of (sequence b, kv head h).
 DF_DEV Unit decode(const AttnArgs& a, const AttnSeqs& sq, int u) {
   Unit w;
-  const int rows_per_block = a.groups * a.q_block;
   int lo = 0, hi = a.batch;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (sq.unit_off[mid] <= u) lo = mid; else hi = mid;
   }
-  w.b = lo;
-  const int nch = sq.n_chunks[w.b];
-  const int r = u - sq.unit_off[w.b];
-  w.h = r / nch;
-  const int c = r - w.h * nch;
+  w.b = sq.order[lo];
+  w.ns = sq.n_split[w.b];
+  const int r = u - sq.unit_off[lo];
+  w.h = r / w.ns;
+  w.c = r - w.h * w.ns;
+  w.pair_unit0 = sq.unit_off[lo] + w.h * w.ns;
   w.len = sq.len[w.b];
-  w.s0_lo = sq.lo[w.b] + c * sq.chunk[w.b];
-  w.s0_hi = min(w.len, w.s0_lo + sq.chunk[w.b]);
-  w.s1_lo = w.s1_hi = 0;
-  w.q_row0 = (w.b * a.n_kv + w.h) * rows_per_block;
-  w.rows = rows_per_block;
-  w.direct = nch == 1;
+  const int k_lo = sq.lo[w.b];
+  const int n_t = (w.len - k_lo + BKEY - 1) / BKEY;
+  const int t0 = (int)((long long)w.c * n_t / w.ns);
+  const int t1 = (int)((long long)(w.c + 1) * n_t / w.ns);
+  w.s0_lo = k_lo + t0 * BKEY;
+  w.s0_hi = min(w.len, k_lo + t1 * BKEY);
+  w.rows = a.groups * a.q_block;
+  w.q_row0 = (w.b * a.n_kv + w.h) * w.rows;
   w.kv_row0 = ((long long)w.b * a.n_kv + w.h) * a.cap;
   return w;
 }
 
 DF_DEV int n_tiles_of(const Unit& w) {
-  const int n0 = w.s0_hi > w.s0_lo ? (w.s0_hi - w.s0_lo + BKEY - 1) / BKEY : 0;
-  const int n1 = w.s1_hi > w.s1_lo ? (w.s1_hi - w.s1_lo + BKEY - 1) / BKEY : 0;
-  return n0 + n1;
+  return w.s0_hi > w.s0_lo ? (w.s0_hi - w.s0_lo + BKEY - 1) / BKEY : 0;
 }
 
-DF_DEV int tile_start(const Unit& w, int j) {
-  const int n0 = w.s0_hi > w.s0_lo ? (w.s0_hi - w.s0_lo + BKEY - 1) / BKEY : 0;
-  return j < n0 ? w.s0_lo + j * BKEY : w.s1_lo + (j - n0) * BKEY;
+DF_DEV int tile_start(const Unit& w, int j) { return w.s0_lo + j * BKEY; }
+
+// the bf16 output row of query row `row` of the unit's Q tile
+DF_DEV __nv_bfloat16* out_row(const AttnArgs& a, const Unit& w, int row) {
+  const int gi = row / a.q_len, t = row - gi * a.q_len;
+  const size_t token = (size_t)w.b * a.q_len + t;
+  return reinterpret_cast<__nv_bfloat16*>(a.out) + token * (size_t)(a.n_kv * a.groups * HD) +
+         (size_t)(w.h * a.groups + gi) * HD;
 }
 
-// On-chip merge of the key splits of one (sequence, kv head), whose C CTAs
-// form a thread-block cluster.  Query row r belongs to rank r / RPO (RPO =
-// ceil(rows / C)).  After a cluster barrier (every CTA is done with its stage
-// buffers) each CTA stores (O, m, l) of each of its rows into the owner's
-// idle K slots 1-2 (O, [source][row] swizzled) and V slot 0 (m, l); after a
-// second barrier the owner merges its rows from local shared memory: one
-// warp per row, lane l holding columns 4l .. 4l+3, sources in rank order (so
-// the result does not depend on timing), rescaled by the largest running max,
-// written as the normalised bf16 row.
-DF_DEV uint32_t merge_slot(int src, int lr, int rpo) { return (uint32_t)(src * rpo + lr); }
-
-DF_DEV void cluster_push_row(uint8_t* obuf, uint8_t* mlbuf, int C, int qr, int rows,
-                             const float (&o)[HD], float m, float l) {
-  const int rpo = (rows + C - 1) / C;
-  const uint32_t owner = (uint32_t)(qr / rpo);
-  const uint32_t slot = merge_slot((int)cluster_ctarank(), qr % rpo, rpo);
-  const uint32_t ob = cluster_map(smem_u32(obuf), owner);
-  const uint32_t mb = cluster_map(smem_u32(mlbuf), owner);
+// One thread's unnormalised partial row (O, running max, running sum) into
+// partial slot `slot` (fp32 [slot][row][d] and [slot][2][row]).
+DF_DEV void write_partial(const AttnArgs& a, int slot, int row, const float (&o)[HD], float m,
+                          float l) {
+  float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * 128 + row) * HD);
 #pragma unroll
   for (int c4 = 0; c4 < HD / 4; ++c4)
-    st_cluster_f4(ob + (slot * 32 + (c4 ^ (slot & 31))) * 16,
-                  make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
-  st_cluster_f32(mb + slot * 4, m);
-  st_cluster_f32(mb + (128 + slot) * 4, l);
+    __stcg(dst + c4, make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
+  __stcg(a.part_ml + (size_t)slot * 256 + row, m);
+  __stcg(a.part_ml + (size_t)slot * 256 + 128 + row, l);
 }
 
-template <int C>
-DF_DEV void cluster_merge_rows(const AttnArgs& a, const Unit& w, const uint8_t* obuf,
-                               const uint8_t* mlbuf, int warp, int lane) {
-  const int rpo = (w.rows + C - 1) / C;
-  const int row0 = (int)cluster_ctarank() * rpo;
-  const float4* ob = reinterpret_cast<const float4*>(obuf);
-  const float* mb = reinterpret_cast<const float*>(mlbuf);
-  const int ld_out = a.n_kv * a.groups * HD;
-  for (int lr = warp - 2; lr < rpo && row0 + lr < w.rows; lr += 4) {
-    float m[C], l[C];
-    float4 t[C];
-#pragma unroll
-    for (int k = 0; k < C; ++k) {
-      const uint32_t slot = merge_slot(k, lr, rpo);
-      m[k] = mb[slot];
-      l[k] = mb[128 + slot];
-      t[k] = ob[slot * 32 + (lane ^ (slot & 31))];
-    }
+// Log-sum-exp merge of rows [r0, r1) over the n partial slots slot0 + i *
+// stride: warp wq of the four softmax warps takes rows r0 + wq, r0 + wq + 4,
+// ...; lane l holds columns 4l .. 4l+3.  Sources are summed in slot order
+// (the result does not depend on which CTA merges, nor when), each rescaled
+// to the largest running max.  The merged row goes to the output as the
+// normalised bf16 row, or (block_slot >= 0) unnormalised with its max and
+// sum into that slot.
+DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, int n, int r0,
+                       int r1, int block_slot, int wq, int lane) {
+  for (int row = r0 + wq; row < r1; row += 4) {
     float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < C; ++k) M = fmaxf(M, m[k]);
+    for (int i = 0; i < n; ++i)
+      M = fmaxf(M, __ldcg(a.part_ml + (size_t)(slot0 + i * stride) * 256 + row));
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < C; ++k) {
-      const float f = m[k] == -INFINITY ? 0.f : fast_exp2(m[k] - M);
-      L += f * l[k];
-      acc.x += f * t[k].x;
-      acc.y += f * t[k].y;
-      acc.z += f * t[k].z;
-      acc.w += f * t[k].w;
+    if (M != -INFINITY) {
+#pragma unroll 4
+      for (int i = 0; i < n; ++i) {
+        const size_t sl = (size_t)(slot0 + i * stride);
+        const float m = __ldcg(a.part_ml + sl * 256 + row);
+        const float l = __ldcg(a.part_ml + sl * 256 + 128 + row);
+        const float4 t =
+            __ldcg(reinterpret_cast<const float4*>(a.part_o + (sl * 128 + row) * HD) + lane);
+        const float f = m == -INFINITY ? 0.f : fast_exp2(m - M);
+        L += f * l;
+        acc.x += f * t.x;
+        acc.y += f * t.y;
+        acc.z += f * t.z;
+        acc.w += f * t.w;
+      }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int row = row0 + lr;
-    const int gi = row / a.q_len, tt = row - gi * a.q_len;
-    const size_t token = (size_t)w.b * a.q_len + tt;
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + token * ld_out +
-                              (size_t)(w.h * a.groups + gi) * HD + lane * 4) = pk;
+    if (block_slot >= 0) {
+      __stcg(reinterpret_cast<float4*>(a.part_o + ((size_t)block_slot * 128 + row) * HD) + lane,
+             acc);
+      if (lane == 0) {
+        __stcg(a.part_ml + (size_t)block_slot * 256 + row, M);
+        __stcg(a.part_ml + (size_t)block_slot * 256 + 128 + row, L);
+      }
+    } else {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      reinterpret_cast<uint2*>(out_row(a, w, row))[lane] = pk;
+    }
   }
 }
 
-DF_DEV void cluster_merge(const AttnArgs& a, const Unit& w, const uint8_t* obuf,
-                          const uint8_t* mlbuf, int warp, int lane) {
-  switch (a.cluster) {
-    case 2: cluster_merge_rows<2>(a, w, obuf, mlbuf, warp, lane); break;
-    case 4: cluster_merge_rows<4>(a, w, obuf, mlbuf, warp, lane); break;
-    case 8: cluster_merge_rows<8>(a, w, obuf, mlbuf, warp, lane); break;
-    default: cluster_merge_rows<16>(a, w, obuf, mlbuf, warp, lane); break;
+// Called by the 128 softmax threads after their partial stores: counts this
+// CTA in at `counter` (one thread, acquire-release at GPU scope, after a
+// barrier that orders every thread's stores before it) and returns, to every
+// one of them, whether it was the n-th arrival.  The n-th arrival resets the
+// counter for the next launch.
+DF_DEV bool last_arrival(int* counter, int n, int et, volatile int* flag) {
+  __threadfence();
+  named_bar_sync(1, 128);
+  if (et == 0) {
+    const int old = atomic_add_acq_rel_gpu(counter, 1);
+    const bool last = old == n - 1;
+    if (last) *counter = 0;
+    *flag = last ? 1 : 0;
   }
+  named_bar_sync(1, 128);
+  const bool last = *flag != 0;
+  if (last) __threadfence();
+  return last;
 }
 
 template <bool DUAL>
@@ -203,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = p_full + 2;      // [2]: PV(j) completes o_done[j & 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Unit w = decode(a, sq, blockIdx.x);
@@ -562,8 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const bool writer = real && (!DUAL || r < 64);
-    if (writer) {
-      if (w.direct) {
+    const int et = threadIdx.x - 64, wq = warp - 2;
+    if (w.ns == 1) {
+      // the unit covers every key of its rows: the normalised row
+      if (writer) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const int ld_out = a.n_kv * a.groups * HD;
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
@@ -577,32 +598,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
           dst[i] = pk;
         }
-      } else if (a.cluster > 1) {
-        // handed to the owner rank below
-      } else {
-        const size_t u = blockIdx.x;
-        float4* po = reinterpret_cast<float4*>(a.part_o + u * 128 * HD);
-#pragma unroll
-        for (int c4 = 0; c4 < HD / 4; ++c4)
-          __stcg(po + c4 * 128 + qr,
-                 make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]));
-        __stcg(a.part_ml + u * 256 + qr, m_run);
-        __stcg(a.part_ml + u * 256 + 128 + qr, l_run);
       }
-    }
-    if (a.cluster > 1) {
-      __syncwarp();
-      cluster_sync();  // every CTA of the cluster is done with its stage buffers
-      if (writer) cluster_push_row(sK + TILE_BYTES, sV, a.cluster, qr, w.rows, o, m_run, l_run);
-      __syncwarp();
-      cluster_sync();  // every row has reached its owner
-      cluster_merge(a, w, sK + TILE_BYTES, sV, warp, lane);
+    } else {
+      // a split: the unnormalised partial rows go to the unit's slot, then
+      // the rows are merged over the pair's splits
+      if (writer) write_partial(a, (int)blockIdx.x, qr, o, m_run, l_run);
+      if (a.cluster > 1) {
+        // every C consecutive splits of the pair are one cluster: after one
+        // barrier each rank merges its share of the rows from the C slots
+        // (through L2); with several clusters per pair, the last cluster to
+        // finish a row block merges the clusters' blocks
+        __syncwarp();
+        cluster_sync();
+        const int C = a.cluster;
+        const int rank = w.c % C, cl = w.c / C;
+        const int rpo = (w.rows + C - 1) / C;
+        const int r0 = min(w.rows, rank * rpo), r1 = min(w.rows, r0 + rpo);
+        if (a.k_clusters == 1) {
+          merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, -1, wq, lane);
+        } else {
+          merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, a.n_units + (int)blockIdx.x,
+                     wq, lane);
+          int* cnt = a.counters + ((size_t)(w.b * a.n_kv + w.h) * C + rank);
+          if (last_arrival(cnt, a.k_clusters, et, last_flag))
+            merge_rows(a, w, a.n_units + w.pair_unit0 + rank, C, a.k_clusters, r0, r1, -1, wq,
+                       lane);
+        }
+      } else if (last_arrival(a.counters + (w.b * a.n_kv + w.h), w.ns, et, last_flag)) {
+        // the pair's last split to finish merges all of its rows
+        merge_rows(a, w, w.pair_unit0, 1, w.ns, 0, w.rows, -1, wq, lane);
+      }
     }
   }
   if (warp < 2 && a.cluster > 1) {
-    // the producer and MMA warps take part in both cluster barriers
+    // the producer and MMA warps take part in the cluster barrier
     __syncwarp();
-    cluster_sync();
     cluster_sync();
   }
 
@@ -980,58 +1010,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   }
 }
 
-// Merge the split partials of one (sequence, kv head): 8 query rows per CTA,
-// thread t takes output columns 4(t / 8) .. +3 of row t % 8, so a warp reads
-// four 128-byte runs of the [unit][column chunk][row] partials.  Two passes:
-// the largest running max over the splits, then the rescaled sums, each over
-// independent loads.  Pairs whose keys fit one unit were finished by the
-// attention kernel and are skipped.
-__global__ void __launch_bounds__(256)
-    attn_combine_kernel(const __grid_constant__ AttnArgs a,
-                        const __grid_constant__ AttnSeqs sq) {
-  const int rows_pair = a.groups * a.q_len;
-  const int groups_per_pair = (rows_pair + 7) / 8;
-  const int pair = blockIdx.x / groups_per_pair;
-  const int b = pair / a.n_kv, h = pair - b * a.n_kv;
-  const int nch = sq.n_chunks[b];
-  if (nch <= 1) return;
-  const int c4 = threadIdx.x >> 3;
-  const int r = (blockIdx.x - pair * groups_per_pair) * 8 + (threadIdx.x & 7);
-  if (r >= rows_pair) return;
-  const size_t base = (size_t)sq.unit_off[b] + (size_t)h * nch;
-  const float* ml = a.part_ml + base * 256 + r;
-  const float4* po = reinterpret_cast<const float4*>(a.part_o + base * 128 * HD) + c4 * 128 + r;
-  grid_dep_sync();
-  float M = -INFINITY;
-#pragma unroll 8
-  for (int u = 0; u < nch; ++u) M = fmaxf(M, __ldcg(ml + (size_t)u * 256));
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-#pragma unroll 8
-    for (int u = 0; u < nch; ++u) {
-      const float m = __ldcg(ml + (size_t)u * 256);
-      const float l = __ldcg(ml + (size_t)u * 256 + 128);
-      const float4 t = __ldcg(po + (size_t)u * (128 * HD / 4));
-      const float f = m == -INFINITY ? 0.f : fast_exp2(m - M);
-      L += f * l;
-      acc.x += f * t.x;
-      acc.y += f * t.y;
-      acc.z += f * t.z;
-      acc.w += f * t.w;
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int gi = r / a.q_len, t = r - gi * a.q_len;
-  const size_t token = (size_t)b * a.q_len + t;
-  const int ld_out = a.n_kv * a.groups * HD;
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + token * ld_out +
-                            (size_t)(h * a.groups + gi) * HD + c4 * 4) = pk;
-}
-
 }  // namespace
 
 namespace {
@@ -1048,9 +1026,9 @@ void set_attn_attrs() {
   mark_device(done);
 }
 
-// clusters of `c` attention CTAs that can be resident at once (0 if none)
+// clusters of `c` decode-attention CTAs that can be resident at once
 int max_active_clusters(int c, bool dual) {
-  static std::atomic<int> cache[2][17];  // the count + 1; 0: not asked yet
+  static std::atomic<int> cache[2][9];  // the count + 1; 0: not asked yet
   const int known = cache[dual][c].load(std::memory_order_acquire);
   if (known != 0) return known - 1;
   set_attn_attrs();
@@ -1066,7 +1044,8 @@ int max_active_clusters(int c, bool dual) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  const void* f = dual ? (const void*)attn_bf16_kernel<true> : (const void*)attn_bf16_kernel<false>;
+  const void* f =
+      dual ? (const void*)attn_bf16_kernel<true> : (const void*)attn_bf16_kernel<false>;
   if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
@@ -1077,12 +1056,99 @@ int max_active_clusters(int c, bool dual) {
 
 }  // namespace
 
-int attn_decode_cluster(int pairs, int num_sms, bool dual) {
-  for (int c = 16; c >= 2; c /= 2) {
-    if ((long long)pairs * c > num_sms) continue;
-    if (max_active_clusters(c, dual) >= pairs) return c;
+size_t decode_attention_slots(int batch, int n_kv, int num_sms) {
+  // balanced plans: at most 4 units per SM plus one per pair; cluster plans:
+  // at most one unit per SM, twice (the clusters' merged row blocks)
+  return (size_t)4 * num_sms + (size_t)batch * n_kv;
+}
+
+size_t decode_attention_counters(int batch, int n_kv) { return (size_t)batch * n_kv * 8; }
+
+int plan_decode_attention(AttnSeqs& sq, int batch, int n_kv, int num_sms, bool dual,
+                          int* cluster, int* k_clusters) {
+  const int pairs = batch * n_kv;
+  std::vector<int> np(batch);
+  int max_np = 1;
+  long long tot = 0;
+  for (int b = 0; b < batch; ++b) {
+    np[b] = std::max(1, (sq.len[b] - sq.lo[b] + BKEY - 1) / BKEY);
+    max_np = std::max(max_np, np[b]);
+    tot += (long long)n_kv * np[b];
   }
-  return 1;
+  *cluster = 1;
+  *k_clusters = 1;
+  // few pairs with few tiles each: C splits per cluster, k clusters per pair,
+  // every cluster resident at once, about one unit per SM and at least two
+  // tiles per unit (pairs with more than 8 tiles per split balance better as
+  // independent units)
+  int C = 8, fit = 0;
+  for (; C >= 2; C >>= 1) {
+    if ((long long)pairs * C > num_sms || C > max_np || max_np > 8 * C) continue;
+    fit = max_active_clusters(C, dual) / pairs;
+    if (fit >= 1) break;
+  }
+  if (C >= 2 && fit >= 1) {
+    const int k = std::max(1, std::min({fit, num_sms / (pairs * C), max_np / (2 * C)}));
+    *cluster = C;
+    *k_clusters = k;
+    sq.unit_off[0] = 0;
+    for (int b = 0; b < batch; ++b) {
+      sq.n_split[b] = C * k;
+      sq.order[b] = b;
+      sq.unit_off[b + 1] = sq.unit_off[b] + n_kv * C * k;
+    }
+    return sq.unit_off[batch];
+  }
+  // many pairs: units of at most U tiles for about m units per SM; keep the
+  // m whose list-scheduling makespan (units dispatched largest first, each
+  // costing its tiles plus a start-up of two tiles and one tile for a merge)
+  // is shortest
+  std::vector<int> best_ns(batch, 1), ns(batch);
+  double best_t = 1e300;
+  for (int m = 1; m <= 4; ++m) {
+    const long long U = std::max<long long>(1, (tot + (long long)m * num_sms - 1) /
+                                                   ((long long)m * num_sms));
+    long long units = 0;
+    for (int b = 0; b < batch; ++b) {
+      ns[b] = (int)std::min<long long>({(np[b] + U - 1) / U, (long long)np[b], 32});
+      units += (long long)n_kv * ns[b];
+    }
+    if (units > (long long)decode_attention_slots(batch, n_kv, num_sms)) continue;
+    std::vector<std::pair<double, int>> groups(batch);
+    for (int b = 0; b < batch; ++b)
+      groups[b] = {(double)np[b] / ns[b] + 2.0 + (ns[b] > 1 ? 1.0 : 0.0), b};
+    std::sort(groups.begin(), groups.end(), [](const auto& x, const auto& y) {
+      return x.first > y.first || (x.first == y.first && x.second < y.second);
+    });
+    std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+    for (int i = 0; i < num_sms; ++i) load.push(0.0);
+    double t = 0.0;
+    for (const auto& g : groups)
+      for (int i = 0; i < n_kv * ns[g.second]; ++i) {
+        const double l = load.top() + g.first;
+        load.pop();
+        load.push(l);
+        t = std::max(t, l);
+      }
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best_ns = ns;
+    }
+  }
+  std::vector<std::pair<double, int>> order(batch);
+  for (int b = 0; b < batch; ++b) {
+    sq.n_split[b] = best_ns[b];
+    order[b] = {(double)np[b] / best_ns[b], b};
+  }
+  std::sort(order.begin(), order.end(), [](const auto& x, const auto& y) {
+    return x.first > y.first || (x.first == y.first && x.second < y.second);
+  });
+  sq.unit_off[0] = 0;
+  for (int i = 0; i < batch; ++i) {
+    sq.order[i] = order[i].second;
+    sq.unit_off[i + 1] = sq.unit_off[i] + n_kv * best_ns[order[i].second];
+  }
+  return sq.unit_off[batch];
 }
 
 int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
@@ -1091,7 +1157,9 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                      cudaStream_t stream) {
   set_attn_attrs();
   if (a.n_units <= 0) return cudaSuccess;
-  if (a.cluster > 1 && (a.mode != 0 || a.cluster > 16 || a.n_units % a.cluster != 0))
+  if (a.cluster > 1 && (a.mode != 0 || a.cluster > 8 || a.n_units % a.cluster != 0))
+    return cudaErrorInvalidValue;
+  if (a.mode == 0 && (a.part_o == nullptr || a.part_ml == nullptr || a.counters == nullptr))
     return cudaErrorInvalidValue;
   if (kv_rows_total >= (1LL << 31) || q_rows_total >= (1LL << 31))
     return cudaErrorInvalidValue;
@@ -1124,13 +1192,7 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                                 SMEM_BYTES, stream, cl, mq, mk, mv, a, sq)
            : launch_pdl_cluster(attn_bf16_kernel<false>, dim3(a.n_units), dim3(kThreads),
                                 SMEM_BYTES, stream, cl, mq, mk, mv, a, sq);
-  if (e != cudaSuccess || a.mode != 0 || a.cluster > 1) return (int)e;
-  bool any_split = false;
-  for (int b = 0; b < a.batch; ++b) any_split |= sq.n_chunks[b] > 1;
-  if (!any_split) return cudaSuccess;
-  const int groups_per_pair = (a.groups * a.q_len + 7) / 8;
-  return (int)launch_pdl(attn_combine_kernel, dim3(a.batch * a.n_kv * groups_per_pair),
-                         dim3(256), 0, stream, a, sq);
+  return (int)e;
 }
 
 }  // namespace df

@@ -249,9 +249,8 @@ int forward_core(dflash_attn* a, const KvView& kv, int batch, int q_len, const v
   if (int r = run_qkv(a, noise, (int)rows_noise, target_hidden, (int)total_ctx, o, st, s))
     return r;
 
-  // attention work list: per sequence the visible key range, split in chunks
+  // attention work list: per sequence the visible key range, split in units
   AttnSeqs sq;
-  long long total_keys = 0;
   for (int b = 0; b < batch; ++b) {
     sq.len[b] = len_before[b] + host_n_ctx[b] + q_len;
     sq.first_new[b] = len_before[b];
@@ -261,29 +260,11 @@ int forward_core(dflash_attn* a, const KvView& kv, int batch, int q_len, const v
     // paged tiles gather whole pages: start the range on a tile boundary
     // (the band still cuts each row's keys)
     if (kv.block_table != nullptr) sq.lo[b] = sq.lo[b] / 128 * 128;
-    total_keys += (long long)a->nkv * (sq.len[b] - sq.lo[b]);
   }
-  // Few (sequence, kv head) pairs: each pair's keys split evenly over the C
-  // CTAs of a thread-block cluster that merge on chip.  Otherwise about one
-  // key chunk per SM, in whole 128-key tiles, at most 4096 keys, merged by a
-  // second kernel.
-  const int cl = a->dt == DFLASH_BF16
-                     ? attn_decode_cluster(batch * a->nkv, a->num_sms, a->g * q_len <= 64)
-                     : 1;
-  int chunk = (int)((total_keys + a->num_sms - 1) / a->num_sms);
-  chunk = std::min(4096, std::max(128, (chunk + 127) / 128 * 128));
-  sq.unit_off[0] = 0;
-  for (int b = 0; b < batch; ++b) {
-    const int keys = sq.len[b] - sq.lo[b];
-    if (cl > 1) {
-      sq.chunk[b] = std::max(128, ((keys + cl - 1) / cl + 127) / 128 * 128);
-      sq.n_chunks[b] = cl;
-    } else {
-      sq.chunk[b] = chunk;
-      sq.n_chunks[b] = std::max(1, (keys + chunk - 1) / chunk);
-    }
-    sq.unit_off[b + 1] = sq.unit_off[b] + a->nkv * sq.n_chunks[b];
-  }
+  int cl = 1, kcl = 1, n_units = batch * a->nkv;
+  if (a->dt == DFLASH_BF16)
+    n_units = plan_decode_attention(sq, batch, a->nkv, a->num_sms, a->g * q_len <= 64, &cl,
+                                    &kcl);
   AttnArgs aa{};
   aa.mode = 0;
   aa.batch = batch;
@@ -301,15 +282,22 @@ int forward_core(dflash_attn* a, const KvView& kv, int batch, int q_len, const v
   aa.n_pages = kv.n_pages;
   aa.window = a->cfg.sliding_window;
   aa.causal = a->cfg.causal != 0;
-  aa.n_units = sq.unit_off[batch];
+  aa.n_units = n_units;
   aa.cluster = cl;
+  aa.k_clusters = kcl;
   aa.out = a->attn_out.p;
   aa.err = a->err;
   if (a->dt == DFLASH_BF16) {
-    DF_CUDA(a->part_o.ensure((size_t)aa.n_units * 128 * 128 * 4), "scratch allocation");
-    DF_CUDA(a->part_ml.ensure((size_t)aa.n_units * 256 * 4), "scratch allocation");
+    // partial slots: one per unit, twice in cluster mode with several
+    // clusters per pair (the clusters' merged row blocks)
+    const size_t slots = (size_t)n_units * (cl > 1 && kcl > 1 ? 2 : 1);
+    DF_CUDA(a->part_o.ensure(slots * 128 * 128 * 4), "scratch allocation");
+    DF_CUDA(a->part_ml.ensure(slots * 256 * 4), "scratch allocation");
+    DF_CUDA(a->attn_counters.ensure(decode_attention_counters(batch, a->nkv) * sizeof(int), true),
+            "scratch allocation");
     aa.part_o = static_cast<float*>(a->part_o.p);
     aa.part_ml = static_cast<float*>(a->part_ml.p);
+    aa.counters = static_cast<int*>(a->attn_counters.p);
     TraceScope tr(a, DFLASH_K_ATTN, s);
     DF_CUDA(launch_attn_bf16(aa, &sq, a->qbuf.p, rows_noise * a->nq, kv.k, kv.v,
                              kv.rows_total, s),
@@ -479,15 +467,13 @@ int dflash_attn_reserve(dflash_attn* a, int max_batch, int max_rows, int max_key
     if (a->nL > 0) {
       if (int r = reserve_gemm_scratch(a, EPI_F32, max_rows, 0, a->H, a->nL * a->H, 0)) return r;
     }
-    // a forward splits each sequence's keys into chunks of at least
-    // max(128, total keys / SMs) and at most 4096 keys: per kv head at most
-    // max(SMs, batch * ceil(keys / 4096)) + batch units
-    const size_t per_head = (size_t)std::max<long long>(
-                                a->num_sms, (long long)max_batch * ((max_keys + 4095) / 4096)) +
-                            max_batch;
-    const size_t units = (size_t)a->nkv * per_head;
-    DF_CUDA(a->part_o.ensure(units * 128 * 128 * 4), "scratch allocation");
-    DF_CUDA(a->part_ml.ensure(units * 256 * 4), "scratch allocation");
+    // the decode attention's partial slots and merge counters
+    const size_t slots = decode_attention_slots(max_batch, a->nkv, a->num_sms);
+    DF_CUDA(a->part_o.ensure(slots * 128 * 128 * 4), "scratch allocation");
+    DF_CUDA(a->part_ml.ensure(slots * 256 * 4), "scratch allocation");
+    DF_CUDA(a->attn_counters.ensure(decode_attention_counters(max_batch, a->nkv) * sizeof(int),
+                                    true),
+            "scratch allocation");
   }
   if (a->nL > 0) DF_CUDA(a->zbuf.ensure((size_t)max_rows * a->H * 4), "scratch allocation");
   return DFLASH_OK;

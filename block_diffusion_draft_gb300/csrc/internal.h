@@ -145,15 +145,18 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
                         int cols, int box_rows);
 
 // ----------------------------------------------------------- attention
-// Per-sequence key ranges of an inference attention call.
+// Per-sequence key ranges and the work split of an inference attention call.
+// Each (sequence, kv head) pair's keys [lo, len) form ceil((len - lo) / 128)
+// tiles, split into n_split units of near-equal tile counts.  Units follow
+// the sequences in `order` (largest units first), kv head-major then split.
 struct AttnSeqs {
   int len[kMaxBatch];          // keys of the sequence after this call's append
   int lo[kMaxBatch];           // first key any query of the block can see
-  int n_chunks[kMaxBatch];     // splits of [lo, len) per kv head
-  int chunk[kMaxBatch];        // keys per split (a multiple of 128)
-  int unit_off[kMaxBatch + 1]; // first work unit of the sequence
   int first_new[kMaxBatch];    // first row this call appends (rows below it
                                // were written by earlier calls)
+  int n_split[kMaxBatch];      // units per (sequence, kv head), by sequence
+  int order[kMaxBatch];        // sequences in unit order
+  int unit_off[kMaxBatch + 1]; // first unit of the i-th sequence of `order`
 };
 
 struct AttnArgs {
@@ -177,19 +180,29 @@ struct AttnArgs {
   int seq;           // packed: context rows per sequence
   const int* anchors;  // packed: [B][n_blocks]
   int n_units;
-  int cluster;       // inference: > 1 = the splits of one (sequence, kv head)
-                     // form a thread-block cluster and merge on chip
-  float* part_o;     // [units][128 rows][d] fp32 partial outputs
-  float* part_ml;    // [units][2][128] running max (log2 units) and sum
-  int* counters;     // [B * n_kv]
+  int cluster;       // inference: C > 1 = every C consecutive splits of a pair
+                     // form a thread-block cluster (n_split = C * k_clusters)
+  int k_clusters;    // clusters per (sequence, kv head)
+  float* part_o;     // [slot][128 rows][d] fp32 partial outputs (slot = unit;
+                     // cluster mode also [n_units + unit]: merged row blocks)
+  float* part_ml;    // [slot][2][128] running max (log2 units) and sum
+  int* counters;     // split merges: [B * n_kv] or [B * n_kv * C], zero
+                     // between calls (the last arriver resets its counter)
   void* out;         // [B*q_len][n_heads*d]
   int* err;
 };
 
-// Splits per (sequence, kv head) for the on-chip merge of a decode step with
-// `pairs` (sequence, kv head) pairs: the largest of 16, 8, 4, 2 whose
-// clusters all fit on the GPU at once, or 1 (separate merge kernel).
-int attn_decode_cluster(int pairs, int num_sms, bool dual);
+// Work split of a decode-attention call (fills n_split, order, unit_off of
+// `sq` from its len and lo): returns the number of units and sets the
+// cluster size C (1 = none) and the clusters per pair.  Few (sequence, kv
+// head) pairs: C = 8 (or fewer) splits per cluster, k clusters per pair;
+// otherwise units of near-equal tile counts, largest first, so that the
+// hardware's in-order dispatch balances the SMs.
+int plan_decode_attention(AttnSeqs& sq, int batch, int n_kv, int num_sms, bool dual,
+                          int* cluster, int* k_clusters);
+// partial slots and merge counters a plan with these sizes can need
+size_t decode_attention_slots(int batch, int n_kv, int num_sms);
+size_t decode_attention_counters(int batch, int n_kv);
 
 int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
                      long long q_rows_total, const void* cache_k,

@@ -474,10 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  // [B stages][A stages][room for the last A stage's full 16 KB MMA read]
-  uint8_t* sB = smem;
-  uint8_t* sA = smem + (size_t)S * B_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sA + (size_t)(S - 1) * p.a_bytes + A_FULL);
+  // A stage holds two 64-column k-blocks, each [A rows (a_bytes) | B tile
+  // (B_BYTES)], so that one wait and one commit of the MMA thread cover eight
+  // MMAs (with four, the synchronisation is not hidden behind the MMAs).
+  // The MMA reads 128 A rows; the rows past the box fall into the stage's own
+  // B tile, which no copy writes while that MMA runs.
+  const size_t half = (size_t)p.a_bytes + B_BYTES;
+  const size_t stride = 2 * half;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + p.a_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stride);
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* accb = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
@@ -491,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = (int)((long long)split * p.n_kb / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
   const int nkb = kb1 - kb0;
+  const int n_st = (nkb + 1) / 2;  // stages of two k-blocks (the last may hold one)
   const bool from_a0 = m_tile < p.n_m0;
   const int a_row0 = (from_a0 ? m_tile : m_tile - p.n_m0) * BM;
   const int n0 = n_tile * BN;
@@ -522,43 +529,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
       // weights first: they do not depend on the previous kernel
-      const int pre = min(S, nkb);
+      const int pre = min(S, n_st);
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], p.a_bytes + B_BYTES);
-        tma_load_2d(sB + (size_t)i * B_BYTES, &tmB, &full[i], (kb0 + i) * BK, n0, pol_w);
+        const int hk = min(2, nkb - 2 * i);
+        mbar_arrive_expect_tx(&full[i], (uint32_t)(hk * half));
+        for (int h = 0; h < hk; ++h)
+          tma_load_2d(sB + (size_t)i * stride + h * half, &tmB, &full[i],
+                      (kb0 + 2 * i + h) * BK, n0, pol_w);
       }
       grid_dep_sync();
-      for (int i = 0; i < nkb; ++i) {
+      for (int i = 0; i < n_st; ++i) {
         const int s = i % S;
-        const int kx = (kb0 + i) * BK;
+        const int hk = min(2, nkb - 2 * i);
         if (i >= pre) {
           const uint32_t ph = (i / S) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
-          mbar_arrive_expect_tx(&full[s], p.a_bytes + B_BYTES);
-          tma_load_2d(sB + (size_t)s * B_BYTES, &tmB, &full[s], kx, n0, pol_w);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(hk * half));
+          for (int h = 0; h < hk; ++h)
+            tma_load_2d(sB + (size_t)s * stride + h * half, &tmB, &full[s],
+                        (kb0 + 2 * i + h) * BK, n0, pol_w);
         }
-        uint8_t* a_dst = sA + (size_t)s * p.a_bytes;
-        tma_load_2d(a_dst, ma, &full[s], kx, a_row0, pol_a);
-        if (p.merged)
-          tma_load_2d(a_dst + (size_t)p.box0 * BK * 2, &tmA1, &full[s], kx, 0, pol_a);
+        for (int h = 0; h < hk; ++h) {
+          const int kx = (kb0 + 2 * i + h) * BK;
+          uint8_t* a_dst = sA + (size_t)s * stride + h * half;
+          tma_load_2d(a_dst, ma, &full[s], kx, a_row0, pol_a);
+          if (p.merged)
+            tma_load_2d(a_dst + (size_t)p.box0 * BK * 2, &tmA1, &full[s], kx, 0, pol_a);
+        }
       }
     }
   } else if (warp == 1) {
     grid_dep_sync();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN, false);
-      for (int i = 0; i < nkb; ++i) {
+      // descriptors of stage 0, k-block 0; the others are address offsets
+      // (the start address field holds address / 16)
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
+      for (int i = 0; i < n_st; ++i) {
         const int s = i % S;
         const uint32_t ph = (i / S) & 1;
+        const int hk = min(2, nkb - 2 * i);
         if (!mbar_wait(&full[s], ph, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + (size_t)s * p.a_bytes);
-        const uint32_t b_base = smem_u32(sB + (size_t)s * B_BYTES);
+        for (int h = 0; h < hk; ++h) {
+          const uint32_t off = (uint32_t)(((size_t)s * stride + h * half) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
-          tc_mma_bf16(tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(tmem, a_desc0 + off + kk * 2, b_desc0 + off + kk * 2, idesc,
+                        (i > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&empty[s]);
       }
@@ -1187,14 +1206,14 @@ Geometry geometry(int epi, int rows0, int rows1, int n, int k, int q_cols, int n
   g.tiles = g.n_q_tiles * g.n_m0 + (g.n_tiles - g.n_q_tiles) * (g.n_m0 + g.n_m1);
   g.splits = choose_splits(g.tiles, g.n_kb, num_sms);
   const size_t b_bytes = (size_t)g.bn * BK * 2;
-  const size_t room = SMEM_LIMIT - SMEM_FIXED - (A_FULL - g.a_bytes);
-  g.stages = (int)std::min<size_t>(MAX_STAGES, room / (b_bytes + g.a_bytes));
+  // a stage holds two k-blocks
+  g.stages = (int)std::min<size_t>(MAX_STAGES,
+                                   (SMEM_LIMIT - SMEM_FIXED) / (2 * (b_bytes + g.a_bytes)));
   return g;
 }
 
 size_t smem_bytes(const Geometry& g) {
-  return SMEM_FIXED + (size_t)g.stages * ((size_t)g.bn * BK * 2 + g.a_bytes) +
-         (A_FULL - g.a_bytes);
+  return SMEM_FIXED + (size_t)g.stages * 2 * ((size_t)g.bn * BK * 2 + g.a_bytes);
 }
 
 template <int EPI, int BN>
@@ -1227,7 +1246,9 @@ int launch_swap(const GemmShape& s, int epi, void* c, int ldc, int num_sms, int*
   SwapPlan p{};
   p.rows = s.a0_rows;
   p.rb = (s.a0_rows + 15) / 16 * 16;
-  p.xb0 = std::min(p.rb, 256);
+  // above 256 rows: two MMA chunks of near-equal width (an MMA costs about
+  // max(N / 2, 64) cycles, so 144 + 128 beats 256 + 16)
+  p.xb0 = p.rb <= 256 ? p.rb : (p.rb / 2 + 15) / 16 * 16;
   p.xb1 = p.rb - p.xb0;
   p.n_kb = s.k / BK;
   const int tiles = s.n / BM;

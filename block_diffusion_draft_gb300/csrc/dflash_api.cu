@@ -475,7 +475,15 @@ int dflash_attn_reserve(dflash_attn* a, int max_batch, int max_rows, int max_key
                                     true),
             "scratch allocation");
   }
-  if (a->nL > 0) DF_CUDA(a->zbuf.ensure((size_t)max_rows * a->H * 4), "scratch allocation");
+  if (a->nL > 0) {
+    // the fc output slices of the largest row count that needs the most
+    size_t zb = (size_t)max_rows * a->H * 4;
+    if (a->dt == DFLASH_BF16)
+      for (int r = 1; r <= max_rows; ++r)
+        zb = std::max(zb, (size_t)gemm_f32_slices(r, a->H, a->nL * a->H, a->num_sms) * r *
+                              a->H * 4);
+    DF_CUDA(a->zbuf.ensure(zb), "scratch allocation");
+  }
   return DFLASH_OK;
 }
 
@@ -567,14 +575,19 @@ int dflash_ctx_project(dflash_attn* a, const void* x, int rows, void* y,
     return fail(DFLASH_ERR_ARG, "bf16 tensors must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int K = a->nL * a->H;
-  DF_CUDA(a->zbuf.ensure((size_t)rows * a->H * 4), "scratch allocation");
+  // bf16: the fc's K splits write one fp32 slice each, summed by the norm
+  const int n_sl = a->dt == DFLASH_BF16 ? gemm_f32_slices(rows, a->H, K, a->num_sms) : 1;
+  const size_t slice = (size_t)rows * a->H;
+  DF_CUDA(a->zbuf.ensure(n_sl * slice * 4), "scratch allocation");
   float* z = static_cast<float*>(a->zbuf.p);
   if (a->dt == DFLASH_BF16) {
     if (int r = ensure_gemm_scratch(a, EPI_F32, rows, 0, a->H, K, 0)) return r;
     GemmShape gs{x, rows, nullptr, 0, &a->tm_fc, &a->tm_fc256, a->H, K, 0};
+    GemmScratch scr = gemm_scratch(a);
+    scr.f32_slices = 1;
+    scr.slice_stride = slice;
     TraceScope tr(a, DFLASH_K_FC, s);
-    DF_CUDA(launch_gemm_bf16(gs, EPI_F32, z, a->H, nullptr, nullptr, gemm_scratch(a),
-                             a->num_sms, a->err, s),
+    DF_CUDA(launch_gemm_bf16(gs, EPI_F32, z, a->H, nullptr, nullptr, scr, a->num_sms, a->err, s),
             "fc launch");
   } else {
     TraceScope tr(a, DFLASH_K_FC, s);
@@ -584,7 +597,7 @@ int dflash_ctx_project(dflash_attn* a, const void* x, int rows, void* y,
   }
   TraceScope tr(a, DFLASH_K_NORM, s);
   DF_CUDA(launch_row_rmsnorm(z, rows, a->H, a->hidden_norm, a->cfg.rms_eps, y,
-                             a->dt == DFLASH_BF16, s),
+                             a->dt == DFLASH_BF16, n_sl, slice, s),
           "hidden_norm launch");
   return DFLASH_OK;
 }

@@ -66,6 +66,8 @@ struct Plan {
   int* counters;
   void* c;
   int* err;
+  int slices;           // EPI_F32: split `sp` writes its partial to slice sp of c
+  size_t slice_stride;  // floats between slices
 };
 
 // Units of one region (M_r m-tiles x N_r n-tiles x splits), ordered by
@@ -271,7 +273,7 @@ DF_DEV int checked_position(const QkvOut& qo, int pos_idx, int* err) {
 // columns starting at output column n0 for source row (src, srow).
 template <int EPI>
 DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, float* v,
-                       int src, int srow, int n0) {
+                       int src, int srow, int n0, size_t c_off = 0) {
   constexpr int BN = HD;
   constexpr int C4 = BN / 4;
   if constexpr (EPI == EPI_SWIGLU) {
@@ -288,7 +290,7 @@ DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, floa
     if constexpr (EPI == EPI_BF16) {
       store_bf16(reinterpret_cast<__nv_bfloat16*>(p.c) + (size_t)srow * p.ldc + n0, v, BN);
     } else {
-      float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) +
+      float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.c) + c_off +
                                              (size_t)srow * p.ldc + n0);
 #pragma unroll
       for (int c4 = 0; c4 < C4; ++c4)
@@ -678,8 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[c * 32 + i] = ok ? t[i] : 0.f;
       }
-      if (p.splits == 1) {
-        if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n0);
+      if (p.splits == 1 || p.slices) {
+        if (src >= 0)
+          finish_row<EPI>(p, qo, st, v, src, srow, n0, p.slices ? split * p.slice_stride : 0);
       } else if (src >= 0) {
         // park the valid rows in this CTA's (now idle) stage buffers, swizzled
         float4* red = reinterpret_cast<float4*>(smem);
@@ -691,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (p.splits > 1 && p.cluster) {
+  if (p.splits > 1 && p.cluster && !p.slices) {
     // The splits of this tile are one thread-block cluster.  Rank c sums the
     // valid rows r with r % splits == c from every rank's shared memory, in
     // rank order (so the result does not depend on timing), one row per warp.
@@ -912,6 +915,164 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- swapped, multicast
+// The fp32 fc output of 129 .. 384 token rows, written as per-split slices
+// that the following row norm sums.  Weights are the M = 128 operand and the
+// token rows N, as in gemm_swap_kernel.  MC weight tiles with the same K range
+// form a thread-block cluster.  Each CTA loads 1/MC of the token tile (P rows)
+// and multicasts it to the cluster, so an SM issues W + X / MC bytes per
+// k-block instead of W + X.  A stage is free again once every CTA of the
+// cluster has consumed it (its MMA commit arrives on the stage's empty barrier
+// in all of them).  No split merge: split sp writes slice sp of the output.
+struct SwapMcPlan {
+  int rows, rb, xb0, xb1;  // token rows, rows rounded to 16, the two MMA chunks
+  int part;                // token rows each CTA loads (a multiple of 8)
+  int tiles, n_kb, splits, stages;
+  uint32_t x_bytes;        // MC * part * 128 bytes of tokens per stage
+  uint32_t tmem_cols;
+  int ldc;
+  size_t slice_stride;
+  float* c;
+  int* err;
+};
+
+template <int MC>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_swapmc_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmW,
+                       const __grid_constant__ SwapMcPlan p) {
+  constexpr uint32_t W_BYTES = BM * BK * 2;
+  constexpr uint16_t kMask = (uint16_t)((1u << MC) - 1u);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint8_t* sW = smem;
+  uint8_t* sX = smem + (size_t)S * W_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + (size_t)S * p.x_bytes);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* accb = empty + MAX_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x % p.tiles, split = blockIdx.x / p.tiles;
+  const int rank = n_tile % MC;  // cluster rank: clusters are MC consecutive tiles
+  const int kb0 = (int)((long long)split * p.n_kb / p.splits);
+  const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
+  const int nkb = kb1 - kb0;
+  const int n0 = n_tile * BM;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], MC);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // every CTA's barriers exist before any multicast copy or commit reaches them
+  if (MC > 1) cluster_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t stage_bytes = W_BYTES + p.x_bytes;
+      // weights first: they do not depend on the previous kernel
+      const int pre = min(S, nkb);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], stage_bytes);
+        tma_load_2d(sW + (size_t)i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pol_w);
+      }
+      grid_dep_sync();
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        const int kx = (kb0 + i) * BK;
+        if (i >= pre) {
+          // every CTA of the cluster is done with stage s
+          if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          tma_load_2d(sW + (size_t)s * W_BYTES, &tmW, &full[s], kx, n0, pol_w);
+        }
+        uint8_t* x_dst = sX + (size_t)s * p.x_bytes + (size_t)rank * p.part * (BK * 2);
+        if (MC > 1)
+          tma_load_2d_mc(x_dst, &tmX, &full[s], kx, rank * p.part, kMask, pol_x);
+        else
+          tma_load_2d(x_dst, &tmX, &full[s], kx, 0, pol_x);
+      }
+    }
+  } else if (warp == 1) {
+    grid_dep_sync();
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_bf16(BM, p.xb0, false);
+      const uint32_t idesc1 = idesc_bf16(BM, p.xb1 > 0 ? p.xb1 : 16, false);
+      const uint64_t w_desc0 = sdesc_sw128(smem_u32(sW), 16, 1024);
+      const uint64_t x_desc0 = sdesc_sw128(smem_u32(sX), 16, 1024);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint64_t wd = w_desc0 + (((size_t)s * W_BYTES) >> 4);
+        const uint64_t xd = x_desc0 + (((size_t)s * p.x_bytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tmem, wd + kk * 2, xd + kk * 2, idesc0, acc);
+          if (p.xb1 > 0)
+            tc_mma_bf16(tmem + (uint32_t)p.xb0, wd + kk * 2,
+                        xd + ((uint32_t)p.xb0 * BK * 2 >> 4) + kk * 2, idesc1, acc);
+        }
+        if (MC > 1)
+          tc_commit_mc(&empty[s], kMask);
+        else
+          tc_commit(&empty[s]);
+      }
+      tc_commit(accb);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    grid_dep_sync();
+    const int q = warp & 3;
+    const int j = q * 32 + lane;  // weight row of the tile = output column n0 + j
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
+    tc_fence_after();
+    float* out = p.c + (size_t)split * p.slice_stride + n0 + j;
+    for (int t0 = 0; t0 < p.rb; t0 += 32) {
+      float v[32];
+      tmem_ld32(trow + (uint32_t)t0, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int t = t0 + i;
+        if (t >= p.rows) break;
+        out[(size_t)t * p.ldc] = ok ? v[i] : 0.f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // no CTA leaves while a peer's copies or commits may still reach it (each
+  // CTA has seen its own last commit complete)
+  if (MC > 1) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
 // ---------------------------------------------------------------- large M
 // Persistent variant for calls with many token rows: one CTA per SM walks
 // its share of 128 x 256 output tiles (round-robin over the grouped order).
@@ -1054,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int src, srow;
       row_source(p, m, r, src, srow);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
-      const bool whole = p.splits == 1;
+      const bool whole = p.splits == 1 || p.slices;
       // split units: sums of the valid rows go to the (tile, split) slot,
       // laid out [column chunk of 4][row] so a warp's access is contiguous
       float4* my_part =
@@ -1076,7 +1237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&acc_empty[buf]);
         }
         if (whole) {
-          if (src >= 0) finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
+          if (src >= 0)
+            finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD,
+                            p.slices ? sp * p.slice_stride : 0);
         } else if (src >= 0) {
 #pragma unroll
           for (int c4 = 0; c4 < HD / 4; ++c4)
@@ -1285,6 +1448,52 @@ int launch_swap(const GemmShape& s, int epi, void* c, int ldc, int num_sms, int*
   return (int)e;
 }
 
+// the multicast fc kernel takes one-source F32 calls of 129 .. 384 rows whose
+// weight tiles pair up into clusters
+bool use_swapmc(int epi, int rows0, int rows1, int n, bool slices) {
+  return slices && epi == EPI_F32 && use_swap(epi, rows0, rows1, n) && (n / BM) % 2 == 0;
+}
+
+int launch_swapmc(const GemmShape& s, float* c, int ldc, size_t slice_stride, int num_sms,
+                  int* err, cudaStream_t stream) {
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!done_on_device(attr_done)) {
+    cudaFuncSetAttribute(gemm_swapmc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_LIMIT);
+    cudaFuncSetAttribute(gemm_swapmc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_LIMIT);
+    mark_device(attr_done);
+  }
+  SwapMcPlan p{};
+  p.rows = s.a0_rows;
+  p.rb = (s.a0_rows + 15) / 16 * 16;
+  p.xb0 = p.rb <= 256 ? p.rb : (p.rb / 2 + 15) / 16 * 16;
+  p.xb1 = p.rb - p.xb0;
+  p.tiles = s.n / BM;
+  p.n_kb = s.k / BK;
+  p.splits = choose_splits(p.tiles, p.n_kb, num_sms);
+  const int mc = p.tiles % 4 == 0 ? 4 : 2;
+  p.part = ((p.rb + mc - 1) / mc + 7) / 8 * 8;
+  p.x_bytes = (uint32_t)(mc * p.part * BK * 2);
+  const size_t stage = (size_t)BM * BK * 2 + p.x_bytes;
+  p.stages = (int)std::min<size_t>(MAX_STAGES, (SMEM_LIMIT - SMEM_FIXED) / stage);
+  if (p.stages < 2 || p.part > 256) return cudaErrorInvalidValue;
+  p.tmem_cols = p.rb <= 256 ? 256u : 512u;
+  p.ldc = ldc;
+  p.slice_stride = slice_stride;
+  p.c = c;
+  p.err = err;
+  CUtensorMap mx;
+  if (make_tmap_bf16_rows(&mx, s.a0, s.a0_rows, s.k, p.part) != 0) return cudaErrorInvalidValue;
+  const size_t smem = SMEM_FIXED + (size_t)p.stages * stage;
+  const dim3 grid(p.tiles * p.splits), block(kThreads);
+  if (mc == 4)
+    return (int)launch_pdl_cluster(gemm_swapmc_kernel<4>, grid, block, smem, stream, 4u, mx,
+                                   *s.b_map, p);
+  return (int)launch_pdl_cluster(gemm_swapmc_kernel<2>, grid, block, smem, stream, 2u, mx,
+                                 *s.b_map, p);
+}
+
 int big_tiles(int rows0, int rows1, int n, int q_cols) {
   const int m0 = (rows0 + BM - 1) / BM, m1 = (rows1 + BM - 1) / BM;
   return (q_cols / BNB) * m0 + (n / BNB - q_cols / BNB) * (m0 + m1);
@@ -1359,6 +1568,13 @@ size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_col
   return (size_t)dense_tiles * g.splits * BM * g.bn * sizeof(float);
 }
 
+int gemm_f32_slices(int rows, int n, int k, int num_sms) {
+  if (use_swapmc(EPI_F32, rows, 0, n, true)) return choose_splits(n / BM, k / BK, num_sms);
+  if (use_swap(EPI_F32, rows, 0, n)) return 1;
+  if (use_big(rows, 0, n, 0)) return big_splits(big_tiles(rows, 0, n, 0), k / BK, num_sms);
+  return geometry(EPI_F32, rows, 0, n, k, 0, num_sms).splits;
+}
+
 int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
                      const QkvOut* qkv, const SeqTable* seqs,
                      const GemmScratch& scr, int num_sms, int* err,
@@ -1372,6 +1588,8 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
     mark_device(attr_done);
   }
   if (s.k % BK != 0) return cudaErrorInvalidValue;
+  if (use_swapmc(epi, s.a0_rows, s.a1_rows, s.n, scr.f32_slices != 0))
+    return launch_swapmc(s, static_cast<float*>(c), ldc, scr.slice_stride, num_sms, err, stream);
   if (use_swap(epi, s.a0_rows, s.a1_rows, s.n))
     return launch_swap(s, epi, c, ldc, num_sms, err, stream);
   if (use_big(s.a0_rows, s.a1_rows, s.n, s.q_cols))
@@ -1385,11 +1603,13 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   p.n_m0 = g.n_m0;
   p.n_m1 = g.n_m1;
   p.merged = g.merged;
-  // plain epilogues merge splits in a cluster; the QKV epilogue (heavier,
-  // and 3-CTA clusters schedule poorly behind the previous kernel) merges
-  // through global partials
-  p.cluster = epi != EPI_QKV;
-  if (g.splits > 1 && !p.cluster) {
+  // plain epilogues merge splits in a cluster (or, F32 with slices, write
+  // one slice per split); the QKV epilogue (heavier, and 3-CTA clusters
+  // schedule poorly behind the previous kernel) merges through global partials
+  p.slices = epi == EPI_F32 && scr.f32_slices && g.splits > 1;
+  p.slice_stride = scr.slice_stride;
+  p.cluster = epi != EPI_QKV && !p.slices;
+  if (g.splits > 1 && !p.cluster && !p.slices) {
     const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * g.bn * 4;
     if (scr.partial == nullptr || scr.partial_bytes < need ||
         scr.n_counters < g.n_tiles * (g.n_m0 + g.n_m1))
@@ -1484,7 +1704,9 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
   p.units_q = p.n_q_tiles * p.splits * p.n_m0;
   const int units = tiles * p.splits;
   p.grid = std::min(units, num_sms);
-  if (p.splits > 1) {
+  p.slices = epi == EPI_F32 && scr.f32_slices && p.splits > 1;
+  p.slice_stride = scr.slice_stride;
+  if (p.splits > 1 && !p.slices) {
     const int dense = p.n_tiles * (p.n_m0 + p.n_m1);
     if (scr.partial == nullptr || scr.n_counters < dense ||
         scr.partial_bytes < (size_t)dense * p.splits * BM * BNB * sizeof(float))

@@ -131,8 +131,13 @@ struct GemmShape {
 };
 
 struct GemmScratch {
-  float* partial; size_t partial_bytes;
-  int* counters; int n_counters;
+  float* partial = nullptr; size_t partial_bytes = 0;
+  int* counters = nullptr; int n_counters = 0;
+  // EPI_F32 only: 1 = every K split writes its fp32 partial to its own slice
+  // of the output (c + split * slice_stride floats) instead of merging them;
+  // gemm_f32_slices() gives the number of slices
+  int f32_slices = 0;
+  size_t slice_stride = 0;
 };
 
 int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
@@ -141,6 +146,9 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
                      cudaStream_t st);
 size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_cols,
                           int num_sms, int* n_counters);
+// slices an EPI_F32 launch of one source of `rows` rows writes when
+// GemmScratch::f32_slices is set (1: it merges its splits itself)
+int gemm_f32_slices(int rows, int n, int k, int num_sms);
 int make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, long long rows,
                         int cols, int box_rows);
 
@@ -212,8 +220,11 @@ int launch_attn_bf16(const AttnArgs& a, const AttnSeqs* seqs, const void* qbuf,
 // ----------------------------------------------------------- small kernels
 int launch_rope_table(float2* tab, int max_pos, int half, float theta,
                       cudaStream_t st);
+// out = w * x / rms(x) per row, x = z[0] + z[1] + ... (n_slices slices of
+// slice_stride floats, summed in slice order)
 int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
-                       float eps, void* out, int out_bf16, cudaStream_t st);
+                       float eps, void* out, int out_bf16, int n_slices,
+                       size_t slice_stride, cudaStream_t st);
 int launch_to_f32(const void* src, int src_bf16, float* dst, size_t n,
                   cudaStream_t st);
 // sum_out = a + b (b may be null), norm_out = w * sum / rms(sum); bf16 rows,

@@ -24,14 +24,16 @@ __global__ void rope_table_kernel(float2* tab, int max_pos, int half,
   }
 }
 
-// out[r] = w * z[r] / sqrt(mean(z[r]^2) + eps): one CTA per row, the row
-// held in registers (up to kNormVec float4 per thread), one reduction.
+// out[r] = w * x / sqrt(mean(x^2) + eps) with x = z[r] summed over the
+// slices in slice order (the K splits of the fc projection): one CTA per
+// row, the row held in registers (up to kNormVec float4 per thread), one
+// reduction.
 constexpr int kNormThreads = 512;
 constexpr int kNormVec = 8;  // cols <= 512 * 4 * 8 = 16384
 
 __global__ void __launch_bounds__(kNormThreads)
     row_rmsnorm_kernel(const float* z, int cols, const float* w, float eps, void* out,
-                       int out_bf16) {
+                       int out_bf16, int n_slices, size_t slice_stride) {
   grid_dep_sync();
   const float4* zr = reinterpret_cast<const float4*>(z + (size_t)blockIdx.x * cols);
   const int n4 = cols / 4;
@@ -41,6 +43,14 @@ __global__ void __launch_bounds__(kNormThreads)
   for (int i = 0; i < kNormVec; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
     x[i] = c < n4 ? __ldcg(zr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 1; sl < n_slices; ++sl) {
+      if (c >= n4) break;
+      const float4 t = __ldcg(zr + sl * (slice_stride / 4) + c);
+      x[i].x += t.x;
+      x[i].y += t.y;
+      x[i].z += t.z;
+      x[i].w += t.w;
+    }
     ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
   }
   __shared__ float red[kNormThreads / 32];
@@ -222,11 +232,14 @@ int launch_rope_table(float2* tab, int max_pos, int half, float theta,
 }
 
 int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
-                       float eps, void* out, int out_bf16, cudaStream_t st) {
+                       float eps, void* out, int out_bf16, int n_slices,
+                       size_t slice_stride, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  if (cols % 4 != 0 || cols > kNormThreads * 4 * kNormVec) return cudaErrorInvalidValue;
+  if (cols % 4 != 0 || cols > kNormThreads * 4 * kNormVec || n_slices < 1 ||
+      (n_slices > 1 && slice_stride % 4 != 0))
+    return cudaErrorInvalidValue;
   return launch_pdl(row_rmsnorm_kernel, dim3(rows), dim3(kNormThreads), 0, st, z, cols, w,
-                    eps, out, out_bf16);
+                    eps, out, out_bf16, n_slices, slice_stride);
 }
 
 int launch_add_rmsnorm(const void* a, const void* b, int rows, int cols, const float* w,

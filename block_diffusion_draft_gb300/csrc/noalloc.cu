@@ -116,7 +116,7 @@ extern "C" int dflash_ctx_project_noalloc(dflash_attn* a, const void* x, int row
   }
   if (e == cudaSuccess)
     e = (cudaError_t)df::launch_row_rmsnorm(z, rows, a->H, a->hidden_norm, a->cfg.rms_eps,
-                                            y, bf, s);
+                                            y, bf, 1, 0, s);
   if (e != cudaSuccess) return dflash_noalloc_fail(DFLASH_ERR_CUDA, cudaGetErrorString(e));
   return DFLASH_OK;
 }

@@ -136,6 +136,18 @@ DF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
       : "memory");
 }
 
+// The same load multicast to the CTAs of `cta_mask` in this thread-block
+// cluster: the box lands at the same shared-memory offset in each of them, and
+// each one's mbarrier at `bar`'s offset receives the transaction bytes.
+DF_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                           uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::"
+      "cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
+      : "memory");
+}
+
 // 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
 // into shared memory, completion signalled on `bar` as transaction bytes
 DF_DEV void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -186,6 +198,16 @@ DF_DEV void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// the same, arriving once on the mbarrier at `bar`'s offset in every CTA of
+// `cta_mask` in this thread-block cluster
+DF_DEV void tc_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster."
+      "b64 [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 

@@ -130,49 +130,66 @@ DF_DEV void write_partial(const AttnArgs& a, int slot, int row, const float (&o)
 }
 
 // Log-sum-exp merge of rows [r0, r1) over the n partial slots slot0 + i *
-// stride: warp wq of the four softmax warps takes rows r0 + wq, r0 + wq + 4,
-// ...; lane l holds columns 4l .. 4l+3.  Sources are summed in slot order
-// (the result does not depend on which CTA merges, nor when), each rescaled
-// to the largest running max.  The merged row goes to the output as the
-// normalised bf16 row, or (block_slot >= 0) unnormalised with its max and
+// stride, by the 128 softmax threads: thread et takes item et, et + 128, ...
+// of (row, 64-column half), so that every row advances at once (one round
+// trip to L2 per source, not per source and row).  Sources are summed in slot
+// order (the result does not depend on which CTA merges, nor when), each
+// rescaled to the largest running max.  The merged row goes to the output as
+// the normalised bf16 row, or (block_slot >= 0) unnormalised with its max and
 // sum into that slot.
 DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, int n, int r0,
-                       int r1, int block_slot, int wq, int lane) {
-  for (int row = r0 + wq; row < r1; row += 4) {
+                       int r1, int block_slot, int et) {
+  for (int item = et; item < (r1 - r0) * 2; item += 128) {
+    const int row = r0 + (item >> 1), hf = item & 1;
     float M = -INFINITY;
     for (int i = 0; i < n; ++i)
       M = fmaxf(M, __ldcg(a.part_ml + (size_t)(slot0 + i * stride) * 256 + row));
     float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-#pragma unroll 4
       for (int i = 0; i < n; ++i) {
         const size_t sl = (size_t)(slot0 + i * stride);
         const float m = __ldcg(a.part_ml + sl * 256 + row);
         const float l = __ldcg(a.part_ml + sl * 256 + 128 + row);
-        const float4 t =
-            __ldcg(reinterpret_cast<const float4*>(a.part_o + (sl * 128 + row) * HD) + lane);
+        const float4* src =
+            reinterpret_cast<const float4*>(a.part_o + (sl * 128 + row) * HD) + hf * 16;
+        float4 t[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) t[c] = __ldcg(src + c);
         const float f = m == -INFINITY ? 0.f : fast_exp2(m - M);
         L += f * l;
-        acc.x += f * t.x;
-        acc.y += f * t.y;
-        acc.z += f * t.z;
-        acc.w += f * t.w;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          acc[c].x += f * t[c].x;
+          acc[c].y += f * t[c].y;
+          acc[c].z += f * t[c].z;
+          acc[c].w += f * t[c].w;
+        }
       }
     }
     if (block_slot >= 0) {
-      __stcg(reinterpret_cast<float4*>(a.part_o + ((size_t)block_slot * 128 + row) * HD) + lane,
-             acc);
-      if (lane == 0) {
+      float4* dst =
+          reinterpret_cast<float4*>(a.part_o + ((size_t)block_slot * 128 + row) * HD) + hf * 16;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) __stcg(dst + c, acc[c]);
+      if (hf == 0) {
         __stcg(a.part_ml + (size_t)block_slot * 256 + row, M);
         __stcg(a.part_ml + (size_t)block_slot * 256 + 128 + row, L);
       }
     } else {
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint2 pk;
-      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      reinterpret_cast<uint2*>(out_row(a, w, row))[lane] = pk;
+      uint4* dst = reinterpret_cast<uint4*>(out_row(a, w, row)) + hf * 8;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 pk;
+        pk.x = pack_bf16x2(acc[2 * c].x * inv, acc[2 * c].y * inv);
+        pk.y = pack_bf16x2(acc[2 * c].z * inv, acc[2 * c].w * inv);
+        pk.z = pack_bf16x2(acc[2 * c + 1].x * inv, acc[2 * c + 1].y * inv);
+        pk.w = pack_bf16x2(acc[2 * c + 1].z * inv, acc[2 * c + 1].w * inv);
+        dst[c] = pk;
+      }
     }
   }
 }
@@ -581,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const bool writer = real && (!DUAL || r < 64);
-    const int et = threadIdx.x - 64, wq = warp - 2;
+    const int et = threadIdx.x - 64;
     if (w.ns == 1) {
       // the unit covers every key of its rows: the normalised row
       if (writer) {
@@ -615,18 +632,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rpo = (w.rows + C - 1) / C;
         const int r0 = min(w.rows, rank * rpo), r1 = min(w.rows, r0 + rpo);
         if (a.k_clusters == 1) {
-          merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, -1, wq, lane);
+          merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, -1, et);
         } else {
           merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, a.n_units + (int)blockIdx.x,
-                     wq, lane);
+                     et);
           int* cnt = a.counters + ((size_t)(w.b * a.n_kv + w.h) * C + rank);
           if (last_arrival(cnt, a.k_clusters, et, last_flag))
-            merge_rows(a, w, a.n_units + w.pair_unit0 + rank, C, a.k_clusters, r0, r1, -1, wq,
-                       lane);
+            merge_rows(a, w, a.n_units + w.pair_unit0 + rank, C, a.k_clusters, r0, r1, -1, et);
         }
       } else if (last_arrival(a.counters + (w.b * a.n_kv + w.h), w.ns, et, last_flag)) {
         // the pair's last split to finish merges all of its rows
-        merge_rows(a, w, w.pair_unit0, 1, w.ns, 0, w.rows, -1, wq, lane);
+        merge_rows(a, w, w.pair_unit0, 1, w.ns, 0, w.rows, -1, et);
       }
     }
   }
@@ -1077,32 +1093,33 @@ int plan_decode_attention(AttnSeqs& sq, int batch, int n_kv, int num_sms, bool d
   }
   *cluster = 1;
   *k_clusters = 1;
-  // few pairs with few tiles each: C splits per cluster, k clusters per pair,
-  // every cluster resident at once, about one unit per SM and at least two
-  // tiles per unit (pairs with more than 8 tiles per split balance better as
-  // independent units)
-  int C = 8, fit = 0;
-  for (; C >= 2; C >>= 1) {
-    if ((long long)pairs * C > num_sms || C > max_np || max_np > 8 * C) continue;
-    fit = max_active_clusters(C, dual) / pairs;
-    if (fit >= 1) break;
-  }
-  if (C >= 2 && fit >= 1) {
+  // Estimated makespans in tile times (about 1.2 us each at the HBM share of
+  // an SM): a unit costs its tiles plus two for its start; a split pair's
+  // merge costs about one round trip to L2 per merged source (~0.5 tile) plus
+  // the arrival, done by the last split alone; a cluster's merge is spread
+  // over its ranks (about three tiles whatever C).  The weights are fitted to
+  // the measured single-sequence, serving and long-context steps.
+  //
+  // Few pairs: C splits per cluster, k clusters per pair, every cluster
+  // resident at once, about one unit per SM and at least two tiles per unit.
+  int best_C = 0, best_k = 1;
+  double t_cluster = 1e300;
+  for (int C = 8; C >= 2; C >>= 1) {
+    if ((long long)pairs * C > num_sms || C > max_np) continue;
+    const int fit = max_active_clusters(C, dual) / pairs;
+    if (fit < 1) continue;
     const int k = std::max(1, std::min({fit, num_sms / (pairs * C), max_np / (2 * C)}));
-    *cluster = C;
-    *k_clusters = k;
-    sq.unit_off[0] = 0;
-    for (int b = 0; b < batch; ++b) {
-      sq.n_split[b] = C * k;
-      sq.order[b] = b;
-      sq.unit_off[b + 1] = sq.unit_off[b] + n_kv * C * k;
+    // several clusters per pair add a second merge through L2 after the
+    // cluster merge (measured: eight tile times more than one cluster)
+    const double t = (double)((max_np + C * k - 1) / (C * k)) + 2.0 + 3.0 + (k > 1 ? 8.0 : 0.0);
+    if (t < t_cluster - 1e-9) {
+      t_cluster = t;
+      best_C = C;
+      best_k = k;
     }
-    return sq.unit_off[batch];
   }
-  // many pairs: units of at most U tiles for about m units per SM; keep the
-  // m whose list-scheduling makespan (units dispatched largest first, each
-  // costing its tiles plus a start-up of two tiles and one tile for a merge)
-  // is shortest
+  // Many pairs: units of at most U tiles for about m units per SM, dispatched
+  // largest first; list scheduling gives the makespan of each m.
   std::vector<int> best_ns(batch, 1), ns(batch);
   double best_t = 1e300;
   for (int m = 1; m <= 4; ++m) {
@@ -1116,7 +1133,7 @@ int plan_decode_attention(AttnSeqs& sq, int batch, int n_kv, int num_sms, bool d
     if (units > (long long)decode_attention_slots(batch, n_kv, num_sms)) continue;
     std::vector<std::pair<double, int>> groups(batch);
     for (int b = 0; b < batch; ++b)
-      groups[b] = {(double)np[b] / ns[b] + 2.0 + (ns[b] > 1 ? 1.0 : 0.0), b};
+      groups[b] = {(double)np[b] / ns[b] + 2.0 + (ns[b] > 1 ? 1.0 + 0.5 * ns[b] : 0.0), b};
     std::sort(groups.begin(), groups.end(), [](const auto& x, const auto& y) {
       return x.first > y.first || (x.first == y.first && x.second < y.second);
     });
@@ -1134,6 +1151,17 @@ int plan_decode_attention(AttnSeqs& sq, int batch, int n_kv, int num_sms, bool d
       best_t = t;
       best_ns = ns;
     }
+  }
+  if (best_C > 0 && t_cluster <= best_t) {
+    *cluster = best_C;
+    *k_clusters = best_k;
+    sq.unit_off[0] = 0;
+    for (int b = 0; b < batch; ++b) {
+      sq.n_split[b] = best_C * best_k;
+      sq.order[b] = b;
+      sq.unit_off[b + 1] = sq.unit_off[b] + n_kv * best_C * best_k;
+    }
+    return sq.unit_off[batch];
   }
   std::vector<std::pair<double, int>> order(batch);
   for (int b = 0; b < batch; ++b) {

@@ -80,12 +80,11 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
-// Residual add + RMSNorm of a decoder layer, one CTA per row: r = a (+ b),
-// (sum_out may alias a or b: each element is read before it is written, by
-// the same thread)
-// stored bf16 (the residual stream), and w * r / sqrt(mean(r^2) + eps) of the
-// stored (bf16) r, also bf16.  Each thread holds up to kAddNormVec groups of 8
-// columns.
+// Residual add + RMSNorm of a decoder layer, one CTA per row: r = a (+ b)
+// in fp32, stored bf16 (the residual stream; sum_out may alias a or b: each
+// element is read before it is written, by the same thread), and
+// w * r / sqrt(mean(r^2) + eps) of the fp32 r, stored bf16.  Each thread
+// holds up to kAddNormVec groups of 8 columns.
 constexpr int kAddNormThreads = 256;
 constexpr int kAddNormVec = 4;  // cols <= 256 * 8 * 4 = 8192
 
@@ -119,14 +118,15 @@ __global__ void __launch_bounds__(kAddNormThreads)
           f[2 * e + 1] += __high2float(pb[e]);
         }
       }
+      // the residual stream is stored in bf16; the norm takes the fp32 sum
+      // (one rounding fewer on the path into the projections)
       uint4 vr;
       uint32_t* pr = reinterpret_cast<uint32_t*>(&vr);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         pr[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&pr[e]);
-        x[i][2 * e] = __low2float(h);
-        x[i][2 * e + 1] = __high2float(h);
+        x[i][2 * e] = f[2 * e];
+        x[i][2 * e + 1] = f[2 * e + 1];
         ss += x[i][2 * e] * x[i][2 * e] + x[i][2 * e + 1] * x[i][2 * e + 1];
       }
       sum_out[row + c] = vr;

@@ -94,15 +94,15 @@ def assert_close_stream(gpu, ref, what):
         f"{what}: scaled max={scaled:.3e} rel_l2={rel:.3e}"
 
 
-# The decoder-layer MLP output passes three bf16 roundings in series (the
-# post-norm input, the SwiGLU activation, the output) and the gate x up
-# product doubles the first: with independent roundings (relative RMS
-# 2^-9/sqrt(3) each) that is 2^-9/sqrt(3) * sqrt(4 + 1 + 1) ~ 2.8e-3, and the
-# SiLU gate correlates them (measured 4.2e-3 .. 4.9e-3 against the fp64
-# oracle; 1.7e-3 against the oracle with y and the activation rounded to
-# bf16).  Bounds for it: relative L2 7.5e-3, max-abs 3e-2 scaled as in
-# assert_close_stream.
-MLP_MAX_ABS, MLP_REL_L2 = 3e-2, 7.5e-3
+# The decoder-layer MLP output passes two bf16 roundings in series before
+# its own (the post-norm input and the SwiGLU activation; the post norm takes
+# the fp32 residual sum), and the gate x up product doubles the first.  Its
+# values reach |y| ~ 10, where half a bf16 ulp is 3.1e-2, and each element's
+# rounding error follows the output's RMS rather than its own value.  So the
+# max-abs bound (3e-2) applies per element relative to max(1, |ref|,
+# rms(ref)), as for the residual stream; the relative L2 bound is the bf16
+# one (5e-3).
+MLP_MAX_ABS, MLP_REL_L2 = 3e-2, 5e-3
 
 
 def assert_close_mlp(gpu, ref, what):

@@ -130,38 +130,40 @@ DF_DEV void write_partial(const AttnArgs& a, int slot, int row, const float (&o)
 }
 
 // Log-sum-exp merge of rows [r0, r1) over the n partial slots slot0 + i *
-// stride, by the 128 softmax threads: thread et takes item et, et + 128, ...
-// of (row, 64-column half), so that every row advances at once (one round
-// trip to L2 per source, not per source and row).  Sources are summed in slot
-// order (the result does not depend on which CTA merges, nor when), each
-// rescaled to the largest running max.  The merged row goes to the output as
-// the normalised bf16 row, or (block_slot >= 0) unnormalised with its max and
-// sum into that slot.
-DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, int n, int r0,
-                       int r1, int block_slot, int et) {
-  for (int item = et; item < (r1 - r0) * 2; item += 128) {
-    const int row = r0 + (item >> 1), hf = item & 1;
+// stride, by the 128 softmax threads: thread et takes items et, et + 128, ...
+// of (row, chunk of NC4 * 4 columns), so that every row advances at once (one
+// round trip to L2 per source, not per source and row).  Sources are summed
+// in slot order (the result does not depend on which CTA merges, nor when),
+// each rescaled to the largest running max.  The merged row goes to the
+// output as the normalised bf16 row, or (block_slot >= 0) unnormalised with
+// its max and sum into that slot.
+template <int NC4>
+DF_DEV void merge_rows_t(const AttnArgs& a, const Unit& w, int slot0, int stride, int n,
+                         int r0, int r1, int block_slot, int et) {
+  constexpr int CH = HD / (4 * NC4);  // chunks per row
+  for (int item = et; item < (r1 - r0) * CH; item += 128) {
+    const int row = r0 + item / CH, ch = item % CH;
     float M = -INFINITY;
     for (int i = 0; i < n; ++i)
       M = fmaxf(M, __ldcg(a.part_ml + (size_t)(slot0 + i * stride) * 256 + row));
     float L = 0.f;
-    float4 acc[16];
+    float4 acc[NC4];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < NC4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
       for (int i = 0; i < n; ++i) {
         const size_t sl = (size_t)(slot0 + i * stride);
         const float m = __ldcg(a.part_ml + sl * 256 + row);
         const float l = __ldcg(a.part_ml + sl * 256 + 128 + row);
         const float4* src =
-            reinterpret_cast<const float4*>(a.part_o + (sl * 128 + row) * HD) + hf * 16;
-        float4 t[16];
+            reinterpret_cast<const float4*>(a.part_o + (sl * 128 + row) * HD) + ch * NC4;
+        float4 t[NC4];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) t[c] = __ldcg(src + c);
+        for (int c = 0; c < NC4; ++c) t[c] = __ldcg(src + c);
         const float f = m == -INFINITY ? 0.f : fast_exp2(m - M);
         L += f * l;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < NC4; ++c) {
           acc[c].x += f * t[c].x;
           acc[c].y += f * t[c].y;
           acc[c].z += f * t[c].z;
@@ -170,19 +172,19 @@ DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, 
       }
     }
     if (block_slot >= 0) {
-      float4* dst =
-          reinterpret_cast<float4*>(a.part_o + ((size_t)block_slot * 128 + row) * HD) + hf * 16;
+      float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)block_slot * 128 + row) * HD) +
+                    ch * NC4;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) __stcg(dst + c, acc[c]);
-      if (hf == 0) {
+      for (int c = 0; c < NC4; ++c) __stcg(dst + c, acc[c]);
+      if (ch == 0) {
         __stcg(a.part_ml + (size_t)block_slot * 256 + row, M);
         __stcg(a.part_ml + (size_t)block_slot * 256 + 128 + row, L);
       }
     } else {
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(out_row(a, w, row)) + hf * 8;
+      uint4* dst = reinterpret_cast<uint4*>(out_row(a, w, row) + ch * NC4 * 4);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < NC4 / 2; ++c) {
         uint4 pk;
         pk.x = pack_bf16x2(acc[2 * c].x * inv, acc[2 * c].y * inv);
         pk.y = pack_bf16x2(acc[2 * c].z * inv, acc[2 * c].w * inv);
@@ -192,6 +194,20 @@ DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, 
       }
     }
   }
+}
+
+// the chunk width that keeps the 128 threads busy for the given row count
+DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, int n, int r0,
+                       int r1, int block_slot, int et) {
+  const int rows = r1 - r0;
+  if (rows >= 64)
+    merge_rows_t<16>(a, w, slot0, stride, n, r0, r1, block_slot, et);
+  else if (rows >= 32)
+    merge_rows_t<8>(a, w, slot0, stride, n, r0, r1, block_slot, et);
+  else if (rows >= 16)
+    merge_rows_t<4>(a, w, slot0, stride, n, r0, r1, block_slot, et);
+  else
+    merge_rows_t<2>(a, w, slot0, stride, n, r0, r1, block_slot, et);
 }
 
 // Called by the 128 softmax threads after their partial stores: counts this

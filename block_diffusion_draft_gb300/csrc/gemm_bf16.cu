@@ -1094,11 +1094,17 @@ DF_DEV void big_unit(const Plan& p, int u, int& m, int& n, int& split, int& k0, 
   tile_id = n * (p.n_m0 + p.n_m1) + m;
 }
 
-template <int EPI>
+// MC = 2: CTAs 2c and 2c+1 form a cluster and take units 2j and 2j+1 (the
+// same weight tile and K split, m-tiles m and m+1; m-tile counts are padded
+// to even, a padded tile's rows store nothing).  Each loads its own A tile and
+// half of the 256-row weight tile, multicast to both, so an SM issues 32 KB
+// of the 48 KB a k-block needs; a stage is free once both have consumed it.
+template <int EPI, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_big_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmBh,
                     const __grid_constant__ Plan p,
                     const __grid_constant__ QkvOut qo,
                     const __grid_constant__ SeqTable st) {
@@ -1121,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES_BIG; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -1131,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA0);
     prefetch_tmap(&tmA1);
-    prefetch_tmap(&tmB);
+    prefetch_tmap(MC > 1 ? &tmBh : &tmB);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -1140,6 +1146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // both CTAs' barriers exist before any multicast copy or commit reaches them
+  if (MC > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
   grid_dep_sync();
 
@@ -1164,7 +1172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&full[s], A_FULL + B_BIG);
           tma_load_2d(sA + s * A_FULL, ma, &full[s], kb * BK, a_row0, pol_a);
-          tma_load_2d(sB + s * B_BIG, &tmB, &full[s], kb * BK, n * BNB, pol_w);
+          if (MC > 1) {
+            const int rk = (int)(blockIdx.x & 1);
+            tma_load_2d_mc(sB + s * B_BIG + rk * (B_BIG / 2), &tmBh, &full[s], kb * BK,
+                           n * BNB + rk * (BNB / 2), (uint16_t)3, pol_w);
+          } else {
+            tma_load_2d(sB + s * B_BIG, &tmB, &full[s], kb * BK, n * BNB, pol_w);
+          }
         }
       }
     }
@@ -1195,7 +1209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_bf16(d, sdesc_sw128(a_base + kk * 32, 16, 1024),
                         sdesc_sw128(b_base + kk * 32, 16, 1024), idesc,
                         (kb > k0 || kk > 0) ? 1u : 0u);
-          tc_commit(&empty[s]);
+          if (MC > 1)
+            tc_commit_mc(&empty[s], (uint16_t)3);
+          else
+            tc_commit(&empty[s]);
         }
         tc_commit(&acc_full[buf]);
       }
@@ -1287,6 +1304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer's copies or commits may still reach it
+  if (MC > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -1494,8 +1513,19 @@ int launch_swapmc(const GemmShape& s, float* c, int ldc, size_t slice_stride, in
                                  *s.b_map, p);
 }
 
+// m-tiles of the persistent kernel's two sources, padded so that both of its
+// regions (block-row tiles; all tiles) hold an even count: the kernel's CTA
+// pairs take m-tiles two at a time
+void big_m_tiles(int rows0, int rows1, int* m0, int* m1) {
+  *m0 = (rows0 + BM - 1) / BM;
+  *m1 = (rows1 + BM - 1) / BM;
+  if (*m0 % 2) ++*m0;
+  if ((*m0 + *m1) % 2) ++*m1;
+}
+
 int big_tiles(int rows0, int rows1, int n, int q_cols) {
-  const int m0 = (rows0 + BM - 1) / BM, m1 = (rows1 + BM - 1) / BM;
+  int m0, m1;
+  big_m_tiles(rows0, rows1, &m0, &m1);
   return (q_cols / BNB) * m0 + (n / BNB - q_cols / BNB) * (m0 + m1);
 }
 
@@ -1551,7 +1581,9 @@ size_t gemm_scratch_bytes(int epi, int rows0, int rows1, int n, int k, int q_col
   if (use_big(rows0, rows1, n, q_cols)) {
     const int tiles = big_tiles(rows0, rows1, n, q_cols);
     const int splits = big_splits(tiles, k / BK, num_sms);
-    const int dense = (n / BNB) * ((rows0 + BM - 1) / BM + (rows1 + BM - 1) / BM);
+    int m0, m1;
+    big_m_tiles(rows0, rows1, &m0, &m1);
+    const int dense = (n / BNB) * (m0 + m1);
     if (n_counters) *n_counters = dense;
     if (splits == 1) return 0;
     return (size_t)dense * splits * BM * BNB * sizeof(float);
@@ -1673,22 +1705,21 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
                cudaStream_t stream) {
   static std::atomic<unsigned long long> attr_done{0};
   if (!done_on_device(attr_done)) {
-    cudaFuncSetAttribute(gemm_big_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_BF16, 2>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BIG);
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_F32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_BIG);
-    cudaFuncSetAttribute(gemm_big_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_QKV, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)SMEM_BIG);
-    cudaFuncSetAttribute(gemm_big_kernel<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)SMEM_BIG);
-    cudaFuncSetAttribute(gemm_big_kernel<EPI_SWIGLU>,
+    cudaFuncSetAttribute(gemm_big_kernel<EPI_SWIGLU, 2>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BIG);
     mark_device(attr_done);
   }
-  if (s.b_map256 == nullptr) return cudaErrorInvalidValue;
+  if (s.b_map256 == nullptr || s.b_map == nullptr) return cudaErrorInvalidValue;
   Plan p{};
   p.a0_rows = s.a0_rows;
   p.a1_rows = s.a1_rows;
-  p.n_m0 = (s.a0_rows + BM - 1) / BM;
-  p.n_m1 = (s.a1_rows + BM - 1) / BM;
+  big_m_tiles(s.a0_rows, s.a1_rows, &p.n_m0, &p.n_m1);
   p.merged = 0;
   p.box0 = p.box1 = BM;
   p.n_tiles = s.n / BNB;
@@ -1702,8 +1733,8 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
   const int tiles = p.n_q_tiles * p.n_m0 + (p.n_tiles - p.n_q_tiles) * (p.n_m0 + p.n_m1);
   p.splits = big_splits(tiles, p.n_kb, num_sms);
   p.units_q = p.n_q_tiles * p.splits * p.n_m0;
-  const int units = tiles * p.splits;
-  p.grid = std::min(units, num_sms);
+  const int units = tiles * p.splits;  // even: the m-tile counts are
+  p.grid = std::min(units, num_sms) & ~1;
   p.slices = epi == EPI_F32 && scr.f32_slices && p.splits > 1;
   p.slice_stride = scr.slice_stride;
   if (p.splits > 1 && !p.slices) {
@@ -1725,20 +1756,21 @@ int launch_big(const GemmShape& s, int epi, void* c, int ldc, const QkvOut* qkv,
   static SeqTable zero_st{};
   const QkvOut& qo = qkv ? *qkv : zero_q;
   const SeqTable& st = seqs ? *seqs : zero_st;
+  if (p.grid < 2) return cudaErrorInvalidValue;
   const dim3 grid(p.grid), block(kThreads);
   cudaError_t e;
   if (epi == EPI_QKV)
-    e = launch_pdl(gemm_big_kernel<EPI_QKV>, grid, block, SMEM_BIG, stream, ma0, ma1,
-                   *s.b_map256, p, qo, st);
+    e = launch_pdl_cluster(gemm_big_kernel<EPI_QKV, 2>, grid, block, SMEM_BIG, stream, 2u, ma0,
+                           ma1, *s.b_map256, *s.b_map, p, qo, st);
   else if (epi == EPI_BF16)
-    e = launch_pdl(gemm_big_kernel<EPI_BF16>, grid, block, SMEM_BIG, stream, ma0, ma1,
-                   *s.b_map256, p, qo, st);
+    e = launch_pdl_cluster(gemm_big_kernel<EPI_BF16, 2>, grid, block, SMEM_BIG, stream, 2u, ma0,
+                           ma1, *s.b_map256, *s.b_map, p, qo, st);
   else if (epi == EPI_SWIGLU)
-    e = launch_pdl(gemm_big_kernel<EPI_SWIGLU>, grid, block, SMEM_BIG, stream, ma0, ma1,
-                   *s.b_map256, p, qo, st);
+    e = launch_pdl_cluster(gemm_big_kernel<EPI_SWIGLU, 2>, grid, block, SMEM_BIG, stream, 2u,
+                           ma0, ma1, *s.b_map256, *s.b_map, p, qo, st);
   else
-    e = launch_pdl(gemm_big_kernel<EPI_F32>, grid, block, SMEM_BIG, stream, ma0, ma1,
-                   *s.b_map256, p, qo, st);
+    e = launch_pdl_cluster(gemm_big_kernel<EPI_F32, 2>, grid, block, SMEM_BIG, stream, 2u, ma0,
+                           ma1, *s.b_map256, *s.b_map, p, qo, st);
   return (int)e;
 }
 

@@ -309,6 +309,16 @@ DF_DEV void finish_row(const Plan& p, const QkvOut& qo, const SeqTable& st, floa
   }
 }
 
+// The QKV epilogue of one row held by one thread, with its destination and
+// position worked out beforehand (while the main loop ran).
+DF_DEV void qkv_apply(const QkvOut& qo, const QkvTarget& g, int pos, float* v) {
+  if (g.kind == 0) return;
+  if (g.kind != 3)
+    norm_rope(v, g.norm, qo.eps, qo.rope + (size_t)pos * (HD / 2),
+              g.kind == 1 ? qo.q_scale : 1.f);
+  store_bf16(g.dst, v, HD);
+}
+
 // The same epilogue with one row spread over a warp: lane l holds columns
 // 4l .. 4l+3.  The RMSNorm sum is a butterfly over the warp, and the RoPE
 // partner of column j < 64 (column j + 64) sits 16 lanes away.
@@ -1226,11 +1236,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       int m, n, sp, k0, k1, tid;
       big_unit(p, u, m, n, sp, k0, k1, tid);
       const uint32_t buf = tc & 1, use = tc >> 1;
+      int src, srow;
+      row_source(p, m, r, src, srow);
+      // QKV: the row's destinations and positions for both heads of the tile
+      // (a search over the sequences and a global load), and its RoPE rows
+      // warmed in L2, while the accumulator is still being computed
+      QkvTarget tg[BNB / HD];
+      int tpos[BNB / HD];
+      if constexpr (EPI == EPI_QKV) {
+#pragma unroll
+        for (int h = 0; h < BNB / HD; ++h) {
+          tg[h].kind = 0;
+          tpos[h] = 0;
+          if (src >= 0) {
+            tg[h] = qkv_target(qo, st, src, srow, n * BNB + h * HD);
+            if (tg[h].kind == 1 || tg[h].kind == 2) {
+              tpos[h] = checked_position(qo, tg[h].pos_idx, p.err);
+              const char* rp = reinterpret_cast<const char*>(qo.rope + (size_t)tpos[h] * (HD / 2));
+#pragma unroll
+              for (int i = 0; i < HD * 4; i += 128) prefetch_l2(rp + i);
+            }
+          }
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1, abort_flag, p.err)))
         break;
       tc_fence_after();
-      int src, srow;
-      row_source(p, m, r, src, srow);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
       const bool whole = p.splits == 1 || p.slices;
       // split units: sums of the valid rows go to the (tile, split) slot,
@@ -1254,9 +1285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&acc_empty[buf]);
         }
         if (whole) {
-          if (src >= 0)
+          if constexpr (EPI == EPI_QKV) {
+            if (src >= 0) qkv_apply(qo, tg[half], tpos[half], v);
+          } else if (src >= 0) {
             finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD,
                             p.slices ? sp * p.slice_stride : 0);
+          }
         } else if (src >= 0) {
 #pragma unroll
           for (int c4 = 0; c4 < HD / 4; ++c4)
@@ -1295,7 +1329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[4 * c4 + 3] += w4.w;
             }
           }
-          finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
+          if constexpr (EPI == EPI_QKV)
+            qkv_apply(qo, tg[half], tpos[half], v);
+          else
+            finish_row<EPI>(p, qo, st, v, src, srow, n * BNB + half * HD);
         }
       }
       if (et == 0) p.counters[tid] = 0;

@@ -210,6 +210,99 @@ DF_DEV void merge_rows(const AttnArgs& a, const Unit& w, int slot0, int stride, 
     merge_rows_t<2>(a, w, slot0, stride, n, r0, r1, block_slot, et);
 }
 
+// The same merge for splits that are the C CTAs of one cluster, reading the
+// partials from the CTAs' shared memory instead of L2: each CTA keeps its
+// partial rows in its idle V stages ([row][HD] fp32, 16-byte chunk c of row r
+// at position c ^ (r & 31)) followed by the rows' max and sum ([2][128]).
+// Every load of an item (all C sources) is issued before any is used.
+constexpr uint32_t SMEM_PART_ML = 128 * HD * 4;  // offset of (max, sum) in the partial area
+
+DF_DEV void write_partial_smem(uint8_t* part, int row, const float (&o)[HD], float m, float l) {
+  float4* dst = reinterpret_cast<float4*>(part) + row * (HD / 4);
+#pragma unroll
+  for (int c4 = 0; c4 < HD / 4; ++c4)
+    dst[c4 ^ (row & 31)] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+  float* ml = reinterpret_cast<float*>(part + SMEM_PART_ML);
+  ml[row] = m;
+  ml[128 + row] = l;
+}
+
+template <int C, int NC4>
+DF_DEV void merge_rows_cluster_t(const AttnArgs& a, const Unit& w, uint32_t part, int r0, int r1,
+                                 int et) {
+  constexpr int CH = HD / (4 * NC4);  // chunks per row
+  for (int item = et; item < (r1 - r0) * CH; item += 128) {
+    const int row = r0 + item / CH, ch = item % CH;
+    float mv[C], lv[C];
+    float4 t[C][NC4];
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      mv[i] = ld_cluster_f32(cluster_map(part + SMEM_PART_ML + row * 4, (uint32_t)i));
+      lv[i] = ld_cluster_f32(cluster_map(part + SMEM_PART_ML + (128 + row) * 4, (uint32_t)i));
+#pragma unroll
+      for (int c = 0; c < NC4; ++c) {
+        const int c4 = ch * NC4 + c;
+        t[i][c] = ld_cluster_f4(
+            cluster_map(part + (uint32_t)((row * (HD / 4) + (c4 ^ (row & 31))) * 16), (uint32_t)i));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < C; ++i) M = fmaxf(M, mv[i]);
+    float L = 0.f;
+    float4 acc[NC4];
+#pragma unroll
+    for (int c = 0; c < NC4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < C; ++i) {
+        const float f = mv[i] == -INFINITY ? 0.f : fast_exp2(mv[i] - M);
+        L += f * lv[i];
+#pragma unroll
+        for (int c = 0; c < NC4; ++c) {
+          acc[c].x += f * t[i][c].x;
+          acc[c].y += f * t[i][c].y;
+          acc[c].z += f * t[i][c].z;
+          acc[c].w += f * t[i][c].w;
+        }
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint4* dst = reinterpret_cast<uint4*>(out_row(a, w, row) + ch * NC4 * 4);
+#pragma unroll
+    for (int c = 0; c < NC4 / 2; ++c) {
+      uint4 pk;
+      pk.x = pack_bf16x2(acc[2 * c].x * inv, acc[2 * c].y * inv);
+      pk.y = pack_bf16x2(acc[2 * c].z * inv, acc[2 * c].w * inv);
+      pk.z = pack_bf16x2(acc[2 * c + 1].x * inv, acc[2 * c + 1].y * inv);
+      pk.w = pack_bf16x2(acc[2 * c + 1].z * inv, acc[2 * c + 1].w * inv);
+      dst[c] = pk;
+    }
+  }
+}
+
+// chunk width by row count, with at most 16 chunks of 16 bytes in flight per
+// thread (C sources x NC4)
+DF_DEV void merge_rows_cluster(const AttnArgs& a, const Unit& w, uint32_t part, int C, int r0,
+                               int r1, int et) {
+  const int rows = r1 - r0;
+  if (C == 8) {
+    merge_rows_cluster_t<8, 2>(a, w, part, r0, r1, et);
+  } else if (C == 4) {
+    if (rows >= 16)
+      merge_rows_cluster_t<4, 4>(a, w, part, r0, r1, et);
+    else
+      merge_rows_cluster_t<4, 2>(a, w, part, r0, r1, et);
+  } else {
+    if (rows >= 32)
+      merge_rows_cluster_t<2, 8>(a, w, part, r0, r1, et);
+    else if (rows >= 16)
+      merge_rows_cluster_t<2, 4>(a, w, part, r0, r1, et);
+    else
+      merge_rows_cluster_t<2, 2>(a, w, part, r0, r1, et);
+  }
+}
+
 // Called by the 128 softmax threads after their partial stores: counts this
 // CTA in at `counter` (one thread, acquire-release at GPU scope, after a
 // barrier that orders every thread's stores before it) and returns, to every
@@ -356,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_kv(pre);
       }
     }
-    grid_dep_sync();
+    grid_dep_wait();
     // A unit with no keys loads no Q either: nothing would wait for the copy,
     // and its softmax warps reuse the Q tile's shared memory to hand over
     // their (empty) row statistics, which a late TMA write would overwrite.
@@ -379,9 +472,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       load_kv(j);
     }
+    // Only once this CTA's last K/V tile has landed may the next kernel
+    // start: its CTAs, on the SMs this grid leaves free, begin by streaming
+    // their weights, and those copies would otherwise compete with our
+    // tiles for HBM.  (Still after our own wait, as every kernel here.)
+    if (T > 0 && lane == 0) {
+      const int s = (T - 1) % NST;
+      const uint32_t ph = ((T - 1) / NST) & 1;
+      if (mbar_wait(&k_full[s], ph, abort_flag, a.err)) mbar_wait(&v_full[s], ph, abort_flag, a.err);
+    }
+    __syncwarp();
+    grid_dep_launch();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    grid_dep_sync();
+    grid_dep_wait();
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, BKEY, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
@@ -424,7 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    grid_dep_sync();
     const int q = warp & 3;
     const int r = q * 32 + lane;                // TMEM lane (accumulator row)
     const int qr = DUAL ? (r & 63) : r;         // query row of the tile
@@ -451,9 +554,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.causal) i1_hi = min(i1_hi, qi + 1);
     }
     float m_run = -INFINITY, l_run = 0.f;
-    for (int j = 0; j < T; ++j) {
+    // Pass -1 runs the tile body on whatever the S and O columns hold, with
+    // every wait, store and state update left out and through the masking
+    // and rescaling branches, before the dependency wait: the body's
+    // instructions reach this SM's instruction cache while the previous
+    // kernel finishes, instead of being fetched piece by piece during the
+    // real tiles (its start is opaque to the compiler so that the pass stays
+    // the same code as the real tiles).
+    int j_first;
+    asm volatile("mov.s32 %0, -1;" : "=r"(j_first));
+    for (int jj = j_first; jj < T; ++jj) {
+      const bool warm = jj < 0;
+      const int j = warm ? 0 : jj;
       const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, a.err)))
+      if (!__all_sync(0xffffffffu,
+                      warm || mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, a.err)))
         break;
       tc_fence_after();
       float s[NC];
@@ -472,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool rescale = false;
       if (real) {
         const int k0 = tile_start(w, j) + col0;
-        if (!(k0 >= i1_lo && k0 + NC <= i1_hi)) {
+        if (warm || !(k0 >= i1_lo && k0 + NC <= i1_hi)) {
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             const int key = k0 + c;
@@ -526,28 +641,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk.z = pack_bf16x2(pv[4], pv[5]);
           pk.w = pack_bf16x2(pv[6], pv[7]);
           const int ch = col0 / 8 + cc;
-          *reinterpret_cast<uint4*>(prow + (ch >> 3) * HALF_BYTES + (((ch & 7) ^ (r & 7)) * 16)) =
-              pk;
+          if (!warm)
+            *reinterpret_cast<uint4*>(prow + (ch >> 3) * HALF_BYTES +
+                                      (((ch & 7) ^ (r & 7)) * 16)) = pk;
         }
         if constexpr (DUAL) {
           const int other = col0 == 0 ? 1 : 0;
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<uint4*>(prow + other * HALF_BYTES + ((cc ^ (r & 7)) * 16)) =
-                make_uint4(0u, 0u, 0u, 0u);
+            if (!warm)
+              *reinterpret_cast<uint4*>(prow + other * HALF_BYTES + ((cc ^ (r & 7)) * 16)) =
+                  make_uint4(0u, 0u, 0u, 0u);
         }
         const float sum = ((psum[0].x + psum[0].y) + (psum[1].x + psum[1].y)) +
                           ((psum[2].x + psum[2].y) + (psum[3].x + psum[3].y));
-        l_run = l_run * alpha + sum;
-        m_run = m_new;
+        if (!warm) {
+          l_run = l_run * alpha + sum;
+          m_run = m_new;
+        }
       }
       // O is touched only to rescale it, and only then must PV(j-1) be
       // complete.  Having seen S(j) complete, PV(j-2) and everything before
       // it are (one thread issues all MMAs, in order), so o_done[(j-1) & 1]
       // has at most the phase of PV(j-1) pending and a parity wait is exact.
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1,
-                                               abort_flag, a.err)))
+      if (__any_sync(0xffffffffu, rescale) || warm) {
+        if (!warm && !__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1],
+                                                        ((j - 1) >> 1) & 1, abort_flag, a.err)))
           break;
         tc_fence_after();
         const float f = rescale ? alpha : 1.f;
@@ -557,8 +676,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(trow + O_COL + c * 32, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st32(trow + O_COL + c * 32, o);
+          if (!warm) tmem_st32(trow + O_COL + c * 32, o);
         }
+      }
+      if (warm) {
+        grid_dep_wait();
+        continue;
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -615,7 +738,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool writer = real && (!DUAL || r < 64);
     const int et = threadIdx.x - 64;
-    if (w.ns == 1) {
+    if (a.cluster > 1 && a.k_clusters == 1) {
+      // a split, and the pair's splits are the C CTAs of one cluster: the
+      // unnormalised partial rows stay in this CTA's V stages (idle: the last
+      // PV has completed and no copy is in flight); after one barrier each
+      // rank merges its share of the rows from the C CTAs' shared memory, in
+      // rank order, and a second barrier keeps every CTA resident until the
+      // others have read its rows
+      const int C = a.cluster;
+      const int rank = w.c % C;
+      if (writer) write_partial_smem(sV, qr, o, m_run, l_run);
+      __syncwarp();
+      cluster_sync();
+      const int rpo = (w.rows + C - 1) / C;
+      const int r0 = min(w.rows, rank * rpo), r1 = min(w.rows, r0 + rpo);
+      merge_rows_cluster(a, w, smem_u32(sV), C, r0, r1, et);
+      __syncwarp();
+      cluster_sync();
+    } else if (w.ns == 1) {
       // the unit covers every key of its rows: the normalised row
       if (writer) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -637,25 +777,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the rows are merged over the pair's splits
       if (writer) write_partial(a, (int)blockIdx.x, qr, o, m_run, l_run);
       if (a.cluster > 1) {
-        // every C consecutive splits of the pair are one cluster: after one
-        // barrier each rank merges its share of the rows from the C slots
-        // (through L2); with several clusters per pair, the last cluster to
-        // finish a row block merges the clusters' blocks
+        // k clusters per pair: after one barrier each rank merges its share
+        // of the rows from its cluster's C slots (through L2) into a block
+        // slot, and the last cluster to finish a row block merges the
+        // clusters' blocks
         __syncwarp();
         cluster_sync();
         const int C = a.cluster;
         const int rank = w.c % C, cl = w.c / C;
         const int rpo = (w.rows + C - 1) / C;
         const int r0 = min(w.rows, rank * rpo), r1 = min(w.rows, r0 + rpo);
-        if (a.k_clusters == 1) {
-          merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, -1, et);
-        } else {
-          merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, a.n_units + (int)blockIdx.x,
-                     et);
-          int* cnt = a.counters + ((size_t)(w.b * a.n_kv + w.h) * C + rank);
-          if (last_arrival(cnt, a.k_clusters, et, last_flag))
-            merge_rows(a, w, a.n_units + w.pair_unit0 + rank, C, a.k_clusters, r0, r1, -1, et);
-        }
+        merge_rows(a, w, w.pair_unit0 + cl * C, 1, C, r0, r1, a.n_units + (int)blockIdx.x, et);
+        int* cnt = a.counters + ((size_t)(w.b * a.n_kv + w.h) * C + rank);
+        if (last_arrival(cnt, a.k_clusters, et, last_flag))
+          merge_rows(a, w, a.n_units + w.pair_unit0 + rank, C, a.k_clusters, r0, r1, -1, et);
       } else if (last_arrival(a.counters + (w.b * a.n_kv + w.h), w.ns, et, last_flag)) {
         // the pair's last split to finish merges all of its rows
         merge_rows(a, w, w.pair_unit0, 1, w.ns, 0, w.rows, -1, et);
@@ -663,9 +798,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp < 2 && a.cluster > 1) {
-    // the producer and MMA warps take part in the cluster barrier
+    // the producer and MMA warps take part in the cluster barriers
     __syncwarp();
     cluster_sync();
+    if (a.k_clusters == 1) cluster_sync();
   }
 
   tc_fence_before();

@@ -1159,12 +1159,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   // both CTAs' barriers exist before any multicast copy or commit reaches them
   if (MC > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_sync();
 
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_a = policy_evict_last();
+      const int rk = MC > 1 ? (int)(blockIdx.x & 1) : 0;
+      // this CTA's share of a weight k-block: half of the 256-row tile
+      // (multicast to the pair), or all of it
+      auto load_b = [&](int s, int n, int kb) {
+        if (MC > 1)
+          tma_load_2d_mc(sB + s * B_BIG + rk * (B_BIG / 2), &tmBh, &full[s], kb * BK,
+                         n * BNB + rk * (BNB / 2), (uint16_t)3, pol_w);
+        else
+          tma_load_2d(sB + s * B_BIG, &tmB, &full[s], kb * BK, n * BNB, pol_w);
+      };
+      // The weights do not depend on the previous kernel: the first stages
+      // get their weight boxes before the dependency wait.
+      int pre = 0;
+      if (blockIdx.x < units) {
+        int m, n, sp, k0, k1, tid;
+        big_unit(p, blockIdx.x, m, n, sp, k0, k1, tid);
+        pre = min(STAGES_BIG, k1 - k0);
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], A_FULL + B_BIG);
+          load_b(i, n, k0 + i);
+        }
+      }
+      grid_dep_sync();
       uint32_t it = 0;
       bool alive = true;
       for (int u = blockIdx.x; alive && u < units; u += gridDim.x) {
@@ -1175,24 +1197,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row0 = (a0 ? m : m - p.n_m0) * BM;
         for (int kb = k0; kb < k1; ++kb, ++it) {
           const int s = it % STAGES_BIG;
-          const uint32_t ph = (it / STAGES_BIG) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) {
-            alive = false;
-            break;
+          if (it >= (uint32_t)pre) {
+            const uint32_t ph = (it / STAGES_BIG) & 1;
+            if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) {
+              alive = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], A_FULL + B_BIG);
+            load_b(s, n, kb);
           }
-          mbar_arrive_expect_tx(&full[s], A_FULL + B_BIG);
           tma_load_2d(sA + s * A_FULL, ma, &full[s], kb * BK, a_row0, pol_a);
-          if (MC > 1) {
-            const int rk = (int)(blockIdx.x & 1);
-            tma_load_2d_mc(sB + s * B_BIG + rk * (B_BIG / 2), &tmBh, &full[s], kb * BK,
-                           n * BNB + rk * (BNB / 2), (uint16_t)3, pol_w);
-          } else {
-            tma_load_2d(sB + s * B_BIG, &tmB, &full[s], kb * BK, n * BNB, pol_w);
-          }
         }
       }
+    } else {
+      grid_dep_sync();
     }
   } else if (warp == 1) {
+    grid_dep_sync();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BNB, false);
       uint32_t it = 0, tc = 0;
@@ -1228,6 +1249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
+    grid_dep_sync();
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int et = threadIdx.x - 64;

@@ -82,6 +82,94 @@ def measured_traffic(workload: str, kernel: str):
     elif any(then.get(f) is None or then.get(f) != now.get(f) for f in srcs):
         return None
     return rec.get("bytes_per_launch")
+
+# DRAM traffic of each workload's dominant kernel, captured by ncu one kernel
+# at a time (a regex on the demangled name, a few launches after set-up):
+#   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum
+#       --clock-control none --kernel-name-base demangled -k regex:<kernel> -s 3 -c 3
+#       --csv --log-file <dir>/traffic_<workload>.csv
+#       python bench.py --workload <workload> --steps 2 --warmup 3 --no-cpu-baseline --no-clocks
+# `python bench.py --ncu-traffic <dir>` turns those logs into profiles/traffic.json
+# (read back by measured_traffic) and profiles/traffic.md.
+_COMMON_SRC = ["dflash_api.cu", "handles.h", "internal.h", "ptx.cuh"]
+TRAFFIC_CAPTURE = {
+    # workload: (trace bucket, kernel regex, source files of that kernel)
+    "qwen3_8b_single": ("fc", r"gemm_bf16_kernel<\(int\)1, \(int\)128>",
+                        ["gemm_bf16.cu"] + _COMMON_SRC),
+    "long_ctx_swa": ("fc", r"gemm_bf16_kernel<\(int\)1, \(int\)128>",
+                     ["gemm_bf16.cu"] + _COMMON_SRC),
+    "serving_b32": ("attn", "attn_bf16_kernel", ["attn_bf16.cu"] + _COMMON_SRC),
+    "serving_b32_paged": ("attn", "attn_bf16_kernel", ["attn_bf16.cu"] + _COMMON_SRC),
+    "long_ctx_full": ("attn", "attn_bf16_kernel", ["attn_bf16.cu"] + _COMMON_SRC),
+    "packed_train": ("qkv", r"gemm_big_kernel<\(int\)2, \(int\)2>",
+                     ["gemm_bf16.cu"] + _COMMON_SRC),
+    "packed_train_bwd": ("bwd", "packed_bwd_kernel", ["attn_bwd.cu"] + _COMMON_SRC),
+}
+
+
+def _ncu_rows(path):
+    """(launch id, kernel name, {metric: value in bytes or ns}) from an ncu --csv log."""
+    import csv
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1.0,
+             "usecond": 1e3, "msecond": 1e6, "second": 1e9}
+    launches = {}
+    with open(path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rd = csv.reader(lines)
+    hdr = next(rd, None)
+    if hdr is None:
+        return []
+    ix = {h: i for i, h in enumerate(hdr)}
+    for r in rd:
+        if len(r) < len(hdr) or r[ix["ID"]] == "ID":
+            continue
+        v = float(r[ix["Metric Value"]].replace(",", ""))
+        rec = launches.setdefault(int(r[ix["ID"]]), [r[ix["Kernel Name"]], {}])
+        rec[1][r[ix["Metric Name"]]] = v * scale.get(r[ix["Metric Unit"]], 1.0)
+    return [(k, n, m) for k, (n, m) in sorted(launches.items())]
+
+
+def launch_table(path):
+    """Markdown rows (kernel, launches, total us, share) of an ncu launch list."""
+    per = {}
+    for _, name, m in _ncu_rows(path):
+        k = name.split("(")[0].replace("void ", "").replace("df::<unnamed>::", "")
+        per.setdefault(k, []).append(m.get("gpu__time_duration.sum", 0.0) / 1e3)
+    tot = sum(sum(v) for v in per.values()) or 1.0
+    return [f"| `{k}` | {len(v)} | {sum(v):.1f} | {100 * sum(v) / tot:.1f}% |"
+            for k, v in sorted(per.items(), key=lambda kv: -sum(kv[1]))]
+
+
+def write_traffic(log_dir):
+    """profiles/traffic.json and traffic.md from the per-workload ncu logs."""
+    kernels, md = {}, []
+    for w, (bucket, kre, srcs) in TRAFFIC_CAPTURE.items():
+        path = os.path.join(log_dir, f"traffic_{w}.csv")
+        if not os.path.exists(path):
+            continue
+        rows = _ncu_rows(path)
+        if not rows:
+            continue
+        rd = [m["dram__bytes_read.sum"] for _, _, m in rows]
+        wr = [m["dram__bytes_write.sum"] for _, _, m in rows]
+        us = [m["gpu__time_duration.sum"] / 1e3 for _, _, m in rows]
+        tot = float(np.median(np.array(rd) + np.array(wr)))
+        kernels[f"{w}:{bucket}"] = {"bytes_per_launch": tot, "launches_used": len(rows),
+                                    "ncu_kernels": [kre], "sources": sorted(srcs)}
+        md.append(f"| {w} | {bucket} | `{rows[0][1].split('(')[0].replace('void ', '')}` | "
+                  f"{len(rows)} | {np.median(rd) / 1e6:.1f} | {np.median(wr) / 1e6:.2f} | "
+                  f"{np.median(us):.1f} |")
+    out = {"how": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,"
+                  "dram__bytes_write.sum --clock-control none --kernel-name-base demangled "
+                  "-k regex:<kernel> -s 3 -c 3 on the bench command of each workload; "
+                  "bytes_per_launch = median over the captured launches of DRAM read + write; "
+                  "an entry holds while its source files match",
+           "file_sha256": source_digests(), "csrc_sha256": csrc_digest(), "kernels": kernels}
+    with open(os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
+        json.dump(out, f, indent=1)
+    return md
+
+
 sys.path.insert(0, ROOT)
 
 METRIC = "draft-attn blocks/s per layer; achieved HBM GB/s (or tensor util) vs GB300 peak"
@@ -102,6 +190,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip the nvidia-smi sampler (for profiler runs)")
+    ap.add_argument("--ncu-traffic", metavar="DIR", default=None,
+                    help="no GPU work: write profiles/traffic.json from the ncu logs in DIR "
+                         "and print the table rows")
+    ap.add_argument("--ncu-launches", metavar="CSV", default=None,
+                    help="no GPU work: print the per-kernel table of an ncu launch list")
     return ap.parse_args()
 
 
@@ -931,6 +1024,12 @@ def job_value(world, units_per_step, ms):
 # --------------------------------------------------------------------------
 def main():
     args = parse()
+    if args.ncu_traffic or args.ncu_launches:
+        rows = write_traffic(args.ncu_traffic) if args.ncu_traffic else \
+            launch_table(args.ncu_launches)
+        for row in rows:
+            print(row)
+        return 0
     world, rank, local = rank_env()
 
     if args.impl == "reference":

@@ -134,10 +134,9 @@ struct KvUnit {
   int rows_valid;  // tile rows inside the unit's segment
 };
 
-DF_DEV KvUnit kv_unit(const PackedBwdArgs& a, int u, bool own) {
+// key tile j of pair `pair`: context rows (own = false) or the blocks' rows
+DF_DEV KvUnit kv_unit(const PackedBwdArgs& a, int pair, int j, bool own) {
   KvUnit w;
-  const int pairs = a.batch * a.n_kv;
-  const int j = u / pairs, pair = u - j * pairs;
   w.b = pair / a.n_kv;
   w.h = pair - w.b * a.n_kv;
   w.own = own;
@@ -156,11 +155,15 @@ DF_DEV KvUnit kv_unit(const PackedBwdArgs& a, int u, bool own) {
   return w;
 }
 
-// next block >= k that sees a key of the tile (blk_hi if none); every role
-// of the CTA walks the same list
-DF_DEV int kv_next(const PackedBwdArgs& a, const KvUnit& w, int k) {
+// The blocks that see a key of the tile, walked from the last candidate
+// down (every role of the CTA walks the same list): the context tiles of a
+// pair differ in where their lists stop, not where they start, so the tiles
+// dispatched together read each block's Q'/dO at about the same time and
+// it is fetched from HBM about once.  kv_prev returns the largest block
+// <= k that sees the tile, below blk_lo if none.
+DF_DEV int kv_prev(const PackedBwdArgs& a, const KvUnit& w, int k) {
   if (w.own) return k;
-  while (k < w.blk_hi && clamp_anchor(a, w.b, k) <= w.k0) ++k;
+  while (k >= w.blk_lo && clamp_anchor(a, w.b, k) <= w.k0) --k;
   return k;
 }
 
@@ -211,7 +214,7 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
   const uint32_t tmem = *tmem_slot;
   grid_dep_sync();
   const long long pair_blk = ((long long)w.b * a.n_kv + w.h) * a.n_blocks;
-  const int first = kv_next(a, w, w.blk_lo);
+  const int first = kv_prev(a, w, w.blk_hi - 1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -225,7 +228,7 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
       tma_load_2d(sV, tmV, kv_full, 0, y, pol_kv);
       tma_load_2d(sV + T128 / 2, tmV, kv_full, 64, y, pol_kv);
       int i = 0;
-      for (int k = first; k < w.blk_hi; k = kv_next(a, w, k + 1), ++i) {
+      for (int k = first; k >= w.blk_lo; k = kv_prev(a, w, k - 1), ++i) {
         const int s = i % NST;
         if (!mbar_wait(&q_empty[s], ((i / NST) & 1) ^ 1, abort_flag, a.err)) break;
         const int qrow = (int)((pair_blk + k) * QB);
@@ -266,10 +269,10 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
         return true;
       };
       int k = first, i = 0;
-      if (alive && k < w.blk_hi) alive = issue_s(0);
-      while (alive && k < w.blk_hi) {
-        const int kn = kv_next(a, w, k + 1);
-        if (kn < w.blk_hi && !issue_s(i + 1)) break;
+      if (alive && k >= w.blk_lo) alive = issue_s(0);
+      while (alive && k >= w.blk_lo) {
+        const int kn = kv_prev(a, w, k - 1);
+        if (kn >= w.blk_lo && !issue_s(i + 1)) break;
         if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
         tc_fence_after();
         const int s = i % NST;
@@ -302,7 +305,7 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
     const int brow = key - a.seq;              // own tiles: row in the blocks' region
     int i = 0;
     bool ok = true;
-    for (int k = first; k < w.blk_hi; k = kv_next(a, w, k + 1), ++i) {
+    for (int k = first; k >= w.blk_lo; k = kv_prev(a, w, k - 1), ++i) {
       const int s = i % NST;
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, a.err))) {
         ok = false;
@@ -385,7 +388,7 @@ DF_DEV void dkdv_body(uint8_t* smem, const CUtensorMap* tmQ, const CUtensorMap* 
 
 // ---------------------------------------------------------------- dQ CTA
 DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                    const PackedBwdArgs& a, int u) {
+                    const PackedBwdArgs& a, int pair, int idx) {
   uint8_t* sK = smem;              // [NKS] 64 key rows
   uint8_t* sV = sK + NKS * T64;    // [NKS]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NKS * T64);
@@ -399,12 +402,10 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmK, const CUtensorMap* tm
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // unit: two blocks of one (sequence, kv head); latest blocks (largest
-  // anchors, longest key ranges) first
-  const int pairs = a.batch * a.n_kv;
+  // unit: two blocks of one (sequence, kv head); idx 0 = the latest blocks
+  // (largest anchors, longest key ranges)
   const int n_qt = (a.n_blocks + 1) / 2;
-  const int qt = n_qt - 1 - u / pairs;
-  const int pair = u - (u / pairs) * pairs;
+  const int qt = n_qt - 1 - idx;
   const int b = pair / a.n_kv, h = pair - (pair / a.n_kv) * a.n_kv;
   const int blk0 = 2 * qt;
   const int nbk = min(2, a.n_blocks - blk0);
@@ -623,9 +624,12 @@ DF_DEV void dq_body(uint8_t* smem, const CUtensorMap* tmK, const CUtensorMap* tm
   }
 }
 
-// One launch, three runs of CTAs: dK/dV over context key tiles (longest
+// One launch.  The (sequence, kv head) pairs are taken kv_group at a time;
+// for each group three runs of CTAs: dK/dV over context key tiles (longest
 // first), dQ over block pairs (longest first), dK/dV over the blocks' own
-// rows (short).
+// rows (short), each run interleaving the group's pairs.  The CTAs resident
+// at a time then work on about one group, whose Q'/dO and K/V L2 holds, so
+// every kind of CTA reads them from HBM about once.
 __global__ void __launch_bounds__(kThreads, 1)
     packed_bwd_kernel(const __grid_constant__ CUtensorMap tmQ64,
                       const __grid_constant__ CUtensorMap tmDO64,
@@ -637,14 +641,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int u = blockIdx.x;
-  if (u < a.n_kv_ctx_units)
-    dkdv_body(smem, &tmQ64, &tmDO64, &tmK128, &tmV128, a, kv_unit(a, u, false));
-  else if (u < a.n_kv_ctx_units + a.n_q_units)
-    dq_body(smem, &tmK64, &tmV64, a, u - a.n_kv_ctx_units);
-  else
+  const int pairs = a.batch * a.n_kv;
+  const int nt = a.n_kv_ctx_units / pairs, nq = a.n_q_units / pairs,
+            no = a.n_kv_own_units / pairs;
+  const int G = max(1, a.kv_group);
+  const int g = (int)blockIdx.x / (G * (nt + nq + no));
+  const int p0 = g * G, gsz = min(G, pairs - p0);
+  int r = (int)blockIdx.x - g * G * (nt + nq + no);
+  if (r < gsz * nt) {
     dkdv_body(smem, &tmQ64, &tmDO64, &tmK128, &tmV128, a,
-              kv_unit(a, u - a.n_kv_ctx_units - a.n_q_units, true));
+              kv_unit(a, p0 + r % gsz, r / gsz, false));
+  } else if ((r -= gsz * nt) < gsz * nq) {
+    dq_body(smem, &tmK64, &tmV64, a, p0 + r % gsz, r / gsz);
+  } else {
+    r -= gsz * nq;
+    dkdv_body(smem, &tmQ64, &tmDO64, &tmK128, &tmV128, a,
+              kv_unit(a, p0 + r % gsz, r / gsz, true));
+  }
 }
 
 }  // namespace

@@ -1201,6 +1201,7 @@ int dflash_packed_attn_core_backward(dflash_attn* a, int batch, int seq, int n_b
   ba.dq_scale = (float)scale;
   const int pairs = batch * a->nkv;
   ba.n_kv_ctx_units = pairs * ((seq + 127) / 128);
+  ba.kv_group = std::max(1, std::min(pairs, a->num_sms / std::max(1, (seq + 127) / 128)));
   ba.n_q_units = pairs * ((n_blocks + 1) / 2);
   ba.n_kv_own_units = pairs * (int)((q_len + 127) / 128);
   ba.err = a->err;

@@ -266,6 +266,8 @@ struct PackedBwdArgs {
   const void* qs;          // Q' (tile layout, bf16)
   const void* do_tile;     // dO (tile layout, bf16)
   int n_kv_ctx_units;      // dK/dV units over context key tiles
+  int kv_group;            // (sequence, kv head) pairs whose units are dispatched together,
+                           // so that their Q'/dO and K/V stay in L2 for every kind of CTA
   int n_q_units;           // dQ units
   int n_kv_own_units;      // dK/dV units over the blocks' own keys
   int* err;

@@ -68,6 +68,7 @@ struct Plan {
   int* err;
   int slices;           // EPI_F32: split `sp` writes its partial to slice sp of c
   size_t slice_stride;  // floats between slices
+  int n_tile0;          // decode-size kernel: first n-tile of this launch
 };
 
 // Units of one region (M_r m-tiles x N_r n-tiles x splits), ordered by
@@ -505,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int m_tile, n_tile, split;
   decode_tile_split(p, blockIdx.x, m_tile, n_tile, split);
+  n_tile += p.n_tile0;
   const int tile_id = n_tile * (p.n_m0 + p.n_m1) + m_tile;
   const int kb0 = (int)((long long)split * p.n_kb / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.n_kb / p.splits);
@@ -1733,25 +1735,46 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   static SeqTable zero_st{};
   const QkvOut& qo = qkv ? *qkv : zero_q;
   const SeqTable& st = seqs ? *seqs : zero_st;
-  const dim3 grid(g.tiles * g.splits), block(kThreads);
   const size_t smem = smem_bytes(g);
-  cudaError_t e;
-  const unsigned cl = p.cluster ? (unsigned)g.splits : 1u;
-  if (epi == EPI_QKV) {
-    if (g.bn != 128) return cudaErrorInvalidValue;
-    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, cl, ma0,
-                           ma1, *s.b_map, p, qo, st);
-  } else if (epi == EPI_BF16) {
-    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream, cl, ma0,
-                           ma1, *s.b_map, p, qo, st);
-  } else if (epi == EPI_SWIGLU) {
-    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_SWIGLU, 128>, grid, block, smem, stream, cl,
-                           ma0, ma1, *s.b_map, p, qo, st);
-  } else {
-    e = launch_pdl_cluster(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream, cl, ma0,
-                           ma1, *s.b_map, p, qo, st);
+  if (g.bn != 128) return cudaErrorInvalidValue;
+  auto launch = [&](const Plan& pl, int ctas) {
+    const dim3 grid(ctas), block(kThreads);
+    const unsigned cl = pl.cluster && pl.splits > 1 ? (unsigned)pl.splits : 1u;
+    if (epi == EPI_QKV)
+      return launch_pdl_cluster(gemm_bf16_kernel<EPI_QKV, 128>, grid, block, smem, stream, cl,
+                                ma0, ma1, *s.b_map, pl, qo, st);
+    if (epi == EPI_BF16)
+      return launch_pdl_cluster(gemm_bf16_kernel<EPI_BF16, 128>, grid, block, smem, stream, cl,
+                                ma0, ma1, *s.b_map, pl, qo, st);
+    if (epi == EPI_SWIGLU)
+      return launch_pdl_cluster(gemm_bf16_kernel<EPI_SWIGLU, 128>, grid, block, smem, stream,
+                                cl, ma0, ma1, *s.b_map, pl, qo, st);
+    return launch_pdl_cluster(gemm_bf16_kernel<EPI_F32, 128>, grid, block, smem, stream, cl,
+                              ma0, ma1, *s.b_map, pl, qo, st);
+  };
+  p.n_tile0 = 0;
+  // Between one and two waves of whole tiles (e.g. the MLP's gate/up
+  // projection at decode size, 192 tiles): the tiles past the first wave
+  // would run alone as a thin second wave, far below the HBM rate.  Those
+  // go to a second launch with their K split over a cluster (2 to 4 CTAs),
+  // which starts on the SMs the first wave frees.
+  const int rem = g.n_tiles - num_sms;
+  if (p.cluster && g.splits == 1 && g.n_m0 + g.n_m1 == 1 && g.n_q_tiles == 0 && rem > 0 &&
+      rem < num_sms) {
+    // (at most about 15/16 of the SMs hold 3- or 4-CTA clusters at once)
+    const int cap = num_sms - num_sms / 16;
+    const int s2 = rem * 4 <= cap ? 4 : rem * 3 <= cap ? 3 : rem * 2 <= num_sms ? 2 : 1;
+    Plan p1 = p;
+    p1.n_tiles = num_sms;
+    const cudaError_t e = launch(p1, num_sms);
+    if (e != cudaSuccess) return (int)e;
+    Plan p2 = p;
+    p2.n_tile0 = num_sms;
+    p2.n_tiles = rem;
+    p2.splits = s2;
+    return (int)launch(p2, rem * s2);
   }
-  return (int)e;
+  return (int)launch(p, g.tiles * g.splits);
 }
 
 }  // namespace df

@@ -30,26 +30,46 @@ __global__ void rope_table_kernel(float2* tab, int max_pos, int half,
 // reduction.
 constexpr int kNormThreads = 512;
 constexpr int kNormVec = 8;  // cols <= 512 * 4 * 8 = 16384
+constexpr int kNormMaxSlices = 8;
 
+// VEC float4 per thread and at most MAXS slices: the smallest instance that
+// covers the call, so that the registers of a thread (the row's values, the
+// slices' loads in flight, the gains) let two CTAs share an SM
+template <int VEC, int MAXS>
 __global__ void __launch_bounds__(kNormThreads)
     row_rmsnorm_kernel(const float* z, int cols, const float* w, float eps, void* out,
                        int out_bf16, int n_slices, size_t slice_stride) {
+  const int n4 = cols / 4;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  // the gains do not depend on the previous kernel: read before its wait
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  float4 gv[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    gv[i] = c < n4 ? __ldg(w4 + c) : zero;
+  }
   grid_dep_sync();
   const float4* zr = reinterpret_cast<const float4*>(z + (size_t)blockIdx.x * cols);
-  const int n4 = cols / 4;
-  float4 x[kNormVec];
+  float4 x[VEC];
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < kNormVec; ++i) {
+  for (int i = 0; i < VEC; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
-    x[i] = c < n4 ? __ldcg(zr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sl = 1; sl < n_slices; ++sl) {
-      if (c >= n4) break;
-      const float4 t = __ldcg(zr + sl * (slice_stride / 4) + c);
-      x[i].x += t.x;
-      x[i].y += t.y;
-      x[i].z += t.z;
-      x[i].w += t.w;
+    // every slice's load issued before the first is used; summed in order
+    float4 t[MAXS];
+#pragma unroll
+    for (int sl = 0; sl < MAXS; ++sl)
+      t[sl] = c < n4 && sl < n_slices ? __ldcg(zr + sl * (slice_stride / 4) + c) : zero;
+    x[i] = t[0];
+#pragma unroll
+    for (int sl = 1; sl < MAXS; ++sl) {
+      if (sl < n_slices) {
+        x[i].x += t[sl].x;
+        x[i].y += t[sl].y;
+        x[i].z += t[sl].z;
+        x[i].w += t[sl].w;
+      }
     }
     ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
   }
@@ -61,12 +81,11 @@ __global__ void __launch_bounds__(kNormThreads)
 #pragma unroll
   for (int i = 0; i < kNormThreads / 32; ++i) tot += red[i];
   const float inv = rsqrtf(tot / cols + eps);
-  const float4* w4 = reinterpret_cast<const float4*>(w);
 #pragma unroll
-  for (int i = 0; i < kNormVec; ++i) {
+  for (int i = 0; i < VEC; ++i) {
     const int c = threadIdx.x + i * kNormThreads;
     if (c >= n4) break;
-    const float4 g = __ldg(w4 + c);
+    const float4 g = gv[i];
     const float4 y = make_float4(x[i].x * inv * g.x, x[i].y * inv * g.y,
                                  x[i].z * inv * g.z, x[i].w * inv * g.w);
     if (out_bf16) {
@@ -236,10 +255,18 @@ int launch_row_rmsnorm(const float* z, int rows, int cols, const float* w,
                        size_t slice_stride, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (cols % 4 != 0 || cols > kNormThreads * 4 * kNormVec || n_slices < 1 ||
-      (n_slices > 1 && slice_stride % 4 != 0))
+      n_slices > kNormMaxSlices || (n_slices > 1 && slice_stride % 4 != 0))
     return cudaErrorInvalidValue;
-  return launch_pdl(row_rmsnorm_kernel, dim3(rows), dim3(kNormThreads), 0, st, z, cols, w,
-                    eps, out, out_bf16, n_slices, slice_stride);
+  const int per = (cols / 4 + kNormThreads - 1) / kNormThreads;  // float4 per thread
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(rows), dim3(kNormThreads), 0, st, z, cols, w, eps, out,
+                      out_bf16, n_slices, slice_stride);
+  };
+  const bool few = n_slices <= 4;
+  if (per <= 1) return few ? go(row_rmsnorm_kernel<1, 4>) : go(row_rmsnorm_kernel<1, 8>);
+  if (per <= 2) return few ? go(row_rmsnorm_kernel<2, 4>) : go(row_rmsnorm_kernel<2, 8>);
+  if (per <= 4) return few ? go(row_rmsnorm_kernel<4, 4>) : go(row_rmsnorm_kernel<4, 8>);
+  return few ? go(row_rmsnorm_kernel<8, 4>) : go(row_rmsnorm_kernel<8, 8>);
 }
 
 int launch_add_rmsnorm(const void* a, const void* b, int rows, int cols, const float* w,

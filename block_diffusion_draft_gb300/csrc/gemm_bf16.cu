@@ -149,9 +149,14 @@ DF_DEV void store_bf16(void* dst, const float* v, int n) {
 // with the row's (cos, sin) table, then an optional scale
 DF_DEV void norm_rope(float* v, const float* w, float eps, const float2* rope_row,
                       float scale) {
-  float ss = 0.f;
+  // the sum of squares as 4 interleaved chains (one chain over 128 values is
+  // a latency chain of 128 dependent FMAs)
+  float ps[4];
 #pragma unroll
-  for (int j = 0; j < HD; ++j) ss = fmaf(v[j], v[j], ss);
+  for (int e = 0; e < 4; ++e) ps[e] = v[e] * v[e];
+#pragma unroll
+  for (int j = 4; j < HD; ++j) ps[j & 3] = fmaf(v[j], v[j], ps[j & 3]);
+  const float ss = (ps[0] + ps[1]) + (ps[2] + ps[3]);
   const float inv = rsqrtf(ss * (1.f / HD) + eps);
 #pragma unroll
   for (int j = 0; j < HD; ++j) v[j] *= inv * __ldg(w + j);

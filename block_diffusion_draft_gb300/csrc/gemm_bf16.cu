@@ -364,21 +364,46 @@ DF_DEV float4 warp_norm_rope(float4 x, float4 w4, float eps, const float2* rope_
 // loop ran; the rows' targets are broadcast from there.
 DF_DEV void qkv_finish_warp(const Plan& p, const QkvOut& qo, int wq, int lane, float4 w4,
                             int lk, __nv_bfloat16* ld, int lp, const float4* stile,
-                            const float* tile_part) {
+                            const float* tile_part, uint32_t cl_base = 0, int cl_rank = 0,
+                            int cl_n = 1) {
   constexpr int C4 = HD / 4;
   const int last_j = __reduce_max_sync(0xffffffffu, lk != 0 ? lane : -1);
-  for (int j0 = 0; j0 <= last_j; j0 += 4) {
-    int kind[4];
+  // rows wq + 4j; with a cluster source (cl_base: the same offset of every
+  // rank's shared memory) this rank takes j = cl_rank, cl_rank + cl_n, ...
+  for (int k0 = 0; cl_rank + cl_n * k0 <= last_j; k0 += 4) {
+    int kind[4], jv[4];
     float4 x[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int rr = wq + 4 * (j0 + i);
-      kind[i] = __shfl_sync(0xffffffffu, lk, (j0 + i) & 31);
-      if (j0 + i >= 32) kind[i] = 0;
+      jv[i] = cl_rank + cl_n * (k0 + i);
+      const int rr = wq + 4 * jv[i];
+      kind[i] = __shfl_sync(0xffffffffu, lk, jv[i] & 31);
+      if (jv[i] >= 32) kind[i] = 0;
       x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (kind[i] != 0 && stile != nullptr) x[i] = stile[rr * C4 + (lane ^ (rr & (C4 - 1)))];
     }
-    if (stile == nullptr) {
+    if (cl_base != 0) {
+      // the rows summed over the cluster's ranks, in rank order
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (kind[i] == 0) continue;
+        const int rr = wq + 4 * jv[i];
+        const uint32_t off = cl_base + (uint32_t)(rr * C4 + (lane ^ (rr & (C4 - 1)))) * 16;
+        float4 t[MAX_SPLITS];
+#pragma unroll
+        for (int c = 0; c < MAX_SPLITS; ++c)
+          if (c < cl_n) t[c] = ld_cluster_f4(cluster_map(off, (uint32_t)c));
+#pragma unroll
+        for (int c = 0; c < MAX_SPLITS; ++c) {
+          if (c < cl_n) {
+            x[i].x += t[c].x;
+            x[i].y += t[c].y;
+            x[i].z += t[c].z;
+            x[i].w += t[c].w;
+          }
+        }
+      }
+    } else if (stile == nullptr) {
 #pragma unroll
       for (int sp = 0; sp < MAX_SPLITS; ++sp) {
         if (sp < p.splits) {
@@ -386,7 +411,7 @@ DF_DEV void qkv_finish_warp(const Plan& p, const QkvOut& qo, int wq, int lane, f
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             if (kind[i] != 0) {
-              const float4 t = __ldcg(part + (wq + 4 * (j0 + i)) * C4 + lane);
+              const float4 t = __ldcg(part + (wq + 4 * jv[i]) * C4 + lane);
               x[i].x += t.x;
               x[i].y += t.y;
               x[i].z += t.z;
@@ -398,7 +423,7 @@ DF_DEV void qkv_finish_warp(const Plan& p, const QkvOut& qo, int wq, int lane, f
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int src_lane = (j0 + i) & 31;
+      const int src_lane = jv[i] & 31;
       const int pos_raw = __shfl_sync(0xffffffffu, lp, src_lane);
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(
           __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(ld), src_lane));
@@ -520,6 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool from_a0 = m_tile < p.n_m0;
   const int a_row0 = (from_a0 ? m_tile : m_tile - p.n_m0) * BM;
   const int n0 = n_tile * BN;
+  // QKV epilogue: the tile's norm gains and, per lane, the target of the
+  // row its warp finishes (set by the epilogue warps during the main loop)
+  float4 qk_w4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  int qk_kind = 0, qk_pos = 0;
+  __nv_bfloat16* qk_dst = nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -636,13 +666,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      qk_w4 = w4;
+      qk_kind = lane_kind;
+      qk_dst = lane_dst;
+      qk_pos = lane_pos;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.err));
       tc_fence_after();
       const int et = threadIdx.x - 64;
       float* tile_part = p.partial + (size_t)tile_id * p.splits * (BM * HD);
       float4* stile = reinterpret_cast<float4*>(smem);
       bool finish = true;
-      if (p.splits == 1) {
+      if (p.splits > 1 && p.cluster) {
+        // the tile's splits are one cluster: the rows wait in this CTA's
+        // idle stage buffers (as the one-split tile) for the merge below
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          float t[32];
+          tmem_ld32(trow + c * 32, t);
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4)
+            stile[r * C4 + ((c * 8 + i4) ^ (r & (C4 - 1)))] =
+                ok ? make_float4(t[4 * i4], t[4 * i4 + 1], t[4 * i4 + 2], t[4 * i4 + 3])
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        finish = false;
+      } else if (p.splits == 1) {
         // accumulator row -> shared tile ([row][column chunk], swizzled)
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
@@ -717,14 +765,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rank order (so the result does not depend on timing), one row per warp.
     cluster_sync();
     if (warp >= 2) {
-      switch (p.splits) {
-        case 2: cluster_sum_rows<EPI, 2>(p, m_tile, n0, smem, warp & 3, lane); break;
-        case 3: cluster_sum_rows<EPI, 3>(p, m_tile, n0, smem, warp & 3, lane); break;
-        case 4: cluster_sum_rows<EPI, 4>(p, m_tile, n0, smem, warp & 3, lane); break;
-        case 5: cluster_sum_rows<EPI, 5>(p, m_tile, n0, smem, warp & 3, lane); break;
-        case 6: cluster_sum_rows<EPI, 6>(p, m_tile, n0, smem, warp & 3, lane); break;
-        case 7: cluster_sum_rows<EPI, 7>(p, m_tile, n0, smem, warp & 3, lane); break;
-        default: cluster_sum_rows<EPI, 8>(p, m_tile, n0, smem, warp & 3, lane); break;
+      if constexpr (EPI == EPI_QKV) {
+        // rank c finishes the rows wq + 4j, j = c mod splits, of every warp wq
+        qkv_finish_warp(p, qo, warp & 3, lane, qk_w4, qk_kind, qk_dst, qk_pos, nullptr, nullptr,
+                        smem_u32(smem), (int)cluster_ctarank(), p.splits);
+      } else {
+        switch (p.splits) {
+          case 2: cluster_sum_rows<EPI, 2>(p, m_tile, n0, smem, warp & 3, lane); break;
+          case 3: cluster_sum_rows<EPI, 3>(p, m_tile, n0, smem, warp & 3, lane); break;
+          case 4: cluster_sum_rows<EPI, 4>(p, m_tile, n0, smem, warp & 3, lane); break;
+          case 5: cluster_sum_rows<EPI, 5>(p, m_tile, n0, smem, warp & 3, lane); break;
+          case 6: cluster_sum_rows<EPI, 6>(p, m_tile, n0, smem, warp & 3, lane); break;
+          case 7: cluster_sum_rows<EPI, 7>(p, m_tile, n0, smem, warp & 3, lane); break;
+          default: cluster_sum_rows<EPI, 8>(p, m_tile, n0, smem, warp & 3, lane); break;
+        }
       }
     }
     cluster_sync();  // no CTA leaves while the others still read its rows
@@ -1702,11 +1756,20 @@ int launch_gemm_bf16(const GemmShape& s, int epi, void* c, int ldc,
   p.n_m1 = g.n_m1;
   p.merged = g.merged;
   // plain epilogues merge splits in a cluster (or, F32 with slices, write
-  // one slice per split); the QKV epilogue (heavier, and 3-CTA clusters
-  // schedule poorly behind the previous kernel) merges through global partials
+  // one slice per split).  The QKV epilogue of block and context rows takes
+  // two splits in a 2-CTA cluster when the tiles allow one wave of them
+  // (3-CTA clusters schedule poorly behind the previous kernel); with block
+  // rows only, or more tiles, its splits merge through global partials
+  // (measured: the 2-CTA clusters sped up the single-sequence and
+  // band-layer steps and the per-layer five-layer schedule, and slowed the
+  // layers that follow a grouped context projection).
   p.slices = epi == EPI_F32 && scr.f32_slices && g.splits > 1;
   p.slice_stride = scr.slice_stride;
   p.cluster = epi != EPI_QKV && !p.slices;
+  if (epi == EPI_QKV && g.splits > 1 && 2 * g.tiles <= num_sms && s.a1_rows > 0) {
+    g.splits = 2;
+    p.cluster = 1;
+  }
   if (g.splits > 1 && !p.cluster && !p.slices) {
     const size_t need = (size_t)g.n_tiles * (g.n_m0 + g.n_m1) * g.splits * BM * g.bn * 4;
     if (scr.partial == nullptr || scr.partial_bytes < need ||

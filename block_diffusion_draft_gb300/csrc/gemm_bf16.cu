@@ -325,6 +325,57 @@ DF_DEV void qkv_apply(const QkvOut& qo, const QkvTarget& g, int pos, float* v) {
   store_bf16(g.dst, v, HD);
 }
 
+// The same epilogue for a row still in TMEM (128 accumulator columns at
+// `col`, this thread's lane), read twice in 32-column pieces: once for the
+// sum of squares, then column pairs (j, j + 64) a piece of each at a time,
+// so that few values, gains and (cos, sin) pairs are live at once.  The
+// gains `w4` and the row's (cos, sin) pairs `r4` are generic pointers
+// (global memory, or copies in shared memory).  Warp-collective (TMEM
+// loads): every lane calls it.
+DF_DEV void qkv_apply_tmem(const QkvOut& qo, const QkvTarget& g, uint32_t col, const float4* w4,
+                           const float4* r4) {
+  const bool live = g.kind != 0;
+  float inv = 1.f;
+  if (__any_sync(0xffffffffu, live && g.kind != 3)) {
+    float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      float t[32];
+      tmem_ld32(col + c * 32, t);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ps[i & 3] = fmaf(t[i], t[i], ps[i & 3]);
+    }
+    inv = rsqrtf(((ps[0] + ps[1]) + (ps[2] + ps[3])) * (1.f / HD) + qo.eps);
+  }
+  const bool rot = live && g.kind != 3;
+  const float scale = g.kind == 1 ? qo.q_scale : 1.f;
+#pragma unroll 1
+  for (int c = 0; c < HD / 64; ++c) {  // columns 32c.. and 64 + 32c..
+    float a[32], b[32];
+    tmem_ld32(col + c * 32, a);
+    tmem_ld32(col + HD / 2 + c * 32, b);
+    if (!live) continue;
+    if (rot) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 ga = w4[c * 8 + q4], gb = w4[HD / 8 + c * 8 + q4];
+        const float4 cs0 = r4[c * 16 + 2 * q4], cs1 = r4[c * 16 + 2 * q4 + 1];
+        const float ga_[4] = {ga.x, ga.y, ga.z, ga.w}, gb_[4] = {gb.x, gb.y, gb.z, gb.w};
+        const float co[4] = {cs0.x, cs0.z, cs1.x, cs1.z}, si[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * q4 + e;
+          const float x = a[i] * (inv * ga_[e]), y = b[i] * (inv * gb_[e]);
+          a[i] = (x * co[e] - y * si[e]) * scale;
+          b[i] = (y * co[e] + x * si[e]) * scale;
+        }
+      }
+    }
+    store_bf16(g.dst + c * 32, a, 32);
+    store_bf16(g.dst + HD / 2 + c * 32, b, 32);
+  }
+}
+
 // The same epilogue with one row spread over a warp: lane l holds columns
 // 4l .. 4l+3.  The RMSNorm sum is a butterfly over the warp, and the RoPE
 // partner of column j < 64 (column j + 64) sits 16 lanes away.
@@ -1188,7 +1239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + STAGES_BIG;
   uint64_t* acc_full = empty + STAGES_BIG;  // [2]
   uint64_t* acc_empty = acc_full + 2;       // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* rope_bar = acc_empty + 2;       // QKV, one unit per CTA: staged RoPE rows
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rope_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
 
@@ -1204,6 +1256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 128);
     }
+    mbar_init(rope_bar, 128);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA0);
@@ -1347,6 +1400,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + buf * BNB;
       const bool whole = p.splits == 1 || p.slices;
+      if constexpr (EPI == EPI_QKV) {
+        if (whole) {
+          // norm, RoPE and stores straight from TMEM, then the accumulator
+          // goes back to the MMA warp.  The tile's two heads share the row's
+          // position and gains.  A CTA with a single unit has idle stage
+          // buffers now (every MMA has completed): the rows' (cos, sin)
+          // pairs and the gains are copied there in one round of bulk
+          // copies rather than read piece by piece from L2 in the epilogue.
+          const float* gains = qkv_col_norm(qo, n * BNB);
+          const bool rot = src >= 0 && (tg[0].kind == 1 || tg[0].kind == 2);
+          const float4* w4 = reinterpret_cast<const float4*>(gains);
+          const float4* r4 = reinterpret_cast<const float4*>(qo.rope + (size_t)tpos[0] * (HD / 2));
+          if ((int)gridDim.x >= units) {
+            // HD / 2 (cos, sin) pairs = HD / 4 float4 = 512 B a row, rows 528 B
+            // apart (a warp's 16-byte reads of 32 rows then spread over all
+            // banks), then the gains
+            constexpr int RS = HD / 4 + 1;
+            float4* s_rope = reinterpret_cast<float4*>(smem) + r * RS;
+            float4* s_gain = reinterpret_cast<float4*>(smem) + BM * RS;
+            const uint32_t bytes = (rot ? 512u : 0u) + (et == 0 && gains != nullptr ? 512u : 0u);
+            if (bytes > 0) {
+              mbar_arrive_expect_tx(rope_bar, bytes);
+              if (rot) bulk_load_1d(s_rope, r4, 512, rope_bar);
+              if (et == 0 && gains != nullptr) bulk_load_1d(s_gain, gains, 512, rope_bar);
+            } else {
+              mbar_arrive(rope_bar);
+            }
+            mbar_wait(rope_bar, 0, abort_flag, p.err);
+            w4 = s_gain;
+            r4 = s_rope;
+          }
+#pragma unroll 1
+          for (int half = 0; half < BNB / HD; ++half) {
+            QkvTarget g = tg[half];
+            if (src < 0) g.kind = 0;
+            qkv_apply_tmem(qo, g, trow + half * HD, w4, r4);
+          }
+          tc_fence_before();
+          mbar_arrive(&acc_empty[buf]);
+          continue;
+        }
+      }
       // split units: sums of the valid rows go to the (tile, split) slot,
       // laid out [column chunk of 4][row] so a warp's access is contiguous
       float4* my_part =

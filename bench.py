@@ -195,6 +195,9 @@ def parse():
                          "and print the table rows")
     ap.add_argument("--ncu-launches", metavar="CSV", default=None,
                     help="no GPU work: print the per-kernel table of an ncu launch list")
+    ap.add_argument("--read-stream", action="store_true",
+                    help="measurement aid instead of the bench: time TMA read passes over "
+                         "the workload's fc weight matrix (one JSON line per launch shape)")
     return ap.parse_args()
 
 
@@ -1022,8 +1025,76 @@ def job_value(world, units_per_step, ms):
 # --------------------------------------------------------------------------
 # main
 # --------------------------------------------------------------------------
+def read_stream(args):
+    """The rate at which TMA alone reads the workload's fc weight matrix
+    ([hidden, n_target_layers * hidden] bf16, 168 MB for the 8B shape) in the
+    boxes the GEMMs read weights in, for several CTA counts and box counts in
+    flight per CTA: the read-side ceiling of the weight-streaming GEMMs at
+    this size.  Each pass is one launch timed with CUDA events on the
+    launching stream after a 512 MiB write (L2 flush); the median of the
+    timed passes is reported, with the clocks sampled meanwhile."""
+    import torch
+    import __graft_entry__ as G
+    G.build()
+    from block_diffusion_draft_gb300 import DFlashAttention
+    from block_diffusion_draft_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sp = W.SPECS[args.workload]
+    w = W.weights(sp, args.seed)
+    attn = DFlashAttention(w, hidden=sp.hidden, n_heads=sp.n_heads, n_kv_heads=sp.n_kv_heads,
+                           head_dim=sp.head_dim, n_target_layers=sp.n_target_layers,
+                           rms_eps=sp.rms_eps, rope_theta=sp.rope_theta,
+                           sliding_window=sp.sliding_window, max_position=sp.max_position,
+                           device=dev)
+    m = w["fc"].to(dev)
+    del w
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nbytes = m.numel() * m.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = None if args.no_clocks else ClockSampler(0)
+    shapes = [(c, s) for c in (64, 96, 128, sms, 2 * sms) for s in (2, 3, 4, 6, 8, 12)
+              if not (c > sms and s > 6)]
+    n_warm, n_time = max(1, args.warmup), 10
+    res = []
+    t0 = time.time()
+    for ctas, stages in shapes:
+        ts = []
+        for r in range(n_warm + n_time):
+            flush.fill_(r & 255)
+            e0.record()
+            attn.read_stream_probe(m, ctas, stages)
+            e1.record()
+            e1.synchronize()
+            if r >= n_warm:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        us = float(np.median(ts))
+        res.append({"probe": "tma_read_stream", "ctas": ctas, "stages": stages,
+                    "inflight_kb_per_sm": stages * 16 * (2 if ctas > sms else 1),
+                    "us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)})
+    t1 = time.time()
+    if clk is not None:
+        clk.stop()
+    err = attn.device_error()
+    if err != 0:
+        raise RuntimeError(f"read-stream probe recorded device error {err}")
+    for r in res:
+        print(json.dumps(r))
+    best = max(res, key=lambda r: r["gbs"])
+    pk = peaks()
+    print(json.dumps({"probe": "tma_read_stream_summary", "bytes": nbytes,
+                      "matrix": list(m.shape), "box": [128, 64], "passes_timed": n_time,
+                      "best": best, "copy_peak_gbs": pk["hbm_gbs"],
+                      "best_frac_of_copy_peak": round(best["gbs"] / pk["hbm_gbs"], 3),
+                      "clocks": clk.summary(t0, t1) if clk is not None else None}))
+    return 0
+
+
 def main():
     args = parse()
+    if args.read_stream:
+        return read_stream(args)
     if args.ncu_traffic or args.ncu_launches:
         rows = write_traffic(args.ncu_traffic) if args.ncu_traffic else \
             launch_table(args.ncu_launches)

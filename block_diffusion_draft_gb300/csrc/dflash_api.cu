@@ -322,7 +322,7 @@ extern "C" {
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
 
-int dflash_abi_version(void) { return 104; }
+int dflash_abi_version(void) { return 105; }
 
 int dflash_attn_create(const dflash_attn_config* cfg_in, const void* wq, const void* wk,
                        const void* wv, const void* wo, const void* q_norm_w,
@@ -1218,6 +1218,26 @@ int dflash_wait_probe(dflash_attn* a, int64_t limit_ns, int arrive, dflash_strea
   DF_CUDA(launch_wait_probe(a->err, (unsigned long long)limit_ns, arrive,
                             static_cast<cudaStream_t>(stream)),
           "wait probe launch");
+  return DFLASH_OK;
+}
+
+int dflash_read_stream_probe(dflash_attn* a, const void* matrix, int64_t rows, int64_t cols,
+                             int ctas, int stages, dflash_stream stream) {
+  if (int r = check_attn(a)) return r;
+  if (matrix == nullptr) return fail(DFLASH_ERR_ARG, "matrix is null");
+  if ((reinterpret_cast<uintptr_t>(matrix) & 15) != 0)
+    return fail(DFLASH_ERR_ARG, "matrix must be 16-byte aligned");
+  if (rows <= 0 || cols <= 0 || rows % 128 != 0 || cols % 64 != 0 || cols > (1 << 30) ||
+      rows / 128 > (1 << 30))
+    return fail(DFLASH_ERR_ARG, "rows must be a positive multiple of 128 and cols of 64");
+  if (stages < 1 || stages > 12) return fail(DFLASH_ERR_ARG, "stages must be in [1, 12]");
+  if (ctas < 1 || ctas > 2 * a->num_sms)
+    return fail(DFLASH_ERR_ARG, "ctas must be in [1, 2 x SMs]");
+  if (ctas > a->num_sms && stages > 6)
+    return fail(DFLASH_ERR_ARG, "more CTAs than SMs take at most 6 stages");
+  DF_CUDA(launch_read_stream(matrix, rows, cols, ctas, stages, a->err,
+                             static_cast<cudaStream_t>(stream)),
+          "read stream probe launch");
   return DFLASH_OK;
 }
 

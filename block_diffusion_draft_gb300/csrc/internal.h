@@ -238,6 +238,8 @@ int launch_packed_positions(const int* anchors, int batch, int seq,
 // one thread waits on an mbarrier for at most limit_ns (a never-completed
 // barrier unless `arrive`); on expiry DFLASH_DEV_WAIT_TIMEOUT goes to `err`
 int launch_wait_probe(int* err, unsigned long long limit_ns, int arrive, cudaStream_t st);
+int launch_read_stream(const void* src, long long rows, long long cols, int ctas, int stages,
+                       int* err, cudaStream_t st);
 
 // ----------------------------------------------------------- fp32 path
 int launch_gemm_f32(const float* a, int rows, const float* b, int n, int k,

@@ -227,6 +227,45 @@ __global__ void wait_probe_kernel(int* err, unsigned long long limit_ns, int arr
   __syncthreads();
 }
 
+
+// Read-stream probe: streams a rows x cols bf16 row-major matrix once through
+// TMA in the boxes the GEMMs read their weights in (128 rows x 64 columns,
+// 128-byte swizzle).  Box b is (row block b / (cols / 64), column block
+// b % (cols / 64)); CTA c takes boxes [c * total / G, (c + 1) * total / G)
+// and keeps `stages` of them in flight, reusing a slot as soon as its box has
+// landed.  The data is discarded: the kernel measures how fast TMA alone
+// moves the bytes.
+constexpr int kProbeBox = 128 * 64 * 2;
+constexpr int kProbeMaxStages = 12;
+
+__global__ void __launch_bounds__(32, 1)
+    read_stream_kernel(const __grid_constant__ CUtensorMap tm, int n_row_blocks, int n_col_blocks,
+                       int stages, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * kProbeBox);
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  const long long total = (long long)n_row_blocks * n_col_blocks;
+  const long long b0 = (long long)blockIdx.x * total / gridDim.x;
+  const int n = (int)((long long)(blockIdx.x + 1) * total / gridDim.x - b0);
+  abort_flag = 0;
+  for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+  fence_mbar_init();
+  const uint64_t pol = policy_evict_first();
+  for (int i = 0; i < n; ++i) {
+    const int s = i % stages;
+    // slot s is free once its previous box (i - stages) has landed
+    if (i >= stages && !mbar_wait(&full[s], ((i / stages) - 1) & 1, &abort_flag, err)) return;
+    mbar_arrive_expect_tx(&full[s], kProbeBox);
+    const long long b = b0 + i;
+    tma_load_2d(smem + (size_t)s * kProbeBox, &tm, &full[s], (int)(b % n_col_blocks) * 64,
+                (int)(b / n_col_blocks) * 128, pol);
+  }
+  for (int i = n > stages ? n - stages : 0; i < n; ++i)
+    if (!mbar_wait(&full[i % stages], (i / stages) & 1, &abort_flag, err)) return;
+}
 }  // namespace
 
 int launch_rope_table(float2* tab, int max_pos, int half, float theta,
@@ -303,4 +342,23 @@ int launch_wait_probe(int* err, unsigned long long limit_ns, int arrive, cudaStr
   return cudaGetLastError();
 }
 
+
+int launch_read_stream(const void* src, long long rows, long long cols, int ctas, int stages,
+                       int* err, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0 || rows % 128 != 0 || cols % 64 != 0 || cols > (1 << 30) ||
+      rows / 128 > (1 << 30) || stages < 1 || stages > kProbeMaxStages || ctas < 1)
+    return cudaErrorInvalidValue;
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!done_on_device(attr_done)) {
+    cudaFuncSetAttribute(read_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kProbeMaxStages * kProbeBox + 2048);
+    mark_device(attr_done);
+  }
+  CUtensorMap tm;
+  if (make_tmap_bf16_rows(&tm, src, rows, cols, 128) != 0) return cudaErrorInvalidValue;
+  count_launch();
+  read_stream_kernel<<<ctas, 32, (size_t)stages * kProbeBox + 2048, st>>>(
+      tm, (int)(rows / 128), (int)(cols / 64), stages, err);
+  return cudaGetLastError();
+}
 }  // namespace df

@@ -79,6 +79,8 @@ _SIGNATURES = {
                                       c_void_p, c_void_p, c_void_p], c_int),
     "dflash_device_error": ([c_void_p, POINTER(c_int32)], c_int),
     "dflash_wait_probe": ([c_void_p, ctypes.c_int64, c_int, c_void_p], c_int),
+    "dflash_read_stream_probe": ([c_void_p, c_void_p, ctypes.c_int64, ctypes.c_int64, c_int,
+                                  c_int, c_void_p], c_int),
     "dflash_kernel_launches": ([POINTER(ctypes.c_uint64)], c_int),
     "dflash_packed_attn_core": ([c_void_p, c_int, c_int, c_int, c_int] + [c_void_p] * 7, c_int),
     "dflash_packed_attn_core_backward": ([c_void_p, c_int, c_int, c_int, c_int] +
@@ -300,6 +302,17 @@ class DFlashAttention:
         with torch.cuda.device(self.device):
             check(lib().dflash_wait_probe(self.handle, int(limit_ns), int(bool(arrive)),
                                           _stream(self.device)))
+
+    def read_stream_probe(self, matrix: torch.Tensor, ctas: int, stages: int) -> None:
+        """Enqueue one TMA read pass over a bf16 [rows, cols] matrix on the
+        current stream (measurement aid: the weight boxes of the GEMMs,
+        `stages` boxes in flight per CTA, data discarded)."""
+        if matrix.dtype != torch.bfloat16 or matrix.dim() != 2 or not matrix.is_contiguous():
+            raise ValueError("matrix must be a contiguous 2-D bf16 tensor")
+        with torch.cuda.device(self.device):
+            check(lib().dflash_read_stream_probe(self.handle, _p(matrix), matrix.shape[0],
+                                                 matrix.shape[1], int(ctas), int(stages),
+                                                 _stream(self.device)))
 
     def close(self) -> None:
         if getattr(self, "handle", None):

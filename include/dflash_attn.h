@@ -116,7 +116,7 @@ typedef struct {
 /* Message for the last failed call on this thread ("" if none). */
 const char* dflash_last_error(void);
 
-/* ABI version of this header (major * 100 + minor): 104. */
+/* ABI version of this header (major * 100 + minor): 105. */
 int dflash_abi_version(void);
 
 /* Create one layer on the current CUDA device.
@@ -466,6 +466,22 @@ int dflash_device_error(dflash_attn* attn, int32_t* code);
  * limit_ns must lie in [1e3, 1e8].  Errors: _ARG, _CUDA. */
 int dflash_wait_probe(dflash_attn* attn, int64_t limit_ns, int arrive,
                       dflash_stream stream);
+
+/* Measurement aid (no counterpart on the pages): the rate at which TMA alone
+ * reads a projection's weights.  Enqueues one kernel on `stream` that streams
+ * the rows x cols bf16 row-major device matrix `matrix` (caller-owned, 16-byte
+ * aligned) once into shared memory in the boxes the GEMMs read weights in
+ * (128 rows x 64 columns, 128-byte swizzle) and discards it.  The boxes, in
+ * (row block, column block) order, are split into `ctas` contiguous shares,
+ * one per CTA; each CTA keeps `stages` boxes (16 KB each) in flight and
+ * reuses a slot as soon as its box has landed.  Nothing is written.  Time it
+ * with events on `stream`.  rows: a positive multiple of 128; cols: a
+ * positive multiple of 64; stages in [1, 12]; ctas in [1, 2 x SMs], and at
+ * most 6 stages when ctas exceeds the SM count (two CTAs per SM).  Its
+ * bounded waits record DFLASH_DEV_WAIT_TIMEOUT in the layer's device error
+ * word like every pipeline of the library.  Errors: _ARG, _CUDA. */
+int dflash_read_stream_probe(dflash_attn* attn, const void* matrix, int64_t rows,
+                             int64_t cols, int ctas, int stages, dflash_stream stream);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ def test_every_declared_function_is_exported(L):
 
 
 def test_abi_version(L):
-    assert L.dflash_abi_version() == 104
+    assert L.dflash_abi_version() == 105
 
 
 def test_create_rejects_null_config(L):
@@ -107,4 +107,10 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 def test_wait_probe_checks_arguments_on_the_host(L):
     stream = ctypes.c_void_p(0)
     assert L.dflash_wait_probe(None, 1_000_000, 0, stream) == -1
+    assert b"null" in L.dflash_last_error()
+
+
+def test_read_stream_probe_checks_arguments_on_the_host(L):
+    stream = ctypes.c_void_p(0)
+    assert L.dflash_read_stream_probe(None, None, 128, 64, 1, 1, stream) == -1
     assert b"null" in L.dflash_last_error()

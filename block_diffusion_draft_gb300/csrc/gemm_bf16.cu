@@ -638,11 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (kb0 + 2 * i + h) * BK, n0, pol_w);
       }
       grid_dep_sync();
-      for (int i = 0; i < n_st; ++i) {
-        const int s = i % S;
+      // slot s and its pass over the ring (phase bit ph) advance with i: the
+      // ring depth is a run-time value, and a division per stage would sit
+      // on this thread's issue path
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < n_st; ++i, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
         const int hk = min(2, nkb - 2 * i);
         if (i >= pre) {
-          const uint32_t ph = (i / S) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
           mbar_arrive_expect_tx(&full[s], (uint32_t)(hk * half));
           for (int h = 0; h < hk; ++h)
@@ -666,9 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (the start address field holds address / 16)
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
       const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
-      for (int i = 0; i < n_st; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (i / S) & 1;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < n_st; ++i, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
         const int hk = min(2, nkb - 2 * i);
         if (!mbar_wait(&full[s], ph, abort_flag, p.err)) break;
         tc_fence_after();
@@ -925,11 +928,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sW + (size_t)i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pol_w);
       }
       grid_dep_sync();
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S;
+      int s = 0;  // slot and phase bit advance with i (no division per stage)
+      uint32_t ph = 0;
+      for (int i = 0; i < nkb; ++i, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
         const int kx = (kb0 + i) * BK;
         if (i >= pre) {
-          if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
           mbar_arrive_expect_tx(&full[s], W_BYTES + p.x_bytes);
           tma_load_2d(sW + (size_t)s * W_BYTES, &tmW, &full[s], kx, n0, pol_w);
         }
@@ -943,9 +947,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc0 = idesc_bf16(BM, p.xb0, false);
       const uint32_t idesc1 = idesc_bf16(BM, p.xb1 > 0 ? p.xb1 : 16, false);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < nkb; ++i, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+        if (!mbar_wait(&full[s], ph, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t w_base = smem_u32(sW + (size_t)s * W_BYTES);
         const uint32_t x_base = smem_u32(sX + (size_t)s * p.x_bytes);
@@ -1119,12 +1124,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sW + (size_t)i * W_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pol_w);
       }
       grid_dep_sync();
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S;
+      int s = 0;  // slot and phase bit advance with i (no division per stage)
+      uint32_t ph = 0;
+      for (int i = 0; i < nkb; ++i, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
         const int kx = (kb0 + i) * BK;
         if (i >= pre) {
           // every CTA of the cluster is done with stage s
-          if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.err)) break;
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           tma_load_2d(sW + (size_t)s * W_BYTES, &tmW, &full[s], kx, n0, pol_w);
         }
@@ -1142,9 +1148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc1 = idesc_bf16(BM, p.xb1 > 0 ? p.xb1 : 16, false);
       const uint64_t w_desc0 = sdesc_sw128(smem_u32(sW), 16, 1024);
       const uint64_t x_desc0 = sdesc_sw128(smem_u32(sX), 16, 1024);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < nkb; ++i, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+        if (!mbar_wait(&full[s], ph, abort_flag, p.err)) break;
         tc_fence_after();
         const uint64_t wd = w_desc0 + (((size_t)s * W_BYTES) >> 4);
         const uint64_t xd = x_desc0 + (((size_t)s * p.x_bytes) >> 4);

@@ -114,3 +114,19 @@ def test_read_stream_probe_checks_arguments_on_the_host(L):
     stream = ctypes.c_void_p(0)
     assert L.dflash_read_stream_probe(None, None, 128, 64, 1, 1, stream) == -1
     assert b"null" in L.dflash_last_error()
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary header compiles as strict C99 (no C++ in the ABI)."""
+    import os
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = tmp_path / "t.c"
+    src.write_text('#include "dflash_attn.h"\nint main(void) { return dflash_abi_version() == 0; }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-fsyntax-only", "-I", inc, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
